@@ -1,0 +1,291 @@
+"""ctypes binding of libdsa_indexer.so: argument marshalling only.
+
+Every computation happens in the library's CUDA kernels.  There is no CPU
+fallback: if the shared library is missing, :func:`load` raises.  Tensors are
+PyTorch tensors used as device buffers; the binding checks dtypes, devices,
+shapes and contiguity, then passes raw pointers and the current CUDA stream.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+from typing import Optional, Sequence
+
+import torch
+
+LIB_PATH = Path(__file__).resolve().parent / "_lib" / "libdsa_indexer.so"
+
+HEAD_DIM = 128
+PAGE_TOKENS = 64
+PAGE_BYTES = 8448
+PAGE_SCALE_OFFSET = 8192
+MAX_TOPK = 2048
+
+DSA_OK = 0
+ERRORS = {
+    -1: "INVALID_ARG",
+    -2: "UNSUPPORTED",
+    -3: "WORKSPACE_TOO_SMALL",
+    -4: "CUDA",
+    -5: "TIMEOUT",
+}
+STATUS_BAD_PAGE = 0x1
+STATUS_BAD_METADATA = 0x2
+STATUS_TIMEOUT = 0x4
+
+# every symbol declared in include/dsa_indexer.h
+EXPORTS = (
+    "dsa_abi_version",
+    "dsa_last_error",
+    "dsa_last_launch_count",
+    "dsa_indexer_write_k",
+    "dsa_quantize_fp8_blocks",
+    "dsa_indexer_workspace_bytes",
+    "dsa_indexer_score_topk",
+    "dsa_layer_is_full",
+    "dsa_layer_stack_run",
+)
+
+
+class DsaError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {message}")
+        self.code = code
+
+
+class LayerIO(ctypes.Structure):
+    _fields_ = [
+        ("k", ctypes.c_void_p),
+        ("q_fp8", ctypes.c_void_p),
+        ("q_scale", ctypes.c_void_p),
+        ("w", ctypes.c_void_p),
+        ("k_cache", ctypes.c_void_p),
+    ]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+
+def _declare(lib: ctypes.CDLL) -> None:
+    lib.dsa_abi_version.restype = _I
+    lib.dsa_abi_version.argtypes = []
+    lib.dsa_last_error.restype = ctypes.c_char_p
+    lib.dsa_last_error.argtypes = []
+    lib.dsa_last_launch_count.restype = _I
+    lib.dsa_last_launch_count.argtypes = []
+    lib.dsa_indexer_write_k.restype = _I
+    lib.dsa_indexer_write_k.argtypes = [_P, _I, _P, _P, _I, _P, _I, _P, _I64, _P, _P, _P]
+    lib.dsa_quantize_fp8_blocks.restype = _I
+    lib.dsa_quantize_fp8_blocks.argtypes = [_P, _I64, _P, _P, _P]
+    lib.dsa_indexer_workspace_bytes.restype = _SZ
+    lib.dsa_indexer_workspace_bytes.argtypes = [_I, _I, _I, _I64, _I]
+    lib.dsa_indexer_score_topk.restype = _I
+    lib.dsa_indexer_score_topk.argtypes = [
+        _P, _P, _P, _I, _I, _P, _I64, _P, _P, _I, _P, _I, _I, _P, _I, _P, _I64, _P, _SZ, _P, _P]
+    lib.dsa_layer_is_full.restype = _I
+    lib.dsa_layer_is_full.argtypes = [_I, ctypes.c_char_p, _I, _I]
+    lib.dsa_layer_stack_run.restype = _I
+    lib.dsa_layer_stack_run.argtypes = [
+        _I, ctypes.c_char_p, _I, _I, ctypes.POINTER(LayerIO), _I, _I, _P, _P, _I, _P, _I, _I64,
+        _I, _P, _I, ctypes.POINTER(ctypes.c_void_p), _P, _P, _SZ, _P, _P]
+
+
+def load() -> ctypes.CDLL:
+    """Load the library (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                "(there is no CPU fallback for the indexer path)")
+        lib = ctypes.CDLL(str(LIB_PATH))
+        _declare(lib)
+        _lib = lib
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != DSA_OK:
+        msg = load().dsa_last_error().decode(errors="replace")
+        raise DsaError(rc, msg)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None:
+        for i, (a, b) in enumerate(zip(t.shape, shape)):
+            if b is not None and a != b:
+                raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+        if len(t.shape) != len(shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+
+
+# ----------------------------------------------------------------------------
+# entry points
+# ----------------------------------------------------------------------------
+
+def abi_version() -> int:
+    return load().dsa_abi_version()
+
+
+def last_launch_count() -> int:
+    return load().dsa_last_launch_count()
+
+
+def layer_is_full(layer_id: int, pattern: Optional[str] = None, freq: int = 1, offset: int = 2) -> bool:
+    rc = load().dsa_layer_is_full(layer_id, None if pattern is None else pattern.encode(), freq, offset)
+    if rc < 0:
+        _check(rc)
+    return bool(rc)
+
+
+def workspace_bytes(T: int, H: int, R: int, index_topk: int, max_ctx: int = 0) -> int:
+    n = load().dsa_indexer_workspace_bytes(T, H, R, max_ctx, index_topk)
+    if n == 0:
+        raise DsaError(-1, f"no workspace size for T={T}, H={H}, R={R}, index_topk={index_topk}")
+    return int(n)
+
+
+def alloc_workspace(T: int, H: int, R: int, index_topk: int, device="cuda") -> torch.Tensor:
+    n = workspace_bytes(T, H, R, index_topk)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def quantize_fp8_blocks(x: torch.Tensor, codes: Optional[torch.Tensor] = None,
+                        scales: Optional[torch.Tensor] = None, stream=None):
+    """x [..., 128] FP32 -> (codes uint8 [..., 128], scales FP32 [...])."""
+    _need(x, "x", torch.float32)
+    if x.shape[-1] != HEAD_DIM:
+        raise ValueError("last dimension must be 128")
+    nb = x.numel() // HEAD_DIM
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    _need(codes, "codes", torch.uint8)
+    _need(scales, "scales", torch.float32)
+    _check(load().dsa_quantize_fp8_blocks(_ptr(x), nb, _ptr(codes), _ptr(scales), _stream(stream)))
+    return codes, scales
+
+
+def write_k(k: torch.Tensor, query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
+            block_table: torch.Tensor, k_cache: torch.Tensor,
+            slot_mapping: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+            stream=None) -> None:
+    T = k.shape[0]
+    R = seq_lens.shape[0]
+    _need(k, "k", torch.float32, (T, HEAD_DIM))
+    _need(query_start_loc, "query_start_loc", torch.int32, (R + 1,))
+    _need(seq_lens, "seq_lens", torch.int32, (R,))
+    _need(block_table, "block_table", torch.int32, (R, None))
+    _need(k_cache, "k_cache", torch.uint8, (None, PAGE_BYTES))
+    if slot_mapping is not None:
+        _need(slot_mapping, "slot_mapping", torch.int64, (T,))
+    if status is not None:
+        _need(status, "status", torch.int32)
+    _check(load().dsa_indexer_write_k(
+        _ptr(k), T, _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table),
+        block_table.shape[1], _ptr(k_cache), k_cache.shape[0], _ptr(slot_mapping), _ptr(status),
+        _stream(stream)))
+
+
+def score_topk(q_fp8: torch.Tensor, q_scale: torch.Tensor, w: torch.Tensor,
+               k_cache: torch.Tensor, query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
+               block_table: torch.Tensor, index_topk: int, topk_buffer: torch.Tensor,
+               workspace: torch.Tensor, scores_out: Optional[torch.Tensor] = None,
+               status: Optional[torch.Tensor] = None, stream=None) -> None:
+    T, H = q_fp8.shape[0], q_fp8.shape[1]
+    R = seq_lens.shape[0]
+    _need(q_fp8, "q_fp8", torch.uint8, (T, H, HEAD_DIM))
+    _need(q_scale, "q_scale", torch.float32, (T, H))
+    _need(w, "w", torch.float32, (T, H))
+    _need(k_cache, "k_cache", torch.uint8, (None, PAGE_BYTES))
+    _need(query_start_loc, "query_start_loc", torch.int32, (R + 1,))
+    _need(seq_lens, "seq_lens", torch.int32, (R,))
+    _need(block_table, "block_table", torch.int32, (R, None))
+    _need(topk_buffer, "topk_buffer", torch.int32, (None, index_topk))
+    _need(workspace, "workspace", torch.uint8)
+    ld = 0
+    if scores_out is not None:
+        _need(scores_out, "scores_out", torch.float32, (T, None))
+        ld = scores_out.shape[1]
+    if status is not None:
+        _need(status, "status", torch.int32)
+    _check(load().dsa_indexer_score_topk(
+        _ptr(q_fp8), _ptr(q_scale), _ptr(w), T, H, _ptr(k_cache), k_cache.shape[0],
+        _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table), block_table.shape[1],
+        index_topk, _ptr(topk_buffer), topk_buffer.shape[0], _ptr(scores_out), ld,
+        _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)))
+
+
+def layer_stack_run(layers: Sequence[Optional[dict]], pattern: Optional[str], freq: int,
+                    offset: int, H: int, query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
+                    block_table: torch.Tensor, num_pages: int, index_topk: int,
+                    topk_buffer: torch.Tensor, workspace: torch.Tensor,
+                    per_layer_out: Optional[Sequence[Optional[torch.Tensor]]] = None,
+                    slot_mapping: Optional[torch.Tensor] = None,
+                    status: Optional[torch.Tensor] = None, T: Optional[int] = None,
+                    stream=None) -> None:
+    """Run the F/S layer stack.  ``layers[l]`` is a dict with keys k, q_fp8,
+    q_scale, w, k_cache for F layers, or None for S layers."""
+    R = seq_lens.shape[0]
+    _need(query_start_loc, "query_start_loc", torch.int32, (R + 1,))
+    _need(seq_lens, "seq_lens", torch.int32, (R,))
+    _need(block_table, "block_table", torch.int32, (R, None))
+    _need(topk_buffer, "topk_buffer", torch.int32, (None, index_topk))
+    _need(workspace, "workspace", torch.uint8)
+    L = len(layers)
+    arr = (LayerIO * L)()
+    for i, io in enumerate(layers):
+        if io is None:
+            continue
+        if T is None:
+            T = io["k"].shape[0]
+        _need(io["k"], f"layers[{i}].k", torch.float32, (T, HEAD_DIM))
+        _need(io["q_fp8"], f"layers[{i}].q_fp8", torch.uint8, (T, H, HEAD_DIM))
+        _need(io["q_scale"], f"layers[{i}].q_scale", torch.float32, (T, H))
+        _need(io["w"], f"layers[{i}].w", torch.float32, (T, H))
+        _need(io["k_cache"], f"layers[{i}].k_cache", torch.uint8, (num_pages, PAGE_BYTES))
+        arr[i] = LayerIO(io["k"].data_ptr(), io["q_fp8"].data_ptr(), io["q_scale"].data_ptr(),
+                         io["w"].data_ptr(), io["k_cache"].data_ptr())
+    if T is None:
+        raise ValueError("no F layer given")
+    outs = None
+    if per_layer_out is not None:
+        outs = (ctypes.c_void_p * L)()
+        for i, o in enumerate(per_layer_out):
+            if o is not None:
+                _need(o, f"per_layer_out[{i}]", torch.int32, (T, index_topk))
+                outs[i] = o.data_ptr()
+    if slot_mapping is not None:
+        _need(slot_mapping, "slot_mapping", torch.int64, (T,))
+    if status is not None:
+        _need(status, "status", torch.int32)
+    _check(load().dsa_layer_stack_run(
+        L, None if pattern is None else pattern.encode(), freq, offset, arr, T, H,
+        _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table), block_table.shape[1],
+        num_pages, index_topk, _ptr(topk_buffer), topk_buffer.shape[0], outs, _ptr(slot_mapping),
+        _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)))

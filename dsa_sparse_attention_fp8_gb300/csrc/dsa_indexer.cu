@@ -1,0 +1,485 @@
+// C ABI of the DSA lightning-indexer library: argument checks, launch
+// configuration, tensor-map encoding and kernel launches.  See
+// include/dsa_indexer.h for the contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "dsa_indexer.h"
+#include "kwrite.cuh"
+#include "plan.cuh"
+#include "score_topk.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+thread_local int g_last_launches = 0;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return DSA_OK;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool supported_heads(int H) {
+  return H == 4 || H == 8 || H == 16 || H == 32 || H == 64 || H == 128;
+}
+
+// ---------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D uint8 view [rows, 128] with a box of `box_rows` x 128 bytes, 128-byte swizzle.
+int make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {128, rows};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return DSA_OK;
+}
+
+// ---------------------------------------------------------------- launch shape
+struct ScoreShape {
+  int G, C, NS, NB, n_max, q_box_per_token;
+  size_t smem_bytes;
+  dsa::ScoreParams offs;  // only the off_* fields are filled
+};
+
+constexpr size_t kSmemLimit = 232448;  // 227 KB opt-in per block on sm_100-family
+
+int candidate_capacity(int k) {
+  int c = (k >= 1024) ? k + k / 2 : (2 * k > k + 128 ? 2 * k : k + 128);
+  return (c + 127) / 128 * 128;
+}
+
+// Rows per group: one row per decode batch (no request has more rows than
+// one), else as many rows as fill N = 256 of the MMA while the candidate
+// buffers stay within 96 KB of shared memory.
+int choose_group(int T, int R, int H, int k) {
+  if (T <= R) return 1;
+  int g = 256 / H;
+  const int by_smem = (96 * 1024) / (candidate_capacity(k) * 8);
+  if (g > by_smem) g = by_smem;
+  return g < 1 ? 1 : g;
+}
+
+size_t up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
+  s->G = choose_group(T, R, H, k);
+  s->C = candidate_capacity(k);
+  s->q_box_per_token = (H % 8 == 0) ? 1 : 0;
+  s->n_max = (s->G * H + 15) / 16 * 16;
+  s->NB = dsa::kTmemCols / s->n_max;
+  if (s->NB > dsa::kMaxAccBufs) s->NB = dsa::kMaxAccBufs;
+  if (s->NB < 2) return false;
+  size_t o = 0;
+  const size_t q_bytes = up((size_t)s->G * H * 128, 1024);
+  // stages go first (1024-aligned); fixed parts after them
+  size_t fixed = 0;
+  fixed += q_bytes;
+  fixed += up((size_t)s->G * s->C * 4, 16) * 2;
+  fixed += up((size_t)s->G * H * 4, 16);
+  fixed += up((size_t)s->G * sizeof(dsa::TokSlot), 16);
+  fixed += 2 * 256 * 4;
+  fixed += up(sizeof(dsa::Misc), 16);
+  fixed += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 3) * 8;
+  const size_t budget = kSmemLimit - 1024 - 64;
+  if (fixed + 2 * dsa::kStageBytes > budget) return false;
+  s->NS = (int)((budget - fixed) / dsa::kStageBytes);
+  if (s->NS > dsa::kMaxStages) s->NS = dsa::kMaxStages;
+  s->offs.off_stage = (uint32_t)o; o += (size_t)s->NS * dsa::kStageBytes;
+  s->offs.off_q = (uint32_t)o;     o += q_bytes;
+  s->offs.off_ckeys = (uint32_t)o; o += up((size_t)s->G * s->C * 4, 16);
+  s->offs.off_cidx = (uint32_t)o;  o += up((size_t)s->G * s->C * 4, 16);
+  s->offs.off_wq = (uint32_t)o;    o += up((size_t)s->G * H * 4, 16);
+  s->offs.off_tok = (uint32_t)o;   o += up((size_t)s->G * sizeof(dsa::TokSlot), 16);
+  s->offs.off_hist = (uint32_t)o;  o += 2 * 256 * 4;
+  s->offs.off_misc = (uint32_t)o;  o += up(sizeof(dsa::Misc), 16);
+  s->offs.off_bar = (uint32_t)o;   o += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 3) * 8;
+  s->smem_bytes = o + 1024;  // slack for aligning the dynamic base to 1024
+  return s->smem_bytes <= kSmemLimit;
+}
+
+template <int H>
+int launch_score_h(const CUtensorMap& tk, const CUtensorMap& tq, const dsa::ScoreParams& p,
+                   size_t smem, int grid, cudaStream_t st) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(dsa::score_topk_kernel<H>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+  });
+  if (attr_err != cudaSuccess)
+    return fail(DSA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+  dsa::score_topk_kernel<H><<<grid, dsa::kScoreThreads, smem, st>>>(tk, tq, p);
+  return check_launch("score_topk_kernel");
+}
+
+int launch_score(int H, const CUtensorMap& tk, const CUtensorMap& tq, const dsa::ScoreParams& p,
+                 size_t smem, int grid, cudaStream_t st) {
+  switch (H) {
+    case 4: return launch_score_h<4>(tk, tq, p, smem, grid, st);
+    case 8: return launch_score_h<8>(tk, tq, p, smem, grid, st);
+    case 16: return launch_score_h<16>(tk, tq, p, smem, grid, st);
+    case 32: return launch_score_h<32>(tk, tq, p, smem, grid, st);
+    case 64: return launch_score_h<64>(tk, tq, p, smem, grid, st);
+    case 128: return launch_score_h<128>(tk, tq, p, smem, grid, st);
+    default: return fail(DSA_ERR_UNSUPPORTED, "H=%d is not supported", H);
+  }
+}
+
+// ---------------------------------------------------------------- shared pieces
+struct Batch {
+  int T, H, R, max_blocks, k, max_num_batched_tokens;
+  int64_t num_pages;
+  const int32_t *qsl, *seq_lens, *block_table;
+  int32_t* topk;
+  void* ws;
+  size_t ws_bytes;
+  int32_t* status;
+  cudaStream_t st;
+};
+
+int check_batch(const Batch& b) {
+  if (b.T < 0) return fail(DSA_ERR_INVALID_ARG, "T=%d < 0", b.T);
+  if (b.R < 1) return fail(DSA_ERR_INVALID_ARG, "R=%d < 1", b.R);
+  if (!supported_heads(b.H)) return fail(DSA_ERR_UNSUPPORTED, "H=%d not in {4,8,16,32,64,128}", b.H);
+  if (b.k < 1 || b.k > DSA_MAX_TOPK)
+    return fail(DSA_ERR_UNSUPPORTED, "index_topk=%d outside [1, %d]", b.k, DSA_MAX_TOPK);
+  if (b.T > b.max_num_batched_tokens)
+    return fail(DSA_ERR_INVALID_ARG, "T=%d exceeds max_num_batched_tokens=%d", b.T,
+                b.max_num_batched_tokens);
+  if (b.max_blocks < 1) return fail(DSA_ERR_INVALID_ARG, "max_blocks=%d < 1", b.max_blocks);
+  if (b.num_pages < 1 || b.num_pages > (int64_t)(INT32_MAX / (DSA_PAGE_BYTES / 128)))
+    return fail(DSA_ERR_INVALID_ARG, "num_pages=%lld outside [1, %d]", (long long)b.num_pages,
+                INT32_MAX / (DSA_PAGE_BYTES / 128));
+  if (!b.qsl || !b.seq_lens || !b.block_table || !b.topk)
+    return fail(DSA_ERR_INVALID_ARG, "null metadata or topk_buffer pointer");
+  if (!b.ws) return fail(DSA_ERR_INVALID_ARG, "null workspace");
+  if (!aligned(b.ws, 256)) return fail(DSA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  const size_t need = dsa_indexer_workspace_bytes(b.T, b.H, b.R, 0, b.k);
+  if (b.ws_bytes < need)
+    return fail(DSA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", b.ws_bytes, need);
+  return DSA_OK;
+}
+
+int launch_plan(const Batch& b, int G, int* launches) {
+  dsa::PlanParams pp;
+  pp.qsl = b.qsl;
+  pp.seq_lens = b.seq_lens;
+  pp.R = b.R;
+  pp.T = b.T;
+  pp.G = G;
+  pp.max_blocks = b.max_blocks;
+  pp.index_topk = b.k;
+  int n = sm_count();
+  if (n <= 0) return fail(DSA_ERR_CUDA, "no CUDA device");
+  pp.target = 2 * n < dsa::kMaxTarget ? 2 * n : dsa::kMaxTarget;
+  pp.topk_buffer = b.topk;
+  pp.ws = static_cast<unsigned char*>(b.ws);
+  pp.L = dsa::ws_layout(b.T, b.R, G, b.k);
+  pp.status = b.status;
+  dsa::plan_kernel<<<1, dsa::kPlanThreads, 0, b.st>>>(pp);
+  ++*launches;
+  return check_launch("plan_kernel");
+}
+
+struct LayerQ {
+  const uint8_t* q_fp8;
+  const float* q_scale;
+  const float* w;
+  const uint8_t* k_cache;
+  float* scores_out;
+  int64_t scores_ld;
+};
+
+int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, int* launches) {
+  CUtensorMap tk, tq;
+  int rc = make_rows128_map(&tk, lq.k_cache, (uint64_t)b.num_pages * (DSA_PAGE_BYTES / 128), 64);
+  if (rc) return rc;
+  rc = make_rows128_map(&tq, lq.q_fp8, (uint64_t)b.T * b.H,
+                        s.q_box_per_token ? (uint32_t)b.H : (uint32_t)(s.G * b.H));
+  if (rc) return rc;
+  const dsa::WsLayout L = dsa::ws_layout(b.T, b.R, s.G, b.k);
+  unsigned char* ws = static_cast<unsigned char*>(b.ws);
+  dsa::ScoreParams p = s.offs;
+  p.qsl = b.qsl;
+  p.seq_lens = b.seq_lens;
+  p.block_table = b.block_table;
+  p.max_blocks = b.max_blocks;
+  p.k_cache = lq.k_cache;
+  p.num_pages = b.num_pages;
+  p.q_scale = lq.q_scale;
+  p.w = lq.w;
+  p.T = b.T;
+  p.H = b.H;
+  p.G = s.G;
+  p.k = b.k;
+  p.C = s.C;
+  p.NS = s.NS;
+  p.NB = s.NB;
+  p.n_max = s.n_max;
+  p.q_box_per_token = s.q_box_per_token;
+  p.items = reinterpret_cast<const dsa::Item*>(ws + L.items);
+  p.hdr = reinterpret_cast<const dsa::PlanHeader*>(ws + L.header);
+  p.cand_keys = reinterpret_cast<uint32_t*>(ws + L.cand_keys);
+  p.cand_idx = reinterpret_cast<int32_t*>(ws + L.cand_idx);
+  p.cand_count = reinterpret_cast<int32_t*>(ws + L.cand_count);
+  p.done = reinterpret_cast<int32_t*>(ws + L.done);
+  p.topk = b.topk;
+  p.scores_out = lq.scores_out;
+  p.scores_ld = lq.scores_ld;
+  p.status = b.status;
+  const int grid = sm_count();
+  rc = launch_score(b.H, tk, tq, p, s.smem_bytes, grid, b.st);
+  if (rc == DSA_OK) ++*launches;
+  return rc;
+}
+
+int launch_write(const float* k, const Batch& b, uint8_t* k_cache, int64_t* slot_mapping,
+                 int* launches) {
+  const int warps_per_block = 8;
+  const int grid = (b.T + warps_per_block - 1) / warps_per_block;
+  dsa::write_k_kernel<<<grid, 32 * warps_per_block, 0, b.st>>>(
+      k, b.T, b.qsl, b.seq_lens, b.R, b.block_table, b.max_blocks, k_cache, b.num_pages,
+      slot_mapping, b.status);
+  ++*launches;
+  return check_launch("write_k_kernel");
+}
+
+__global__ void copy_rows_kernel(const int4* __restrict__ src, int4* __restrict__ dst, int64_t n16) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+       i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
+}  // namespace
+
+// ============================================================================
+// C ABI
+// ============================================================================
+extern "C" {
+
+int dsa_abi_version(void) { return 100; }
+
+const char* dsa_last_error(void) { return g_last_error.c_str(); }
+
+int dsa_last_launch_count(void) { return g_last_launches; }
+
+int dsa_layer_is_full(int layer_id, const char* pattern, int freq, int offset) {
+  if (layer_id < 0) return fail(DSA_ERR_INVALID_ARG, "layer_id=%d < 0", layer_id);
+  if (pattern) {
+    const size_t n = strlen(pattern);
+    for (size_t i = 0; i < n; ++i)
+      if (pattern[i] != 'F' && pattern[i] != 'S')
+        return fail(DSA_ERR_INVALID_ARG, "pattern character %zu is '%c', not F or S", i,
+                    pattern[i]);
+    if ((size_t)layer_id >= n) return 1;  // beyond the pattern: F
+    return pattern[layer_id] == 'F' ? 1 : 0;
+  }
+  if (freq <= 0) return fail(DSA_ERR_INVALID_ARG, "index_topk_freq=%d <= 0", freq);
+  int x = layer_id - offset + 1;
+  if (x < 0) x = 0;
+  return (x % freq) == 0 ? 1 : 0;
+}
+
+size_t dsa_indexer_workspace_bytes(int T, int H, int R, int64_t max_ctx, int index_topk) {
+  (void)max_ctx;
+  if (T < 0 || R < 1 || !supported_heads(H) || index_topk < 1 || index_topk > DSA_MAX_TOPK)
+    return 0;
+  const int G = choose_group(T, R, H, index_topk);
+  return dsa::ws_layout(T, R, G, index_topk).total;
+}
+
+int dsa_quantize_fp8_blocks(const float* x, int64_t n_blocks, uint8_t* codes, float* scales,
+                            dsa_stream_t stream) {
+  g_last_launches = 0;
+  if (n_blocks < 0) return fail(DSA_ERR_INVALID_ARG, "n_blocks < 0");
+  if (n_blocks == 0) return DSA_OK;
+  if (!x || !codes || !scales) return fail(DSA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(x, 16) || !aligned(codes, 4))
+    return fail(DSA_ERR_INVALID_ARG, "x must be 16-byte and codes 4-byte aligned");
+  const int64_t threads = n_blocks * 32;
+  const int64_t grid = (threads + 255) / 256;
+  if (grid > INT32_MAX) return fail(DSA_ERR_INVALID_ARG, "too many blocks");
+  dsa::quantize_blocks_kernel<<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(x, n_blocks, codes,
+                                                                                scales);
+  g_last_launches = 1;
+  return check_launch("quantize_blocks_kernel");
+}
+
+int dsa_indexer_write_k(const float* k, int T, const int32_t* query_start_loc,
+                        const int32_t* seq_lens, int R, const int32_t* block_table,
+                        int max_blocks, uint8_t* k_cache, int64_t num_pages,
+                        int64_t* slot_mapping, int32_t* dev_status, dsa_stream_t stream) {
+  g_last_launches = 0;
+  if (T < 0) return fail(DSA_ERR_INVALID_ARG, "T=%d < 0", T);
+  if (R < 1) return fail(DSA_ERR_INVALID_ARG, "R=%d < 1", R);
+  if (max_blocks < 1) return fail(DSA_ERR_INVALID_ARG, "max_blocks < 1");
+  if (num_pages < 1) return fail(DSA_ERR_INVALID_ARG, "num_pages < 1");
+  if (T == 0) return DSA_OK;
+  if (!k || !query_start_loc || !seq_lens || !block_table || !k_cache)
+    return fail(DSA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(k, 16) || !aligned(k_cache, 16))
+    return fail(DSA_ERR_INVALID_ARG, "k and k_cache must be 16-byte aligned");
+  Batch b{};
+  b.T = T;
+  b.R = R;
+  b.max_blocks = max_blocks;
+  b.num_pages = num_pages;
+  b.qsl = query_start_loc;
+  b.seq_lens = seq_lens;
+  b.block_table = block_table;
+  b.status = dev_status;
+  b.st = (cudaStream_t)stream;
+  int launches = 0;
+  const int rc = launch_write(k, b, k_cache, slot_mapping, &launches);
+  g_last_launches = launches;
+  return rc;
+}
+
+int dsa_indexer_score_topk(const uint8_t* q_fp8, const float* q_scale, const float* w, int T,
+                           int H, const uint8_t* k_cache, int64_t num_pages,
+                           const int32_t* query_start_loc, const int32_t* seq_lens, int R,
+                           const int32_t* block_table, int max_blocks, int index_topk,
+                           int32_t* topk_buffer, int max_num_batched_tokens, float* scores_out,
+                           int64_t scores_ld, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, dsa_stream_t stream) {
+  g_last_launches = 0;
+  Batch b{T, H, R, max_blocks, index_topk, max_num_batched_tokens, num_pages, query_start_loc,
+          seq_lens, block_table, topk_buffer, workspace, workspace_bytes, dev_status,
+          (cudaStream_t)stream};
+  int rc = check_batch(b);
+  if (rc) return rc;
+  if (T == 0) return DSA_OK;
+  if (!q_fp8 || !q_scale || !w || !k_cache) return fail(DSA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned(q_fp8, 16) || !aligned(k_cache, 16))
+    return fail(DSA_ERR_INVALID_ARG, "q_fp8 and k_cache must be 16-byte aligned");
+  if (scores_out && scores_ld < 1) return fail(DSA_ERR_INVALID_ARG, "scores_ld < 1");
+  ScoreShape s;
+  if (!score_shape(T, R, H, index_topk, &s))
+    return fail(DSA_ERR_UNSUPPORTED, "no shared-memory configuration for H=%d, index_topk=%d", H,
+                index_topk);
+  int launches = 0;
+  rc = launch_plan(b, s.G, &launches);
+  if (rc == DSA_OK) {
+    LayerQ lq{q_fp8, q_scale, w, k_cache, scores_out, scores_ld};
+    rc = launch_score_layer(b, s, lq, &launches);
+  }
+  g_last_launches = launches;
+  return rc;
+}
+
+int dsa_layer_stack_run(int num_layers, const char* pattern, int freq, int offset,
+                        const dsa_layer_io* layers, int T, int H,
+                        const int32_t* query_start_loc, const int32_t* seq_lens, int R,
+                        const int32_t* block_table, int max_blocks, int64_t num_pages,
+                        int index_topk, int32_t* topk_buffer, int max_num_batched_tokens,
+                        int32_t* const* per_layer_topk_out, int64_t* slot_mapping,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        dsa_stream_t stream) {
+  g_last_launches = 0;
+  if (num_layers < 1) return fail(DSA_ERR_INVALID_ARG, "num_layers=%d < 1", num_layers);
+  if (!layers) return fail(DSA_ERR_INVALID_ARG, "null layers array");
+  Batch b{T, H, R, max_blocks, index_topk, max_num_batched_tokens, num_pages, query_start_loc,
+          seq_lens, block_table, topk_buffer, workspace, workspace_bytes, dev_status,
+          (cudaStream_t)stream};
+  int rc = check_batch(b);
+  if (rc) return rc;
+  // schedule and per-layer inputs are checked before anything is launched
+  for (int l = 0; l < num_layers; ++l) {
+    const int full = dsa_layer_is_full(l, pattern, freq, offset);
+    if (full < 0) return full;
+    if (l == 0 && !full)
+      return fail(DSA_ERR_INVALID_ARG,
+                  "layer 0 is S: no F layer has written the top-k buffer in this pass");
+    if (full) {
+      const dsa_layer_io& io = layers[l];
+      if (!io.k || !io.q_fp8 || !io.q_scale || !io.w || !io.k_cache)
+        return fail(DSA_ERR_INVALID_ARG, "F layer %d has a null input", l);
+      if (!aligned(io.k, 16) || !aligned(io.q_fp8, 16) || !aligned(io.k_cache, 16))
+        return fail(DSA_ERR_INVALID_ARG, "F layer %d: k, q_fp8, k_cache must be 16-byte aligned", l);
+    }
+  }
+  if (T == 0) return DSA_OK;
+  ScoreShape s;
+  if (!score_shape(T, R, H, index_topk, &s))
+    return fail(DSA_ERR_UNSUPPORTED, "no shared-memory configuration for H=%d, index_topk=%d", H,
+                index_topk);
+  int launches = 0;
+  rc = launch_plan(b, s.G, &launches);
+  bool first_full = true;
+  for (int l = 0; l < num_layers && rc == DSA_OK; ++l) {
+    const int full = dsa_layer_is_full(l, pattern, freq, offset);
+    if (full) {
+      const dsa_layer_io& io = layers[l];
+      rc = launch_write(io.k, b, io.k_cache, first_full ? slot_mapping : nullptr, &launches);
+      first_full = false;
+      if (rc) break;
+      LayerQ lq{io.q_fp8, io.q_scale, io.w, io.k_cache, nullptr, 0};
+      rc = launch_score_layer(b, s, lq, &launches);
+      if (rc) break;
+    }
+    if (per_layer_topk_out && per_layer_topk_out[l]) {
+      const int64_t bytes = (int64_t)T * index_topk * 4;
+      if (bytes % 16 == 0 && aligned(per_layer_topk_out[l], 16) && aligned(topk_buffer, 16)) {
+        copy_rows_kernel<<<256, 256, 0, b.st>>>(reinterpret_cast<const int4*>(topk_buffer),
+                                                reinterpret_cast<int4*>(per_layer_topk_out[l]),
+                                                bytes / 16);
+        ++launches;
+        rc = check_launch("copy_rows_kernel");
+      } else {
+        if (cudaMemcpyAsync(per_layer_topk_out[l], topk_buffer, (size_t)bytes,
+                            cudaMemcpyDeviceToDevice, b.st) != cudaSuccess)
+          rc = fail(DSA_ERR_CUDA, "snapshot copy of layer %d failed", l);
+      }
+    }
+  }
+  g_last_launches = launches;
+  return rc;
+}
+
+}  // extern "C"

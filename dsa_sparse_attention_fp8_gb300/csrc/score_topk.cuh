@@ -1,0 +1,541 @@
+// Paged lightning-indexer scoring + exact streaming top-k, one persistent
+// kernel per F layer.
+//
+// Score (DeepSeek-V3.2 report, arXiv:2512.02556, listed in the references of
+// "GLM-5.3 推理全链路(十二)"):
+//   score(t, s) = k_scale[s] * sum_h (w[t,h] * q_scale[t,h]) * ReLU(q[t,h] . k[s])
+// with q, k the E4M3 codes; the FP32 scales are positive, so they factor out
+// of the ReLU.  Keys are gathered page by page through the block table
+// ("GLM-5.3 推理全链路(十二)", "64 token 页的由来": the paged-MQA read is by
+// 64-token pages); the result is the top `index_topk` key positions per query
+// row, -1 padded ("vLLM IndexCache 实战指南" §二: -1 clear, then scatter into
+// the shared [max_num_batched_tokens, index_topk] buffer).
+//
+// Structure (one CTA per SM, 10 warps):
+//   warp 0      producer: per key tile (128 keys = 2 pages) two TMA loads of
+//               64 x 128 B key rows into a 128B-swizzled stage; the query
+//               tile of the item once.
+//   warp 1      owns tensor memory; one lane issues 4 tcgen05.mma (K = 32
+//               each) per tile: D[key, row*H + head] += k . q, FP32 in TMEM.
+//   warps 2-9   epilogue, two warpgroups; thread = one key row of the tile
+//               (its TMEM lane).  For each query row of the group: read the
+//               H accumulators, ReLU, weight, sum, times the key's scale,
+//               then stream the score into an exact top-k buffer in shared
+//               memory (append above the running threshold; when the buffer
+//               fills, radix-select the k largest and raise the threshold).
+// No score row ever goes to global memory (except the optional debug dump).
+#pragma once
+
+#include <cstdint>
+
+#include "plan.cuh"
+#include "ptx.cuh"
+
+namespace dsa {
+
+constexpr int kScoreThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kTileKeys = 128;
+constexpr int kStageBytes = kTileKeys * kHeadDim;  // 16 KB of key rows
+constexpr int kMaxStages = 16;
+constexpr int kMaxAccBufs = 8;
+constexpr int kTmemCols = 512;
+constexpr int kMaxCandPerThread = 32;  // candidate capacity C <= 128 * 32
+
+struct TokSlot {
+  int32_t count;   // candidates held
+  uint32_t thr;    // keys <= thr are not admitted
+  int32_t pos;     // position of the query row in its request
+  int32_t t;       // query row
+};
+
+struct ScoreParams {
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  const int32_t* block_table;
+  int max_blocks;
+  const uint8_t* k_cache;
+  int64_t num_pages;
+  const float* q_scale;
+  const float* w;
+  int T, H, G, k, C, NS, NB, n_max;
+  int q_box_per_token;
+  const Item* items;
+  const PlanHeader* hdr;
+  uint32_t* cand_keys;
+  int32_t* cand_idx;
+  int32_t* cand_count;
+  int32_t* done;
+  int32_t* topk;
+  float* scores_out;
+  int64_t scores_ld;
+  int32_t* status;
+  // dynamic shared memory offsets (from a 1024-aligned base)
+  uint32_t off_stage, off_q, off_ckeys, off_cidx, off_wq, off_tok, off_hist, off_misc, off_bar;
+};
+
+struct Misc {
+  int abort;
+  uint32_t tmem_base;
+  int merge_flag;
+  int pad;
+  // per-warpgroup radix-select scratch
+  int sel_bin[2], sel_above[2], sel_cnt[2], out_ctr[2], tie_ctr[2];
+  int scan[2][4];
+};
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Append one candidate per thread of a warp if its key beats the threshold.
+__device__ __forceinline__ void cand_append(uint32_t key, int32_t idx, uint32_t thr,
+                                            TokSlot* ts, uint32_t* ckeys, int32_t* cidx) {
+  const bool pass = key > thr;
+  const uint32_t m = __ballot_sync(0xffffffffu, pass);
+  if (m == 0) return;
+  int base = 0;
+  if (lane_id() == 0) base = atomicAdd(&ts->count, __popc(m));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  if (pass) {
+    const int p = base + __popc(m & lanemask_lt());
+    ckeys[p] = key;
+    cidx[p] = idx;
+  }
+}
+
+// Exact selection of the k largest keys among the n > k held by slot `ts`,
+// compacted to positions [0, k).  Run by the 128 threads of one warpgroup.
+// Radix select over 8-bit digits from the top: each pass histograms the
+// candidates that share the already fixed prefix, finds the digit bin where
+// the running count from the top crosses k, and either stops (that bin is
+// taken whole) or refines inside it.
+__device__ __noinline__ void cand_compress(TokSlot* ts, uint32_t* ckeys, int32_t* cidx, int k,
+                                           int* hist, Misc* misc, int wg, int tid) {
+  const uint32_t bar_id = 1 + wg;
+  const int n = ts->count;
+  uint32_t kr[kMaxCandPerThread];
+  int32_t ir[kMaxCandPerThread];
+#pragma unroll
+  for (int j = 0; j < kMaxCandPerThread; ++j) {
+    const int i = tid + 128 * j;
+    kr[j] = (i < n) ? ckeys[i] : 0u;
+    ir[j] = (i < n) ? cidx[i] : -1;
+  }
+  int need = k;
+  uint32_t prefix = 0, mask = 0;
+  bool early = false;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    hist[tid] = 0;
+    hist[tid + 128] = 0;
+    named_bar_sync(bar_id, 128);
+#pragma unroll
+    for (int j = 0; j < kMaxCandPerThread; ++j)
+      if (kr[j] != 0u && (kr[j] & mask) == prefix) atomicAdd(&hist[(kr[j] >> shift) & 255u], 1);
+    named_bar_sync(bar_id, 128);
+    // descending bins: thread tid covers bins 255-2*tid and 254-2*tid
+    const int b_hi = 255 - 2 * tid, b_lo = 254 - 2 * tid;
+    const int c_hi = hist[b_hi], c_lo = hist[b_lo];
+    int incl = c_hi + c_lo;
+    const int lane = tid & 31, w = tid >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) misc->scan[wg][w] = incl;
+    named_bar_sync(bar_id, 128);
+    int warp_off = 0;
+    for (int u = 0; u < w; ++u) warp_off += misc->scan[wg][u];
+    const int above_hi = warp_off + incl - (c_hi + c_lo);  // keys in bins > b_hi
+    if (above_hi < need && need <= above_hi + c_hi) {
+      misc->sel_bin[wg] = b_hi;
+      misc->sel_above[wg] = above_hi;
+      misc->sel_cnt[wg] = c_hi;
+    } else if (above_hi + c_hi < need && need <= above_hi + c_hi + c_lo) {
+      misc->sel_bin[wg] = b_lo;
+      misc->sel_above[wg] = above_hi + c_hi;
+      misc->sel_cnt[wg] = c_lo;
+    }
+    named_bar_sync(bar_id, 128);
+    const int b = misc->sel_bin[wg];
+    need -= misc->sel_above[wg];
+    const int cnt = misc->sel_cnt[wg];
+    prefix |= (uint32_t)b << shift;
+    mask |= 255u << shift;
+    named_bar_sync(bar_id, 128);  // scratch read by all before the next pass rewrites it
+    if (cnt == need) {
+      early = true;
+      break;
+    }
+  }
+  if (tid == 0) {
+    misc->out_ctr[wg] = 0;
+    misc->tie_ctr[wg] = 0;
+  }
+  named_bar_sync(bar_id, 128);
+  const int definite = k - (early ? 0 : need);  // keys strictly above the k-th
+#pragma unroll
+  for (int j = 0; j < kMaxCandPerThread; ++j) {
+    const bool valid = kr[j] != 0u;
+    const bool sel = valid && (early ? (kr[j] & mask) >= prefix : kr[j] > prefix);
+    const uint32_t m = __ballot_sync(0xffffffffu, sel);
+    int base = 0;
+    if (m && (tid & 31) == 0) base = atomicAdd(&misc->out_ctr[wg], __popc(m));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (sel) {
+      const int p = base + __popc(m & lanemask_lt());
+      ckeys[p] = kr[j];
+      cidx[p] = ir[j];
+    }
+    if (!early && valid && kr[j] == prefix) {
+      const int q = atomicAdd(&misc->tie_ctr[wg], 1);
+      if (q < need) {
+        ckeys[definite + q] = kr[j];
+        cidx[definite + q] = ir[j];
+      }
+    }
+  }
+  named_bar_sync(bar_id, 128);
+  if (tid == 0) {
+    ts->count = k;
+    ts->thr = prefix;
+  }
+  named_bar_sync(bar_id, 128);
+}
+
+template <int H>
+__device__ __forceinline__ float relu_weighted_sum(uint32_t taddr, const float* wq) {
+  constexpr int CH = H >= 32 ? 32 : H;
+  float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+  for (int c = 0; c < H; c += CH) {
+    uint32_t v[CH];
+    tmem_ld<CH>(taddr + c, v);
+    tmem_ld_wait();
+    const float4* w4 = reinterpret_cast<const float4*>(wq + c);
+#pragma unroll
+    for (int h = 0; h < CH; h += 4) {
+      const float4 ww = w4[h >> 2];
+      acc0 = fmaf(ww.x, fmaxf(__uint_as_float(v[h + 0]), 0.f), acc0);
+      acc1 = fmaf(ww.y, fmaxf(__uint_as_float(v[h + 1]), 0.f), acc1);
+      acc0 = fmaf(ww.z, fmaxf(__uint_as_float(v[h + 2]), 0.f), acc0);
+      acc1 = fmaf(ww.w, fmaxf(__uint_as_float(v[h + 3]), 0.f), acc1);
+    }
+  }
+  return acc0 + acc1;
+}
+
+// Write the final rows of one query: n valid indices then -1 up to k.
+__device__ __forceinline__ void write_row(int32_t* out_row, const int32_t* cidx, int n, int k,
+                                          int tid) {
+  for (int i = tid; i < k; i += 128) out_row[i] = (i < n) ? cidx[i] : -1;
+}
+
+template <int H>
+__global__ void __launch_bounds__(kScoreThreads, 1)
+    score_topk_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_q, const ScoreParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  uint8_t* stage_base = smem + p.off_stage;
+  uint8_t* q_tile = smem + p.off_q;
+  uint32_t* ckeys_all = reinterpret_cast<uint32_t*>(smem + p.off_ckeys);
+  int32_t* cidx_all = reinterpret_cast<int32_t*>(smem + p.off_cidx);
+  float* wq_all = reinterpret_cast<float*>(smem + p.off_wq);
+  TokSlot* tok = reinterpret_cast<TokSlot*>(smem + p.off_tok);
+  int* hist_all = reinterpret_cast<int*>(smem + p.off_hist);
+  Misc* misc = reinterpret_cast<Misc*>(smem + p.off_misc);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+  const uint32_t bar_full = smem_u32(bars);
+  const uint32_t bar_empty = bar_full + 8 * kMaxStages;
+  const uint32_t bar_tfull = bar_empty + 8 * kMaxStages;
+  const uint32_t bar_tempty = bar_tfull + 8 * kMaxAccBufs;
+  const uint32_t bar_qfull = bar_tempty + 8 * kMaxAccBufs;
+  const uint32_t bar_qempty = bar_qfull + 8;
+  const uint32_t bar_drain = bar_qempty + 8;
+  volatile int* abort_flag = &misc->abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.NS; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < p.NB; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, kEpiWarps);
+    }
+    mbar_init(bar_qfull, 1);
+    mbar_init(bar_qempty, 1);
+    mbar_init(bar_drain, 1);
+    misc->abort = 0;
+    misc->merge_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&misc->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_q);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc->tmem_base;
+  const int n_items = p.hdr->n_items;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t sphase = 0;
+      uint32_t issued_mask = 0;
+      uint32_t last_par[kMaxStages];
+      int item_i = 0;
+      int q_issued = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_i) {
+        const Item I = p.items[it];
+        if (!mbar_wait(bar_qempty, (item_i & 1) ^ 1, abort_flag)) { ok = false; break; }
+        q_issued = item_i + 1;
+        if (p.q_box_per_token) {
+          mbar_arrive_expect_tx(bar_qfull, (uint32_t)(I.gcount * H * kHeadDim));
+          for (int g = 0; g < I.gcount; ++g)
+            tma_load_2d(smem_u32(q_tile + g * H * kHeadDim), &tm_q, 0, (I.t0 + g) * H, bar_qfull);
+        } else {
+          mbar_arrive_expect_tx(bar_qfull, (uint32_t)(p.G * H * kHeadDim));
+          tma_load_2d(smem_u32(q_tile), &tm_q, 0, I.t0 * H, bar_qfull);
+        }
+        const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
+        const int32_t* bt_row = p.block_table + (int64_t)I.r * p.max_blocks;
+        for (int j = 0; j < ntiles; ++j) {
+          if (!mbar_wait(bar_empty + 8 * stage, sphase ^ 1, abort_flag)) { ok = false; break; }
+          const int kt = I.k0 + j * kTileKeys;
+          int64_t pg[2];
+          uint32_t bytes = 0;
+#pragma unroll
+          for (int pi = 0; pi < 2; ++pi) {
+            pg[pi] = -1;
+            const int ks = kt + pi * kPageTokens;
+            if (ks < I.k1) {
+              const int64_t page = __ldg(bt_row + ks / kPageTokens);
+              if (page >= 0 && page < p.num_pages) {
+                pg[pi] = page;
+                bytes += kPageTokens * kHeadDim;
+              }
+            }
+          }
+          mbar_arrive_expect_tx(bar_full + 8 * stage, bytes);
+          const uint32_t dst = smem_u32(stage_base + stage * kStageBytes);
+#pragma unroll
+          for (int pi = 0; pi < 2; ++pi)
+            if (pg[pi] >= 0)
+              tma_load_2d(dst + pi * kPageTokens * kHeadDim, &tm_k, 0,
+                          (int32_t)(pg[pi] * (kPageBytes / kHeadDim)), bar_full + 8 * stage);
+          issued_mask |= 1u << stage;
+          last_par[stage] = sphase;
+          if (++stage == p.NS) { stage = 0; sphase ^= 1; }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        raise_status(p.status, kStatusTimeout);
+      }
+      // never leave with bulk copies in flight into this CTA's shared memory
+      for (int s = 0; s < p.NS; ++s)
+        if (issued_mask & (1u << s)) mbar_wait(bar_full + 8 * s, last_par[s], nullptr);
+      if (q_issued) mbar_wait(bar_qfull, (q_issued - 1) & 1, nullptr);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t sphase = 0, aphase = 0;
+      int item_i = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_i) {
+        const Item I = p.items[it];
+        const uint32_t N = (uint32_t)((I.gcount * H + 15) & ~15);
+        const uint32_t idesc = idesc_e4m3_f32(128, N);
+        if (!mbar_wait(bar_qfull, item_i & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t qaddr = smem_u32(q_tile);
+        const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
+        for (int j = 0; j < ntiles; ++j) {
+          if (!mbar_wait(bar_full + 8 * stage, sphase, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar_tempty + 8 * acc, aphase ^ 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t aaddr = smem_u32(stage_base + stage * kStageBytes);
+          const uint32_t d = tmem_base + (uint32_t)(acc * p.n_max);
+#pragma unroll
+          for (int kk = 0; kk < kHeadDim / 32; ++kk)
+            umma_f8(d, sw128_desc(aaddr + kk * 32), sw128_desc(qaddr + kk * 32), idesc, kk > 0);
+          umma_commit(bar_empty + 8 * stage);
+          umma_commit(bar_tfull + 8 * acc);
+          if (++stage == p.NS) { stage = 0; sphase ^= 1; }
+          if (++acc == p.NB) { acc = 0; aphase ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit(bar_qempty);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        raise_status(p.status, kStatusTimeout);
+      }
+      // wait for every MMA this thread issued before tensor memory is released
+      umma_commit(bar_drain);
+      mbar_wait(bar_drain, 0, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int epi = warp - 2;          // 0..7
+    const int wg = epi >> 2;           // warpgroup 0/1
+    const int tid = (epi & 3) * 32 + lane;
+    const int quad = warp & 3;         // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane;  // key row of the tile = TMEM lane
+    int* hist = hist_all + wg * 256;
+    int acc = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const Item I = p.items[it];
+      const int qb = __ldg(p.qsl + I.r);
+      const int q_len = __ldg(p.qsl + I.r + 1) - qb;
+      const int seq_len = __ldg(p.seq_lens + I.r);
+      const int nsplit = I.split >> 16;
+      const int split = I.split & 0xFFFF;
+      // per-row setup by the owning warpgroup
+      for (int g = wg; g < I.gcount; g += 2) {
+        const int t = I.t0 + g;
+        for (int h = tid; h < H; h += 128)
+          wq_all[g * H + h] = __ldg(p.w + (int64_t)t * H + h) * __ldg(p.q_scale + (int64_t)t * H + h);
+        if (tid == 0) {
+          tok[g].count = 0;
+          tok[g].thr = 0u;
+          tok[g].pos = seq_len - q_len + (t - qb);
+          tok[g].t = t;
+        }
+      }
+      named_bar_sync(1 + wg, 128);
+      const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
+      const int32_t* bt_row = p.block_table + (int64_t)I.r * p.max_blocks;
+      for (int j = 0; j < ntiles; ++j) {
+        const int key = I.k0 + j * kTileKeys + row;
+        float kscale = 0.f;
+        bool kvalid = false;
+        if (key < I.k1) {
+          const int64_t page = __ldg(bt_row + key / kPageTokens);
+          if (page >= 0 && page < p.num_pages) {
+            kvalid = true;
+            kscale = __ldg(reinterpret_cast<const float*>(p.k_cache + page * kPageBytes +
+                                                          kPageScaleOffset) +
+                           (key % kPageTokens));
+          } else if (lane == 0) {
+            raise_status(p.status, kStatusBadPage);
+          }
+        }
+        // no early exit on the abort flag here: all eight epilogue warps must take
+        // the same branch, so they all wait on the same phase with the same limit
+        if (!mbar_wait(bar_tfull + 8 * acc, aphase, nullptr)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * p.n_max);
+        for (int g = wg; g < I.gcount; g += 2) {
+          const float s = relu_weighted_sum<H>(tbase + (uint32_t)(g * H), wq_all + g * H);
+          const float score = s * kscale;
+          const bool valid = kvalid && key <= tok[g].pos;
+          if (p.scores_out && valid && key < p.scores_ld) p.scores_out[(int64_t)tok[g].t * p.scores_ld + key] = score;
+          const uint32_t kk = valid ? score_key(score) : 0u;
+          cand_append(kk, key, tok[g].thr, &tok[g], ckeys_all + (size_t)g * p.C,
+                      cidx_all + (size_t)g * p.C);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+        if (++acc == p.NB) { acc = 0; aphase ^= 1; }
+        named_bar_sync(1 + wg, 128);
+        for (int g = wg; g < I.gcount; g += 2)
+          if (tok[g].count > p.C - kTileKeys)
+            cand_compress(&tok[g], ckeys_all + (size_t)g * p.C, cidx_all + (size_t)g * p.C, p.k,
+                          hist, misc, wg, tid);
+      }
+      if (!ok) break;
+      // finalize this item's rows
+      for (int g = wg; g < I.gcount; g += 2) {
+        uint32_t* ck = ckeys_all + (size_t)g * p.C;
+        int32_t* ci = cidx_all + (size_t)g * p.C;
+        if (tok[g].count > p.k) cand_compress(&tok[g], ck, ci, p.k, hist, misc, wg, tid);
+        const int n = min(tok[g].count, p.k);
+        if (nsplit == 1) {
+          write_row(p.topk + (int64_t)tok[g].t * p.k, ci, n, p.k, tid);
+        } else {
+          const int64_t blk = (int64_t)I.cand_block + (int64_t)g * nsplit + split;
+          for (int i = tid; i < n; i += 128) {
+            p.cand_keys[blk * p.k + i] = ck[i];
+            p.cand_idx[blk * p.k + i] = ci[i];
+          }
+          if (tid == 0) p.cand_count[blk] = n;
+        }
+      }
+      if (nsplit > 1) {
+        // last split of the group to finish merges the candidates of all splits
+        __threadfence();
+        named_bar_sync(3, 128 * 2);
+        if (epi == 0 && lane == 0) {
+          const int prev = atomicAdd(p.done + I.sgroup, 1);
+          misc->merge_flag = (prev == nsplit - 1);
+        }
+        named_bar_sync(3, 128 * 2);
+        if (misc->merge_flag) {
+          __threadfence();
+          for (int g = wg; g < I.gcount; g += 2) {
+            uint32_t* ck = ckeys_all + (size_t)g * p.C;
+            int32_t* ci = cidx_all + (size_t)g * p.C;
+            if (tid == 0) {
+              tok[g].count = 0;
+              tok[g].thr = 0u;
+            }
+            named_bar_sync(1 + wg, 128);
+            for (int sj = 0; sj < nsplit; ++sj) {
+              const int64_t blk = (int64_t)I.cand_block + (int64_t)g * nsplit + sj;
+              const int nb = __ldcg(p.cand_count + blk);
+              for (int i0 = 0; i0 < nb; i0 += 128) {
+                const int i = i0 + tid;
+                const uint32_t kk = (i < nb) ? __ldcg(p.cand_keys + blk * p.k + i) : 0u;
+                const int32_t ix = (i < nb) ? __ldcg(p.cand_idx + blk * p.k + i) : -1;
+                cand_append(kk, ix, tok[g].thr, &tok[g], ck, ci);
+                named_bar_sync(1 + wg, 128);
+                if (tok[g].count > p.C - kTileKeys)
+                  cand_compress(&tok[g], ck, ci, p.k, hist, misc, wg, tid);
+              }
+            }
+            if (tok[g].count > p.k) cand_compress(&tok[g], ck, ci, p.k, hist, misc, wg, tid);
+            write_row(p.topk + (int64_t)tok[g].t * p.k, ci, min(tok[g].count, p.k), p.k, tid);
+          }
+          if (epi == 0 && lane == 0) p.done[I.sgroup] = 0;  // ready for the next layer
+        }
+        named_bar_sync(3, 128 * 2);
+      } else {
+        named_bar_sync(1 + wg, 128);
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      if (lane == 0) raise_status(p.status, kStatusTimeout);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+}  // namespace dsa

@@ -1,0 +1,201 @@
+/*
+ * dsa_indexer.h -- C ABI of the DSA lightning-indexer step on one GB300 GPU
+ * (library: libdsa_indexer.so, kernels for sm_103a).
+ *
+ * The step, per F ("full") layer of a DeepSeek Sparse Attention model:
+ *   1. write each new token's 128-d indexer key into the paged FP8 cache;
+ *   2. score every query token against its request's cached keys;
+ *   3. keep the top `index_topk` keys per query in a shared int32 buffer;
+ * and, over a layer stack, 4. the IndexCache F/S schedule: S ("shared")
+ * layers run no indexer and read what the last F layer wrote in this pass.
+ *
+ * Sources, by page title and section:
+ *   [IC]  "vLLM IndexCache 实战指南" -- §二 How It Works (shared
+ *         topk_indices_buffer, -1 clear before scatter, S layers read the
+ *         buffer written earlier in the same forward pass), §三 配置参数参考
+ *         (index_topk_freq, index_topk_pattern, index_skip_topk_offset and
+ *         the skip rule), §四 方式二 (layers beyond the pattern are F).
+ *   [KV]  "GLM-5.3 推理全链路(十二): 主 KV 与索引器缓存的分页预算、前缀命中与驱逐"
+ *         -- byte-accounting table (132 B per token per layer), SGLang
+ *         _buffer_shape (8448-byte page rows), IndexKeyCache.move comment
+ *         (all key bytes of a page, then all scale bytes), the
+ *         topk_indices_buffer passage, the write-path section
+ *         (store_quantized), and "64 token 页的由来" (64-token pages).
+ *   [HBM] "HBM 索引架构设计" -- §2.3 (slot = block_table[req, pos/bs]*bs + pos%bs).
+ *   [DSA] DeepSeek-V3.2 report (arXiv:2512.02556, in [KV]'s references):
+ *         score(t,s) = sum_h w[t,h] * ReLU(q[t,h] . k[s]).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers unless stated; the caller owns
+ *     every buffer (caches, outputs, workspace).  Nothing here allocates,
+ *     frees or synchronises: each call only enqueues kernels on `stream`
+ *     (a cudaStream_t; NULL = legacy default stream) and returns.
+ *   - head_dim is 128 and the page is 64 tokens; both are fixed.
+ *   - Page layout (one uint8 row of DSA_PAGE_BYTES per physical page): the
+ *     E4M3 key of in-page offset o at bytes [o*128, o*128+128), its FP32
+ *     scale at byte DSA_PAGE_SCALE_OFFSET + 4*o.
+ *   - Batch metadata (int32, device): query_start_loc [R+1] with
+ *     query_start_loc[0] = 0 and query_start_loc[R] = T (request r owns query
+ *     rows [qsl[r], qsl[r+1])); seq_lens [R] = context length of request r
+ *     AFTER this step (its new tokens are the last q_len[r] positions);
+ *     block_table [R, max_blocks] row-major, physical page of each 64-token
+ *     block of the request.
+ *   - Quantisation: one FP32 scale per 128-element block, s = amax/448 in
+ *     FP32 (s = 1 for an all-zero block), codes = E4M3(x / s) rounded to
+ *     nearest-even with saturation to +-448.  Inputs must be finite.
+ *   - Returned top-k indices are logical token positions inside the request
+ *     (0 .. ctx-1), in no particular order; row t holds min(ctx(t), index_topk)
+ *     valid indices followed by -1, ctx(t) = pos(t)+1 (causal, self included).
+ *   - Return value: DSA_OK or a negative DSA_ERR_*; the message of the last
+ *     failing call on this thread is dsa_last_error().  Faults in device-side
+ *     metadata (e.g. a block id outside [0, num_pages)) do not trap: the
+ *     affected keys/tokens are skipped and a DSA_STATUS_* bit is OR-ed into
+ *     *dev_status (int32, device, may be NULL) for the caller to read later.
+ */
+#ifndef DSA_INDEXER_H_
+#define DSA_INDEXER_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dsa_stream_t; /* same type as cudaStream_t */
+
+#define DSA_HEAD_DIM 128
+#define DSA_PAGE_TOKENS 64
+#define DSA_TOKEN_BYTES 132               /* [KV] byte-accounting table */
+#define DSA_PAGE_BYTES 8448               /* [KV] 64 * (128 + 128/128*4) */
+#define DSA_PAGE_SCALE_OFFSET 8192        /* [KV] keys first, then scales */
+#define DSA_MAX_TOPK 2048
+
+/* return codes */
+#define DSA_OK 0
+#define DSA_ERR_INVALID_ARG (-1)
+#define DSA_ERR_UNSUPPORTED (-2)
+#define DSA_ERR_WORKSPACE_TOO_SMALL (-3)
+#define DSA_ERR_CUDA (-4)
+#define DSA_ERR_TIMEOUT (-5)
+
+/* bits OR-ed into *dev_status by the kernels */
+#define DSA_STATUS_BAD_PAGE 0x1      /* block_table entry outside [0, num_pages) */
+#define DSA_STATUS_BAD_METADATA 0x2  /* q_len < 0, seq_len < q_len, seq_len > 64*max_blocks */
+#define DSA_STATUS_TIMEOUT 0x4       /* a bounded on-chip wait gave up; results invalid */
+
+/* Version of this ABI (major*100 + minor). */
+int dsa_abi_version(void);
+
+/* Thread-local message describing the last non-zero return on this thread. */
+const char* dsa_last_error(void);
+
+/*
+ * Steps 1 ([HBM] §2.3 and [KV] write path): quantise the FP32 key of every
+ * new token and store it in the paged cache.
+ *   k              [T, 128] FP32, row t = key of query row t.
+ *   k_cache        [num_pages, 8448] uint8, this layer's page pool (written).
+ *   slot_mapping   [T] int64 or NULL; receives page*64 + pos%64 per token.
+ * Tokens whose page is invalid are not written (slot -1, DSA_STATUS_BAD_PAGE).
+ * Errors: INVALID_ARG (null required pointer, T < 0, R < 1, max_blocks < 1,
+ * num_pages < 1); CUDA (launch failure).
+ */
+int dsa_indexer_write_k(const float* k, int T, const int32_t* query_start_loc,
+                        const int32_t* seq_lens, int R, const int32_t* block_table,
+                        int max_blocks, uint8_t* k_cache, int64_t num_pages,
+                        int64_t* slot_mapping, int32_t* dev_status, dsa_stream_t stream);
+
+/*
+ * Per-block FP8 quantiser used for keys, exposed for queries: x [n_blocks, 128]
+ * FP32 -> codes [n_blocks, 128] E4M3 bytes + scales [n_blocks] FP32, same rule
+ * as the cache write ([KV] byte-accounting table: 128 FP8 bytes + one FP32
+ * scale per 128-element block).  Used to produce q_fp8 / q_scale.
+ */
+int dsa_quantize_fp8_blocks(const float* x, int64_t n_blocks, uint8_t* codes, float* scales,
+                            dsa_stream_t stream);
+
+/*
+ * Bytes of device workspace that dsa_indexer_score_topk / dsa_layer_stack_run
+ * need for a batch of T query rows with H heads and this index_topk.  R and
+ * max_ctx are accepted for forward compatibility.  Returns 0 for invalid
+ * arguments.  Pure host function.
+ */
+size_t dsa_indexer_workspace_bytes(int T, int H, int R, int64_t max_ctx, int index_topk);
+
+/*
+ * Steps 2-3 ([DSA] score, [IC] §二 top-k into the shared buffer): for every
+ * query row t in [0, T), score the keys s <= pos(t) of its request,
+ *   score = k_scale[s] * sum_h (w[t,h] * q_scale[t,h]) * ReLU(q_fp8[t,h] . k_fp8[s])
+ * and write the indices of the index_topk largest into row t of topk_buffer,
+ * then -1 up to index_topk.  Rows >= T are not touched.
+ *   q_fp8      [T, H, 128] E4M3 bytes; q_scale, w: [T, H] FP32.
+ *   k_cache    [num_pages, 8448] uint8, already holding every key s < seq_len.
+ *   topk_buffer [max_num_batched_tokens, index_topk] int32, T <= max_num_batched_tokens.
+ *   scores_out optional [T, scores_ld] FP32 debug dump: scores_out[t, s] for
+ *              every visible key (other entries untouched); NULL in production.
+ *   workspace  >= dsa_indexer_workspace_bytes(T, H, R, 0, index_topk) bytes,
+ *              256-byte aligned, contents need not be initialised.
+ * H must be one of 4, 8, 16, 32, 64, 128 and 1 <= index_topk <= 2048
+ * (UNSUPPORTED otherwise).  Errors: INVALID_ARG, UNSUPPORTED,
+ * WORKSPACE_TOO_SMALL, CUDA.
+ */
+int dsa_indexer_score_topk(const uint8_t* q_fp8, const float* q_scale, const float* w, int T,
+                           int H, const uint8_t* k_cache, int64_t num_pages,
+                           const int32_t* query_start_loc, const int32_t* seq_lens, int R,
+                           const int32_t* block_table, int max_blocks, int index_topk,
+                           int32_t* topk_buffer, int max_num_batched_tokens, float* scores_out,
+                           int64_t scores_ld, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, dsa_stream_t stream);
+
+/*
+ * Step 4, [IC] §三/§四: 1 if DSA layer `layer_id` is an F layer, 0 if S, <0 on
+ * error.  With a pattern (NUL-terminated string of 'F'/'S') the pattern
+ * decides and layers at or beyond its length are F; otherwise the layer
+ * skips iff max(layer_id - offset + 1, 0) % freq != 0.  Pure host function.
+ */
+int dsa_layer_is_full(int layer_id, const char* pattern, int freq, int offset);
+
+/* Per-layer inputs of dsa_layer_stack_run; S layers may leave every field NULL. */
+typedef struct dsa_layer_io {
+  const float* k;         /* [T, 128] FP32 new-token keys of this layer */
+  const uint8_t* q_fp8;   /* [T, H, 128] E4M3 queries */
+  const float* q_scale;   /* [T, H] */
+  const float* w;         /* [T, H] head weights */
+  uint8_t* k_cache;       /* [num_pages, 8448] this layer's page pool */
+} dsa_layer_io;
+
+/*
+ * Steps 1-4 over a layer stack in one call ([IC] §二: F layers write the
+ * shared topk buffer; S layers build no indexer and consume what the last F
+ * layer wrote in this pass).  The batch plan is built once and reused by all
+ * F layers.
+ *   layers                HOST array [num_layers] of device-pointer structs.
+ *   pattern / freq / offset  as dsa_layer_is_full; the first layer must be F.
+ *   per_layer_topk_out    HOST array [num_layers] of device pointers, each
+ *                         [T, index_topk] int32 or NULL, or NULL altogether:
+ *                         receives rows [0, T) of the buffer as layer l
+ *                         consumes it (a copy made after layer l).
+ *   slot_mapping          [T] int64 or NULL, from the first F layer.
+ * Errors: as dsa_indexer_score_topk, plus INVALID_ARG for a bad pattern,
+ * freq <= 0, a first layer that is S, or an F layer with a NULL field.
+ */
+int dsa_layer_stack_run(int num_layers, const char* pattern, int freq, int offset,
+                        const dsa_layer_io* layers, int T, int H,
+                        const int32_t* query_start_loc, const int32_t* seq_lens, int R,
+                        const int32_t* block_table, int max_blocks, int64_t num_pages,
+                        int index_topk, int32_t* topk_buffer, int max_num_batched_tokens,
+                        int32_t* const* per_layer_topk_out, int64_t* slot_mapping,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        dsa_stream_t stream);
+
+/*
+ * Number of kernel launches the last successful call of each entry point on
+ * this thread enqueued (for launch accounting by benchmarks).
+ */
+int dsa_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_INDEXER_H_ */
