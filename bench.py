@@ -1,0 +1,387 @@
+"""Benchmark of the DSA lightning-indexer step on GB300.
+
+Default workload: batched decode -- 64 requests with one new token each,
+contexts uniform in [1024, 8192], H = 64 indexer heads, index_topk = 2048,
+4-layer stack (all F).  One step = one pass of the whole path over the batch:
+for every F layer, write the new keys into the paged FP8 cache, score every
+query row against its request's cached keys, select the top-k into the shared
+buffer (S layers launch nothing).  Metric: query-key pairs per second
+(sum over F layers of the keys each query row sees, divided by step time).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`--impl reference` times the FP64 CPU oracle (the correctness reference) on a
+bounded sample of the same workload, on this machine's host cores.
+Under torchrun each rank runs its own batch (weak scaling, no data-path
+collective); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "DSA indexer score+top-k query-key pairs/s; % of HBM / FP8 roofline"
+UNIT = "pairs/s"
+BYTES_PER_PAIR = 132 + 4 / 64          # FP8 key + FP32 scale + its share of a block-table entry
+L2_FLUSH_BYTES = 256 << 20             # larger than the 129 MB L2
+KERNEL_SOURCES = ["score_topk.cuh", "ptx.cuh", "plan.cuh", "kwrite.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=1, help="workload id (1 = batched decode)")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def read_peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        h.update((ROOT / "dsa_sparse_attention_fp8_gb300" / "csrc" / name).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per scoring launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = ROOT / "profiles" / f"score_topk_{workload_name}.md"
+    if not p.exists():
+        return None
+    text = p.read_text()
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    m_h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m_b or not m_h or m_h.group(1) != kernel_source_hash():
+        return None
+    return int(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        self.file.flush()
+        rows = []
+        try:
+            with open(self.file.name) as f:
+                for r in csv.reader(f):
+                    if len(r) >= 9:
+                        rows.append([x.strip() for x in r])
+        finally:
+            os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle legs
+# ----------------------------------------------------------------------------
+
+def oracle_sample_setup(wl, layer=0):
+    """Oracle state for timing: the page pool holding every cached prefix (not timed)."""
+    import oracle as O
+    cache = np.zeros((wl.num_pages, O.PAGE_BYTES), np.uint8)
+    for r in range(wl.R):
+        P = int(wl.prefix_lens[r])
+        if P:
+            O.write_k_cache(cache, wl.k_prefix(layer, r),
+                            O.slot_mapping(np.array([0, P]), np.array([P]), wl.block_table[r:r + 1]))
+    qc, qs = O.quantize_blocks(wl.q(layer))
+    return cache, wl.k_new(layer), qc, qs, wl.w(layer)
+
+
+def oracle_time_rows(wl, state, rows):
+    """Time one oracle indexer layer (key write + scores + full sort) on `rows`."""
+    import oracle as O
+    cache, k_new, qc, qs, w = state
+    buf = np.full((wl.max_num_batched_tokens, wl.index_topk), -1, np.int32)
+    c = cache.copy()
+    t0 = time.perf_counter()
+    O.indexer_layer(c, k_new, qc, qs, w, wl.query_start_loc, wl.seq_lens, wl.block_table,
+                    wl.index_topk, buf, rows=rows)
+    dt = time.perf_counter() - t0
+    _, pos = O.token_positions(wl.query_start_loc, wl.seq_lens)
+    pairs = int(sum(int(pos[t]) + 1 for t in rows))
+    return pairs, dt
+
+
+def cpu_cores() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+def cpu_baseline(wl, budget_s: float) -> dict:
+    """The oracle on layer 0 of the same workload, rows in order (wrapping to
+    row 0 again) until about `budget_s` seconds of CPU work are done."""
+    state = oracle_sample_setup(wl)
+    done_pairs, done_s, n = 0, 0.0, 0
+    chunk = max(1, wl.T // 16)
+    while done_s < budget_s:
+        a = n % wl.T
+        rows = list(range(a, min(wl.T, a + chunk)))
+        p, dt = oracle_time_rows(wl, state, rows)
+        done_pairs += p
+        done_s += dt
+        n += len(rows)
+    return {"value": done_pairs / done_s, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"layer 0, {n} query rows in order ({n / wl.T:.2f} x the {wl.T}-row batch; "
+                      f"{done_pairs} pairs, {done_s:.1f} s; numpy FP64, BLAS threads per the host default)"}
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    state = oracle_sample_setup(wl)
+    rows = list(range(min(wl.T, 8)))
+    for _ in range(args.warmup):
+        oracle_time_rows(wl, state, rows)
+    pairs = secs = 0.0
+    for _ in range(args.steps):
+        p, dt = oracle_time_rows(wl, state, rows)
+        pairs += p
+        secs += dt
+    value = pairs / secs
+    sample = (f"layer 0, query rows 0..{len(rows) - 1} of {wl.T} per step "
+              f"({int(pairs / args.steps)} pairs per step)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.name, **{k: v for k, v in wl.describe().items()
+                                                                if k != "workload"}},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# GPU leg
+# ----------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    wl = synth.make_workload(args.workload, seed=args.seed + rank)
+    if args.impl == "reference":
+        run_reference(args, wl)
+        return
+
+    import torch
+    from dsa_sparse_attention_fp8_gb300 import _build, binding, staging
+    from dsa_sparse_attention_fp8_gb300.step import IndexerStep
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    _build.build_library(quiet=True)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    # ---- stage: caches with every cached prefix, this step's inputs
+    meta = staging.stage_metadata(wl, dev)
+    full = [binding.layer_is_full(l, wl.pattern, wl.freq, wl.offset) for l in range(wl.num_layers)]
+    caches, host_layers = [], {}
+    for l in range(wl.num_layers):
+        if not full[l]:
+            caches.append(None)
+            continue
+        io = staging.stage_layer(wl, l, meta, dev)
+        caches.append(io["k_cache"])
+        host_layers[l] = tuple(t.cpu().pin_memory() for t in (io["k"], io["q_fp8"], io["q_scale"], io["w"]))
+    step = IndexerStep(num_layers=wl.num_layers, pattern=wl.pattern, freq=wl.freq,
+                       offset=wl.offset, H=wl.H, index_topk=wl.index_topk, T=wl.T, R=wl.R,
+                       max_blocks=wl.max_blocks, num_pages=wl.num_pages,
+                       max_num_batched_tokens=wl.max_num_batched_tokens, k_caches=caches,
+                       device=dev, time_score_kernels=True)
+    host_meta = tuple(torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in
+                      (wl.query_start_loc, wl.seq_lens.astype(np.int32), wl.block_table))
+    host = {"meta": host_meta, "layers": host_layers}
+    step.set_metadata(*host_meta)
+    for l, io in host_layers.items():
+        step.set_layer(l, *io)
+    torch.cuda.synchronize()
+
+    n_full = sum(full)
+    pairs_per_step = wl.pairs_per_full_layer * n_full
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # ---- warm-up (eager once, then capture), then timed steps
+    step.launch()
+    torch.cuda.synchronize()
+    if not args.no_graph:
+        step.capture()
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    assert step.status.item() == 0, f"device status {step.status.item()}"
+    launches = step.launches_per_step
+
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    score_ms = []
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)                 # evict L2 between timed steps
+            ev0[i].record(stream)
+            step.run()
+            ev1[i].record(stream)
+            ev1[i].synchronize()
+            score_ms.extend(step.score_kernel_ms())
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    ms = sum(step_ms) / len(step_ms)
+
+    # ---- end to end through the public API with host buffers
+    out = torch.empty((wl.T, wl.index_topk), dtype=torch.int32).pin_memory()
+    h2d = step.host_input_bytes(host)
+    d2h = out.numel() * out.element_size()
+    for _ in range(max(1, args.warmup)):
+        step.run_from_host(host, out)
+    torch.cuda.synchronize()
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e0[i].record(stream)
+        step.run_from_host(host, out)
+        e1[i].record(stream)
+        e1[i].synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / args.steps
+
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = t.tolist()
+        pr = torch.tensor([pairs_per_step], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(pr)
+        total_pairs = pr.item()
+    else:
+        total_pairs = pairs_per_step
+    clk = clocks.summary()
+
+    # ---- roofline of the dominant kernel (scoring + top-k), per launch
+    peaks = read_peaks()
+    k_ms = sum(score_ms) / len(score_ms)
+    rows_bytes = wl.T * (wl.H * (128 + 4 + 4) + wl.index_topk * 4)   # q, q_scale, w in; top-k out
+    alg_bytes = wl.pairs_per_full_layer * BYTES_PER_PAIR + rows_bytes
+    achieved = alg_bytes / (k_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(wl.name)
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+            "kernel": "score_topk_kernel", "kernel_ms": k_ms, "algorithmic_bytes": alg_bytes,
+            "peak_source": peaks["source"]}
+
+    line = {
+        "metric": METRIC, "value": total_pairs / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": wl.name, **{k: v for k, v in wl.describe().items() if k != "workload"},
+                   "pairs_per_step": pairs_per_step, "full_layers": n_full,
+                   "cuda_graph": not args.no_graph, "l2": "flushed between timed steps",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": wl.T * n_full * world / (ms * 1e-3),
+        "roofline": roof,
+        "e2e": {"value": total_pairs / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "clocks": clk,
+        "gpu_launches": launches * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget_s)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

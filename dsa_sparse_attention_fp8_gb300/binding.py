@@ -61,6 +61,8 @@ class LayerIO(ctypes.Structure):
         ("q_scale", ctypes.c_void_p),
         ("w", ctypes.c_void_p),
         ("k_cache", ctypes.c_void_p),
+        ("score_begin", ctypes.c_void_p),
+        ("score_end", ctypes.c_void_p),
     ]
 
 
@@ -250,7 +252,8 @@ def layer_stack_run(layers: Sequence[Optional[dict]], pattern: Optional[str], fr
                     status: Optional[torch.Tensor] = None, T: Optional[int] = None,
                     stream=None) -> None:
     """Run the F/S layer stack.  ``layers[l]`` is a dict with keys k, q_fp8,
-    q_scale, w, k_cache for F layers, or None for S layers."""
+    q_scale, w, k_cache (and optionally score_begin / score_end, torch.cuda.Event
+    objects created with enable_timing=True) for F layers, or None for S layers."""
     R = seq_lens.shape[0]
     _need(query_start_loc, "query_start_loc", torch.int32, (R + 1,))
     _need(seq_lens, "seq_lens", torch.int32, (R,))
@@ -269,8 +272,11 @@ def layer_stack_run(layers: Sequence[Optional[dict]], pattern: Optional[str], fr
         _need(io["q_scale"], f"layers[{i}].q_scale", torch.float32, (T, H))
         _need(io["w"], f"layers[{i}].w", torch.float32, (T, H))
         _need(io["k_cache"], f"layers[{i}].k_cache", torch.uint8, (num_pages, PAGE_BYTES))
+        ev0, ev1 = io.get("score_begin"), io.get("score_end")
         arr[i] = LayerIO(io["k"].data_ptr(), io["q_fp8"].data_ptr(), io["q_scale"].data_ptr(),
-                         io["w"].data_ptr(), io["k_cache"].data_ptr())
+                         io["w"].data_ptr(), io["k_cache"].data_ptr(),
+                         None if ev0 is None else ev0.cuda_event,
+                         None if ev1 is None else ev1.cuda_event)
     if T is None:
         raise ValueError("no F layer given")
     outs = None

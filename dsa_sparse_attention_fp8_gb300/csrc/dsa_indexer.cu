@@ -460,8 +460,16 @@ int dsa_layer_stack_run(int num_layers, const char* pattern, int freq, int offse
       first_full = false;
       if (rc) break;
       LayerQ lq{io.q_fp8, io.q_scale, io.w, io.k_cache, nullptr, 0};
+      if (io.score_begin && cudaEventRecord((cudaEvent_t)io.score_begin, b.st) != cudaSuccess) {
+        rc = fail(DSA_ERR_CUDA, "recording score_begin of layer %d failed", l);
+        break;
+      }
       rc = launch_score_layer(b, s, lq, &launches);
       if (rc) break;
+      if (io.score_end && cudaEventRecord((cudaEvent_t)io.score_end, b.st) != cudaSuccess) {
+        rc = fail(DSA_ERR_CUDA, "recording score_end of layer %d failed", l);
+        break;
+      }
     }
     if (per_layer_topk_out && per_layer_topk_out[l]) {
       const int64_t bytes = (int64_t)T * index_topk * 4;

@@ -1,0 +1,123 @@
+"""One indexer forward step over an F/S layer stack, with reusable buffers.
+
+`IndexerStep` owns the per-step device buffers (query rows, new keys, batch
+metadata, the shared top-k buffer, workspace) and calls
+``dsa_layer_stack_run`` on them, eagerly or as a captured CUDA graph.
+`run_from_host` is the end-to-end call a serving loop makes: copy this
+step's inputs from (pinned) host memory, run the stack, copy the top-k rows
+back.  The page pools are device-resident state and are not copied.
+"""
+
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import torch
+
+from . import binding
+
+
+class IndexerStep:
+    def __init__(self, *, num_layers: int, pattern: Optional[str], freq: int, offset: int,
+                 H: int, index_topk: int, T: int, R: int, max_blocks: int, num_pages: int,
+                 max_num_batched_tokens: int, k_caches: Sequence[Optional[torch.Tensor]],
+                 device="cuda", time_score_kernels: bool = False):
+        self.num_layers, self.pattern, self.freq, self.offset = num_layers, pattern, freq, offset
+        self.H, self.k, self.T, self.R = H, index_topk, T, R
+        self.max_blocks, self.num_pages = max_blocks, num_pages
+        self.device = torch.device(device)
+        self.full = [binding.layer_is_full(l, pattern, freq, offset) for l in range(num_layers)]
+        dev = self.device
+        self.query_start_loc = torch.zeros(R + 1, dtype=torch.int32, device=dev)
+        self.seq_lens = torch.zeros(R, dtype=torch.int32, device=dev)
+        self.block_table = torch.zeros((R, max_blocks), dtype=torch.int32, device=dev)
+        self.topk = torch.full((max_num_batched_tokens, index_topk), -1, dtype=torch.int32,
+                               device=dev)
+        self.workspace = binding.alloc_workspace(T, H, R, index_topk, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.layers: list[Optional[dict]] = []
+        for l in range(num_layers):
+            if not self.full[l]:
+                self.layers.append(None)
+                continue
+            cache = k_caches[l]
+            assert cache is not None and cache.shape == (num_pages, binding.PAGE_BYTES)
+            io = {
+                "k": torch.zeros((T, binding.HEAD_DIM), dtype=torch.float32, device=dev),
+                "q_fp8": torch.zeros((T, H, binding.HEAD_DIM), dtype=torch.uint8, device=dev),
+                "q_scale": torch.ones((T, H), dtype=torch.float32, device=dev),
+                "w": torch.zeros((T, H), dtype=torch.float32, device=dev),
+                "k_cache": cache,
+            }
+            if time_score_kernels:
+                io["score_begin"] = torch.cuda.Event(enable_timing=True)
+                io["score_end"] = torch.cuda.Event(enable_timing=True)
+                # torch creates the CUDA event on first record
+                io["score_begin"].record()
+                io["score_end"].record()
+            self.layers.append(io)
+        self.graph: Optional[torch.cuda.CUDAGraph] = None
+        self.launches_per_step = 0
+
+    # -------------------------------------------------------------- inputs
+    def set_metadata(self, query_start_loc, seq_lens, block_table, non_blocking=False) -> None:
+        self.query_start_loc.copy_(query_start_loc, non_blocking=non_blocking)
+        self.seq_lens.copy_(seq_lens, non_blocking=non_blocking)
+        self.block_table.copy_(block_table, non_blocking=non_blocking)
+
+    def set_layer(self, layer: int, k, q_fp8, q_scale, w, non_blocking=False) -> None:
+        io = self.layers[layer]
+        io["k"].copy_(k, non_blocking=non_blocking)
+        io["q_fp8"].copy_(q_fp8, non_blocking=non_blocking)
+        io["q_scale"].copy_(q_scale, non_blocking=non_blocking)
+        io["w"].copy_(w, non_blocking=non_blocking)
+
+    # -------------------------------------------------------------- running
+    def launch(self) -> None:
+        binding.layer_stack_run(self.layers, self.pattern, self.freq, self.offset, self.H,
+                                self.query_start_loc, self.seq_lens, self.block_table,
+                                self.num_pages, self.k, self.topk, self.workspace,
+                                status=self.status, T=self.T)
+        self.launches_per_step = binding.last_launch_count()
+
+    def capture(self) -> None:
+        """Record one step as a CUDA graph (after one eager step for warm-up)."""
+        self.launch()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.launch()
+        torch.cuda.synchronize()
+        self.graph = g
+
+    def run(self) -> None:
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self.launch()
+
+    def score_kernel_ms(self) -> list[float]:
+        """Durations of the last step's scoring kernels (needs time_score_kernels)."""
+        return [io["score_begin"].elapsed_time(io["score_end"])
+                for io in self.layers if io is not None and "score_begin" in io]
+
+    # -------------------------------------------------------------- end to end
+    def host_input_bytes(self, host: dict) -> int:
+        n = sum(t.numel() * t.element_size() for t in host["meta"])
+        for l, io in host["layers"].items():
+            n += sum(t.numel() * t.element_size() for t in io)
+        return n
+
+    def run_from_host(self, host: dict, out: torch.Tensor) -> None:
+        """H2D of this step's inputs, the stack, D2H of rows [0, T) of the top-k buffer.
+
+        ``host["meta"]`` = (query_start_loc, seq_lens, block_table) and
+        ``host["layers"][l]`` = (k, q_fp8, q_scale, w), pinned CPU tensors;
+        ``out`` is a pinned int32 [T, index_topk] CPU tensor.  Asynchronous on
+        the current stream.
+        """
+        self.set_metadata(*host["meta"], non_blocking=True)
+        for l, io in host["layers"].items():
+            self.set_layer(l, *io, non_blocking=True)
+        self.run()
+        out.copy_(self.topk[: self.T], non_blocking=True)

@@ -155,13 +155,18 @@ int dsa_indexer_score_topk(const uint8_t* q_fp8, const float* q_scale, const flo
  */
 int dsa_layer_is_full(int layer_id, const char* pattern, int freq, int offset);
 
-/* Per-layer inputs of dsa_layer_stack_run; S layers may leave every field NULL. */
+/* Per-layer inputs of dsa_layer_stack_run; S layers may leave every field NULL.
+ * score_begin / score_end: optional cudaEvent_t handles (NULL = none) that are
+ * recorded on the stream immediately before and after this layer's scoring
+ * kernel, so a caller can time that kernel inside a larger (or captured) step. */
 typedef struct dsa_layer_io {
   const float* k;         /* [T, 128] FP32 new-token keys of this layer */
   const uint8_t* q_fp8;   /* [T, H, 128] E4M3 queries */
   const float* q_scale;   /* [T, H] */
   const float* w;         /* [T, H] head weights */
   uint8_t* k_cache;       /* [num_pages, 8448] this layer's page pool */
+  void* score_begin;      /* cudaEvent_t or NULL */
+  void* score_end;        /* cudaEvent_t or NULL */
 } dsa_layer_io;
 
 /*

@@ -105,7 +105,7 @@ def test_stack_rejects_bad_schedules(lib):
     fake = P(0x1000)
     layers = (LayerIO * 3)()
     for i in range(3):
-        layers[i] = LayerIO(0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
+        layers[i] = LayerIO(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, None, None)
 
     def run(pattern, freq, lay=layers, n=3):
         return lib.dsa_layer_stack_run(n, pattern, freq, 2, lay, 4, 64, fake, fake, 1, fake, 4,
@@ -114,7 +114,7 @@ def test_stack_rejects_bad_schedules(lib):
     assert run(b"FQF", 1) == -1                 # bad character
     assert run(None, 0) == -1                   # freq 0
     empty = (LayerIO * 3)()
-    empty[0] = LayerIO(0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
+    empty[0] = LayerIO(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, None, None)
     assert run(b"FSF", 1, empty) == -1          # F layer 2 lacks inputs
     assert b"layer 2" in lib.dsa_last_error()
     # T == 0: valid no-op, nothing launched

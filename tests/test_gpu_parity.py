@@ -191,6 +191,7 @@ def test_bad_page_is_reported_not_faulted(B):
     wl = _custom([1, 1], [200, 150], H=4, k=16)
     meta = staging.stage_metadata(wl)
     io = staging.stage_layer(wl, 0, meta)
+    binding.write_k(io["k"], meta.query_start_loc, meta.seq_lens, meta.block_table, io["k_cache"])
     bt = meta.block_table.clone()
     bt[1, 1] = wl.num_pages + 1000      # out of the pool
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -214,6 +215,7 @@ def test_bad_metadata_is_reported(B):
     wl = _custom([2, 1], [100, 50], H=4, k=8)
     meta = staging.stage_metadata(wl)
     io = staging.stage_layer(wl, 0, meta)
+    binding.write_k(io["k"], meta.query_start_loc, meta.seq_lens, meta.block_table, io["k_cache"])
     sl = meta.seq_lens.clone()
     sl[0] = 1                           # fewer context tokens than new rows
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
