@@ -279,6 +279,18 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   return rc;
 }
 
+// Record a caller's timing event on the stream; inside stream capture it must
+// become an event-record node of the graph (external event), otherwise the
+// event would only express a dependency and never be recorded on replay.
+cudaError_t record_event(void* ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs == cudaStreamCaptureStatusActive)
+    return cudaEventRecordWithFlags((cudaEvent_t)ev, st, cudaEventRecordExternal);
+  return cudaEventRecord((cudaEvent_t)ev, st);
+}
+
 int launch_write(const float* k, const Batch& b, uint8_t* k_cache, int64_t* slot_mapping,
                  int* launches) {
   const int warps_per_block = 8;
@@ -460,13 +472,13 @@ int dsa_layer_stack_run(int num_layers, const char* pattern, int freq, int offse
       first_full = false;
       if (rc) break;
       LayerQ lq{io.q_fp8, io.q_scale, io.w, io.k_cache, nullptr, 0};
-      if (io.score_begin && cudaEventRecord((cudaEvent_t)io.score_begin, b.st) != cudaSuccess) {
+      if (io.score_begin && record_event(io.score_begin, b.st) != cudaSuccess) {
         rc = fail(DSA_ERR_CUDA, "recording score_begin of layer %d failed", l);
         break;
       }
       rc = launch_score_layer(b, s, lq, &launches);
       if (rc) break;
-      if (io.score_end && cudaEventRecord((cudaEvent_t)io.score_end, b.st) != cudaSuccess) {
+      if (io.score_end && record_event(io.score_end, b.st) != cudaSuccess) {
         rc = fail(DSA_ERR_CUDA, "recording score_end of layer %d failed", l);
         break;
       }
