@@ -307,6 +307,7 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed_steps")
     with ClockSampler(dev.index) as clocks:
         for i in range(args.steps):
             flush.fill_(i & 0xFF)                 # evict L2 between timed steps
@@ -320,6 +321,7 @@ def main():
                 except RuntimeError:
                     timing_failed = True
         torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     if world > 1:
         torch.distributed.barrier()
     step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
