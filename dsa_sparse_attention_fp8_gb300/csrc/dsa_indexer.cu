@@ -7,6 +7,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -82,15 +83,20 @@ int make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t b
 
 // ---------------------------------------------------------------- launch shape
 struct ScoreShape {
-  int G, C, NS, NB, n_max, q_box_per_token;
+  int G, C, NS, NB, NQ, n_max, q_box_per_token;
+  uint32_t q_bytes;
   size_t smem_bytes;
   dsa::ScoreParams offs;  // only the off_* fields are filled
 };
 
 constexpr size_t kSmemLimit = 232448;  // 227 KB opt-in per block on sm_100-family
 
-int candidate_capacity(int k) {
-  int c = (k >= 1024) ? k + k / 2 : (2 * k > k + 128 ? 2 * k : k + 128);
+// Candidate-buffer capacity per query row.  A decode layout (one row per
+// group) keeps whole splits of up to 8K keys without intermediate selection;
+// otherwise the buffer holds k plus room for at least one 512-candidate batch.
+int candidate_capacity(int k, bool decode) {
+  int c = k + (k / 2 > 512 ? k / 2 : 512);
+  if (decode && c < 8192) c = 8192;
   return (c + 127) / 128 * 128;
 }
 
@@ -100,7 +106,7 @@ int candidate_capacity(int k) {
 int choose_group(int T, int R, int H, int k) {
   if (T <= R) return 1;
   int g = 256 / H;
-  const int by_smem = (96 * 1024) / (candidate_capacity(k) * 8);
+  const int by_smem = (96 * 1024) / (candidate_capacity(k, false) * 8);
   if (g > by_smem) g = by_smem;
   return g < 1 ? 1 : g;
 }
@@ -109,38 +115,50 @@ size_t up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   s->G = choose_group(T, R, H, k);
-  s->C = candidate_capacity(k);
+  s->C = candidate_capacity(k, s->G == 1);
   s->q_box_per_token = (H % 8 == 0) ? 1 : 0;
   s->n_max = (s->G * H + 15) / 16 * 16;
   s->NB = dsa::kTmemCols / s->n_max;
   if (s->NB > dsa::kMaxAccBufs) s->NB = dsa::kMaxAccBufs;
   if (s->NB < 2) return false;
-  size_t o = 0;
-  const size_t q_bytes = up((size_t)s->G * H * 128, 1024);
-  // stages go first (1024-aligned); fixed parts after them
+  s->q_bytes = (uint32_t)up((size_t)s->G * H * 128, 1024);
+  s->NQ = s->q_bytes <= 16384 ? 2 : 1;
   size_t fixed = 0;
-  fixed += q_bytes;
+  fixed += (size_t)s->NQ * s->q_bytes;
   fixed += up((size_t)s->G * s->C * 4, 16) * 2;
   fixed += up((size_t)s->G * H * 4, 16);
   fixed += up((size_t)s->G * sizeof(dsa::TokSlot), 16);
-  fixed += 2 * 256 * 4;
+  fixed += 2 * dsa::kHistBins * 4;
   fixed += up(sizeof(dsa::Misc), 16);
-  fixed += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 3) * 8;
+  fixed += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 2 * dsa::kMaxQBufs + 1) * 8;
+  const size_t per_stage = dsa::kStageBytes + dsa::kStageScaleBytes;
   const size_t budget = kSmemLimit - 1024 - 64;
-  if (fixed + 2 * dsa::kStageBytes > budget) return false;
-  s->NS = (int)((budget - fixed) / dsa::kStageBytes);
+  if (fixed + 2 * per_stage > budget) return false;
+  s->NS = (int)((budget - fixed) / per_stage);
   if (s->NS > dsa::kMaxStages) s->NS = dsa::kMaxStages;
+  size_t o = 0;  // stages first: every key stage starts on a 1024-byte boundary
   s->offs.off_stage = (uint32_t)o; o += (size_t)s->NS * dsa::kStageBytes;
-  s->offs.off_q = (uint32_t)o;     o += q_bytes;
+  s->offs.off_q = (uint32_t)o;     o += (size_t)s->NQ * s->q_bytes;
+  s->offs.off_scale = (uint32_t)o; o += (size_t)s->NS * dsa::kStageScaleBytes;
   s->offs.off_ckeys = (uint32_t)o; o += up((size_t)s->G * s->C * 4, 16);
   s->offs.off_cidx = (uint32_t)o;  o += up((size_t)s->G * s->C * 4, 16);
   s->offs.off_wq = (uint32_t)o;    o += up((size_t)s->G * H * 4, 16);
   s->offs.off_tok = (uint32_t)o;   o += up((size_t)s->G * sizeof(dsa::TokSlot), 16);
-  s->offs.off_hist = (uint32_t)o;  o += 2 * 256 * 4;
+  s->offs.off_hist = (uint32_t)o;  o += 2 * dsa::kHistBins * 4;
   s->offs.off_misc = (uint32_t)o;  o += up(sizeof(dsa::Misc), 16);
-  s->offs.off_bar = (uint32_t)o;   o += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 3) * 8;
+  s->offs.off_bar = (uint32_t)o;
+  o += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 2 * dsa::kMaxQBufs + 1) * 8;
   s->smem_bytes = o + 1024;  // slack for aligning the dynamic base to 1024
   return s->smem_bytes <= kSmemLimit;
+}
+
+// Split policy: target work items per SM and the shortest key range worth a
+// split of its own.  DSA_ITEMS_PER_SM / DSA_MIN_SPLIT override the defaults.
+int env_int(const char* name, int dflt, int lo, int hi) {
+  const char* v = getenv(name);
+  if (!v || !*v) return dflt;
+  const int x = atoi(v);
+  return x < lo ? lo : (x > hi ? hi : x);
 }
 
 template <int H>
@@ -217,7 +235,10 @@ int launch_plan(const Batch& b, int G, int* launches) {
   pp.index_topk = b.k;
   int n = sm_count();
   if (n <= 0) return fail(DSA_ERR_CUDA, "no CUDA device");
-  pp.target = 2 * n < dsa::kMaxTarget ? 2 * n : dsa::kMaxTarget;
+  const int per_sm = env_int("DSA_ITEMS_PER_SM", 2, 1, 2);
+  pp.target = per_sm * n < dsa::kMaxTarget ? per_sm * n : dsa::kMaxTarget;
+  pp.min_split = env_int("DSA_MIN_SPLIT", 2048, 128, 1 << 20) / 128 * 128;
+  pp.max_split = 1 << 30;
   pp.topk_buffer = b.topk;
   pp.ws = static_cast<unsigned char*>(b.ws);
   pp.L = dsa::ws_layout(b.T, b.R, G, b.k);
@@ -261,6 +282,8 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   p.C = s.C;
   p.NS = s.NS;
   p.NB = s.NB;
+  p.NQ = s.NQ;
+  p.q_bytes = s.q_bytes;
   p.n_max = s.n_max;
   p.q_box_per_token = s.q_box_per_token;
   p.items = reinterpret_cast<const dsa::Item*>(ws + L.items);

@@ -8,8 +8,10 @@
 // ("splits") that run on different SMs; each split keeps an exact local
 // top-k and the last split of a group to finish merges them.
 //
-// S = max(kMinSplit, total visible keys / target items), so the number of
-// items is at most (#groups + target) and at most `target` groups are split.
+// S = clamp(total visible keys / target items, min_split, max_split), so the
+// number of items is at most (#groups + target) and at most `target` groups
+// are split whenever S is not capped by max_split (the host sizes the
+// workspace for the capped case too).
 #pragma once
 
 #include <cstdint>
@@ -29,7 +31,6 @@ struct Item {
 };
 static_assert(sizeof(Item) == 32, "Item must stay 32 bytes");
 
-constexpr int kMinSplit = 1024;     // keys; multiple of 128
 constexpr int kMaxTarget = 320;     // upper bound on work-item target (2 per SM, <=160 SMs)
 constexpr int kPlanThreads = 1024;
 
@@ -100,6 +101,7 @@ struct PlanParams {
   const int32_t* qsl;
   const int32_t* seq_lens;
   int R, T, G, max_blocks, index_topk, target;
+  int min_split, max_split;  // bounds on the split length S (multiples of 128)
   int32_t* topk_buffer;  // for -1 rows of malformed requests
   unsigned char* ws;
   WsLayout L;
@@ -156,8 +158,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
       group_prefix[p.R] = (int32_t)groups_carry;
       long long S = (tot + p.target - 1) / p.target;
       S = ((S + 127) / 128) * 128;
-      if (S < kMinSplit) S = kMinSplit;
-      if (S > (1ll << 30)) S = 1ll << 30;
+      if (S < p.min_split) S = p.min_split;
+      if (S > p.max_split) S = p.max_split;
+      if (S < 128) S = 128;
       s_split_len = (int)S;
     }
   }

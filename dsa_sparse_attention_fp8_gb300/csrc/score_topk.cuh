@@ -13,8 +13,9 @@
 //
 // Structure (one CTA per SM, 10 warps):
 //   warp 0      producer: per key tile (128 keys = 2 pages) two TMA loads of
-//               64 x 128 B key rows into a 128B-swizzled stage; the query
-//               tile of the item once.
+//               64 x 128 B key rows into a 128B-swizzled stage plus two 256 B
+//               bulk copies of the pages' scales; the query tile of each item
+//               (double-buffered when it is small).
 //   warp 1      owns tensor memory; one lane issues 4 tcgen05.mma (K = 32
 //               each) per tile: D[key, row*H + head] += k . q, FP32 in TMEM.
 //   warps 2-9   epilogue, two warpgroups; thread = one key row of the tile
@@ -23,7 +24,7 @@
 //               then stream the score into an exact top-k buffer in shared
 //               memory (append above the running threshold; when the buffer
 //               fills, radix-select the k largest and raise the threshold).
-// No score row ever goes to global memory (except the optional debug dump).
+// No score row goes to global memory (except the optional debug dump).
 #pragma once
 
 #include <cstdint>
@@ -37,10 +38,14 @@ constexpr int kScoreThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kTileKeys = 128;
 constexpr int kStageBytes = kTileKeys * kHeadDim;  // 16 KB of key rows
+constexpr int kStageScaleBytes = kTileKeys * 4;    // the tile's 128 FP32 scales
 constexpr int kMaxStages = 16;
 constexpr int kMaxAccBufs = 8;
+constexpr int kMaxQBufs = 2;
 constexpr int kTmemCols = 512;
-constexpr int kMaxCandPerThread = 32;  // candidate capacity C <= 128 * 32
+constexpr int kSelPer = 4;                 // elements per thread per selection chunk
+constexpr int kSelChunk = 128 * kSelPer;   // one warpgroup handles 512 per chunk
+constexpr int kHistBins = 2048;            // 11-bit radix digits
 
 struct TokSlot {
   int32_t count;   // candidates held
@@ -58,8 +63,9 @@ struct ScoreParams {
   int64_t num_pages;
   const float* q_scale;
   const float* w;
-  int T, H, G, k, C, NS, NB, n_max;
+  int T, H, G, k, C, NS, NB, NQ, n_max;
   int q_box_per_token;
+  uint32_t q_bytes;  // bytes of one query-tile buffer
   const Item* items;
   const PlanHeader* hdr;
   uint32_t* cand_keys;
@@ -71,7 +77,8 @@ struct ScoreParams {
   int64_t scores_ld;
   int32_t* status;
   // dynamic shared memory offsets (from a 1024-aligned base)
-  uint32_t off_stage, off_q, off_ckeys, off_cidx, off_wq, off_tok, off_hist, off_misc, off_bar;
+  uint32_t off_stage, off_scale, off_q, off_ckeys, off_cidx, off_wq, off_tok, off_hist, off_misc,
+      off_bar;
 };
 
 struct Misc {
@@ -79,9 +86,16 @@ struct Misc {
   uint32_t tmem_base;
   int merge_flag;
   int pad;
-  // per-warpgroup radix-select scratch
-  int sel_bin[2], sel_above[2], sel_cnt[2], out_ctr[2], tie_ctr[2];
+  // per-warpgroup selection scratch
+  int sel_bin[2], sel_above[2], sel_cnt[2], pad2[2];
   int scan[2][4];
+  int cnt_a[2][16], cnt_b[2][16];
+};
+
+struct Thresh {
+  uint32_t prefix, mask;
+  int need;   // keys equal to prefix still to take (exact threshold only)
+  int early;  // 1: take every key whose masked value is >= prefix
 };
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -106,104 +120,170 @@ __device__ __forceinline__ void cand_append(uint32_t key, int32_t idx, uint32_t 
   }
 }
 
-// Exact selection of the k largest keys among the n > k held by slot `ts`,
-// compacted to positions [0, k).  Run by the 128 threads of one warpgroup.
-// Radix select over 8-bit digits from the top: each pass histograms the
-// candidates that share the already fixed prefix, finds the digit bin where
-// the running count from the top crosses k, and either stops (that bin is
-// taken whole) or refines inside it.
-__device__ __noinline__ void cand_compress(TokSlot* ts, uint32_t* ckeys, int32_t* cidx, int k,
-                                           int* hist, Misc* misc, int wg, int tid) {
-  const uint32_t bar_id = 1 + wg;
-  const int n = ts->count;
-  uint32_t kr[kMaxCandPerThread];
-  int32_t ir[kMaxCandPerThread];
-#pragma unroll
-  for (int j = 0; j < kMaxCandPerThread; ++j) {
-    const int i = tid + 128 * j;
-    kr[j] = (i < n) ? ckeys[i] : 0u;
-    ir[j] = (i < n) ? cidx[i] : -1;
-  }
-  int need = k;
-  uint32_t prefix = 0, mask = 0;
-  bool early = false;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    hist[tid] = 0;
-    hist[tid + 128] = 0;
-    named_bar_sync(bar_id, 128);
-#pragma unroll
-    for (int j = 0; j < kMaxCandPerThread; ++j)
-      if (kr[j] != 0u && (kr[j] & mask) == prefix) atomicAdd(&hist[(kr[j] >> shift) & 255u], 1);
-    named_bar_sync(bar_id, 128);
-    // descending bins: thread tid covers bins 255-2*tid and 254-2*tid
-    const int b_hi = 255 - 2 * tid, b_lo = 254 - 2 * tid;
-    const int c_hi = hist[b_hi], c_lo = hist[b_lo];
-    int incl = c_hi + c_lo;
-    const int lane = tid & 31, w = tid >> 5;
+// Radix select (11-, 11-, 10-bit digits from the top) of the k-th largest key
+// among keys[0, n), n > k.  128 threads of warpgroup `wg`.  Each pass
+// histograms the keys that share the prefix fixed so far (same-bin lanes of a
+// warp are merged with match.any before one shared atomic), finds the digit
+// where the count from the top crosses k, and stops early when that bin is
+// taken whole.
+__device__ __noinline__ Thresh find_threshold(const uint32_t* keys, int n, int k, int* hist,
+                                              Misc* misc, int wg, int tid) {
+  const uint32_t bar = 1 + wg;
+  const int lane = tid & 31, w = tid >> 5;
+  Thresh th{0u, 0u, k, 0};
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const int nbins = pass == 2 ? 1024 : 2048;
+    const uint32_t dm = (uint32_t)nbins - 1u;
+    for (int b = tid; b < nbins; b += 128) hist[b] = 0;
+    named_bar_sync(bar, 128);
+    for (int base = 0; base < n; base += 128) {
+      const int i = base + tid;
+      const uint32_t key = (i < n) ? keys[i] : 0u;
+      const bool m = (i < n) && (key & th.mask) == th.prefix;
+      const uint32_t active = __ballot_sync(0xffffffffu, m);
+      if (m) {
+        const uint32_t bin = (key >> shift) & dm;
+        const uint32_t peers = __match_any_sync(active, bin);
+        if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+      }
+    }
+    named_bar_sync(bar, 128);
+    const int per = nbins / 128;               // bins per thread, highest first
+    const int top = nbins - 1 - tid * per;
+    int local = 0;
+    for (int j = 0; j < per; ++j) local += hist[top - j];
+    int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
     if (lane == 31) misc->scan[wg][w] = incl;
-    named_bar_sync(bar_id, 128);
-    int warp_off = 0;
-    for (int u = 0; u < w; ++u) warp_off += misc->scan[wg][u];
-    const int above_hi = warp_off + incl - (c_hi + c_lo);  // keys in bins > b_hi
-    if (above_hi < need && need <= above_hi + c_hi) {
-      misc->sel_bin[wg] = b_hi;
-      misc->sel_above[wg] = above_hi;
-      misc->sel_cnt[wg] = c_hi;
-    } else if (above_hi + c_hi < need && need <= above_hi + c_hi + c_lo) {
-      misc->sel_bin[wg] = b_lo;
-      misc->sel_above[wg] = above_hi + c_hi;
-      misc->sel_cnt[wg] = c_lo;
+    named_bar_sync(bar, 128);
+    int above = incl - local;
+    for (int u = 0; u < w; ++u) above += misc->scan[wg][u];
+    if (above < th.need && th.need <= above + local) {
+      for (int j = 0; j < per; ++j) {
+        const int c = hist[top - j];
+        if (th.need <= above + c) {
+          misc->sel_bin[wg] = top - j;
+          misc->sel_above[wg] = above;
+          misc->sel_cnt[wg] = c;
+          break;
+        }
+        above += c;
+      }
     }
-    named_bar_sync(bar_id, 128);
-    const int b = misc->sel_bin[wg];
-    need -= misc->sel_above[wg];
+    named_bar_sync(bar, 128);
+    const uint32_t b = (uint32_t)misc->sel_bin[wg];
+    th.need -= misc->sel_above[wg];
     const int cnt = misc->sel_cnt[wg];
-    prefix |= (uint32_t)b << shift;
-    mask |= 255u << shift;
-    named_bar_sync(bar_id, 128);  // scratch read by all before the next pass rewrites it
-    if (cnt == need) {
-      early = true;
+    th.prefix |= b << shift;
+    th.mask |= dm << shift;
+    named_bar_sync(bar, 128);  // scratch read by all before it is rewritten
+    if (cnt == th.need) {
+      th.early = 1;
       break;
     }
   }
-  if (tid == 0) {
-    misc->out_ctr[wg] = 0;
-    misc->tie_ctr[wg] = 0;
-  }
-  named_bar_sync(bar_id, 128);
-  const int definite = k - (early ? 0 : need);  // keys strictly above the k-th
+  return th;
+}
+
+// Copy the keys selected by `th` from keys/idx[0, n) to dkeys/didx[0, ...) in
+// scan order (deterministic; dkeys may be null; dst may alias src because an
+// element never moves to a higher position and every chunk is read before it
+// is written).  Ties at an exact threshold are taken in scan order up to the
+// quota.  Returns the number written.  128 threads of warpgroup `wg`.
+__device__ __noinline__ int compact_selected(const uint32_t* keys, const int32_t* idx, int n,
+                                             Thresh th, uint32_t* dkeys, int32_t* didx,
+                                             Misc* misc, int wg, int tid) {
+  const uint32_t bar = 1 + wg;
+  const int lane = tid & 31, w = tid >> 5;
+  const uint32_t lt = lanemask_lt();
+  const int quota = th.early ? 0 : th.need;
+  int out = 0, ties = 0;
+  for (int base = 0; base < n; base += kSelChunk) {
+    uint32_t key[kSelPer];
+    int32_t ix[kSelPer];
+    bool def[kSelPer], tie[kSelPer];
+    uint32_t bt[kSelPer];
 #pragma unroll
-  for (int j = 0; j < kMaxCandPerThread; ++j) {
-    const bool valid = kr[j] != 0u;
-    const bool sel = valid && (early ? (kr[j] & mask) >= prefix : kr[j] > prefix);
-    const uint32_t m = __ballot_sync(0xffffffffu, sel);
-    int base = 0;
-    if (m && (tid & 31) == 0) base = atomicAdd(&misc->out_ctr[wg], __popc(m));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (sel) {
-      const int p = base + __popc(m & lanemask_lt());
-      ckeys[p] = kr[j];
-      cidx[p] = ir[j];
+    for (int u = 0; u < kSelPer; ++u) {
+      const int i = base + u * 128 + tid;
+      const bool valid = i < n;
+      key[u] = valid ? keys[i] : 0u;
+      ix[u] = valid ? idx[i] : 0;
+      def[u] = valid && (th.early ? (key[u] & th.mask) >= th.prefix : key[u] > th.prefix);
+      tie[u] = valid && !th.early && key[u] == th.prefix;
+      bt[u] = __ballot_sync(0xffffffffu, tie[u]);
+      if (lane == 0) misc->cnt_a[wg][u * 4 + w] = __popc(bt[u]);
     }
-    if (!early && valid && kr[j] == prefix) {
-      const int q = atomicAdd(&misc->tie_ctr[wg], 1);
-      if (q < need) {
-        ckeys[definite + q] = kr[j];
-        cidx[definite + q] = ir[j];
+    named_bar_sync(bar, 128);  // every read of this chunk is done
+    int pre_a[kSelPer], tot_a = 0;
+#pragma unroll
+    for (int u = 0; u < kSelPer; ++u) {
+      int p = tot_a;
+      for (int v = 0; v < 4; ++v) {
+        const int c = misc->cnt_a[wg][u * 4 + v];
+        if (v < w) p += c;
+        tot_a += c;
+      }
+      pre_a[u] = p;
+    }
+    uint32_t bs[kSelPer];
+    bool sel[kSelPer];
+#pragma unroll
+    for (int u = 0; u < kSelPer; ++u) {
+      const int trank = ties + pre_a[u] + __popc(bt[u] & lt);
+      sel[u] = def[u] || (tie[u] && trank < quota);
+      bs[u] = __ballot_sync(0xffffffffu, sel[u]);
+      if (lane == 0) misc->cnt_b[wg][u * 4 + w] = __popc(bs[u]);
+    }
+    named_bar_sync(bar, 128);
+    int tot_b = 0;
+#pragma unroll
+    for (int u = 0; u < kSelPer; ++u) {
+      int p = tot_b;
+      for (int v = 0; v < 4; ++v) {
+        const int c = misc->cnt_b[wg][u * 4 + v];
+        if (v < w) p += c;
+        tot_b += c;
+      }
+      if (sel[u]) {
+        const int q = out + p + __popc(bs[u] & lt);
+        if (dkeys) dkeys[q] = key[u];
+        didx[q] = ix[u];
       }
     }
+    out += tot_b;
+    ties += tot_a;
+    named_bar_sync(bar, 128);  // counters are rewritten by the next chunk
   }
-  named_bar_sync(bar_id, 128);
+  return out;
+}
+
+// Keep the k largest of the slot's candidates (in place) and raise its threshold.
+__device__ __forceinline__ void cand_compress(TokSlot* ts, uint32_t* ck, int32_t* ci, int k,
+                                              int* hist, Misc* misc, int wg, int tid) {
+  const int n = ts->count;
+  const Thresh th = find_threshold(ck, n, k, hist, misc, wg, tid);
+  compact_selected(ck, ci, n, th, ck, ci, misc, wg, tid);
   if (tid == 0) {
     ts->count = k;
-    ts->thr = prefix;
+    ts->thr = th.prefix;
   }
-  named_bar_sync(bar_id, 128);
+  named_bar_sync(1 + wg, 128);
+}
+
+// Emit min(count, k) selected candidates of a slot to global memory; returns how many.
+__device__ __forceinline__ int cand_emit(TokSlot* ts, const uint32_t* ck, const int32_t* ci,
+                                        int k, uint32_t* dkeys, int32_t* didx, int* hist,
+                                        Misc* misc, int wg, int tid) {
+  const int n = ts->count;
+  Thresh th{0u, 0u, 0, 1};  // everything
+  if (n > k) th = find_threshold(ck, n, k, hist, misc, wg, tid);
+  return compact_selected(ck, ci, n, th, dkeys, didx, misc, wg, tid);
 }
 
 template <int H>
@@ -228,12 +308,6 @@ __device__ __forceinline__ float relu_weighted_sum(uint32_t taddr, const float* 
   return acc0 + acc1;
 }
 
-// Write the final rows of one query: n valid indices then -1 up to k.
-__device__ __forceinline__ void write_row(int32_t* out_row, const int32_t* cidx, int n, int k,
-                                          int tid) {
-  for (int i = tid; i < k; i += 128) out_row[i] = (i < n) ? cidx[i] : -1;
-}
-
 template <int H>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_topk_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -245,7 +319,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int lane = threadIdx.x & 31;
 
   uint8_t* stage_base = smem + p.off_stage;
-  uint8_t* q_tile = smem + p.off_q;
+  const float* scale_base = reinterpret_cast<const float*>(smem + p.off_scale);
+  uint8_t* q_base = smem + p.off_q;
   uint32_t* ckeys_all = reinterpret_cast<uint32_t*>(smem + p.off_ckeys);
   int32_t* cidx_all = reinterpret_cast<int32_t*>(smem + p.off_cidx);
   float* wq_all = reinterpret_cast<float*>(smem + p.off_wq);
@@ -258,21 +333,24 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const uint32_t bar_tfull = bar_empty + 8 * kMaxStages;
   const uint32_t bar_tempty = bar_tfull + 8 * kMaxAccBufs;
   const uint32_t bar_qfull = bar_tempty + 8 * kMaxAccBufs;
-  const uint32_t bar_qempty = bar_qfull + 8;
-  const uint32_t bar_drain = bar_qempty + 8;
+  const uint32_t bar_qempty = bar_qfull + 8 * kMaxQBufs;
+  const uint32_t bar_drain = bar_qempty + 8 * kMaxQBufs;
   volatile int* abort_flag = &misc->abort;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+      // a stage is free once its MMAs completed and every epilogue warp read its scales
+      mbar_init(bar_empty + 8 * s, 1 + kEpiWarps);
     }
     for (int b = 0; b < p.NB; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
       mbar_init(bar_tempty + 8 * b, kEpiWarps);
     }
-    mbar_init(bar_qfull, 1);
-    mbar_init(bar_qempty, 1);
+    for (int b = 0; b < p.NQ; ++b) {
+      mbar_init(bar_qfull + 8 * b, 1);
+      mbar_init(bar_qempty + 8 * b, 1);
+    }
     mbar_init(bar_drain, 1);
     misc->abort = 0;
     misc->merge_flag = 0;
@@ -299,20 +377,24 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       uint32_t sphase = 0;
       uint32_t issued_mask = 0;
       uint32_t last_par[kMaxStages];
+      int q_last[kMaxQBufs] = {-1, -1};
       int item_i = 0;
-      int q_issued = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_i) {
         const Item I = p.items[it];
-        if (!mbar_wait(bar_qempty, (item_i & 1) ^ 1, abort_flag)) { ok = false; break; }
-        q_issued = item_i + 1;
+        const int qb = item_i % p.NQ;
+        const uint32_t qpar = (uint32_t)((item_i / p.NQ) & 1);
+        if (!mbar_wait(bar_qempty + 8 * qb, qpar ^ 1, abort_flag)) { ok = false; break; }
+        q_last[qb] = item_i;
+        uint8_t* q_tile = q_base + qb * p.q_bytes;
         if (p.q_box_per_token) {
-          mbar_arrive_expect_tx(bar_qfull, (uint32_t)(I.gcount * H * kHeadDim));
+          mbar_arrive_expect_tx(bar_qfull + 8 * qb, (uint32_t)(I.gcount * H * kHeadDim));
           for (int g = 0; g < I.gcount; ++g)
-            tma_load_2d(smem_u32(q_tile + g * H * kHeadDim), &tm_q, 0, (I.t0 + g) * H, bar_qfull);
+            tma_load_2d(smem_u32(q_tile + g * H * kHeadDim), &tm_q, 0, (I.t0 + g) * H,
+                        bar_qfull + 8 * qb);
         } else {
-          mbar_arrive_expect_tx(bar_qfull, (uint32_t)(p.G * H * kHeadDim));
-          tma_load_2d(smem_u32(q_tile), &tm_q, 0, I.t0 * H, bar_qfull);
+          mbar_arrive_expect_tx(bar_qfull + 8 * qb, (uint32_t)(p.G * H * kHeadDim));
+          tma_load_2d(smem_u32(q_tile), &tm_q, 0, I.t0 * H, bar_qfull + 8 * qb);
         }
         const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
         const int32_t* bt_row = p.block_table + (int64_t)I.r * p.max_blocks;
@@ -329,17 +411,22 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
               const int64_t page = __ldg(bt_row + ks / kPageTokens);
               if (page >= 0 && page < p.num_pages) {
                 pg[pi] = page;
-                bytes += kPageTokens * kHeadDim;
+                bytes += kPageTokens * kHeadDim + kPageTokens * 4;
               }
             }
           }
           mbar_arrive_expect_tx(bar_full + 8 * stage, bytes);
           const uint32_t dst = smem_u32(stage_base + stage * kStageBytes);
+          const uint32_t sdst = smem_u32(scale_base + stage * kTileKeys);
 #pragma unroll
           for (int pi = 0; pi < 2; ++pi)
-            if (pg[pi] >= 0)
+            if (pg[pi] >= 0) {
               tma_load_2d(dst + pi * kPageTokens * kHeadDim, &tm_k, 0,
                           (int32_t)(pg[pi] * (kPageBytes / kHeadDim)), bar_full + 8 * stage);
+              bulk_load(sdst + pi * kPageTokens * 4,
+                        p.k_cache + pg[pi] * kPageBytes + kPageScaleOffset, kPageTokens * 4,
+                        bar_full + 8 * stage);
+            }
           issued_mask |= 1u << stage;
           last_par[stage] = sphase;
           if (++stage == p.NS) { stage = 0; sphase ^= 1; }
@@ -352,7 +439,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       // never leave with bulk copies in flight into this CTA's shared memory
       for (int s = 0; s < p.NS; ++s)
         if (issued_mask & (1u << s)) mbar_wait(bar_full + 8 * s, last_par[s], nullptr);
-      if (q_issued) mbar_wait(bar_qfull, (q_issued - 1) & 1, nullptr);
+      for (int b = 0; b < p.NQ; ++b)
+        if (q_last[b] >= 0) mbar_wait(bar_qfull + 8 * b, (uint32_t)((q_last[b] / p.NQ) & 1), nullptr);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -365,9 +453,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const Item I = p.items[it];
         const uint32_t N = (uint32_t)((I.gcount * H + 15) & ~15);
         const uint32_t idesc = idesc_e4m3_f32(128, N);
-        if (!mbar_wait(bar_qfull, item_i & 1, abort_flag)) { ok = false; break; }
+        const int qb = item_i % p.NQ;
+        if (!mbar_wait(bar_qfull + 8 * qb, (uint32_t)((item_i / p.NQ) & 1), abort_flag)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        const uint32_t qaddr = smem_u32(q_tile);
+        const uint32_t qaddr = smem_u32(q_base + qb * p.q_bytes);
         const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
         for (int j = 0; j < ntiles; ++j) {
           if (!mbar_wait(bar_full + 8 * stage, sphase, abort_flag)) { ok = false; break; }
@@ -384,7 +476,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           if (++acc == p.NB) { acc = 0; aphase ^= 1; }
         }
         if (!ok) break;
-        umma_commit(bar_qempty);
+        umma_commit(bar_qempty + 8 * qb);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -401,14 +493,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int tid = (epi & 3) * 32 + lane;
     const int quad = warp & 3;         // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;  // key row of the tile = TMEM lane
-    int* hist = hist_all + wg * 256;
-    int acc = 0;
+    int* hist = hist_all + wg * kHistBins;
+    int acc = 0, stage = 0;
     uint32_t aphase = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const Item I = p.items[it];
-      const int qb = __ldg(p.qsl + I.r);
-      const int q_len = __ldg(p.qsl + I.r + 1) - qb;
+      const int qb0 = __ldg(p.qsl + I.r);
+      const int q_len = __ldg(p.qsl + I.r + 1) - qb0;
       const int seq_len = __ldg(p.seq_lens + I.r);
       const int nsplit = I.split >> 16;
       const int split = I.split & 0xFFFF;
@@ -420,7 +512,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (tid == 0) {
           tok[g].count = 0;
           tok[g].thr = 0u;
-          tok[g].pos = seq_len - q_len + (t - qb);
+          tok[g].pos = seq_len - q_len + (t - qb0);
           tok[g].t = t;
         }
       }
@@ -429,29 +521,27 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const int32_t* bt_row = p.block_table + (int64_t)I.r * p.max_blocks;
       for (int j = 0; j < ntiles; ++j) {
         const int key = I.k0 + j * kTileKeys + row;
-        float kscale = 0.f;
         bool kvalid = false;
         if (key < I.k1) {
           const int64_t page = __ldg(bt_row + key / kPageTokens);
-          if (page >= 0 && page < p.num_pages) {
-            kvalid = true;
-            kscale = __ldg(reinterpret_cast<const float*>(p.k_cache + page * kPageBytes +
-                                                          kPageScaleOffset) +
-                           (key % kPageTokens));
-          } else if (lane == 0) {
-            raise_status(p.status, kStatusBadPage);
-          }
+          kvalid = page >= 0 && page < p.num_pages;
+          if (!kvalid && lane == 0) raise_status(p.status, kStatusBadPage);
         }
         // no early exit on the abort flag here: all eight epilogue warps must take
         // the same branch, so they all wait on the same phase with the same limit
         if (!mbar_wait(bar_tfull + 8 * acc, aphase, nullptr)) { ok = false; break; }
         tc_fence_after();
+        const float kscale = scale_base[stage * kTileKeys + row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
+        if (++stage == p.NS) stage = 0;
         const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * p.n_max);
         for (int g = wg; g < I.gcount; g += 2) {
           const float s = relu_weighted_sum<H>(tbase + (uint32_t)(g * H), wq_all + g * H);
           const float score = s * kscale;
           const bool valid = kvalid && key <= tok[g].pos;
-          if (p.scores_out && valid && key < p.scores_ld) p.scores_out[(int64_t)tok[g].t * p.scores_ld + key] = score;
+          if (p.scores_out && valid && key < p.scores_ld)
+            p.scores_out[(int64_t)tok[g].t * p.scores_ld + key] = score;
           const uint32_t kk = valid ? score_key(score) : 0u;
           cand_append(kk, key, tok[g].thr, &tok[g], ckeys_all + (size_t)g * p.C,
                       cidx_all + (size_t)g * p.C);
@@ -471,16 +561,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       for (int g = wg; g < I.gcount; g += 2) {
         uint32_t* ck = ckeys_all + (size_t)g * p.C;
         int32_t* ci = cidx_all + (size_t)g * p.C;
-        if (tok[g].count > p.k) cand_compress(&tok[g], ck, ci, p.k, hist, misc, wg, tid);
-        const int n = min(tok[g].count, p.k);
         if (nsplit == 1) {
-          write_row(p.topk + (int64_t)tok[g].t * p.k, ci, n, p.k, tid);
+          int32_t* out_row = p.topk + (int64_t)tok[g].t * p.k;
+          const int n = cand_emit(&tok[g], ck, ci, p.k, nullptr, out_row, hist, misc, wg, tid);
+          for (int i = n + tid; i < p.k; i += 128) out_row[i] = -1;
         } else {
           const int64_t blk = (int64_t)I.cand_block + (int64_t)g * nsplit + split;
-          for (int i = tid; i < n; i += 128) {
-            p.cand_keys[blk * p.k + i] = ck[i];
-            p.cand_idx[blk * p.k + i] = ci[i];
-          }
+          const int n = cand_emit(&tok[g], ck, ci, p.k, p.cand_keys + blk * p.k,
+                                  p.cand_idx + blk * p.k, hist, misc, wg, tid);
           if (tid == 0) p.cand_count[blk] = n;
         }
       }
@@ -506,18 +594,28 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             for (int sj = 0; sj < nsplit; ++sj) {
               const int64_t blk = (int64_t)I.cand_block + (int64_t)g * nsplit + sj;
               const int nb = __ldcg(p.cand_count + blk);
-              for (int i0 = 0; i0 < nb; i0 += 128) {
-                const int i = i0 + tid;
-                const uint32_t kk = (i < nb) ? __ldcg(p.cand_keys + blk * p.k + i) : 0u;
-                const int32_t ix = (i < nb) ? __ldcg(p.cand_idx + blk * p.k + i) : -1;
-                cand_append(kk, ix, tok[g].thr, &tok[g], ck, ci);
+              const uint32_t* gk = p.cand_keys + blk * p.k;
+              const int32_t* gi = p.cand_idx + blk * p.k;
+              for (int i0 = 0; i0 < nb; i0 += kSelChunk) {
+                uint32_t kk[kSelPer];
+                int32_t ix[kSelPer];
+#pragma unroll
+                for (int u = 0; u < kSelPer; ++u) {
+                  const int i = i0 + u * 128 + tid;
+                  kk[u] = (i < nb) ? __ldcg(gk + i) : 0u;
+                  ix[u] = (i < nb) ? __ldcg(gi + i) : -1;
+                }
+                const uint32_t thr = tok[g].thr;
+#pragma unroll
+                for (int u = 0; u < kSelPer; ++u) cand_append(kk[u], ix[u], thr, &tok[g], ck, ci);
                 named_bar_sync(1 + wg, 128);
-                if (tok[g].count > p.C - kTileKeys)
+                if (tok[g].count > p.C - kSelChunk)
                   cand_compress(&tok[g], ck, ci, p.k, hist, misc, wg, tid);
               }
             }
-            if (tok[g].count > p.k) cand_compress(&tok[g], ck, ci, p.k, hist, misc, wg, tid);
-            write_row(p.topk + (int64_t)tok[g].t * p.k, ci, min(tok[g].count, p.k), p.k, tid);
+            int32_t* out_row = p.topk + (int64_t)tok[g].t * p.k;
+            const int n = cand_emit(&tok[g], ck, ci, p.k, nullptr, out_row, hist, misc, wg, tid);
+            for (int i = n + tid; i < p.k; i += 128) out_row[i] = -1;
           }
           if (epi == 0 && lane == 0) p.done[I.sgroup] = 0;  // ready for the next layer
         }
