@@ -131,6 +131,7 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   fixed += 2 * dsa::kHistBins * 4;
   fixed += up(sizeof(dsa::Misc), 16);
   fixed += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 2 * dsa::kMaxQBufs + 1) * 8;
+  fixed += dsa::kMaxStages * 4;
   const size_t per_stage = dsa::kStageBytes + dsa::kStageScaleBytes;
   const size_t budget = kSmemLimit - 1024 - 64;
   if (fixed + 2 * per_stage > budget) return false;
@@ -148,6 +149,8 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   s->offs.off_misc = (uint32_t)o;  o += up(sizeof(dsa::Misc), 16);
   s->offs.off_bar = (uint32_t)o;
   o += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 2 * dsa::kMaxQBufs + 1) * 8;
+  s->offs.off_valid = (uint32_t)o;
+  o += dsa::kMaxStages * 4;
   s->smem_bytes = o + 1024;  // slack for aligning the dynamic base to 1024
   return s->smem_bytes <= kSmemLimit;
 }

@@ -78,7 +78,7 @@ struct ScoreParams {
   int32_t* status;
   // dynamic shared memory offsets (from a 1024-aligned base)
   uint32_t off_stage, off_scale, off_q, off_ckeys, off_cidx, off_wq, off_tok, off_hist, off_misc,
-      off_bar;
+      off_bar, off_valid;
 };
 
 struct Misc {
@@ -288,16 +288,18 @@ __device__ __forceinline__ int cand_emit(TokSlot* ts, const uint32_t* ck, const 
 
 template <int H>
 __device__ __forceinline__ float relu_weighted_sum(uint32_t taddr, const float* wq) {
-  constexpr int CH = H >= 32 ? 32 : H;
+  constexpr int CH = H >= 32 ? 32 : H;              // columns per tcgen05.ld
+  constexpr int BATCH = H >= 64 ? 64 : H;           // columns loaded before one wait
   float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-  for (int c = 0; c < H; c += CH) {
-    uint32_t v[CH];
-    tmem_ld<CH>(taddr + c, v);
-    tmem_ld_wait();
-    const float4* w4 = reinterpret_cast<const float4*>(wq + c);
+  for (int c0 = 0; c0 < H; c0 += BATCH) {
+    uint32_t v[BATCH];
 #pragma unroll
-    for (int h = 0; h < CH; h += 4) {
+    for (int c = 0; c < BATCH; c += CH) tmem_ld<CH>(taddr + c0 + c, v + c);
+    tmem_ld_wait();
+    const float4* w4 = reinterpret_cast<const float4*>(wq + c0);
+#pragma unroll
+    for (int h = 0; h < BATCH; h += 4) {
       const float4 ww = w4[h >> 2];
       acc0 = fmaf(ww.x, fmaxf(__uint_as_float(v[h + 0]), 0.f), acc0);
       acc1 = fmaf(ww.y, fmaxf(__uint_as_float(v[h + 1]), 0.f), acc1);
@@ -320,6 +322,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
   uint8_t* stage_base = smem + p.off_stage;
   const float* scale_base = reinterpret_cast<const float*>(smem + p.off_scale);
+  int* stage_valid = reinterpret_cast<int*>(smem + p.off_valid);  // bit pi: page pi of the tile loaded
   uint8_t* q_base = smem + p.off_q;
   uint32_t* ckeys_all = reinterpret_cast<uint32_t*>(smem + p.off_ckeys);
   int32_t* cidx_all = reinterpret_cast<int32_t*>(smem + p.off_cidx);
@@ -372,20 +375,25 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t sphase = 0;
-      uint32_t issued_mask = 0;
-      uint32_t last_par[kMaxStages];
-      int q_last[kMaxQBufs] = {-1, -1};
-      int item_i = 0;
-      bool ok = true;
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_i) {
-        const Item I = p.items[it];
-        const int qb = item_i % p.NQ;
-        const uint32_t qpar = (uint32_t)((item_i / p.NQ) & 1);
-        if (!mbar_wait(bar_qempty + 8 * qb, qpar ^ 1, abort_flag)) { ok = false; break; }
-        q_last[qb] = item_i;
+    // The whole warp walks the tiles; lane 0 waits and issues the copies.  The
+    // page ids of 16 tiles (32 pages) come from one coalesced load, fetched one
+    // chunk ahead, so no copy waits on a block-table read.
+    int stage = 0;
+    uint32_t sphase = 0;
+    uint32_t issued_mask = 0;
+    uint32_t last_par[kMaxStages];
+    int q_last[kMaxQBufs] = {-1, -1};
+    int item_i = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_i) {
+      const Item I = p.items[it];
+      const int qb = item_i % p.NQ;
+      const uint32_t qpar = (uint32_t)((item_i / p.NQ) & 1);
+      int okv = 1;
+      if (lane == 0) okv = mbar_wait(bar_qempty + 8 * qb, qpar ^ 1, abort_flag);
+      if (!__shfl_sync(0xffffffffu, okv, 0)) { ok = false; break; }
+      q_last[qb] = item_i;
+      if (lane == 0) {
         uint8_t* q_tile = q_base + qb * p.q_bytes;
         if (p.q_box_per_token) {
           mbar_arrive_expect_tx(bar_qfull + 8 * qb, (uint32_t)(I.gcount * H * kHeadDim));
@@ -396,42 +404,65 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           mbar_arrive_expect_tx(bar_qfull + 8 * qb, (uint32_t)(p.G * H * kHeadDim));
           tma_load_2d(smem_u32(q_tile), &tm_q, 0, I.t0 * H, bar_qfull + 8 * qb);
         }
-        const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
-        const int32_t* bt_row = p.block_table + (int64_t)I.r * p.max_blocks;
-        for (int j = 0; j < ntiles; ++j) {
-          if (!mbar_wait(bar_empty + 8 * stage, sphase ^ 1, abort_flag)) { ok = false; break; }
-          const int kt = I.k0 + j * kTileKeys;
-          int64_t pg[2];
-          uint32_t bytes = 0;
-#pragma unroll
-          for (int pi = 0; pi < 2; ++pi) {
-            pg[pi] = -1;
-            const int ks = kt + pi * kPageTokens;
-            if (ks < I.k1) {
-              const int64_t page = __ldg(bt_row + ks / kPageTokens);
-              if (page >= 0 && page < p.num_pages) {
-                pg[pi] = page;
-                bytes += kPageTokens * kHeadDim + kPageTokens * 4;
+      }
+      const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
+      const int32_t* bt_row = p.block_table + (int64_t)I.r * p.max_blocks;
+      const int page0 = I.k0 / kPageTokens;
+      auto load_pages = [&](int chunk) -> int64_t {  // this lane's page of a 32-page chunk
+        const int pidx = page0 + chunk * 32 + lane;
+        int64_t page = -1;
+        if (chunk * 16 < ntiles && pidx * kPageTokens < I.k1) {
+          page = __ldg(bt_row + pidx);
+          if (page < 0 || page >= p.num_pages) page = -1;
+        }
+        return page;
+      };
+      int64_t cur = load_pages(0);
+      for (int c = 0; c * 16 < ntiles && ok; ++c) {
+        const int64_t nxt = load_pages(c + 1);
+        const int jend = min(16, ntiles - c * 16);
+        for (int jj = 0; jj < jend; ++jj) {
+          const int64_t pg0 = __shfl_sync(0xffffffffu, cur, 2 * jj);
+          const int64_t pg1 = __shfl_sync(0xffffffffu, cur, 2 * jj + 1);
+          okv = 1;
+          if (lane == 0) {
+            okv = mbar_wait(bar_empty + 8 * stage, sphase ^ 1, abort_flag);
+            if (okv) {
+              const int kt = I.k0 + (c * 16 + jj) * kTileKeys;
+              int valid = 0;
+              uint32_t bytes = 0;
+              if (pg0 >= 0) { valid |= 1; bytes += kPageTokens * (kHeadDim + 4); }
+              if (pg1 >= 0) { valid |= 2; bytes += kPageTokens * (kHeadDim + 4); }
+              // a page that holds keys of this range but has an invalid id
+              if ((pg0 < 0 && kt < I.k1) || (pg1 < 0 && kt + kPageTokens < I.k1))
+                raise_status(p.status, kStatusBadPage);
+              stage_valid[stage] = valid;
+              mbar_arrive_expect_tx(bar_full + 8 * stage, bytes);
+              const uint32_t dst = smem_u32(stage_base + stage * kStageBytes);
+              const uint32_t sdst = smem_u32(scale_base + stage * kTileKeys);
+              if (pg0 >= 0) {
+                tma_load_2d(dst, &tm_k, 0, (int32_t)(pg0 * (kPageBytes / kHeadDim)),
+                            bar_full + 8 * stage);
+                bulk_load(sdst, p.k_cache + pg0 * kPageBytes + kPageScaleOffset,
+                          kPageTokens * 4, bar_full + 8 * stage);
+              }
+              if (pg1 >= 0) {
+                tma_load_2d(dst + kPageTokens * kHeadDim, &tm_k, 0,
+                            (int32_t)(pg1 * (kPageBytes / kHeadDim)), bar_full + 8 * stage);
+                bulk_load(sdst + kPageTokens * 4, p.k_cache + pg1 * kPageBytes + kPageScaleOffset,
+                          kPageTokens * 4, bar_full + 8 * stage);
               }
             }
           }
-          mbar_arrive_expect_tx(bar_full + 8 * stage, bytes);
-          const uint32_t dst = smem_u32(stage_base + stage * kStageBytes);
-          const uint32_t sdst = smem_u32(scale_base + stage * kTileKeys);
-#pragma unroll
-          for (int pi = 0; pi < 2; ++pi)
-            if (pg[pi] >= 0) {
-              tma_load_2d(dst + pi * kPageTokens * kHeadDim, &tm_k, 0,
-                          (int32_t)(pg[pi] * (kPageBytes / kHeadDim)), bar_full + 8 * stage);
-              bulk_load(sdst + pi * kPageTokens * 4,
-                        p.k_cache + pg[pi] * kPageBytes + kPageScaleOffset, kPageTokens * 4,
-                        bar_full + 8 * stage);
-            }
+          if (!__shfl_sync(0xffffffffu, okv, 0)) { ok = false; break; }
           issued_mask |= 1u << stage;
           last_par[stage] = sphase;
           if (++stage == p.NS) { stage = 0; sphase ^= 1; }
         }
+        cur = nxt;
       }
+    }
+    if (lane == 0) {
       if (!ok) {
         *abort_flag = 1;
         raise_status(p.status, kStatusTimeout);
@@ -495,7 +526,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int row = quad * 32 + lane;  // key row of the tile = TMEM lane
     int* hist = hist_all + wg * kHistBins;
     int acc = 0, stage = 0;
-    uint32_t aphase = 0;
+    uint32_t aphase = 0, sphase = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const Item I = p.items[it];
@@ -518,23 +549,21 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
       named_bar_sync(1 + wg, 128);
       const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
-      const int32_t* bt_row = p.block_table + (int64_t)I.r * p.max_blocks;
+      // an item whose whole key range fits the buffer never needs an in-loop selection
+      const bool may_fill = (I.k1 - I.k0) > p.C - kTileKeys;
       for (int j = 0; j < ntiles; ++j) {
         const int key = I.k0 + j * kTileKeys + row;
-        bool kvalid = false;
-        if (key < I.k1) {
-          const int64_t page = __ldg(bt_row + key / kPageTokens);
-          kvalid = page >= 0 && page < p.num_pages;
-          if (!kvalid && lane == 0) raise_status(p.status, kStatusBadPage);
-        }
         // no early exit on the abort flag here: all eight epilogue warps must take
         // the same branch, so they all wait on the same phase with the same limit
         if (!mbar_wait(bar_tfull + 8 * acc, aphase, nullptr)) { ok = false; break; }
+        // the stage's copies (scales, page flags) are complete: its full phase is done
+        if (!mbar_wait(bar_full + 8 * stage, sphase, nullptr)) { ok = false; break; }
         tc_fence_after();
+        const bool kvalid = key < I.k1 && ((stage_valid[stage] >> (row >> 6)) & 1);
         const float kscale = scale_base[stage * kTileKeys + row];
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
-        if (++stage == p.NS) stage = 0;
+        if (++stage == p.NS) { stage = 0; sphase ^= 1; }
         const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * p.n_max);
         for (int g = wg; g < I.gcount; g += 2) {
           const float s = relu_weighted_sum<H>(tbase + (uint32_t)(g * H), wq_all + g * H);
@@ -550,12 +579,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
         if (++acc == p.NB) { acc = 0; aphase ^= 1; }
-        named_bar_sync(1 + wg, 128);
-        for (int g = wg; g < I.gcount; g += 2)
-          if (tok[g].count > p.C - kTileKeys)
-            cand_compress(&tok[g], ckeys_all + (size_t)g * p.C, cidx_all + (size_t)g * p.C, p.k,
-                          hist, misc, wg, tid);
+        if (may_fill) {
+          named_bar_sync(1 + wg, 128);
+          for (int g = wg; g < I.gcount; g += 2)
+            if (tok[g].count > p.C - kTileKeys)
+              cand_compress(&tok[g], ckeys_all + (size_t)g * p.C, cidx_all + (size_t)g * p.C,
+                            p.k, hist, misc, wg, tid);
+        }
       }
+      named_bar_sync(1 + wg, 128);  // every append of the item is done
       if (!ok) break;
       // finalize this item's rows
       for (int g = wg; g < I.gcount; g += 2) {
