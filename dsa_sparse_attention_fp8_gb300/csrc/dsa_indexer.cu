@@ -131,8 +131,7 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   fixed += 2 * dsa::kHistBins * 4;
   fixed += up(sizeof(dsa::Misc), 16);
   fixed += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 2 * dsa::kMaxQBufs + 1) * 8;
-  fixed += dsa::kMaxStages * 4;
-  const size_t per_stage = dsa::kStageBytes + dsa::kStageScaleBytes;
+  const size_t per_stage = dsa::kStageBytes;
   const size_t budget = kSmemLimit - 1024 - 64;
   if (fixed + 2 * per_stage > budget) return false;
   s->NS = (int)((budget - fixed) / per_stage);
@@ -140,7 +139,6 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   size_t o = 0;  // stages first: every key stage starts on a 1024-byte boundary
   s->offs.off_stage = (uint32_t)o; o += (size_t)s->NS * dsa::kStageBytes;
   s->offs.off_q = (uint32_t)o;     o += (size_t)s->NQ * s->q_bytes;
-  s->offs.off_scale = (uint32_t)o; o += (size_t)s->NS * dsa::kStageScaleBytes;
   s->offs.off_ckeys = (uint32_t)o; o += up((size_t)s->G * s->C * 4, 16);
   s->offs.off_cidx = (uint32_t)o;  o += up((size_t)s->G * s->C * 4, 16);
   s->offs.off_wq = (uint32_t)o;    o += up((size_t)s->G * H * 4, 16);
@@ -149,8 +147,6 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   s->offs.off_misc = (uint32_t)o;  o += up(sizeof(dsa::Misc), 16);
   s->offs.off_bar = (uint32_t)o;
   o += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 2 * dsa::kMaxQBufs + 1) * 8;
-  s->offs.off_valid = (uint32_t)o;
-  o += dsa::kMaxStages * 4;
   s->smem_bytes = o + 1024;  // slack for aligning the dynamic base to 1024
   return s->smem_bytes <= kSmemLimit;
 }

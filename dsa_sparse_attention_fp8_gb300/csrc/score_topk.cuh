@@ -38,7 +38,6 @@ constexpr int kScoreThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kTileKeys = 128;
 constexpr int kStageBytes = kTileKeys * kHeadDim;  // 16 KB of key rows
-constexpr int kStageScaleBytes = kTileKeys * 4;    // the tile's 128 FP32 scales
 constexpr int kMaxStages = 16;
 constexpr int kMaxAccBufs = 8;
 constexpr int kMaxQBufs = 2;
@@ -77,15 +76,14 @@ struct ScoreParams {
   int64_t scores_ld;
   int32_t* status;
   // dynamic shared memory offsets (from a 1024-aligned base)
-  uint32_t off_stage, off_scale, off_q, off_ckeys, off_cidx, off_wq, off_tok, off_hist, off_misc,
-      off_bar, off_valid;
+  uint32_t off_stage, off_q, off_ckeys, off_cidx, off_wq, off_tok, off_hist, off_misc, off_bar;
 };
 
 struct Misc {
-  int abort;
+  int abort;       // any role gave up (producer and MMA stop early on it)
   uint32_t tmem_base;
   int merge_flag;
-  int pad;
+  int epi_abort;   // an epilogue wait gave up; read by the epilogue only after barriers
   // per-warpgroup selection scratch
   int sel_bin[2], sel_above[2], sel_cnt[2], pad2[2];
   int scan[2][4];
@@ -321,8 +319,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int lane = threadIdx.x & 31;
 
   uint8_t* stage_base = smem + p.off_stage;
-  const float* scale_base = reinterpret_cast<const float*>(smem + p.off_scale);
-  int* stage_valid = reinterpret_cast<int*>(smem + p.off_valid);  // bit pi: page pi of the tile loaded
   uint8_t* q_base = smem + p.off_q;
   uint32_t* ckeys_all = reinterpret_cast<uint32_t*>(smem + p.off_ckeys);
   int32_t* cidx_all = reinterpret_cast<int32_t*>(smem + p.off_cidx);
@@ -343,12 +339,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      // a stage is free once its MMAs completed and every epilogue warp read its scales
-      mbar_init(bar_empty + 8 * s, 1 + kEpiWarps);
+      mbar_init(bar_empty + 8 * s, 1);  // freed by the MMA commit
     }
     for (int b = 0; b < p.NB; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
-      mbar_init(bar_tempty + 8 * b, kEpiWarps);
+      // decode layout: one warpgroup reads a tile; otherwise both do
+      mbar_init(bar_tempty + 8 * b, p.G == 1 ? kEpiWarps / 2 : kEpiWarps);
     }
     for (int b = 0; b < p.NQ; ++b) {
       mbar_init(bar_qfull + 8 * b, 1);
@@ -356,6 +352,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
     mbar_init(bar_drain, 1);
     misc->abort = 0;
+    misc->epi_abort = 0;
     misc->merge_flag = 0;
     fence_barrier_init();
   }
@@ -375,9 +372,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // The whole warp walks the tiles; lane 0 waits and issues the copies.  The
-    // page ids of 16 tiles (32 pages) come from one coalesced load, fetched one
-    // chunk ahead, so no copy waits on a block-table read.
+    // The whole warp walks the tiles; lane 0 waits and issues the two key-page
+    // copies of each tile (each bulk-copy issue costs the thread ~100 cycles,
+    // so nothing else is issued here).  The page ids of 16 tiles (32 pages)
+    // come from one coalesced load, fetched one chunk ahead.
     int stage = 0;
     uint32_t sphase = 0;
     uint32_t issued_mask = 0;
@@ -428,30 +426,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           if (lane == 0) {
             okv = mbar_wait(bar_empty + 8 * stage, sphase ^ 1, abort_flag);
             if (okv) {
-              const int kt = I.k0 + (c * 16 + jj) * kTileKeys;
-              int valid = 0;
-              uint32_t bytes = 0;
-              if (pg0 >= 0) { valid |= 1; bytes += kPageTokens * (kHeadDim + 4); }
-              if (pg1 >= 0) { valid |= 2; bytes += kPageTokens * (kHeadDim + 4); }
-              // a page that holds keys of this range but has an invalid id
-              if ((pg0 < 0 && kt < I.k1) || (pg1 < 0 && kt + kPageTokens < I.k1))
-                raise_status(p.status, kStatusBadPage);
-              stage_valid[stage] = valid;
+              const uint32_t bytes = (pg0 >= 0 ? kPageTokens * kHeadDim : 0) +
+                                     (pg1 >= 0 ? kPageTokens * kHeadDim : 0);
               mbar_arrive_expect_tx(bar_full + 8 * stage, bytes);
               const uint32_t dst = smem_u32(stage_base + stage * kStageBytes);
-              const uint32_t sdst = smem_u32(scale_base + stage * kTileKeys);
-              if (pg0 >= 0) {
+              if (pg0 >= 0)
                 tma_load_2d(dst, &tm_k, 0, (int32_t)(pg0 * (kPageBytes / kHeadDim)),
                             bar_full + 8 * stage);
-                bulk_load(sdst, p.k_cache + pg0 * kPageBytes + kPageScaleOffset,
-                          kPageTokens * 4, bar_full + 8 * stage);
-              }
-              if (pg1 >= 0) {
+              if (pg1 >= 0)
                 tma_load_2d(dst + kPageTokens * kHeadDim, &tm_k, 0,
                             (int32_t)(pg1 * (kPageBytes / kHeadDim)), bar_full + 8 * stage);
-                bulk_load(sdst + kPageTokens * 4, p.k_cache + pg1 * kPageBytes + kPageScaleOffset,
-                          kPageTokens * 4, bar_full + 8 * stage);
-              }
             }
           }
           if (!__shfl_sync(0xffffffffu, okv, 0)) { ok = false; break; }
@@ -519,14 +503,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Thread = one key row of a tile (its TMEM lane).  With one query row per
+    // item (decode) the two warpgroups take alternate tiles and share the
+    // row's candidate buffer; otherwise each warpgroup owns alternate rows of
+    // the group and both read every tile.  Each thread fetches its key's scale
+    // and page id itself, a few tiles ahead of use.
     const int epi = warp - 2;          // 0..7
     const int wg = epi >> 2;           // warpgroup 0/1
     const int tid = (epi & 3) * 32 + lane;
     const int quad = warp & 3;         // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;  // key row of the tile = TMEM lane
+    const bool alt = (p.G == 1);
+    const int step = alt ? 2 : 1;
     int* hist = hist_all + wg * kHistBins;
-    int acc = 0, stage = 0;
-    uint32_t aphase = 0, sphase = 0;
+    long long tile_base = 0;  // tiles of earlier items of this CTA (all roles count alike)
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const Item I = p.items[it];
@@ -535,62 +525,107 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const int seq_len = __ldg(p.seq_lens + I.r);
       const int nsplit = I.split >> 16;
       const int split = I.split & 0xFFFF;
-      // per-row setup by the owning warpgroup
-      for (int g = wg; g < I.gcount; g += 2) {
+      // per-row setup by the owning warpgroup (both share row 0 in the decode layout)
+      for (int g = alt ? 0 : wg; g < I.gcount; g += 2) {
         const int t = I.t0 + g;
-        for (int h = tid; h < H; h += 128)
-          wq_all[g * H + h] = __ldg(p.w + (int64_t)t * H + h) * __ldg(p.q_scale + (int64_t)t * H + h);
-        if (tid == 0) {
-          tok[g].count = 0;
-          tok[g].thr = 0u;
-          tok[g].pos = seq_len - q_len + (t - qb0);
-          tok[g].t = t;
+        if (!alt || wg == 0) {
+          for (int h = tid; h < H; h += 128)
+            wq_all[g * H + h] =
+                __ldg(p.w + (int64_t)t * H + h) * __ldg(p.q_scale + (int64_t)t * H + h);
+          if (tid == 0) {
+            tok[g].count = 0;
+            tok[g].thr = 0u;
+            tok[g].pos = seq_len - q_len + (t - qb0);
+            tok[g].t = t;
+          }
         }
       }
-      named_bar_sync(1 + wg, 128);
+      named_bar_sync(3, 256);
       const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
       // an item whose whole key range fits the buffer never needs an in-loop selection
-      const bool may_fill = (I.k1 - I.k0) > p.C - kTileKeys;
-      for (int j = 0; j < ntiles; ++j) {
-        const int key = I.k0 + j * kTileKeys + row;
-        // no early exit on the abort flag here: all eight epilogue warps must take
-        // the same branch, so they all wait on the same phase with the same limit
-        if (!mbar_wait(bar_tfull + 8 * acc, aphase, nullptr)) { ok = false; break; }
-        // the stage's copies (scales, page flags) are complete: its full phase is done
-        if (!mbar_wait(bar_full + 8 * stage, sphase, nullptr)) { ok = false; break; }
-        tc_fence_after();
-        const bool kvalid = key < I.k1 && ((stage_valid[stage] >> (row >> 6)) & 1);
-        const float kscale = scale_base[stage * kTileKeys + row];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
-        if (++stage == p.NS) { stage = 0; sphase ^= 1; }
-        const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * p.n_max);
-        for (int g = wg; g < I.gcount; g += 2) {
-          const float s = relu_weighted_sum<H>(tbase + (uint32_t)(g * H), wq_all + g * H);
-          const float score = s * kscale;
-          const bool valid = kvalid && key <= tok[g].pos;
-          if (p.scores_out && valid && key < p.scores_ld)
-            p.scores_out[(int64_t)tok[g].t * p.scores_ld + key] = score;
-          const uint32_t kk = valid ? score_key(score) : 0u;
-          cand_append(kk, key, tok[g].thr, &tok[g], ckeys_all + (size_t)g * p.C,
-                      cidx_all + (size_t)g * p.C);
+      const bool may_fill = (I.k1 - I.k0) > p.C - 2 * kTileKeys;
+      const int32_t* bt_row = p.block_table + (int64_t)I.r * p.max_blocks;
+      auto page_of = [&](int jj) -> int64_t {  // -1: beyond the range, -2: invalid id
+        const int key = I.k0 + jj * kTileKeys + row;
+        if (jj >= ntiles || key >= I.k1) return -1;
+        const int64_t pg = __ldg(bt_row + key / kPageTokens);
+        return (pg >= 0 && pg < p.num_pages) ? pg : -2;
+      };
+      auto scale_of = [&](int64_t pg, int jj) -> float {
+        if (pg < 0) return 0.f;
+        const int key = I.k0 + jj * kTileKeys + row;
+        return __ldg(reinterpret_cast<const float*>(p.k_cache + pg * kPageBytes +
+                                                    kPageScaleOffset) + (key % kPageTokens));
+      };
+      const int j0 = alt ? wg : 0;
+      int64_t pg0 = page_of(j0), pg1 = page_of(j0 + step), pg2 = page_of(j0 + 2 * step),
+              pg3 = page_of(j0 + 3 * step), pg4 = page_of(j0 + 4 * step);
+      float sc0 = scale_of(pg0, j0), sc1 = scale_of(pg1, j0 + step), sc2 = scale_of(pg2, j0 + 2 * step);
+      const int iters = alt ? (ntiles + 1) / 2 : ntiles;
+      for (int m = 0; m < iters; ++m) {
+        const int j = j0 + m * step;
+        // prefetch: scale three own tiles ahead, page id five ahead
+        const float sc3 = scale_of(pg3, j + 3 * step);
+        const int64_t pg5 = page_of(j + 5 * step);
+        if (j < ntiles) {
+          const long long seq = tile_base + j;
+          const int acc = (int)(seq % p.NB);
+          const uint32_t aphase = (uint32_t)((seq / p.NB) & 1);
+          const int key = I.k0 + j * kTileKeys + row;
+          const bool kvalid = pg0 >= 0;
+          if (pg0 == -2 && lane == 0) raise_status(p.status, kStatusBadPage);
+          // no early exit on the abort flag here: the warps of a warpgroup must take
+          // the same branch, so they all wait on the same phase with the same limit
+          if (!mbar_wait(bar_tfull + 8 * acc, aphase, nullptr)) ok = false;
+          if (ok) {
+            tc_fence_after();
+            const uint32_t tbase =
+                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * p.n_max);
+            for (int g = alt ? 0 : wg; g < I.gcount; g += 2) {
+              const float s = relu_weighted_sum<H>(tbase + (uint32_t)(g * H), wq_all + g * H);
+              const float score = s * sc0;
+              const bool valid = kvalid && key <= tok[g].pos;
+              if (p.scores_out && valid && key < p.scores_ld)
+                p.scores_out[(int64_t)tok[g].t * p.scores_ld + key] = score;
+              const uint32_t kk = valid ? score_key(score) : 0u;
+              cand_append(kk, key, tok[g].thr, &tok[g], ckeys_all + (size_t)g * p.C,
+                          cidx_all + (size_t)g * p.C);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+          }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
-        if (++acc == p.NB) { acc = 0; aphase ^= 1; }
-        if (may_fill) {
-          named_bar_sync(1 + wg, 128);
-          for (int g = wg; g < I.gcount; g += 2)
-            if (tok[g].count > p.C - kTileKeys)
-              cand_compress(&tok[g], ckeys_all + (size_t)g * p.C, cidx_all + (size_t)g * p.C,
-                            p.k, hist, misc, wg, tid);
+        // a timed-out wait is seen by every thread of both warpgroups before any
+        // of them reaches the next barrier
+        if (may_fill || !alt) {
+          if (!ok) misc->epi_abort = 1;
+          named_bar_sync(3, 256);
+          if (misc->epi_abort) { ok = false; break; }
+          if (may_fill) {
+            if (alt) {
+              if (wg == 0 && tok[0].count > p.C - 2 * kTileKeys)
+                cand_compress(&tok[0], ckeys_all, cidx_all, p.k, hist, misc, wg, tid);
+              named_bar_sync(3, 256);
+            } else {
+              for (int g = wg; g < I.gcount; g += 2)
+                if (tok[g].count > p.C - kTileKeys)
+                  cand_compress(&tok[g], ckeys_all + (size_t)g * p.C,
+                                cidx_all + (size_t)g * p.C, p.k, hist, misc, wg, tid);
+            }
+          }
+        } else if (!ok) {
+          misc->epi_abort = 1;
         }
+        pg0 = pg1; pg1 = pg2; pg2 = pg3; pg3 = pg4; pg4 = pg5;
+        sc0 = sc1; sc1 = sc2; sc2 = sc3;
       }
-      named_bar_sync(1 + wg, 128);  // every append of the item is done
-      if (!ok) break;
-      // finalize this item's rows
-      for (int g = wg; g < I.gcount; g += 2) {
+      tile_base += ntiles;
+      if (!ok) misc->epi_abort = 1;
+      named_bar_sync(3, 256);  // every append of the item is done
+      if (misc->epi_abort) { ok = false; break; }
+      // finalize this item's rows (warpgroup 0 alone in the decode layout)
+      for (int g = wg; g < I.gcount && (!alt || wg == 0); g += 2) {
         uint32_t* ck = ckeys_all + (size_t)g * p.C;
         int32_t* ci = cidx_all + (size_t)g * p.C;
         if (nsplit == 1) {
@@ -615,7 +650,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         named_bar_sync(3, 128 * 2);
         if (misc->merge_flag) {
           __threadfence();
-          for (int g = wg; g < I.gcount; g += 2) {
+          for (int g = wg; g < I.gcount && (!alt || wg == 0); g += 2) {
             uint32_t* ck = ckeys_all + (size_t)g * p.C;
             int32_t* ci = cidx_all + (size_t)g * p.C;
             if (tid == 0) {
@@ -651,10 +686,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           }
           if (epi == 0 && lane == 0) p.done[I.sgroup] = 0;  // ready for the next layer
         }
-        named_bar_sync(3, 128 * 2);
-      } else {
-        named_bar_sync(1 + wg, 128);
       }
+      named_bar_sync(3, 128 * 2);
     }
     if (!ok) {
       *abort_flag = 1;
