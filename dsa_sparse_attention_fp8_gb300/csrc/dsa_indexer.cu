@@ -99,6 +99,7 @@ int candidate_capacity(int k, bool decode) {
   if (decode && c < 8192) c = 8192;
   return (c + 127) / 128 * 128;
 }
+static_assert(dsa::kSelRegs * 128 >= 2048 + 1024, "a warpgroup must hold a full buffer");
 
 // Rows per group: one row per decode batch (no request has more rows than
 // one), else as many rows as fill N = 256 of the MMA while the candidate
@@ -128,7 +129,7 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   fixed += up((size_t)s->G * s->C * 4, 16) * 2;
   fixed += up((size_t)s->G * H * 4, 16);
   fixed += up((size_t)s->G * sizeof(dsa::TokSlot), 16);
-  fixed += 2 * dsa::kHistBins * 4;
+  fixed += 2 * dsa::kBins * 4;
   fixed += up(sizeof(dsa::Misc), 16);
   fixed += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 2 * dsa::kMaxQBufs + 1) * 8;
   const size_t per_stage = dsa::kStageBytes;
@@ -143,7 +144,7 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   s->offs.off_cidx = (uint32_t)o;  o += up((size_t)s->G * s->C * 4, 16);
   s->offs.off_wq = (uint32_t)o;    o += up((size_t)s->G * H * 4, 16);
   s->offs.off_tok = (uint32_t)o;   o += up((size_t)s->G * sizeof(dsa::TokSlot), 16);
-  s->offs.off_hist = (uint32_t)o;  o += 2 * dsa::kHistBins * 4;
+  s->offs.off_hist = (uint32_t)o;  o += 2 * dsa::kBins * 4;
   s->offs.off_misc = (uint32_t)o;  o += up(sizeof(dsa::Misc), 16);
   s->offs.off_bar = (uint32_t)o;
   o += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 2 * dsa::kMaxQBufs + 1) * 8;

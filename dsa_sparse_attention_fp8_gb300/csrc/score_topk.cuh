@@ -42,9 +42,7 @@ constexpr int kMaxStages = 16;
 constexpr int kMaxAccBufs = 8;
 constexpr int kMaxQBufs = 2;
 constexpr int kTmemCols = 512;
-constexpr int kSelPer = 4;                 // elements per thread per selection chunk
-constexpr int kSelChunk = 128 * kSelPer;   // one warpgroup handles 512 per chunk
-constexpr int kHistBins = 2048;            // 11-bit radix digits
+constexpr int kMergePer = 4;              // candidates per thread per merge batch
 
 struct TokSlot {
   int32_t count;   // candidates held
@@ -79,21 +77,40 @@ struct ScoreParams {
   uint32_t off_stage, off_q, off_ckeys, off_cidx, off_wq, off_tok, off_hist, off_misc, off_bar;
 };
 
+struct SelScratch {
+  int scan[8];                 // per-warp partials of a block scan (up to 256 threads)
+  int bin, above, cnt;
+  uint32_t lo, hi;
+  int pad[3];
+};
+
 struct Misc {
   int abort;       // any role gave up (producer and MMA stop early on it)
   uint32_t tmem_base;
   int merge_flag;
   int epi_abort;   // an epilogue wait gave up; read by the epilogue only after barriers
-  // per-warpgroup selection scratch
-  int sel_bin[2], sel_above[2], sel_cnt[2], pad2[2];
-  int scan[2][4];
-  int cnt_a[2][16], cnt_b[2][16];
+  SelScratch sel[2];
 };
 
+// The candidates of one query row are selected by a "selector": either one
+// warpgroup (128 threads, its own rows) or both (256 threads, the single row
+// of a decode item).  A selector names its threads, its named barrier and its
+// scratch.
+struct Selector {
+  int nt;          // threads
+  int tid;         // this thread, 0..nt-1
+  uint32_t bar;    // named barrier id
+  int* hist;       // 2048 ints
+  SelScratch* s;
+};
+
+constexpr int kSelRegs = 32;   // candidates a selector thread holds in registers
+constexpr int kBins = 2048;
+
 struct Thresh {
-  uint32_t prefix, mask;
-  int need;   // keys equal to prefix still to take (exact threshold only)
-  int early;  // 1: take every key whose masked value is >= prefix
+  uint32_t prefix;  // keys >= prefix are taken (early), or > prefix plus `need` ties (exact)
+  int need;
+  int early;
 };
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -118,170 +135,188 @@ __device__ __forceinline__ void cand_append(uint32_t key, int32_t idx, uint32_t 
   }
 }
 
-// Radix select (11-, 11-, 10-bit digits from the top) of the k-th largest key
-// among keys[0, n), n > k.  128 threads of warpgroup `wg`.  Each pass
-// histograms the keys that share the prefix fixed so far (same-bin lanes of a
-// warp are merged with match.any before one shared atomic), finds the digit
-// where the count from the top crosses k, and stops early when that bin is
-// taken whole.
-__device__ __noinline__ Thresh find_threshold(const uint32_t* keys, int n, int k, int* hist,
-                                              Misc* misc, int wg, int tid) {
-  const uint32_t bar = 1 + wg;
-  const int lane = tid & 31, w = tid >> 5;
-  Thresh th{0u, 0u, k, 0};
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const int nbins = pass == 2 ? 1024 : 2048;
-    const uint32_t dm = (uint32_t)nbins - 1u;
-    for (int b = tid; b < nbins; b += 128) hist[b] = 0;
-    named_bar_sync(bar, 128);
-    for (int base = 0; base < n; base += 128) {
-      const int i = base + tid;
-      const uint32_t key = (i < n) ? keys[i] : 0u;
-      const bool m = (i < n) && (key & th.mask) == th.prefix;
-      const uint32_t active = __ballot_sync(0xffffffffu, m);
-      if (m) {
-        const uint32_t bin = (key >> shift) & dm;
-        const uint32_t peers = __match_any_sync(active, bin);
-        if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
-      }
-    }
-    named_bar_sync(bar, 128);
-    const int per = nbins / 128;               // bins per thread, highest first
-    const int top = nbins - 1 - tid * per;
-    int local = 0;
-    for (int j = 0; j < per; ++j) local += hist[top - j];
-    int incl = local;
+// Exclusive scan of one int per selector thread; *total gets the sum.
+__device__ __forceinline__ int sel_scan(const Selector& S, int v, int* total) {
+  const int lane = S.tid & 31, w = S.tid >> 5, nw = S.nt >> 5;
+  int x = v;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) S.s->scan[w] = x;
+  named_bar_sync(S.bar, S.nt);
+  int off = 0, tot = 0;
+  for (int u = 0; u < nw; ++u) {
+    const int c = S.s->scan[u];
+    if (u < w) off += c;
+    tot += c;
+  }
+  named_bar_sync(S.bar, S.nt);
+  *total = tot;
+  return off + x - v;
+}
+
+// k-th largest key among the selector's register-held keys (0 = empty slot;
+// more than k keys in total).  Buckets are laid over [min, max] of the keys
+// still in play, 2048 per pass, so the histogram atomics of nearby lanes
+// rarely collide whatever the score distribution; each pass narrows the range
+// by 2^11 and at most three passes reach a single value.
+__device__ __forceinline__ Thresh find_threshold(const Selector& S, const uint32_t* kr, int k) {
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll
+  for (int j = 0; j < kSelRegs; ++j)
+    if (kr[j]) {
+      lo = min(lo, kr[j]);
+      hi = max(hi, kr[j]);
     }
-    if (lane == 31) misc->scan[wg][w] = incl;
-    named_bar_sync(bar, 128);
-    int above = incl - local;
-    for (int u = 0; u < w; ++u) above += misc->scan[wg][u];
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  const int lane = S.tid & 31, w = S.tid >> 5, nw = S.nt >> 5;
+  if (lane == 0) {
+    atomicMin(&S.s->lo, lo);
+    atomicMax(&S.s->hi, hi);
+  }
+  named_bar_sync(S.bar, S.nt);
+  uint32_t base = S.s->lo;
+  uint32_t range = S.s->hi - base;
+  Thresh th{0u, k, 0};
+  const int per = kBins / S.nt;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = (range >> 11) == 0u ? 0 : 32 - __clz(range >> 11);
+    for (int b = S.tid; b < kBins; b += S.nt) S.hist[b] = 0;
+    named_bar_sync(S.bar, S.nt);
+#pragma unroll
+    for (int j = 0; j < kSelRegs; ++j) {
+      const uint32_t d = kr[j] - base;
+      if (kr[j] && kr[j] >= base && d <= range) atomicAdd(&S.hist[d >> shift], 1);
+    }
+    named_bar_sync(S.bar, S.nt);
+    const int top = kBins - 1 - S.tid * per;  // this thread's bins, highest first
+    int local = 0;
+    for (int j = 0; j < per; ++j) local += S.hist[top - j];
+    int total;
+    int above = sel_scan(S, local, &total);
     if (above < th.need && th.need <= above + local) {
       for (int j = 0; j < per; ++j) {
-        const int c = hist[top - j];
+        const int c = S.hist[top - j];
         if (th.need <= above + c) {
-          misc->sel_bin[wg] = top - j;
-          misc->sel_above[wg] = above;
-          misc->sel_cnt[wg] = c;
+          S.s->bin = top - j;
+          S.s->above = above;
+          S.s->cnt = c;
           break;
         }
         above += c;
       }
     }
-    named_bar_sync(bar, 128);
-    const uint32_t b = (uint32_t)misc->sel_bin[wg];
-    th.need -= misc->sel_above[wg];
-    const int cnt = misc->sel_cnt[wg];
-    th.prefix |= b << shift;
-    th.mask |= dm << shift;
-    named_bar_sync(bar, 128);  // scratch read by all before it is rewritten
-    if (cnt == th.need) {
+    named_bar_sync(S.bar, S.nt);
+    const uint32_t b = (uint32_t)S.s->bin;
+    th.need -= S.s->above;
+    const int cnt = S.s->cnt;
+    named_bar_sync(S.bar, S.nt);  // scratch read by all before it is rewritten
+    const uint32_t nbase = base + (b << shift);
+    if (cnt == th.need) {  // the whole bin is taken: every key >= its lower edge
+      th.prefix = nbase;
       th.early = 1;
       break;
     }
+    if (shift == 0) {  // single value: the k-th key itself
+      th.prefix = nbase;
+      break;
+    }
+    const uint32_t width = (1u << shift) - 1u;
+    range = min(width, range - (b << shift));
+    base = nbase;
+  }
+  (void)w;
+  (void)nw;
+  if (S.tid == 0) {
+    S.s->lo = 0xFFFFFFFFu;  // ready for the next selection
+    S.s->hi = 0u;
   }
   return th;
 }
 
-// Copy the keys selected by `th` from keys/idx[0, n) to dkeys/didx[0, ...) in
-// scan order (deterministic; dkeys may be null; dst may alias src because an
-// element never moves to a higher position and every chunk is read before it
-// is written).  Ties at an exact threshold are taken in scan order up to the
-// quota.  Returns the number written.  128 threads of warpgroup `wg`.
-__device__ __noinline__ int compact_selected(const uint32_t* keys, const int32_t* idx, int n,
-                                             Thresh th, uint32_t* dkeys, int32_t* didx,
-                                             Misc* misc, int wg, int tid) {
-  const uint32_t bar = 1 + wg;
-  const int lane = tid & 31, w = tid >> 5;
-  const uint32_t lt = lanemask_lt();
-  const int quota = th.early ? 0 : th.need;
-  int out = 0, ties = 0;
-  for (int base = 0; base < n; base += kSelChunk) {
-    uint32_t key[kSelPer];
-    int32_t ix[kSelPer];
-    bool def[kSelPer], tie[kSelPer];
-    uint32_t bt[kSelPer];
+// Write the selected keys (th) of the selector's registers kr (with their
+// indices from idx_src[tid + nt*j]) to dkeys/didx[0, ...), in (register,
+// thread) order: deterministic.  Ties at an exact threshold are taken in that
+// order up to the quota.  dst may alias the source buffers.  Returns the
+// number written (k, or all keys when th takes everything).
+__device__ __forceinline__ int compact_selected(const Selector& S, const uint32_t* kr,
+                                             const int32_t* idx_src, Thresh th, uint32_t* dkeys,
+                                             int32_t* didx) {
+  int nsel = 0, ntie = 0;
 #pragma unroll
-    for (int u = 0; u < kSelPer; ++u) {
-      const int i = base + u * 128 + tid;
-      const bool valid = i < n;
-      key[u] = valid ? keys[i] : 0u;
-      ix[u] = valid ? idx[i] : 0;
-      def[u] = valid && (th.early ? (key[u] & th.mask) >= th.prefix : key[u] > th.prefix);
-      tie[u] = valid && !th.early && key[u] == th.prefix;
-      bt[u] = __ballot_sync(0xffffffffu, tie[u]);
-      if (lane == 0) misc->cnt_a[wg][u * 4 + w] = __popc(bt[u]);
-    }
-    named_bar_sync(bar, 128);  // every read of this chunk is done
-    int pre_a[kSelPer], tot_a = 0;
-#pragma unroll
-    for (int u = 0; u < kSelPer; ++u) {
-      int p = tot_a;
-      for (int v = 0; v < 4; ++v) {
-        const int c = misc->cnt_a[wg][u * 4 + v];
-        if (v < w) p += c;
-        tot_a += c;
-      }
-      pre_a[u] = p;
-    }
-    uint32_t bs[kSelPer];
-    bool sel[kSelPer];
-#pragma unroll
-    for (int u = 0; u < kSelPer; ++u) {
-      const int trank = ties + pre_a[u] + __popc(bt[u] & lt);
-      sel[u] = def[u] || (tie[u] && trank < quota);
-      bs[u] = __ballot_sync(0xffffffffu, sel[u]);
-      if (lane == 0) misc->cnt_b[wg][u * 4 + w] = __popc(bs[u]);
-    }
-    named_bar_sync(bar, 128);
-    int tot_b = 0;
-#pragma unroll
-    for (int u = 0; u < kSelPer; ++u) {
-      int p = tot_b;
-      for (int v = 0; v < 4; ++v) {
-        const int c = misc->cnt_b[wg][u * 4 + v];
-        if (v < w) p += c;
-        tot_b += c;
-      }
-      if (sel[u]) {
-        const int q = out + p + __popc(bs[u] & lt);
-        if (dkeys) dkeys[q] = key[u];
-        didx[q] = ix[u];
-      }
-    }
-    out += tot_b;
-    ties += tot_a;
-    named_bar_sync(bar, 128);  // counters are rewritten by the next chunk
+  for (int j = 0; j < kSelRegs; ++j) {
+    const uint32_t key = kr[j];
+    if (!key) continue;
+    if (th.early ? key >= th.prefix : key > th.prefix) ++nsel;
+    else if (!th.early && key == th.prefix) ++ntie;
   }
-  return out;
+  int tie_tot;
+  const int tie_off = sel_scan(S, ntie, &tie_tot);
+  const int quota = th.early ? 0 : th.need;
+  int take = quota - tie_off;
+  take = take < 0 ? 0 : (take > ntie ? ntie : take);
+  int total;
+  int pos = sel_scan(S, nsel + take, &total);
+  int32_t ix[kSelRegs];
+#pragma unroll
+  for (int j = 0; j < kSelRegs; ++j) ix[j] = kr[j] ? idx_src[S.tid + S.nt * j] : 0;
+  named_bar_sync(S.bar, S.nt);  // every source index is read before any write
+  int ties = 0;
+#pragma unroll
+  for (int j = 0; j < kSelRegs; ++j) {
+    const uint32_t key = kr[j];
+    if (!key) continue;
+    bool sel = th.early ? key >= th.prefix : key > th.prefix;
+    if (!sel && !th.early && key == th.prefix && ties < take) {
+      sel = true;
+      ++ties;
+    }
+    if (sel) {
+      if (dkeys) dkeys[pos] = key;
+      didx[pos] = ix[j];
+      ++pos;
+    }
+  }
+  named_bar_sync(S.bar, S.nt);
+  return total;
+}
+
+__device__ __forceinline__ void load_regs(const Selector& S, const uint32_t* ck, int n,
+                                          uint32_t* kr) {
+#pragma unroll
+  for (int j = 0; j < kSelRegs; ++j) {
+    const int i = S.tid + S.nt * j;
+    kr[j] = (i < n) ? ck[i] : 0u;
+  }
 }
 
 // Keep the k largest of the slot's candidates (in place) and raise its threshold.
-__device__ __forceinline__ void cand_compress(TokSlot* ts, uint32_t* ck, int32_t* ci, int k,
-                                              int* hist, Misc* misc, int wg, int tid) {
+__device__ __noinline__ void cand_compress(const Selector& S, TokSlot* ts, uint32_t* ck,
+                                           int32_t* ci, int k) {
+  uint32_t kr[kSelRegs];
   const int n = ts->count;
-  const Thresh th = find_threshold(ck, n, k, hist, misc, wg, tid);
-  compact_selected(ck, ci, n, th, ck, ci, misc, wg, tid);
-  if (tid == 0) {
+  load_regs(S, ck, n, kr);
+  const Thresh th = find_threshold(S, kr, k);
+  compact_selected(S, kr, ci, th, ck, ci);
+  if (S.tid == 0) {
     ts->count = k;
     ts->thr = th.prefix;
   }
-  named_bar_sync(1 + wg, 128);
+  named_bar_sync(S.bar, S.nt);
 }
 
 // Emit min(count, k) selected candidates of a slot to global memory; returns how many.
-__device__ __forceinline__ int cand_emit(TokSlot* ts, const uint32_t* ck, const int32_t* ci,
-                                        int k, uint32_t* dkeys, int32_t* didx, int* hist,
-                                        Misc* misc, int wg, int tid) {
+__device__ __noinline__ int cand_emit(const Selector& S, TokSlot* ts, const uint32_t* ck,
+                                      const int32_t* ci, int k, uint32_t* dkeys, int32_t* didx) {
+  uint32_t kr[kSelRegs];
   const int n = ts->count;
-  Thresh th{0u, 0u, 0, 1};  // everything
-  if (n > k) th = find_threshold(ck, n, k, hist, misc, wg, tid);
-  return compact_selected(ck, ci, n, th, dkeys, didx, misc, wg, tid);
+  load_regs(S, ck, n, kr);
+  Thresh th{0u, 0, 1};  // everything
+  if (n > k) th = find_threshold(S, kr, k);
+  return compact_selected(S, kr, ci, th, dkeys, didx);
 }
 
 template <int H>
@@ -354,6 +389,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     misc->abort = 0;
     misc->epi_abort = 0;
     misc->merge_flag = 0;
+    for (int i = 0; i < 2; ++i) {
+      misc->sel[i].lo = 0xFFFFFFFFu;
+      misc->sel[i].hi = 0u;
+    }
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -515,7 +554,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int row = quad * 32 + lane;  // key row of the tile = TMEM lane
     const bool alt = (p.G == 1);
     const int step = alt ? 2 : 1;
-    int* hist = hist_all + wg * kHistBins;
+    // who selects a row's candidates: both warpgroups for a decode row, else its warpgroup
+    const Selector S = alt ? Selector{256, epi * 32 + lane, 3u, hist_all, &misc->sel[0]}
+                           : Selector{128, tid, 1u + wg, hist_all + wg * kBins, &misc->sel[wg]};
+    // buffer-fill checks every `chk` iterations, leaving room for what they append
+    const int chk = alt ? 8 : 4;
+    const int headroom = chk * kTileKeys * (alt ? 2 : 1);
     long long tile_base = 0;  // tiles of earlier items of this CTA (all roles count alike)
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -525,8 +569,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const int seq_len = __ldg(p.seq_lens + I.r);
       const int nsplit = I.split >> 16;
       const int split = I.split & 0xFFFF;
-      // per-row setup by the owning warpgroup (both share row 0 in the decode layout)
-      for (int g = alt ? 0 : wg; g < I.gcount; g += 2) {
+      const int g_first = alt ? 0 : wg;  // this thread's rows: g_first, g_first + 2, ...
+      // per-row setup (warpgroup 0 for the shared decode row)
+      for (int g = g_first; g < I.gcount; g += 2) {
         const int t = I.t0 + g;
         if (!alt || wg == 0) {
           for (int h = tid; h < H; h += 128)
@@ -542,8 +587,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
       named_bar_sync(3, 256);
       const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
-      // an item whose whole key range fits the buffer never needs an in-loop selection
-      const bool may_fill = (I.k1 - I.k0) > p.C - 2 * kTileKeys;
+      const bool may_fill = (I.k1 - I.k0) > p.C;
       const int32_t* bt_row = p.block_table + (int64_t)I.r * p.max_blocks;
       auto page_of = [&](int jj) -> int64_t {  // -1: beyond the range, -2: invalid id
         const int key = I.k0 + jj * kTileKeys + row;
@@ -567,7 +611,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         // prefetch: scale three own tiles ahead, page id five ahead
         const float sc3 = scale_of(pg3, j + 3 * step);
         const int64_t pg5 = page_of(j + 5 * step);
-        if (j < ntiles) {
+        if (j < ntiles && ok) {
           const long long seq = tile_base + j;
           const int acc = (int)(seq % p.NB);
           const uint32_t aphase = (uint32_t)((seq / p.NB) & 1);
@@ -581,7 +625,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             tc_fence_after();
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * p.n_max);
-            for (int g = alt ? 0 : wg; g < I.gcount; g += 2) {
+            for (int g = g_first; g < I.gcount; g += 2) {
               const float s = relu_weighted_sum<H>(tbase + (uint32_t)(g * H), wq_all + g * H);
               const float score = s * sc0;
               const bool valid = kvalid && key <= tok[g].pos;
@@ -596,26 +640,18 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
           }
         }
-        // a timed-out wait is seen by every thread of both warpgroups before any
-        // of them reaches the next barrier
-        if (may_fill || !alt) {
+        if (may_fill && (m % chk) == chk - 1 && m + 1 < iters) {
           if (!ok) misc->epi_abort = 1;
-          named_bar_sync(3, 256);
-          if (misc->epi_abort) { ok = false; break; }
-          if (may_fill) {
-            if (alt) {
-              if (wg == 0 && tok[0].count > p.C - 2 * kTileKeys)
-                cand_compress(&tok[0], ckeys_all, cidx_all, p.k, hist, misc, wg, tid);
-              named_bar_sync(3, 256);
-            } else {
-              for (int g = wg; g < I.gcount; g += 2)
-                if (tok[g].count > p.C - kTileKeys)
-                  cand_compress(&tok[g], ckeys_all + (size_t)g * p.C,
-                                cidx_all + (size_t)g * p.C, p.k, hist, misc, wg, tid);
-            }
+          named_bar_sync(3, 256);  // every append so far is visible
+          if (misc->epi_abort) {
+            ok = false;
+          } else {
+            for (int g = g_first; g < I.gcount; g += 2)
+              if (tok[g].count > p.C - headroom)
+                cand_compress(S, &tok[g], ckeys_all + (size_t)g * p.C, cidx_all + (size_t)g * p.C,
+                              p.k);
           }
-        } else if (!ok) {
-          misc->epi_abort = 1;
+          named_bar_sync(3, 256);
         }
         pg0 = pg1; pg1 = pg2; pg2 = pg3; pg3 = pg4; pg4 = pg5;
         sc0 = sc1; sc1 = sc2; sc2 = sc3;
@@ -624,70 +660,70 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (!ok) misc->epi_abort = 1;
       named_bar_sync(3, 256);  // every append of the item is done
       if (misc->epi_abort) { ok = false; break; }
-      // finalize this item's rows (warpgroup 0 alone in the decode layout)
-      for (int g = wg; g < I.gcount && (!alt || wg == 0); g += 2) {
+      // finalize this item's rows
+      for (int g = g_first; g < I.gcount; g += 2) {
         uint32_t* ck = ckeys_all + (size_t)g * p.C;
         int32_t* ci = cidx_all + (size_t)g * p.C;
         if (nsplit == 1) {
           int32_t* out_row = p.topk + (int64_t)tok[g].t * p.k;
-          const int n = cand_emit(&tok[g], ck, ci, p.k, nullptr, out_row, hist, misc, wg, tid);
-          for (int i = n + tid; i < p.k; i += 128) out_row[i] = -1;
+          const int n = cand_emit(S, &tok[g], ck, ci, p.k, nullptr, out_row);
+          for (int i = n + S.tid; i < p.k; i += S.nt) out_row[i] = -1;
         } else {
           const int64_t blk = (int64_t)I.cand_block + (int64_t)g * nsplit + split;
-          const int n = cand_emit(&tok[g], ck, ci, p.k, p.cand_keys + blk * p.k,
-                                  p.cand_idx + blk * p.k, hist, misc, wg, tid);
-          if (tid == 0) p.cand_count[blk] = n;
+          const int n = cand_emit(S, &tok[g], ck, ci, p.k, p.cand_keys + blk * p.k,
+                                  p.cand_idx + blk * p.k);
+          if (S.tid == 0) p.cand_count[blk] = n;
         }
       }
       if (nsplit > 1) {
         // last split of the group to finish merges the candidates of all splits
         __threadfence();
-        named_bar_sync(3, 128 * 2);
+        named_bar_sync(3, 256);
         if (epi == 0 && lane == 0) {
           const int prev = atomicAdd(p.done + I.sgroup, 1);
           misc->merge_flag = (prev == nsplit - 1);
         }
-        named_bar_sync(3, 128 * 2);
+        named_bar_sync(3, 256);
         if (misc->merge_flag) {
           __threadfence();
-          for (int g = wg; g < I.gcount && (!alt || wg == 0); g += 2) {
+          const int batch = S.nt * kMergePer;
+          for (int g = g_first; g < I.gcount; g += 2) {
             uint32_t* ck = ckeys_all + (size_t)g * p.C;
             int32_t* ci = cidx_all + (size_t)g * p.C;
-            if (tid == 0) {
+            if (S.tid == 0) {
               tok[g].count = 0;
               tok[g].thr = 0u;
             }
-            named_bar_sync(1 + wg, 128);
+            named_bar_sync(S.bar, S.nt);
             for (int sj = 0; sj < nsplit; ++sj) {
               const int64_t blk = (int64_t)I.cand_block + (int64_t)g * nsplit + sj;
               const int nb = __ldcg(p.cand_count + blk);
               const uint32_t* gk = p.cand_keys + blk * p.k;
               const int32_t* gi = p.cand_idx + blk * p.k;
-              for (int i0 = 0; i0 < nb; i0 += kSelChunk) {
-                uint32_t kk[kSelPer];
-                int32_t ix[kSelPer];
+              for (int i0 = 0; i0 < nb; i0 += batch) {
+                uint32_t kk[kMergePer];
+                int32_t ix[kMergePer];
 #pragma unroll
-                for (int u = 0; u < kSelPer; ++u) {
-                  const int i = i0 + u * 128 + tid;
+                for (int u = 0; u < kMergePer; ++u) {
+                  const int i = i0 + u * S.nt + S.tid;
                   kk[u] = (i < nb) ? __ldcg(gk + i) : 0u;
                   ix[u] = (i < nb) ? __ldcg(gi + i) : -1;
                 }
                 const uint32_t thr = tok[g].thr;
 #pragma unroll
-                for (int u = 0; u < kSelPer; ++u) cand_append(kk[u], ix[u], thr, &tok[g], ck, ci);
-                named_bar_sync(1 + wg, 128);
-                if (tok[g].count > p.C - kSelChunk)
-                  cand_compress(&tok[g], ck, ci, p.k, hist, misc, wg, tid);
+                for (int u = 0; u < kMergePer; ++u) cand_append(kk[u], ix[u], thr, &tok[g], ck, ci);
+                named_bar_sync(S.bar, S.nt);
+                if (tok[g].count > p.C - batch) cand_compress(S, &tok[g], ck, ci, p.k);
               }
             }
             int32_t* out_row = p.topk + (int64_t)tok[g].t * p.k;
-            const int n = cand_emit(&tok[g], ck, ci, p.k, nullptr, out_row, hist, misc, wg, tid);
-            for (int i = n + tid; i < p.k; i += 128) out_row[i] = -1;
+            const int n = cand_emit(S, &tok[g], ck, ci, p.k, nullptr, out_row);
+            for (int i = n + S.tid; i < p.k; i += S.nt) out_row[i] = -1;
           }
           if (epi == 0 && lane == 0) p.done[I.sgroup] = 0;  // ready for the next layer
         }
       }
-      named_bar_sync(3, 128 * 2);
+      named_bar_sync(3, 256);
     }
     if (!ok) {
       *abort_flag = 1;
