@@ -126,7 +126,7 @@ __device__ __forceinline__ void cand_append(uint32_t key, int32_t idx, uint32_t 
   const uint32_t m = __ballot_sync(0xffffffffu, pass);
   if (m == 0) return;
   int base = 0;
-  if (lane_id() == 0) base = atomicAdd(&ts->count, __popc(m));
+  if (lane_id() == 0) base = (int)atom_add_shared(smem_u32(&ts->count), (uint32_t)__popc(m));
   base = __shfl_sync(0xffffffffu, base, 0);
   if (pass) {
     const int p = base + __popc(m & lanemask_lt());
@@ -174,8 +174,8 @@ __device__ __forceinline__ Thresh find_threshold(const Selector& S, const uint32
   hi = __reduce_max_sync(0xffffffffu, hi);
   const int lane = S.tid & 31, w = S.tid >> 5, nw = S.nt >> 5;
   if (lane == 0) {
-    atomicMin(&S.s->lo, lo);
-    atomicMax(&S.s->hi, hi);
+    red_min_shared(smem_u32(&S.s->lo), lo);
+    red_max_shared(smem_u32(&S.s->hi), hi);
   }
   named_bar_sync(S.bar, S.nt);
   uint32_t base = S.s->lo;
@@ -184,22 +184,23 @@ __device__ __forceinline__ Thresh find_threshold(const Selector& S, const uint32
   const int per = kBins / S.nt;
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = (range >> 11) == 0u ? 0 : 32 - __clz(range >> 11);
-    for (int b = S.tid; b < kBins; b += S.nt) S.hist[b] = 0;
+    const uint32_t hist_s = smem_u32(S.hist);
+    for (int b = S.tid; b < kBins; b += S.nt) sts_u32(hist_s + 4 * b, 0u);
     named_bar_sync(S.bar, S.nt);
 #pragma unroll
     for (int j = 0; j < kSelRegs; ++j) {
       const uint32_t d = kr[j] - base;
-      if (kr[j] && kr[j] >= base && d <= range) atomicAdd(&S.hist[d >> shift], 1);
+      if (kr[j] && kr[j] >= base && d <= range) red_add_shared(hist_s + 4 * (d >> shift), 1u);
     }
     named_bar_sync(S.bar, S.nt);
     const int top = kBins - 1 - S.tid * per;  // this thread's bins, highest first
     int local = 0;
-    for (int j = 0; j < per; ++j) local += S.hist[top - j];
+    for (int j = 0; j < per; ++j) local += (int)lds_u32(hist_s + 4 * (top - j));
     int total;
     int above = sel_scan(S, local, &total);
     if (above < th.need && th.need <= above + local) {
       for (int j = 0; j < per; ++j) {
-        const int c = S.hist[top - j];
+        const int c = (int)lds_u32(hist_s + 4 * (top - j));
         if (th.need <= above + c) {
           S.s->bin = top - j;
           S.s->above = above;
@@ -261,8 +262,9 @@ __device__ __forceinline__ int compact_selected(const Selector& S, const uint32_
   int total;
   int pos = sel_scan(S, nsel + take, &total);
   int32_t ix[kSelRegs];
+  const uint32_t ia = smem_u32(idx_src);
 #pragma unroll
-  for (int j = 0; j < kSelRegs; ++j) ix[j] = kr[j] ? idx_src[S.tid + S.nt * j] : 0;
+  for (int j = 0; j < kSelRegs; ++j) ix[j] = kr[j] ? (int32_t)lds_u32(ia + 4 * (S.tid + S.nt * j)) : 0;
   named_bar_sync(S.bar, S.nt);  // every source index is read before any write
   int ties = 0;
 #pragma unroll
@@ -286,10 +288,11 @@ __device__ __forceinline__ int compact_selected(const Selector& S, const uint32_
 
 __device__ __forceinline__ void load_regs(const Selector& S, const uint32_t* ck, int n,
                                           uint32_t* kr) {
+  const uint32_t a = smem_u32(ck);
 #pragma unroll
   for (int j = 0; j < kSelRegs; ++j) {
     const int i = S.tid + S.nt * j;
-    kr[j] = (i < n) ? ck[i] : 0u;
+    kr[j] = (i < n) ? lds_u32(a + 4 * i) : 0u;
   }
 }
 
@@ -348,8 +351,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     score_topk_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_q, const ScoreParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // align to 1024 by pointer arithmetic on the shared array itself, so the
+  // compiler keeps every access below in the shared address space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
