@@ -129,7 +129,7 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   fixed += up((size_t)s->G * s->C * 4, 16) * 2;
   fixed += up((size_t)s->G * H * 4, 16);
   fixed += up((size_t)s->G * sizeof(dsa::TokSlot), 16);
-  fixed += 2 * dsa::kBins * 4;
+  fixed += (size_t)s->G * dsa::kBins * 4;
   fixed += up(sizeof(dsa::Misc), 16);
   fixed += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 2 * dsa::kMaxQBufs + 1) * 8;
   const size_t per_stage = dsa::kStageBytes;
@@ -144,7 +144,7 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   s->offs.off_cidx = (uint32_t)o;  o += up((size_t)s->G * s->C * 4, 16);
   s->offs.off_wq = (uint32_t)o;    o += up((size_t)s->G * H * 4, 16);
   s->offs.off_tok = (uint32_t)o;   o += up((size_t)s->G * sizeof(dsa::TokSlot), 16);
-  s->offs.off_hist = (uint32_t)o;  o += 2 * dsa::kBins * 4;
+  s->offs.off_hist = (uint32_t)o;  o += (size_t)s->G * dsa::kBins * 4;
   s->offs.off_misc = (uint32_t)o;  o += up(sizeof(dsa::Misc), 16);
   s->offs.off_bar = (uint32_t)o;
   o += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 2 * dsa::kMaxQBufs + 1) * 8;

@@ -19,7 +19,7 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
   uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
 __device__ __forceinline__ void sts_u32(uint32_t a, uint32_t v) {
@@ -32,6 +32,22 @@ __device__ __forceinline__ uint32_t atom_add_shared(uint32_t a, uint32_t v) {
   uint32_t r;
   asm volatile("atom.shared.add.u32 %0, [%1], %2;" : "=r"(r) : "r"(a), "r"(v) : "memory");
   return r;
+}
+// Predicated forms: no branch around the access, so an unrolled loop of them
+// does not diverge per element.
+__device__ __forceinline__ void red_add_shared_if(bool pred, uint32_t a, uint32_t v) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p red.shared.add.u32 [%0], %1;\n\t}" ::"r"(a),
+      "r"(v), "r"((uint32_t)pred)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t lds_u32_if(bool pred, uint32_t a) {
+  uint32_t v;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\tmov.u32 %0, 0;\n\t@p ld.shared.u32 %0, [%1];\n\t}"
+      : "=r"(v)
+      : "r"(a), "r"((uint32_t)pred));
+  return v;
 }
 __device__ __forceinline__ void red_min_shared(uint32_t a, uint32_t v) {
   asm volatile("red.shared.min.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");

@@ -100,7 +100,7 @@ struct Selector {
   int nt;          // threads
   int tid;         // this thread, 0..nt-1
   uint32_t bar;    // named barrier id
-  int* hist;       // 2048 ints
+  int* unused;
   SelScratch* s;
 };
 
@@ -119,24 +119,8 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-// Append one candidate per thread of a warp if its key beats the threshold.
-__device__ __forceinline__ void cand_append(uint32_t key, int32_t idx, uint32_t thr,
-                                            TokSlot* ts, uint32_t* ckeys, int32_t* cidx) {
-  const bool pass = key > thr;
-  const uint32_t m = __ballot_sync(0xffffffffu, pass);
-  if (m == 0) return;
-  int base = 0;
-  if (lane_id() == 0) base = (int)atom_add_shared(smem_u32(&ts->count), (uint32_t)__popc(m));
-  base = __shfl_sync(0xffffffffu, base, 0);
-  if (pass) {
-    const int p = base + __popc(m & lanemask_lt());
-    ckeys[p] = key;
-    cidx[p] = idx;
-  }
-}
-
 // Exclusive scan of one int per selector thread; *total gets the sum.
-__device__ __forceinline__ int sel_scan(const Selector& S, int v, int* total) {
+__device__ __forceinline__ int sel_scan(const Selector S, int v, int* total) {
   const int lane = S.tid & 31, w = S.tid >> 5, nw = S.nt >> 5;
   int x = v;
 #pragma unroll
@@ -157,102 +141,94 @@ __device__ __forceinline__ int sel_scan(const Selector& S, int v, int* total) {
   return off + x - v;
 }
 
-// k-th largest key among the selector's register-held keys (0 = empty slot;
-// more than k keys in total).  Buckets are laid over [min, max] of the keys
-// still in play, 2048 per pass, so the histogram atomics of nearby lanes
-// rarely collide whatever the score distribution; each pass narrows the range
-// by 2^11 and at most three passes reach a single value.
-__device__ __forceinline__ Thresh find_threshold(const Selector& S, const uint32_t* kr, int k) {
-  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+constexpr int kHistShift = 21;  // level-1 bin of a key: its top 11 bits (sign, exponent, 2 mantissa)
+
+struct BinCut {
+  int bin;    // the bin holding the need-th largest key
+  int above;  // keys in higher bins
+  int cnt;    // keys in that bin
+};
+
+// Walk a 2048-bin histogram (shared memory) from the top; find the bin where
+// the running count reaches `need`.  Every selector thread gets the result.
+__device__ __forceinline__ BinCut find_bin(const Selector S, uint32_t hist_s, int need) {
+  const int per = kBins / S.nt;               // 8 or 16 bins per thread, highest first
+  const int top = kBins - 1 - S.tid * per;
+  uint32_t hv[kBins / 128];
 #pragma unroll
-  for (int j = 0; j < kSelRegs; ++j)
-    if (kr[j]) {
-      lo = min(lo, kr[j]);
-      hi = max(hi, kr[j]);
+  for (int j = 0; j < kBins / 128; ++j) hv[j] = lds_u32_if(j < per, hist_s + 4 * (top - j));
+  int local = 0;
+#pragma unroll
+  for (int j = 0; j < kBins / 128; ++j) local += (int)hv[j];
+  int total;
+  int above = sel_scan(S, local, &total);
+  if (above < need && need <= above + local) {
+    for (int j = 0; j < per; ++j) {
+      const int c = (int)hv[j];
+      if (need <= above + c) {
+        S.s->bin = top - j;
+        S.s->above = above;
+        S.s->cnt = c;
+        break;
+      }
+      above += c;
     }
-  lo = __reduce_min_sync(0xffffffffu, lo);
-  hi = __reduce_max_sync(0xffffffffu, hi);
-  const int lane = S.tid & 31, w = S.tid >> 5, nw = S.nt >> 5;
-  if (lane == 0) {
-    red_min_shared(smem_u32(&S.s->lo), lo);
-    red_max_shared(smem_u32(&S.s->hi), hi);
   }
   named_bar_sync(S.bar, S.nt);
-  uint32_t base = S.s->lo;
-  uint32_t range = S.s->hi - base;
-  Thresh th{0u, k, 0};
-  const int per = kBins / S.nt;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = (range >> 11) == 0u ? 0 : 32 - __clz(range >> 11);
-    const uint32_t hist_s = smem_u32(S.hist);
-    for (int b = S.tid; b < kBins; b += S.nt) sts_u32(hist_s + 4 * b, 0u);
+  const BinCut r{S.s->bin, S.s->above, S.s->cnt};
+  named_bar_sync(S.bar, S.nt);
+  return r;
+}
+
+// Exact threshold of the k-th largest register-held key, starting from the
+// level-1 bin cut `c` (taken from the incremental histogram): refine inside
+// that bin on key bits 20..10, then 9..0, using scratch_s (2048 ints of
+// shared memory) for the sub-histograms.  Stops as soon as a whole sub-bin is
+// taken.
+__device__ __forceinline__ Thresh refine_in_bin(const Selector S, const uint32_t* kr, BinCut c,
+                                                int k, uint32_t scratch_s) {
+  Thresh th{(uint32_t)c.bin << kHistShift, k - c.above, 0};
+  uint32_t mask = 0xFFFFFFFFu << kHistShift;
+  if (c.cnt == th.need) {
+    th.early = 1;
+    return th;
+  }
+  for (int level = 0; level < 2; ++level) {
+    const int shift = level == 0 ? 10 : 0;
+    const uint32_t dm = level == 0 ? 2047u : 1023u;
+    for (int b = S.tid; b < kBins; b += S.nt) sts_u32(scratch_s + 4 * b, 0u);
     named_bar_sync(S.bar, S.nt);
 #pragma unroll
-    for (int j = 0; j < kSelRegs; ++j) {
-      const uint32_t d = kr[j] - base;
-      if (kr[j] && kr[j] >= base && d <= range) red_add_shared(hist_s + 4 * (d >> shift), 1u);
-    }
+    for (int j = 0; j < kSelRegs; ++j)
+      red_add_shared_if(kr[j] != 0u && (kr[j] & mask) == th.prefix,
+                        scratch_s + 4 * ((kr[j] >> shift) & dm), 1u);
     named_bar_sync(S.bar, S.nt);
-    const int top = kBins - 1 - S.tid * per;  // this thread's bins, highest first
-    int local = 0;
-    for (int j = 0; j < per; ++j) local += (int)lds_u32(hist_s + 4 * (top - j));
-    int total;
-    int above = sel_scan(S, local, &total);
-    if (above < th.need && th.need <= above + local) {
-      for (int j = 0; j < per; ++j) {
-        const int c = (int)lds_u32(hist_s + 4 * (top - j));
-        if (th.need <= above + c) {
-          S.s->bin = top - j;
-          S.s->above = above;
-          S.s->cnt = c;
-          break;
-        }
-        above += c;
-      }
-    }
-    named_bar_sync(S.bar, S.nt);
-    const uint32_t b = (uint32_t)S.s->bin;
-    th.need -= S.s->above;
-    const int cnt = S.s->cnt;
-    named_bar_sync(S.bar, S.nt);  // scratch read by all before it is rewritten
-    const uint32_t nbase = base + (b << shift);
-    if (cnt == th.need) {  // the whole bin is taken: every key >= its lower edge
-      th.prefix = nbase;
+    const BinCut c2 = find_bin(S, scratch_s, th.need);
+    th.need -= c2.above;
+    th.prefix |= (uint32_t)c2.bin << shift;
+    mask |= dm << shift;
+    if (c2.cnt == th.need) {
       th.early = 1;
       break;
     }
-    if (shift == 0) {  // single value: the k-th key itself
-      th.prefix = nbase;
-      break;
-    }
-    const uint32_t width = (1u << shift) - 1u;
-    range = min(width, range - (b << shift));
-    base = nbase;
-  }
-  (void)w;
-  (void)nw;
-  if (S.tid == 0) {
-    S.s->lo = 0xFFFFFFFFu;  // ready for the next selection
-    S.s->hi = 0u;
   }
   return th;
 }
 
 // Write the selected keys (th) of the selector's registers kr (with their
-// indices from idx_src[tid + nt*j]) to dkeys/didx[0, ...), in (register,
-// thread) order: deterministic.  Ties at an exact threshold are taken in that
-// order up to the quota.  dst may alias the source buffers.  Returns the
-// number written (k, or all keys when th takes everything).
-__device__ __forceinline__ int compact_selected(const Selector& S, const uint32_t* kr,
-                                             const int32_t* idx_src, Thresh th, uint32_t* dkeys,
-                                             int32_t* didx) {
+// indices from idx_src[tid + nt*j]) to dkeys/didx[0, ...), in (thread,
+// register) order: deterministic.  Ties at an exact threshold are taken in
+// that order up to the quota.  dst may alias the source buffers (everything is
+// read before anything is written).  Returns the number written.
+__device__ __forceinline__ int compact_selected(const Selector S, const uint32_t* kr,
+                                                const int32_t* idx_src, Thresh th,
+                                                uint32_t* dkeys, int32_t* didx) {
   int nsel = 0, ntie = 0;
 #pragma unroll
   for (int j = 0; j < kSelRegs; ++j) {
     const uint32_t key = kr[j];
-    if (!key) continue;
-    if (th.early ? key >= th.prefix : key > th.prefix) ++nsel;
-    else if (!th.early && key == th.prefix) ++ntie;
+    nsel += (key != 0u && (th.early ? key >= th.prefix : key > th.prefix)) ? 1 : 0;
+    ntie += (key != 0u && !th.early && key == th.prefix) ? 1 : 0;
   }
   int tie_tot;
   const int tie_off = sel_scan(S, ntie, &tie_tot);
@@ -264,19 +240,16 @@ __device__ __forceinline__ int compact_selected(const Selector& S, const uint32_
   int32_t ix[kSelRegs];
   const uint32_t ia = smem_u32(idx_src);
 #pragma unroll
-  for (int j = 0; j < kSelRegs; ++j) ix[j] = kr[j] ? (int32_t)lds_u32(ia + 4 * (S.tid + S.nt * j)) : 0;
+  for (int j = 0; j < kSelRegs; ++j) ix[j] = (int32_t)lds_u32_if(kr[j] != 0u, ia + 4 * (S.tid + S.nt * j));
   named_bar_sync(S.bar, S.nt);  // every source index is read before any write
   int ties = 0;
 #pragma unroll
   for (int j = 0; j < kSelRegs; ++j) {
     const uint32_t key = kr[j];
-    if (!key) continue;
-    bool sel = th.early ? key >= th.prefix : key > th.prefix;
-    if (!sel && !th.early && key == th.prefix && ties < take) {
-      sel = true;
-      ++ties;
-    }
-    if (sel) {
+    const bool above = key != 0u && (th.early ? key >= th.prefix : key > th.prefix);
+    const bool tie = key != 0u && !th.early && key == th.prefix && ties < take;
+    ties += tie ? 1 : 0;
+    if (above || tie) {
       if (dkeys) dkeys[pos] = key;
       didx[pos] = ix[j];
       ++pos;
@@ -286,40 +259,89 @@ __device__ __forceinline__ int compact_selected(const Selector& S, const uint32_
   return total;
 }
 
-__device__ __forceinline__ void load_regs(const Selector& S, const uint32_t* ck, int n,
+__device__ __forceinline__ void load_regs(const Selector S, const uint32_t* ck, int n,
                                           uint32_t* kr) {
   const uint32_t a = smem_u32(ck);
 #pragma unroll
   for (int j = 0; j < kSelRegs; ++j) {
     const int i = S.tid + S.nt * j;
-    kr[j] = (i < n) ? lds_u32(a + 4 * i) : 0u;
+    kr[j] = lds_u32_if(i < n, a + 4 * i);
   }
 }
 
-// Keep the k largest of the slot's candidates (in place) and raise its threshold.
-__device__ __noinline__ void cand_compress(const Selector& S, TokSlot* ts, uint32_t* ck,
-                                           int32_t* ci, int k) {
+__device__ __forceinline__ void hist_clear(const Selector S, uint32_t hist_s) {
+  for (int b = S.tid; b < kBins; b += S.nt) sts_u32(hist_s + 4 * b, 0u);
+}
+
+// Shrink a slot's buffer while streaming: keep every candidate in or above the
+// level-1 bin of the k-th largest (at least k, usually a little more), zero
+// the histogram below it and raise the admission threshold to that bin's lower
+// edge.  If that bin alone would not leave `limit` room, select exactly k.
+__device__ __noinline__ void slot_compress(const Selector S, TokSlot* ts, uint32_t* ck,
+                                           int32_t* ci, uint32_t hist_s, int k, int limit) {
   uint32_t kr[kSelRegs];
   const int n = ts->count;
   load_regs(S, ck, n, kr);
-  const Thresh th = find_threshold(S, kr, k);
-  compact_selected(S, kr, ci, th, ck, ci);
-  if (S.tid == 0) {
-    ts->count = k;
-    ts->thr = th.prefix;
+  const BinCut c = find_bin(S, hist_s, k);
+  if (c.above + c.cnt <= limit) {
+    const Thresh th{(uint32_t)c.bin << kHistShift, 0, 1};
+    const int kept = compact_selected(S, kr, ci, th, ck, ci);
+    const int per = kBins / S.nt;
+    const int top = kBins - 1 - S.tid * per;
+    for (int j = 0; j < per; ++j)
+      if (top - j < c.bin) sts_u32(hist_s + 4 * (top - j), 0u);
+    if (S.tid == 0) {
+      ts->count = kept;
+      ts->thr = th.prefix > 0u ? th.prefix - 1u : 0u;
+    }
+  } else {
+    const Thresh th = refine_in_bin(S, kr, c, k, hist_s);
+    const int kept = compact_selected(S, kr, ci, th, ck, ci);
+    // rebuild the histogram of what is kept
+    hist_clear(S, hist_s);
+    named_bar_sync(S.bar, S.nt);
+    load_regs(S, ck, kept, kr);
+#pragma unroll
+    for (int j = 0; j < kSelRegs; ++j)
+      red_add_shared_if(kr[j] != 0u, hist_s + 4 * (kr[j] >> kHistShift), 1u);
+    if (S.tid == 0) {
+      ts->count = kept;
+      ts->thr = th.early ? (th.prefix > 0u ? th.prefix - 1u : 0u) : th.prefix;
+    }
   }
   named_bar_sync(S.bar, S.nt);
 }
 
-// Emit min(count, k) selected candidates of a slot to global memory; returns how many.
-__device__ __noinline__ int cand_emit(const Selector& S, TokSlot* ts, const uint32_t* ck,
-                                      const int32_t* ci, int k, uint32_t* dkeys, int32_t* didx) {
+// Final selection of a slot: write its min(count, k) largest candidates
+// (keys to dkeys unless null, indices to didx).  The slot's histogram serves
+// as scratch and is left undefined.  Returns how many were written.
+__device__ __noinline__ int slot_emit(const Selector S, TokSlot* ts, const uint32_t* ck,
+                                      const int32_t* ci, uint32_t hist_s, int k, uint32_t* dkeys,
+                                      int32_t* didx) {
   uint32_t kr[kSelRegs];
   const int n = ts->count;
   load_regs(S, ck, n, kr);
   Thresh th{0u, 0, 1};  // everything
-  if (n > k) th = find_threshold(S, kr, k);
+  if (n > k) th = refine_in_bin(S, kr, find_bin(S, hist_s, k), k, hist_s);
   return compact_selected(S, kr, ci, th, dkeys, didx);
+}
+
+// Append one candidate per thread of a warp if its key beats the threshold,
+// and count it in the slot's level-1 histogram.
+__device__ __forceinline__ void slot_append(uint32_t key, int32_t idx, uint32_t thr, TokSlot* ts,
+                                            uint32_t* ckeys, int32_t* cidx, uint32_t hist_s) {
+  const bool pass = key > thr;
+  const uint32_t m = __ballot_sync(0xffffffffu, pass);
+  if (m == 0) return;
+  int base = 0;
+  if (lane_id() == 0) base = (int)atom_add_shared(smem_u32(&ts->count), (uint32_t)__popc(m));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  red_add_shared_if(pass, hist_s + 4 * (key >> kHistShift), 1u);
+  if (pass) {
+    const int p = base + __popc(m & lanemask_lt());
+    ckeys[p] = key;
+    cidx[p] = idx;
+  }
 }
 
 template <int H>
@@ -559,8 +581,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const bool alt = (p.G == 1);
     const int step = alt ? 2 : 1;
     // who selects a row's candidates: both warpgroups for a decode row, else its warpgroup
-    const Selector S = alt ? Selector{256, epi * 32 + lane, 3u, hist_all, &misc->sel[0]}
-                           : Selector{128, tid, 1u + wg, hist_all + wg * kBins, &misc->sel[wg]};
+    const Selector S = alt ? Selector{256, epi * 32 + lane, 3u, nullptr, &misc->sel[0]}
+                           : Selector{128, tid, 1u + wg, nullptr, &misc->sel[wg]};
+    // level-1 histogram of each row slot's candidates (2048 bins per slot)
+    const uint32_t hist0_s = smem_u32(hist_all);
+    auto hist_of = [&](int g) -> uint32_t { return hist0_s + (uint32_t)g * kBins * 4u; };
     // buffer-fill checks every `chk` iterations, leaving room for what they append
     const int chk = alt ? 8 : 4;
     const int headroom = chk * kTileKeys * (alt ? 2 : 1);
@@ -589,6 +614,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           }
         }
       }
+      for (int g = g_first; g < I.gcount; g += 2) hist_clear(S, hist_of(g));
       named_bar_sync(3, 256);
       const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
       const bool may_fill = (I.k1 - I.k0) > p.C;
@@ -636,8 +662,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
               if (p.scores_out && valid && key < p.scores_ld)
                 p.scores_out[(int64_t)tok[g].t * p.scores_ld + key] = score;
               const uint32_t kk = valid ? score_key(score) : 0u;
-              cand_append(kk, key, tok[g].thr, &tok[g], ckeys_all + (size_t)g * p.C,
-                          cidx_all + (size_t)g * p.C);
+              slot_append(kk, key, tok[g].thr, &tok[g], ckeys_all + (size_t)g * p.C,
+                          cidx_all + (size_t)g * p.C, hist_of(g));
             }
             tc_fence_before();
             __syncwarp();
@@ -652,8 +678,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           } else {
             for (int g = g_first; g < I.gcount; g += 2)
               if (tok[g].count > p.C - headroom)
-                cand_compress(S, &tok[g], ckeys_all + (size_t)g * p.C, cidx_all + (size_t)g * p.C,
-                              p.k);
+                slot_compress(S, &tok[g], ckeys_all + (size_t)g * p.C, cidx_all + (size_t)g * p.C,
+                              hist_of(g), p.k, p.C - headroom);
           }
           named_bar_sync(3, 256);
         }
@@ -670,11 +696,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         int32_t* ci = cidx_all + (size_t)g * p.C;
         if (nsplit == 1) {
           int32_t* out_row = p.topk + (int64_t)tok[g].t * p.k;
-          const int n = cand_emit(S, &tok[g], ck, ci, p.k, nullptr, out_row);
+          const int n = slot_emit(S, &tok[g], ck, ci, hist_of(g), p.k, nullptr, out_row);
           for (int i = n + S.tid; i < p.k; i += S.nt) out_row[i] = -1;
         } else {
           const int64_t blk = (int64_t)I.cand_block + (int64_t)g * nsplit + split;
-          const int n = cand_emit(S, &tok[g], ck, ci, p.k, p.cand_keys + blk * p.k,
+          const int n = slot_emit(S, &tok[g], ck, ci, hist_of(g), p.k, p.cand_keys + blk * p.k,
                                   p.cand_idx + blk * p.k);
           if (S.tid == 0) p.cand_count[blk] = n;
         }
@@ -698,6 +724,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
               tok[g].count = 0;
               tok[g].thr = 0u;
             }
+            hist_clear(S, hist_of(g));
             named_bar_sync(S.bar, S.nt);
             for (int sj = 0; sj < nsplit; ++sj) {
               const int64_t blk = (int64_t)I.cand_block + (int64_t)g * nsplit + sj;
@@ -715,13 +742,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 }
                 const uint32_t thr = tok[g].thr;
 #pragma unroll
-                for (int u = 0; u < kMergePer; ++u) cand_append(kk[u], ix[u], thr, &tok[g], ck, ci);
+                for (int u = 0; u < kMergePer; ++u)
+                  slot_append(kk[u], ix[u], thr, &tok[g], ck, ci, hist_of(g));
                 named_bar_sync(S.bar, S.nt);
-                if (tok[g].count > p.C - batch) cand_compress(S, &tok[g], ck, ci, p.k);
+                if (tok[g].count > p.C - batch)
+                  slot_compress(S, &tok[g], ck, ci, hist_of(g), p.k, p.C - batch);
               }
             }
             int32_t* out_row = p.topk + (int64_t)tok[g].t * p.k;
-            const int n = cand_emit(S, &tok[g], ck, ci, p.k, nullptr, out_row);
+            const int n = slot_emit(S, &tok[g], ck, ci, hist_of(g), p.k, nullptr, out_row);
             for (int i = n + S.tid; i < p.k; i += S.nt) out_row[i] = -1;
           }
           if (epi == 0 && lane == 0) p.done[I.sgroup] = 0;  // ready for the next layer
