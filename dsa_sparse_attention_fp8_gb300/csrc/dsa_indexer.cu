@@ -95,19 +95,21 @@ constexpr size_t kSmemLimit = 232448;  // 227 KB opt-in per block on sm_100-fami
 // group) keeps whole splits of up to 8K keys without intermediate selection;
 // otherwise the buffer holds k plus room for at least one 512-candidate batch.
 int candidate_capacity(int k, bool decode) {
-  int c = k + (k / 2 > 512 ? k / 2 : 512);
+  int c = k + 1024;
   if (decode && c < 8192) c = 8192;
   return (c + 127) / 128 * 128;
 }
 static_assert(dsa::kSelRegs * 128 >= 2048 + 1024, "a warpgroup must hold a full buffer");
+static_assert(dsa::kSelRegs * 256 >= 8192, "both warpgroups must hold a decode buffer");
 
 // Rows per group: one row per decode batch (no request has more rows than
-// one), else as many rows as fill N = 256 of the MMA while the candidate
-// buffers stay within 96 KB of shared memory.
+// one), else as many rows as fill N = 256 of the MMA while each row's
+// candidate buffer and histogram stay within 128 KB of shared memory.
 int choose_group(int T, int R, int H, int k) {
   if (T <= R) return 1;
   int g = 256 / H;
-  const int by_smem = (96 * 1024) / (candidate_capacity(k, false) * 8);
+  const int per_row = candidate_capacity(k, false) * 8 + dsa::kBins * 4;
+  const int by_smem = (128 * 1024) / per_row;
   if (g > by_smem) g = by_smem;
   return g < 1 ? 1 : g;
 }
