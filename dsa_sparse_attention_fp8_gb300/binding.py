@@ -43,6 +43,8 @@ EXPORTS = (
     "dsa_quantize_fp8_blocks",
     "dsa_indexer_workspace_bytes",
     "dsa_indexer_score_topk",
+    "dsa_indexer_score_topk_no_alloc",
+    "dsa_indexer_no_alloc_workspace_bytes",
     "dsa_layer_is_full",
     "dsa_layer_stack_run",
 )
@@ -90,6 +92,11 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.dsa_indexer_score_topk.restype = _I
     lib.dsa_indexer_score_topk.argtypes = [
         _P, _P, _P, _I, _I, _P, _I64, _P, _P, _I, _P, _I, _I, _P, _I, _P, _I64, _P, _SZ, _P, _P]
+    lib.dsa_indexer_score_topk_no_alloc.restype = _I
+    lib.dsa_indexer_score_topk_no_alloc.argtypes = [
+        _P, _P, _P, _I, _I, _P, _I64, _P, _P, _I, _P, _I, _I, _P, _I, _P, _P]
+    lib.dsa_indexer_no_alloc_workspace_bytes.restype = _SZ
+    lib.dsa_indexer_no_alloc_workspace_bytes.argtypes = []
     lib.dsa_layer_is_full.restype = _I
     lib.dsa_layer_is_full.argtypes = [_I, ctypes.c_char_p, _I, _I]
     lib.dsa_layer_stack_run.restype = _I
@@ -241,6 +248,35 @@ def score_topk(q_fp8: torch.Tensor, q_scale: torch.Tensor, w: torch.Tensor,
         _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table), block_table.shape[1],
         index_topk, _ptr(topk_buffer), topk_buffer.shape[0], _ptr(scores_out), ld,
         _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)))
+
+
+def score_topk_no_alloc(q_fp8: torch.Tensor, q_scale: torch.Tensor, w: torch.Tensor,
+                        k_cache: torch.Tensor, query_start_loc: torch.Tensor,
+                        seq_lens: torch.Tensor, block_table: torch.Tensor, index_topk: int,
+                        topk_buffer: torch.Tensor, status: Optional[torch.Tensor] = None,
+                        stream=None) -> None:
+    """score_topk without a workspace argument: the library's built-in
+    workspace is used and nothing is allocated (see include/dsa_indexer.h)."""
+    T, H = q_fp8.shape[0], q_fp8.shape[1]
+    R = seq_lens.shape[0]
+    _need(q_fp8, "q_fp8", torch.uint8, (T, H, HEAD_DIM))
+    _need(q_scale, "q_scale", torch.float32, (T, H))
+    _need(w, "w", torch.float32, (T, H))
+    _need(k_cache, "k_cache", torch.uint8, (None, PAGE_BYTES))
+    _need(query_start_loc, "query_start_loc", torch.int32, (R + 1,))
+    _need(seq_lens, "seq_lens", torch.int32, (R,))
+    _need(block_table, "block_table", torch.int32, (R, None))
+    _need(topk_buffer, "topk_buffer", torch.int32, (None, index_topk))
+    if status is not None:
+        _need(status, "status", torch.int32)
+    _check(load().dsa_indexer_score_topk_no_alloc(
+        _ptr(q_fp8), _ptr(q_scale), _ptr(w), T, H, _ptr(k_cache), k_cache.shape[0],
+        _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table), block_table.shape[1],
+        index_topk, _ptr(topk_buffer), topk_buffer.shape[0], _ptr(status), _stream(stream)))
+
+
+def no_alloc_workspace_bytes() -> int:
+    return int(load().dsa_indexer_no_alloc_workspace_bytes())
 
 
 def layer_stack_run(layers: Sequence[Optional[dict]], pattern: Optional[str], freq: int,

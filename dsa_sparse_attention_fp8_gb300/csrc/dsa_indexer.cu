@@ -333,6 +333,38 @@ __global__ void copy_rows_kernel(const int4* __restrict__ src, int4* __restrict_
     dst[i] = src[i];
 }
 
+// ---------------------------------------------------------------- built-in workspace
+// Workspace for callers that cannot allocate device memory.  It is a
+// file-scope device array, so every GPU that loads this library holds it
+// until the process exits.  Host code must not use the symbol itself as a
+// device address (on the host it is only a stand-in): the real address is
+// looked up once per device with cudaGetSymbolAddress while that device is
+// current, and cached.
+constexpr size_t kStaticWorkspaceBytes = size_t(16) << 20;
+static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_ws_mutex;
+void* g_static_ws_ptr[kMaxDevices] = {};
+
+int static_workspace(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(DSA_ERR_UNSUPPORTED, "device %d >= %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_static_ws_mutex);
+  if (!g_static_ws_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_workspace);
+    if (e != cudaSuccess || !p)
+      return fail(DSA_ERR_CUDA, "cudaGetSymbolAddress of the built-in workspace: %s",
+                  cudaGetErrorString(e));
+    g_static_ws_ptr[dev] = p;
+  }
+  *out = g_static_ws_ptr[dev];
+  return DSA_OK;
+}
+
 }  // namespace
 
 // ============================================================================
@@ -449,6 +481,33 @@ int dsa_indexer_score_topk(const uint8_t* q_fp8, const float* q_scale, const flo
   g_last_launches = launches;
   return rc;
 }
+
+int dsa_indexer_score_topk_no_alloc(const uint8_t* q_fp8, const float* q_scale, const float* w,
+                                    int T, int H, const uint8_t* k_cache, int64_t num_pages,
+                                    const int32_t* query_start_loc, const int32_t* seq_lens, int R,
+                                    const int32_t* block_table, int max_blocks, int index_topk,
+                                    int32_t* topk_buffer, int max_num_batched_tokens,
+                                    int32_t* dev_status, dsa_stream_t stream) {
+  g_last_launches = 0;
+  const size_t need = dsa_indexer_workspace_bytes(T, H, R, 0, index_topk);
+  if (need == 0)
+    return fail(DSA_ERR_UNSUPPORTED, "no workspace size for T=%d, H=%d, R=%d, index_topk=%d", T,
+                H, R, index_topk);
+  if (need > kStaticWorkspaceBytes)
+    return fail(DSA_ERR_WORKSPACE_TOO_SMALL,
+                "this batch needs %zu bytes of workspace; the built-in workspace holds %zu "
+                "(use dsa_indexer_score_topk with a caller-provided workspace)",
+                need, kStaticWorkspaceBytes);
+  void* ws = nullptr;
+  const int rc = static_workspace(&ws);
+  if (rc) return rc;
+  return dsa_indexer_score_topk(q_fp8, q_scale, w, T, H, k_cache, num_pages, query_start_loc,
+                                seq_lens, R, block_table, max_blocks, index_topk, topk_buffer,
+                                max_num_batched_tokens, nullptr, 0, ws, kStaticWorkspaceBytes,
+                                dev_status, stream);
+}
+
+size_t dsa_indexer_no_alloc_workspace_bytes(void) { return kStaticWorkspaceBytes; }
 
 int dsa_layer_stack_run(int num_layers, const char* pattern, int freq, int offset,
                         const dsa_layer_io* layers, int T, int H,

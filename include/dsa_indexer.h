@@ -148,6 +148,40 @@ int dsa_indexer_score_topk(const uint8_t* q_fp8, const float* q_scale, const flo
                            int32_t* dev_status, dsa_stream_t stream);
 
 /*
+ * Same computation and arguments as dsa_indexer_score_topk (without the debug
+ * score dump), but it allocates nothing and takes no workspace argument: it
+ * uses a workspace of DSA_NO_ALLOC_WORKSPACE_BYTES compiled into the library
+ * as a static device array.  The pages describe no such entry point; it
+ * exists for callers that cannot call cudaMalloc or take memory from their
+ * host framework at the moment they run the indexer -- e.g. an inference
+ * server whose device memory is fully owned by its own pool, a plugin host
+ * that forbids allocation inside its enqueue callback, or code running while
+ * another component captures the stream into a CUDA graph.
+ *   - Memory: every GPU that loads this library holds the array until the
+ *     process exits.
+ *   - Set-up: the first call on each device looks the array's device address
+ *     up (cudaGetSymbolAddress) with that device current and caches it; make
+ *     that first call before any stream capture.
+ *   - Sharing: all calls share the one array and it keeps the previous call's
+ *     contents (each call re-initialises what it needs).  Calls whose kernels
+ *     overlap on the GPU (other streams, other threads) race on it: serialise
+ *     them.
+ *   - Limit: batches needing more than DSA_NO_ALLOC_WORKSPACE_BYTES of
+ *     workspace (dsa_indexer_workspace_bytes) return
+ *     DSA_ERR_WORKSPACE_TOO_SMALL; use dsa_indexer_score_topk for those.
+ */
+#define DSA_NO_ALLOC_WORKSPACE_BYTES ((size_t)16 << 20)
+int dsa_indexer_score_topk_no_alloc(const uint8_t* q_fp8, const float* q_scale, const float* w,
+                                    int T, int H, const uint8_t* k_cache, int64_t num_pages,
+                                    const int32_t* query_start_loc, const int32_t* seq_lens, int R,
+                                    const int32_t* block_table, int max_blocks, int index_topk,
+                                    int32_t* topk_buffer, int max_num_batched_tokens,
+                                    int32_t* dev_status, dsa_stream_t stream);
+
+/* Size in bytes of the workspace built into the library for the entry point above. */
+size_t dsa_indexer_no_alloc_workspace_bytes(void);
+
+/*
  * Step 4, [IC] §三/§四: 1 if DSA layer `layer_id` is an F layer, 0 if S, <0 on
  * error.  With a pattern (NUL-terminated string of 'F'/'S') the pattern
  * decides and layers at or beyond its length are F; otherwise the layer
