@@ -239,7 +239,7 @@ int launch_plan(const Batch& b, int G, int* launches) {
   if (n <= 0) return fail(DSA_ERR_CUDA, "no CUDA device");
   const int per_sm = env_int("DSA_ITEMS_PER_SM", 2, 1, 2);
   pp.target = per_sm * n < dsa::kMaxTarget ? per_sm * n : dsa::kMaxTarget;
-  pp.min_split = env_int("DSA_MIN_SPLIT", 2048, 128, 1 << 20) / 128 * 128;
+  pp.min_split = env_int("DSA_MIN_SPLIT", 8192, 128, 1 << 20) / 128 * 128;
   pp.max_split = 1 << 30;
   pp.topk_buffer = b.topk;
   pp.ws = static_cast<unsigned char*>(b.ws);
