@@ -45,6 +45,14 @@ int sm_count() {
   return n;
 }
 
+// CTAs of the scoring launch: one per SM, at most kMaxCtas.  Without a
+// device (sizing only) the bound itself is used, which over-sizes safely.
+int grid_ctas() {
+  const int n = sm_count();
+  if (n <= 0 || n > dsa::kMaxCtas) return dsa::kMaxCtas;
+  return n;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool supported_heads(int H) {
@@ -83,7 +91,7 @@ int make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t b
 
 // ---------------------------------------------------------------- launch shape
 struct ScoreShape {
-  int G, C, NS, NB, NQ, n_max, q_box_per_token;
+  int G, C, NS, NB, NQ, NR, n_max, q_box_per_token;
   uint32_t q_bytes;
   size_t smem_bytes;
   dsa::ScoreParams offs;  // only the off_* fields are filled
@@ -99,8 +107,11 @@ int candidate_capacity(int k, bool decode) {
   if (decode && c < 8192) c = 8192;
   return (c + 127) / 128 * 128;
 }
-static_assert(dsa::kSelRegs * 128 >= 2048 + 1024, "a warpgroup must hold a full buffer");
-static_assert(dsa::kSelRegs * 256 >= 8192, "both warpgroups must hold a decode buffer");
+// A compaction's table holds one count per (chunk of nt candidates, warp), at
+// most 256 of them and at most one per selector thread: a buffer may hold at
+// most 32 * nt candidates (4096 for a warpgroup, 8192 for both).
+static_assert((DSA_MAX_TOPK + 1024 + 127) / 128 * 128 <= 32 * 128, "prefill buffer too large");
+static_assert(8192 <= 32 * 256, "decode buffer too large");
 
 // Rows per group: one row per decode batch (no request has more rows than
 // one), else as many rows as fill N = 256 of the MMA while each row's
@@ -134,13 +145,16 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   fixed += (size_t)s->G * dsa::kBins * 4;
   fixed += up(sizeof(dsa::Misc), 16);
   fixed += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 2 * dsa::kMaxQBufs + 1) * 8;
-  const size_t per_stage = dsa::kStageBytes;
+  fixed += (size_t)s->NB * dsa::kScaleSlotBytes;  // scale ring: NS + NB slots
+  const size_t per_stage = dsa::kStageBytes + dsa::kScaleSlotBytes;
   const size_t budget = kSmemLimit - 1024 - 64;
   if (fixed + 2 * per_stage > budget) return false;
   s->NS = (int)((budget - fixed) / per_stage);
   if (s->NS > dsa::kMaxStages) s->NS = dsa::kMaxStages;
+  s->NR = s->NS + s->NB;
   size_t o = 0;  // stages first: every key stage starts on a 1024-byte boundary
   s->offs.off_stage = (uint32_t)o; o += (size_t)s->NS * dsa::kStageBytes;
+  s->offs.off_scale = (uint32_t)o; o += (size_t)s->NR * dsa::kScaleSlotBytes;
   s->offs.off_q = (uint32_t)o;     o += (size_t)s->NQ * s->q_bytes;
   s->offs.off_ckeys = (uint32_t)o; o += up((size_t)s->G * s->C * 4, 16);
   s->offs.off_cidx = (uint32_t)o;  o += up((size_t)s->G * s->C * 4, 16);
@@ -154,8 +168,8 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   return s->smem_bytes <= kSmemLimit;
 }
 
-// Split policy: target work items per SM and the shortest key range worth a
-// split of its own.  DSA_ITEMS_PER_SM / DSA_MIN_SPLIT override the defaults.
+// Balance policy: the smallest per-CTA share of key tiles worth a piece of
+// its own (DSA_MIN_SPLIT, in keys, overrides the default of 1024).
 int env_int(const char* name, int dflt, int lo, int hi) {
   const char* v = getenv(name);
   if (!v || !*v) return dflt;
@@ -235,15 +249,12 @@ int launch_plan(const Batch& b, int G, int* launches) {
   pp.G = G;
   pp.max_blocks = b.max_blocks;
   pp.index_topk = b.k;
-  int n = sm_count();
-  if (n <= 0) return fail(DSA_ERR_CUDA, "no CUDA device");
-  const int per_sm = env_int("DSA_ITEMS_PER_SM", 2, 1, 2);
-  pp.target = per_sm * n < dsa::kMaxTarget ? per_sm * n : dsa::kMaxTarget;
-  pp.min_split = env_int("DSA_MIN_SPLIT", 8192, 128, 1 << 20) / 128 * 128;
-  pp.max_split = 1 << 30;
+  if (sm_count() <= 0) return fail(DSA_ERR_CUDA, "no CUDA device");
+  pp.n_cta = grid_ctas();
+  pp.min_tiles = env_int("DSA_MIN_SPLIT", 1024, 128, 1 << 20) / 128;
   pp.topk_buffer = b.topk;
   pp.ws = static_cast<unsigned char*>(b.ws);
-  pp.L = dsa::ws_layout(b.T, b.R, G, b.k);
+  pp.L = dsa::ws_layout(b.T, b.R, G, b.k, pp.n_cta);
   pp.status = b.status;
   dsa::plan_kernel<<<1, dsa::kPlanThreads, 0, b.st>>>(pp);
   ++*launches;
@@ -266,7 +277,8 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   rc = make_rows128_map(&tq, lq.q_fp8, (uint64_t)b.T * b.H,
                         s.q_box_per_token ? (uint32_t)b.H : (uint32_t)(s.G * b.H));
   if (rc) return rc;
-  const dsa::WsLayout L = dsa::ws_layout(b.T, b.R, s.G, b.k);
+  const int grid = grid_ctas();
+  const dsa::WsLayout L = dsa::ws_layout(b.T, b.R, s.G, b.k, grid);
   unsigned char* ws = static_cast<unsigned char*>(b.ws);
   dsa::ScoreParams p = s.offs;
   p.qsl = b.qsl;
@@ -285,11 +297,13 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   p.NS = s.NS;
   p.NB = s.NB;
   p.NQ = s.NQ;
+  p.NR = s.NR;
   p.q_bytes = s.q_bytes;
   p.n_max = s.n_max;
   p.q_box_per_token = s.q_box_per_token;
   p.items = reinterpret_cast<const dsa::Item*>(ws + L.items);
-  p.hdr = reinterpret_cast<const dsa::PlanHeader*>(ws + L.header);
+  p.cta_start = reinterpret_cast<const int32_t*>(ws + L.cta_start);
+  p.CB = L.cb;
   p.cand_keys = reinterpret_cast<uint32_t*>(ws + L.cand_keys);
   p.cand_idx = reinterpret_cast<int32_t*>(ws + L.cand_idx);
   p.cand_count = reinterpret_cast<int32_t*>(ws + L.cand_count);
@@ -298,7 +312,6 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   p.scores_out = lq.scores_out;
   p.scores_ld = lq.scores_ld;
   p.status = b.status;
-  const int grid = sm_count();
   rc = launch_score(b.H, tk, tq, p, s.smem_bytes, grid, b.st);
   if (rc == DSA_OK) ++*launches;
   return rc;
@@ -400,7 +413,7 @@ size_t dsa_indexer_workspace_bytes(int T, int H, int R, int64_t max_ctx, int ind
   if (T < 0 || R < 1 || !supported_heads(H) || index_topk < 1 || index_topk > DSA_MAX_TOPK)
     return 0;
   const int G = choose_group(T, R, H, index_topk);
-  return dsa::ws_layout(T, R, G, index_topk).total;
+  return dsa::ws_layout(T, R, G, index_topk, grid_ctas()).total;
 }
 
 int dsa_quantize_fp8_blocks(const float* x, int64_t n_blocks, uint8_t* codes, float* scales,

@@ -3,15 +3,15 @@
 //
 // A work item is (request r, a group of up to G consecutive query rows of r,
 // a key range [k0, k1) of r's context).  Groups of rows share every key tile
-// they load (the rows' heads are the N side of one MMA).  A group whose
-// visible context is longer than the split length S is cut into key ranges
-// ("splits") that run on different SMs; each split keeps an exact local
-// top-k and the last split of a group to finish merges them.
+// they load (the rows' heads are the N side of one MMA).
 //
-// S = clamp(total visible keys / target items, min_split, max_split), so the
-// number of items is at most (#groups + target) and at most `target` groups
-// are split whenever S is not capped by max_split (the host sizes the
-// workspace for the capped case too).
+// Balance: the groups' key tiles (128 keys each) are laid end to end, W tiles
+// in all, and CTA c of the n_cta persistent CTAs takes the tiles
+// [c*Q, (c+1)*Q) with Q = max(ceil(W / n_cta), min_tiles).  A group that
+// straddles a CTA boundary is cut there into pieces ("splits") that run on
+// different CTAs; each piece keeps a superset of its rows' top-k and the last
+// piece of a group to finish merges them.  CTA c walks the items
+// [cta_start[c], cta_start[c+1]).
 #pragma once
 
 #include <cstdint>
@@ -25,46 +25,60 @@ struct Item {
   int32_t t0;          // first query row of the group
   int32_t gcount;      // rows in the group (1..G)
   int32_t k0, k1;      // key range [k0, k1) (logical positions); k0 % 128 == 0
-  int32_t split;       // split index | (number of splits << 16)
+  int32_t split;       // piece index | (number of pieces << 16)
   int32_t cand_block;  // first candidate block of the group (split groups), else -1
   int32_t sgroup;      // split-group id (index of its done counter), else -1
 };
 static_assert(sizeof(Item) == 32, "Item must stay 32 bytes");
 
-constexpr int kMaxTarget = 320;     // upper bound on work-item target (2 per SM, <=160 SMs)
+constexpr int kMaxCtas = 320;       // upper bound on the scoring grid (one CTA per SM)
 constexpr int kPlanThreads = 1024;
+constexpr int kTileKeysPlan = 128;  // keys per tile, the unit of the balance
 
 struct PlanHeader {
   int32_t n_items;
   int32_t n_split_groups;
   int32_t n_cand_blocks;
-  int32_t split_len;
+  int32_t tiles_per_cta;
   int32_t total_groups;
-  int32_t pad[59];
+  int32_t n_used_ctas;
+  int32_t pad[58];
 };
 static_assert(sizeof(PlanHeader) == 256, "PlanHeader is one 256-byte line");
 
+// Candidate-block capacity of one row of one piece: the piece's top-k plus
+// room for the rest of the level-1 bin that holds its k-th largest key.
+__host__ __device__ inline int cand_block_capacity(int k) {
+  const int c = k + (k < 1024 ? k : 1024);
+  return (c + 31) / 32 * 32;
+}
+
 // Workspace carve-up; identical on host and device.
 struct WsLayout {
-  size_t header, group_prefix, items, done, cand_count, cand_keys, cand_idx, total;
-  int max_items, max_split_groups, max_cand_blocks;
+  size_t header, group_prefix, cta_start, items, done, cand_count, cand_keys, cand_idx, total;
+  int max_items, max_split_groups, max_cand_blocks, cb;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-__host__ __device__ inline WsLayout ws_layout(int T, int R, int G, int k) {
+// A piece boundary is a CTA boundary inside a group, so at most n_cta - 1 of
+// them: at most T + n_cta items, n_cta split groups and 2 n_cta pieces of
+// split groups (G candidate blocks each).
+__host__ __device__ inline WsLayout ws_layout(int T, int R, int G, int k, int n_cta) {
   WsLayout L;
-  L.max_items = T + kMaxTarget;
-  L.max_split_groups = kMaxTarget;
-  L.max_cand_blocks = G * 2 * kMaxTarget;
+  L.max_items = T + n_cta;
+  L.max_split_groups = n_cta;
+  L.max_cand_blocks = G * 2 * n_cta;
+  L.cb = cand_block_capacity(k);
   size_t o = 0;
   L.header = o;       o = align256(o + sizeof(PlanHeader));
   L.group_prefix = o; o = align256(o + sizeof(int32_t) * (size_t)(R + 1));
+  L.cta_start = o;    o = align256(o + sizeof(int32_t) * (size_t)(n_cta + 1));
   L.items = o;        o = align256(o + sizeof(Item) * (size_t)L.max_items);
   L.done = o;         o = align256(o + sizeof(int32_t) * (size_t)L.max_split_groups);
   L.cand_count = o;   o = align256(o + sizeof(int32_t) * (size_t)L.max_cand_blocks);
-  L.cand_keys = o;    o = align256(o + sizeof(uint32_t) * (size_t)L.max_cand_blocks * k);
-  L.cand_idx = o;     o = align256(o + sizeof(int32_t) * (size_t)L.max_cand_blocks * k);
+  L.cand_keys = o;    o = align256(o + sizeof(uint32_t) * (size_t)L.max_cand_blocks * L.cb);
+  L.cand_idx = o;     o = align256(o + sizeof(int32_t) * (size_t)L.max_cand_blocks * L.cb);
   L.total = o;
   return L;
 }
@@ -100,8 +114,9 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 struct PlanParams {
   const int32_t* qsl;
   const int32_t* seq_lens;
-  int R, T, G, max_blocks, index_topk, target;
-  int min_split, max_split;  // bounds on the split length S (multiples of 128)
+  int R, T, G, max_blocks, index_topk;
+  int n_cta;       // CTAs of the scoring launch (<= kMaxCtas)
+  int min_tiles;   // smallest per-CTA share worth a piece of its own
   int32_t* topk_buffer;  // for -1 rows of malformed requests
   unsigned char* ws;
   WsLayout L;
@@ -116,15 +131,16 @@ __device__ __forceinline__ long long group_keys(long long P, int q, int G, int g
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   __shared__ long long warp_sums[32];
-  __shared__ int s_split_len;
+  __shared__ long long s_Q;
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.L.header);
   int32_t* group_prefix = reinterpret_cast<int32_t*>(p.ws + p.L.group_prefix);
+  int32_t* cta_start = reinterpret_cast<int32_t*>(p.ws + p.L.cta_start);
   Item* items = reinterpret_cast<Item*>(p.ws + p.L.items);
   int32_t* done = reinterpret_cast<int32_t*>(p.ws + p.L.done);
   const int G = p.G;
 
-  // Phase A: groups per request (prefix sums) and the total number of visible keys.
-  long long groups_carry = 0, keys_acc = 0;
+  // Phase A: groups per request (prefix sums).
+  long long groups_carry = 0;
   for (int base = 0; base < p.R; base += kPlanThreads) {
     const int r = base + threadIdx.x;
     long long groups = 0;
@@ -140,10 +156,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
           for (int i = 0; i < p.index_topk; ++i) p.topk_buffer[(size_t)t * p.index_topk + i] = -1;
       } else if (q > 0) {
         groups = (q + G - 1) / G;
-        const long long P = seq - q;
-        const long long nfull = q / G;
-        keys_acc += nfull * P + (long long)G * nfull * (nfull + 1) / 2;
-        if (q % G) keys_acc += P + q;
       }
     }
     long long tot;
@@ -151,25 +163,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     if (r < p.R) group_prefix[r] = (int32_t)(groups_carry + ex);
     groups_carry += tot;
   }
-  {
-    long long tot;
-    block_exclusive_scan(keys_acc, &tot, warp_sums);
-    if (threadIdx.x == 0) {
-      group_prefix[p.R] = (int32_t)groups_carry;
-      long long S = (tot + p.target - 1) / p.target;
-      S = ((S + 127) / 128) * 128;
-      if (S < p.min_split) S = p.min_split;
-      if (S > p.max_split) S = p.max_split;
-      if (S < 128) S = 128;
-      s_split_len = (int)S;
-    }
-  }
+  if (threadIdx.x == 0) group_prefix[p.R] = (int32_t)groups_carry;
   __syncthreads();
   const int total_groups = (int)groups_carry;
-  const long long S = s_split_len;
 
-  // Phase B: count items / split groups / candidate blocks (for reversed placement).
-  auto describe = [&](int gi, int& r, int& t0, int& gcount, long long& keys, int& nsplit) {
+  auto describe = [&](int gi, int& r, int& t0, int& gcount, long long& keys) {
     int lo = 0, hi = p.R - 1;  // last r with group_prefix[r] <= gi
     while (lo < hi) {
       int mid = (lo + hi + 1) >> 1;
@@ -181,70 +179,90 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     t0 = qb + g * G;
     gcount = min(G, q - g * G);
     keys = group_keys((long long)p.seq_lens[r] - q, q, G, g);
-    nsplit = (int)((keys + S - 1) / S);
   };
 
-  long long n_items = 0;
+  // Phase B: total tiles W, the per-CTA share Q and the number of items.
+  long long W = 0;
   for (int base = 0; base < total_groups; base += kPlanThreads) {
     const int gi = base + threadIdx.x;
     long long my = 0;
     if (gi < total_groups) {
-      int r, t0, gc, ns; long long keys;
-      describe(gi, r, t0, gc, keys, ns);
-      my = ns;
+      int r, t0, gc; long long keys;
+      describe(gi, r, t0, gc, keys);
+      my = (keys + kTileKeysPlan - 1) / kTileKeysPlan;
     }
     long long tot;
     block_exclusive_scan(my, &tot, warp_sums);
-    n_items += tot;
+    W += tot;
   }
+  if (threadIdx.x == 0) {
+    long long Q = (W + p.n_cta - 1) / p.n_cta;
+    if (Q < p.min_tiles) Q = p.min_tiles;
+    if (Q < 1) Q = 1;
+    s_Q = Q;
+  }
+  __syncthreads();
+  const long long Q = s_Q;
+  const int n_used = (int)((W + Q - 1) / Q);
 
-  // Phase C: emit items, last group first (later rows of a chunk see more keys,
-  // so the static round-robin over CTAs starts with the longest items).
-  long long item_carry = 0, sg_carry = 0, cb_carry = 0;
-  const bool overflow = n_items > p.L.max_items;
+  // Phase C: emit the pieces in tile order; CTA c's items are contiguous.
+  long long tile_carry = 0, item_carry = 0, sg_carry = 0, cb_carry = 0;
+  bool overflow = false;
   for (int base = 0; base < total_groups; base += kPlanThreads) {
     const int gi = base + threadIdx.x;
-    int r = 0, t0 = 0, gc = 0, ns = 0;
-    long long keys = 0;
-    if (gi < total_groups) describe(gi, r, t0, gc, keys, ns);
-    const bool is_split = ns > 1;
-    long long t_items, t_sg, t_cb;
-    const long long ex_items = block_exclusive_scan(ns, &t_items, warp_sums);
-    const long long ex_sg = block_exclusive_scan(is_split ? 1 : 0, &t_sg, warp_sums);
-    const long long ex_cb = block_exclusive_scan(is_split ? (long long)gc * ns : 0, &t_cb, warp_sums);
-    if (gi < total_groups && !overflow) {
-      const long long my_sg = sg_carry + ex_sg;
-      const long long my_cb = cb_carry + ex_cb;
-      const bool fits = !is_split || (my_sg < p.L.max_split_groups &&
-                                      my_cb + (long long)gc * ns <= p.L.max_cand_blocks);
-      if (!fits) raise_status(p.status, kStatusBadMetadata);
-      for (int j = 0; j < ns && fits; ++j) {
-        Item it;
-        it.r = r;
-        it.t0 = t0;
-        it.gcount = gc;
-        it.k0 = (int)(j * S);
-        it.k1 = (int)min((long long)(j + 1) * S, keys);
-        it.split = j | (ns << 16);
-        it.cand_block = is_split ? (int)my_cb : -1;
-        it.sgroup = is_split ? (int)my_sg : -1;
-        const long long slot = n_items - 1 - (item_carry + ex_items + j);
-        items[slot] = it;
-      }
+    int r = 0, t0 = 0, gc = 0;
+    long long keys = 0, tiles = 0, pieces = 0;
+    if (gi < total_groups) {
+      describe(gi, r, t0, gc, keys);
+      tiles = (keys + kTileKeysPlan - 1) / kTileKeysPlan;
     }
+    long long t_tiles;
+    const long long P = tile_carry + block_exclusive_scan(tiles, &t_tiles, warp_sums);
+    if (tiles > 0) pieces = (P + tiles - 1) / Q - P / Q + 1;
+    const bool is_split = pieces > 1;
+    long long t_items, t_sg, t_cb;
+    const long long my_item = item_carry + block_exclusive_scan(pieces, &t_items, warp_sums);
+    const long long my_sg = sg_carry + block_exclusive_scan(is_split ? 1 : 0, &t_sg, warp_sums);
+    const long long my_cb =
+        cb_carry + block_exclusive_scan(is_split ? (long long)gc * pieces : 0, &t_cb, warp_sums);
+    const bool fits = my_item + pieces <= p.L.max_items &&
+                      (!is_split || (my_sg < p.L.max_split_groups &&
+                                     my_cb + (long long)gc * pieces <= p.L.max_cand_blocks));
+    if (!fits) overflow = true;
+    for (long long j = 0; j < pieces && fits; ++j) {
+      const long long c = P / Q + j;  // CTA of this piece
+      const long long s0 = max(P, c * Q), s1 = min(P + tiles, (c + 1) * Q);
+      Item it;
+      it.r = r;
+      it.t0 = t0;
+      it.gcount = gc;
+      it.k0 = (int)((s0 - P) * kTileKeysPlan);
+      it.k1 = (int)min((s1 - P) * kTileKeysPlan, keys);
+      it.split = (int)j | ((int)pieces << 16);
+      it.cand_block = is_split ? (int)my_cb : -1;
+      it.sgroup = is_split ? (int)my_sg : -1;
+      items[my_item + j] = it;
+      if (s0 == c * Q) cta_start[c] = (int)(my_item + j);  // the piece that opens CTA c
+    }
+    tile_carry += t_tiles;
     item_carry += t_items;
     sg_carry += t_sg;
     cb_carry += t_cb;
   }
-  if (overflow) raise_status(p.status, kStatusBadMetadata);
+  const int any_overflow = __syncthreads_or(overflow ? 1 : 0);
+  if (any_overflow) raise_status(p.status, kStatusBadMetadata);
+  const int n_items = any_overflow ? 0 : (int)item_carry;
+  for (int c = threadIdx.x; c <= p.n_cta; c += kPlanThreads)
+    if (any_overflow || c >= n_used) cta_start[c] = n_items;
   for (int i = threadIdx.x; i < (int)min(sg_carry, (long long)p.L.max_split_groups); i += kPlanThreads)
     done[i] = 0;
   if (threadIdx.x == 0) {
-    hdr->n_items = overflow ? 0 : (int32_t)n_items;
+    hdr->n_items = n_items;
     hdr->n_split_groups = (int32_t)sg_carry;
     hdr->n_cand_blocks = (int32_t)cb_carry;
-    hdr->split_len = (int32_t)S;
+    hdr->tiles_per_cta = (int32_t)Q;
     hdr->total_groups = total_groups;
+    hdr->n_used_ctas = n_used;
   }
 }
 

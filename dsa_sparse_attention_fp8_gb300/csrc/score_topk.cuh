@@ -13,9 +13,10 @@
 //
 // Structure (one CTA per SM, 10 warps):
 //   warp 0      producer: per key tile (128 keys = 2 pages) two TMA loads of
-//               64 x 128 B key rows into a 128B-swizzled stage plus two 256 B
-//               bulk copies of the pages' scales; the query tile of each item
-//               (double-buffered when it is small).
+//               64 x 128 B key rows into a 128B-swizzled stage, and 16-byte
+//               cp.async copies of the pages' 2 x 256 B of scales into a ring
+//               of scale slots; the query tile of each item (double-buffered
+//               when it is small).
 //   warp 1      owns tensor memory; one lane issues 4 tcgen05.mma (K = 32
 //               each) per tile: D[key, row*H + head] += k . q, FP32 in TMEM.
 //   warps 2-9   epilogue, two warpgroups; thread = one key row of the tile
@@ -38,11 +39,11 @@ constexpr int kScoreThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kTileKeys = 128;
 constexpr int kStageBytes = kTileKeys * kHeadDim;  // 16 KB of key rows
+constexpr int kScaleSlotBytes = kTileKeys * 4;      // the FP32 scales of one tile's keys
 constexpr int kMaxStages = 16;
 constexpr int kMaxAccBufs = 8;
 constexpr int kMaxQBufs = 2;
 constexpr int kTmemCols = 512;
-constexpr int kMergePer = 4;              // candidates per thread per merge batch
 
 struct TokSlot {
   int32_t count;   // candidates held
@@ -60,11 +61,12 @@ struct ScoreParams {
   int64_t num_pages;
   const float* q_scale;
   const float* w;
-  int T, H, G, k, C, NS, NB, NQ, n_max;
+  int T, H, G, k, C, NS, NB, NQ, NR, n_max;
   int q_box_per_token;
   uint32_t q_bytes;  // bytes of one query-tile buffer
   const Item* items;
-  const PlanHeader* hdr;
+  const int32_t* cta_start;  // CTA c walks items [cta_start[c], cta_start[c+1])
+  int CB;                    // capacity of one candidate block
   uint32_t* cand_keys;
   int32_t* cand_idx;
   int32_t* cand_count;
@@ -74,14 +76,14 @@ struct ScoreParams {
   int64_t scores_ld;
   int32_t* status;
   // dynamic shared memory offsets (from a 1024-aligned base)
-  uint32_t off_stage, off_q, off_ckeys, off_cidx, off_wq, off_tok, off_hist, off_misc, off_bar;
+  uint32_t off_stage, off_scale, off_q, off_ckeys, off_cidx, off_wq, off_tok, off_hist, off_misc,
+      off_bar;
 };
 
 struct SelScratch {
-  int scan[8];                 // per-warp partials of a block scan (up to 256 threads)
-  int bin, above, cnt;
-  uint32_t lo, hi;
-  int pad[3];
+  int scan[8];                 // per-warp partials of a scan (up to 256 threads)
+  int res[4];                  // a bin search's result (bin, above, count)
+  uint32_t table[256];         // per-(chunk, warp) counts of a compaction, then their offsets
 };
 
 struct Misc {
@@ -90,12 +92,20 @@ struct Misc {
   int merge_flag;
   int epi_abort;   // an epilogue wait gave up; read by the epilogue only after barriers
   SelScratch sel[2];
+  int2 piece_pre[2 * (kMaxCtas + 1)];  // per selector: a merge's piece prefix sums
 };
 
 // The candidates of one query row are selected by a "selector": either one
 // warpgroup (128 threads, its own rows) or both (256 threads, the single row
 // of a decode item).  A selector names its threads, its named barrier and its
 // scratch.
+//
+// Selection runs once per row and item, so its code is written as small
+// rolled loops in out-of-line functions: a long unrolled sequence that runs
+// once costs an instruction-cache miss per 128 bytes of code, which on this
+// part dominated the arithmetic.  Candidates stay in shared memory (key
+// buffer ck, index buffer ci; key 0 = none) and are visited as chunks of nt:
+// candidate i = chunk * nt + tid.
 struct Selector {
   int nt;          // threads
   int tid;         // this thread, 0..nt-1
@@ -104,13 +114,19 @@ struct Selector {
   SelScratch* s;
 };
 
-constexpr int kSelRegs = 32;   // candidates a selector thread holds in registers
 constexpr int kBins = 2048;
+constexpr int kHistShift = 21;  // level-1 bin of a key: its top 11 bits (sign, exponent, 2 mantissa)
 
 struct Thresh {
   uint32_t prefix;  // keys >= prefix are taken (early), or > prefix plus `need` ties (exact)
   int need;
   int early;
+};
+
+struct BinCut {
+  int bin;    // the bin holding the need-th largest key
+  int above;  // keys in higher bins
+  int cnt;    // keys in that bin
 };
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -119,74 +135,90 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-// Exclusive scan of one int per selector thread; *total gets the sum.
-__device__ __forceinline__ int sel_scan(const Selector S, int v, int* total) {
-  const int lane = S.tid & 31, w = S.tid >> 5, nw = S.nt >> 5;
-  int x = v;
+__device__ __forceinline__ uint32_t warp_inclusive_sum(uint32_t x) {
+  const int lane = lane_id();
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) S.s->scan[w] = x;
-  named_bar_sync(S.bar, S.nt);
-  int off = 0, tot = 0;
-  for (int u = 0; u < nw; ++u) {
-    const int c = S.s->scan[u];
-    if (u < w) off += c;
-    tot += c;
-  }
-  named_bar_sync(S.bar, S.nt);
-  *total = tot;
-  return off + x - v;
+  return x;
 }
 
-constexpr int kHistShift = 21;  // level-1 bin of a key: its top 11 bits (sign, exponent, 2 mantissa)
+__device__ __forceinline__ uint32_t u4_at(const uint4& v, int e) {
+  return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
 
-struct BinCut {
-  int bin;    // the bin holding the need-th largest key
-  int above;  // keys in higher bins
-  int cnt;    // keys in that bin
-};
+__device__ __forceinline__ void clear_bins(const Selector S, uint32_t a, int nbins) {
+  for (int b = 4 * S.tid; b < nbins; b += 4 * S.nt) sts_v4(a + 4u * b, make_uint4(0, 0, 0, 0));
+}
 
-// Walk a 2048-bin histogram (shared memory) from the top; find the bin where
-// the running count reaches `need`.  Every selector thread gets the result.
-__device__ __forceinline__ BinCut find_bin(const Selector S, uint32_t hist_s, int need) {
-  const int per = kBins / S.nt;               // 8 or 16 bins per thread, highest first
-  const int top = kBins - 1 - S.tid * per;
-  uint32_t hv[kBins / 128];
+// Exclusive scan of one value per selector thread (one barrier); *total gets
+// the sum.  The scratch is reused only after another barrier of the selector.
+__device__ __forceinline__ uint32_t sel_scan(const Selector S, uint32_t v, uint32_t* total) {
+  const int lane = S.tid & 31, w = S.tid >> 5, nw = S.nt >> 5;
+  const uint32_t inc = warp_inclusive_sum(v);
+  if (lane == 31) S.s->scan[w] = (int)inc;
+  named_bar_sync(S.bar, S.nt);
+  uint32_t off = inc - v, tot = 0;
+  for (int u = 0; u < nw; ++u) {
+    const uint32_t c = (uint32_t)S.s->scan[u];
+    off += u < w ? c : 0u;
+    tot += c;
+  }
+  *total = tot;
+  return off;
+}
+
+// In an nbins-bin histogram (shared memory; nbins/nt in {4, 8, 16}), the bin
+// where the count from the top reaches `need` (1 <= need <= total).  Thread t
+// holds the nbins/nt consecutive bins below the top t*nbins/nt in registers; a
+// scan over threads finds the owner of the crossing, which walks its bins.
+__device__ __noinline__ BinCut find_bin(const Selector S, uint32_t hist_s, int nbins, int need) {
+  const int per = nbins / S.nt;
+  const uint32_t lo = (uint32_t)(nbins - (S.tid + 1) * per);  // this thread's lowest bin
+  uint4 q[4];
 #pragma unroll
-  for (int j = 0; j < kBins / 128; ++j) hv[j] = lds_u32_if(j < per, hist_s + 4 * (top - j));
-  int local = 0;
+  for (int i = 0; i < 4; ++i) q[i] = 4 * i < per ? lds_v4(hist_s + 4u * (lo + 4u * i)) : make_uint4(0, 0, 0, 0);
+  uint32_t local = 0;
 #pragma unroll
-  for (int j = 0; j < kBins / 128; ++j) local += (int)hv[j];
-  int total;
-  int above = sel_scan(S, local, &total);
-  if (above < need && need <= above + local) {
-    for (int j = 0; j < per; ++j) {
-      const int c = (int)hv[j];
-      if (need <= above + c) {
-        S.s->bin = top - j;
-        S.s->above = above;
-        S.s->cnt = c;
-        break;
+  for (int i = 0; i < 4; ++i) local += q[i].x + q[i].y + q[i].z + q[i].w;
+  uint32_t tot;
+  uint32_t above = sel_scan(S, local, &tot);  // threads before this one hold higher bins
+  const uint32_t un = (uint32_t)need;
+  if (above < un && un <= above + local) {
+    int bin = (int)lo + per - 1;
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int i = 15; i >= 0; --i) {  // from this thread's highest bin down
+      if (i < per) {
+        const uint32_t c = u4_at(q[i >> 2], i & 3);
+        if (cnt == 0 && un <= above + c) {
+          bin = (int)lo + i;
+          cnt = c;
+        } else if (cnt == 0) {
+          above += c;
+        }
       }
-      above += c;
     }
+    S.s->res[0] = bin;
+    S.s->res[1] = (int)above;
+    S.s->res[2] = (int)cnt;
   }
   named_bar_sync(S.bar, S.nt);
-  const BinCut r{S.s->bin, S.s->above, S.s->cnt};
-  named_bar_sync(S.bar, S.nt);
+  const BinCut r{S.s->res[0], S.s->res[1], S.s->res[2]};
+  named_bar_sync(S.bar, S.nt);  // result read before the scratch is reused
   return r;
 }
 
-// Exact threshold of the k-th largest register-held key, starting from the
-// level-1 bin cut `c` (taken from the incremental histogram): refine inside
-// that bin on key bits 20..10, then 9..0, using scratch_s (2048 ints of
-// shared memory) for the sub-histograms.  Stops as soon as a whole sub-bin is
-// taken.
-__device__ __forceinline__ Thresh refine_in_bin(const Selector S, const uint32_t* kr, BinCut c,
-                                                int k, uint32_t scratch_s) {
+// Exact threshold of the k-th largest of the slot's n candidates, starting
+// from the level-1 bin cut `c`: refine inside that bin on key bits 20..10,
+// then 9..0, with scratch_s (2048 ints of shared memory) holding the
+// sub-histograms.  Stops as soon as a whole sub-bin is taken.  The caller's
+// reads of scratch_s are complete (find_bin ends with a barrier).
+__device__ __noinline__ Thresh refine_in_bin(const Selector S, const uint32_t* ck, int n, BinCut c,
+                                             int k, uint32_t scratch_s) {
+  const uint32_t ck_s = smem_u32(ck);
   Thresh th{(uint32_t)c.bin << kHistShift, k - c.above, 0};
   uint32_t mask = 0xFFFFFFFFu << kHistShift;
   if (c.cnt == th.need) {
@@ -195,15 +227,24 @@ __device__ __forceinline__ Thresh refine_in_bin(const Selector S, const uint32_t
   }
   for (int level = 0; level < 2; ++level) {
     const int shift = level == 0 ? 10 : 0;
-    const uint32_t dm = level == 0 ? 2047u : 1023u;
-    for (int b = S.tid; b < kBins; b += S.nt) sts_u32(scratch_s + 4 * b, 0u);
+    const int nb = level == 0 ? 2048 : 1024;
+    const uint32_t dm = (uint32_t)nb - 1u;
+    clear_bins(S, scratch_s, nb);
     named_bar_sync(S.bar, S.nt);
+    for (int i0 = 0; i0 < n; i0 += 4 * S.nt) {
+      uint32_t kk[4];
 #pragma unroll
-    for (int j = 0; j < kSelRegs; ++j)
-      red_add_shared_if(kr[j] != 0u && (kr[j] & mask) == th.prefix,
-                        scratch_s + 4 * ((kr[j] >> shift) & dm), 1u);
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * S.nt + S.tid;
+        kk[u] = lds_u32_if(i < n, ck_s + 4u * (uint32_t)i);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        red_add_shared_if(kk[u] != 0u && (kk[u] & mask) == th.prefix,
+                          scratch_s + 4u * ((kk[u] >> shift) & dm), 1u);
+    }
     named_bar_sync(S.bar, S.nt);
-    const BinCut c2 = find_bin(S, scratch_s, th.need);
+    const BinCut c2 = find_bin(S, scratch_s, nb, th.need);
     th.need -= c2.above;
     th.prefix |= (uint32_t)c2.bin << shift;
     mask |= dm << shift;
@@ -215,115 +256,157 @@ __device__ __forceinline__ Thresh refine_in_bin(const Selector S, const uint32_t
   return th;
 }
 
-// Write the selected keys (th) of the selector's registers kr (with their
-// indices from idx_src[tid + nt*j]) to dkeys/didx[0, ...), in (thread,
-// register) order: deterministic.  Ties at an exact threshold are taken in
-// that order up to the quota.  dst may alias the source buffers (everything is
-// read before anything is written).  Returns the number written.
-__device__ __forceinline__ int compact_selected(const Selector S, const uint32_t* kr,
-                                                const int32_t* idx_src, Thresh th,
-                                                uint32_t* dkeys, int32_t* didx) {
-  int nsel = 0, ntie = 0;
+__device__ __forceinline__ bool sel_above(uint32_t key, Thresh th) {
+  return key != 0u && (th.early ? key >= th.prefix : key > th.prefix);
+}
+__device__ __forceinline__ bool sel_tie(uint32_t key, Thresh th) {
+  return key != 0u && !th.early && key == th.prefix;
+}
+
+// Write the selected candidates (th) among the slot's n (ck, ci) to dk/di
+// (keys only if dk is not null; dk/di must not alias ck/ci) in thread-major
+// order: thread t's candidates t, t + nt, ... come after those of threads
+// before it, so the result is deterministic, and ties at an exact threshold
+// are taken in that order up to the quota.  One counting pass, one scan, one
+// writing pass.  Returns the number written, visible on return.
+__device__ __noinline__ int compact_selected(const Selector S, const uint32_t* ck, const int32_t* ci,
+                                             int n, Thresh th, uint32_t* dk, int32_t* di) {
+  const uint32_t ck_s = smem_u32(ck);
+  uint32_t cnt = 0;  // above | ties << 16
+  for (int i0 = 0; i0 < n; i0 += 4 * S.nt) {
+    uint32_t kk[4];
 #pragma unroll
-  for (int j = 0; j < kSelRegs; ++j) {
-    const uint32_t key = kr[j];
-    nsel += (key != 0u && (th.early ? key >= th.prefix : key > th.prefix)) ? 1 : 0;
-    ntie += (key != 0u && !th.early && key == th.prefix) ? 1 : 0;
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * S.nt + S.tid;
+      kk[u] = lds_u32_if(i < n, ck_s + 4u * (uint32_t)i);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      cnt += (sel_above(kk[u], th) ? 1u : 0u) + (sel_tie(kk[u], th) ? 0x10000u : 0u);
   }
-  int tie_tot;
-  const int tie_off = sel_scan(S, ntie, &tie_tot);
-  const int quota = th.early ? 0 : th.need;
-  int take = quota - tie_off;
-  take = take < 0 ? 0 : (take > ntie ? ntie : take);
-  int total;
-  int pos = sel_scan(S, nsel + take, &total);
-  int32_t ix[kSelRegs];
-  const uint32_t ia = smem_u32(idx_src);
+  uint32_t tot;
+  const uint32_t off = sel_scan(S, cnt, &tot);
+  const uint32_t quota = th.early ? 0u : (uint32_t)th.need;
+  const uint32_t tie_off = off >> 16;
+  uint32_t pos = (off & 0xFFFFu) + min(quota, tie_off);
+  uint32_t take = min(quota - min(quota, tie_off), cnt >> 16);
+  if ((cnt & 0xFFFFu) + take > 0u) {
+    for (int i0 = 0; i0 < n; i0 += 4 * S.nt) {
+      uint32_t kk[4];
 #pragma unroll
-  for (int j = 0; j < kSelRegs; ++j) ix[j] = (int32_t)lds_u32_if(kr[j] != 0u, ia + 4 * (S.tid + S.nt * j));
-  named_bar_sync(S.bar, S.nt);  // every source index is read before any write
-  int ties = 0;
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * S.nt + S.tid;
+        kk[u] = lds_u32_if(i < n, ck_s + 4u * (uint32_t)i);
+      }
 #pragma unroll
-  for (int j = 0; j < kSelRegs; ++j) {
-    const uint32_t key = kr[j];
-    const bool above = key != 0u && (th.early ? key >= th.prefix : key > th.prefix);
-    const bool tie = key != 0u && !th.early && key == th.prefix && ties < take;
-    ties += tie ? 1 : 0;
-    if (above || tie) {
-      if (dkeys) dkeys[pos] = key;
-      didx[pos] = ix[j];
-      ++pos;
+      for (int u = 0; u < 4; ++u) {
+        const bool tie = sel_tie(kk[u], th) && take > 0u;
+        take -= tie ? 1u : 0u;
+        if (sel_above(kk[u], th) || tie) {
+          const int i = i0 + u * S.nt + S.tid;
+          if (dk) dk[pos] = kk[u];
+          di[pos] = ci[i];
+          ++pos;
+        }
+      }
     }
   }
   named_bar_sync(S.bar, S.nt);
-  return total;
+  return (int)((tot & 0xFFFFu) + min(quota, tot >> 16));
 }
 
-__device__ __forceinline__ void load_regs(const Selector S, const uint32_t* ck, int n,
-                                          uint32_t* kr) {
-  const uint32_t a = smem_u32(ck);
-#pragma unroll
-  for (int j = 0; j < kSelRegs; ++j) {
-    const int i = S.tid + S.nt * j;
-    kr[j] = lds_u32_if(i < n, a + 4 * i);
-  }
-}
-
-__device__ __forceinline__ void hist_clear(const Selector S, uint32_t hist_s) {
-  for (int b = S.tid; b < kBins; b += S.nt) sts_u32(hist_s + 4 * b, 0u);
-}
-
-// Shrink a slot's buffer while streaming: keep every candidate in or above the
-// level-1 bin of the k-th largest (at least k, usually a little more), zero
-// the histogram below it and raise the admission threshold to that bin's lower
-// edge.  If that bin alone would not leave `limit` room, select exactly k.
-__device__ __noinline__ void slot_compress(const Selector S, TokSlot* ts, uint32_t* ck,
-                                           int32_t* ci, uint32_t hist_s, int k, int limit) {
-  uint32_t kr[kSelRegs];
-  const int n = ts->count;
-  load_regs(S, ck, n, kr);
-  const BinCut c = find_bin(S, hist_s, k);
-  if (c.above + c.cnt <= limit) {
-    const Thresh th{(uint32_t)c.bin << kHistShift, 0, 1};
-    const int kept = compact_selected(S, kr, ci, th, ck, ci);
-    const int per = kBins / S.nt;
-    const int top = kBins - 1 - S.tid * per;
-    for (int j = 0; j < per; ++j)
-      if (top - j < c.bin) sts_u32(hist_s + 4 * (top - j), 0u);
-    if (S.tid == 0) {
-      ts->count = kept;
-      ts->thr = th.prefix > 0u ? th.prefix - 1u : 0u;
-    }
+// Exact top-min(n, k) of a slot's n candidates (buffer and level-1 histogram)
+// to a row of the top-k buffer, -1 after them.  The histogram is left
+// undefined.
+__device__ __noinline__ void slot_select_row(const Selector S, int n, const uint32_t* ck,
+                                             const int32_t* ci, uint32_t hist_s, int k,
+                                             int32_t* out_row) {
+  int m = n;
+  if (n <= k) {
+    for (int i = S.tid; i < n; i += S.nt) __stcg(out_row + i, ci[i]);
   } else {
-    const Thresh th = refine_in_bin(S, kr, c, k, hist_s);
-    const int kept = compact_selected(S, kr, ci, th, ck, ci);
-    // rebuild the histogram of what is kept
-    hist_clear(S, hist_s);
-    named_bar_sync(S.bar, S.nt);
-    load_regs(S, ck, kept, kr);
-#pragma unroll
-    for (int j = 0; j < kSelRegs; ++j)
-      red_add_shared_if(kr[j] != 0u, hist_s + 4 * (kr[j] >> kHistShift), 1u);
-    if (S.tid == 0) {
-      ts->count = kept;
-      ts->thr = th.early ? (th.prefix > 0u ? th.prefix - 1u : 0u) : th.prefix;
-    }
+    const BinCut c = find_bin(S, hist_s, kBins, k);
+    const Thresh th = refine_in_bin(S, ck, n, c, k, hist_s);
+    m = compact_selected(S, ck, ci, n, th, nullptr, out_row);
   }
-  named_bar_sync(S.bar, S.nt);
+  for (int i = m + S.tid; i < k; i += S.nt) __stcg(out_row + i, -1);
 }
 
-// Final selection of a slot: write its min(count, k) largest candidates
-// (keys to dkeys unless null, indices to didx).  The slot's histogram serves
-// as scratch and is left undefined.  Returns how many were written.
-__device__ __noinline__ int slot_emit(const Selector S, TokSlot* ts, const uint32_t* ck,
-                                      const int32_t* ci, uint32_t hist_s, int k, uint32_t* dkeys,
-                                      int32_t* didx) {
-  uint32_t kr[kSelRegs];
-  const int n = ts->count;
-  load_regs(S, ck, n, kr);
-  Thresh th{0u, 0, 1};  // everything
-  if (n > k) th = refine_in_bin(S, kr, find_bin(S, hist_s, k), k, hist_s);
-  return compact_selected(S, kr, ci, th, dkeys, didx);
+// Threshold for a superset of the slot's top-k of at most `limit` (>= k)
+// candidates: every candidate in or above the level-1 bin of the k-th
+// largest if that fits, else exactly k.  n > limit.
+__device__ __forceinline__ Thresh shrink_threshold(const Selector S, const uint32_t* ck, int n,
+                                                   uint32_t hist_s, int k, int limit) {
+  const BinCut c = find_bin(S, hist_s, kBins, k);
+  if (c.above + c.cnt <= limit) return Thresh{(uint32_t)c.bin << kHistShift, 0, 1};
+  return refine_in_bin(S, ck, n, c, k, hist_s);
+}
+
+// A superset of a piece's top-k of at most `limit` candidates to its global
+// candidate block (gk, gi): all n if n <= limit, else as shrink_threshold.
+// Returns the count.  The histogram is left undefined.
+__device__ __noinline__ int slot_emit_block(const Selector S, int n, const uint32_t* ck,
+                                            const int32_t* ci, uint32_t hist_s, int k, int limit,
+                                            uint32_t* gk, int32_t* gi) {
+  if (n <= limit) {
+    for (int i = S.tid; i < n; i += S.nt) {
+      __stcg(gk + i, ck[i]);
+      __stcg(gi + i, ci[i]);
+    }
+    return n;
+  }
+  const Thresh th = shrink_threshold(S, ck, n, hist_s, k, limit);
+  return compact_selected(S, ck, ci, n, th, gk, gi);
+}
+
+// Shrink a slot in place to a superset of its top-k of at most `limit`
+// candidates (n > limit >= k), as shrink_threshold; the histogram is made to
+// match and *thr gets the admission threshold that goes with the kept set
+// (keys <= *thr may be dropped from now on).  Every thread first takes its
+// own candidates (at most kShrinkRegs) into registers, so the compaction
+// (thread-major, as compact_selected) can overwrite the buffer.  Returns the
+// new count.
+constexpr int kShrinkRegs = 32;
+__device__ __noinline__ int slot_shrink(const Selector S, int n, uint32_t* ck, int32_t* ci,
+                                        uint32_t hist_s, int k, int limit, uint32_t* thr) {
+  const Thresh th = shrink_threshold(S, ck, n, hist_s, k, limit);
+  const uint32_t ck_s = smem_u32(ck), ci_s = smem_u32(ci);
+  uint32_t kr[kShrinkRegs];
+  int32_t ir[kShrinkRegs];
+  uint32_t cnt = 0;
+#pragma unroll
+  for (int j = 0; j < kShrinkRegs; ++j) {
+    const int i = j * S.nt + S.tid;
+    kr[j] = lds_u32_if(i < n, ck_s + 4u * (uint32_t)i);
+  }
+#pragma unroll
+  for (int j = 0; j < kShrinkRegs; ++j) {
+    const int i = j * S.nt + S.tid;
+    const bool keep = sel_above(kr[j], th) || sel_tie(kr[j], th);
+    ir[j] = (int32_t)lds_u32_if(keep, ci_s + 4u * (uint32_t)i);
+    cnt += (sel_above(kr[j], th) ? 1u : 0u) + (sel_tie(kr[j], th) ? 0x10000u : 0u);
+  }
+  uint32_t tot;
+  const uint32_t off = sel_scan(S, cnt, &tot);  // every candidate is read
+  const uint32_t quota = th.early ? 0u : (uint32_t)th.need;
+  const uint32_t tie_off = off >> 16;
+  uint32_t pos = (off & 0xFFFFu) + min(quota, tie_off);
+  uint32_t take = min(quota - min(quota, tie_off), cnt >> 16);
+  clear_bins(S, hist_s, kBins);
+  named_bar_sync(S.bar, S.nt);
+#pragma unroll
+  for (int j = 0; j < kShrinkRegs; ++j) {
+    const bool tie = sel_tie(kr[j], th) && take > 0u;
+    take -= tie ? 1u : 0u;
+    const bool wr = sel_above(kr[j], th) || tie;
+    sts_u32_if(wr, ck_s + 4u * pos, kr[j]);
+    sts_u32_if(wr, ci_s + 4u * pos, (uint32_t)ir[j]);
+    red_add_shared_if(wr, hist_s + 4u * (kr[j] >> kHistShift), 1u);
+    pos += wr ? 1u : 0u;
+  }
+  *thr = th.early ? (th.prefix > 0u ? th.prefix - 1u : 0u) : th.prefix;
+  named_bar_sync(S.bar, S.nt);
+  return (int)((tot & 0xFFFFu) + min(quota, tot >> 16));
 }
 
 // Append one candidate per thread of a warp if its key beats the threshold,
@@ -341,6 +424,152 @@ __device__ __forceinline__ void slot_append(uint32_t key, int32_t idx, uint32_t 
     const int p = base + __popc(m & lanemask_lt());
     ckeys[p] = key;
     cidx[p] = idx;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Merging the candidate blocks of a group's pieces.  Piece sj of a row holds
+// cnt[sj] keys and indices at block sj (capacity cb, a multiple of 32, so a
+// block starts on a 16-byte boundary).  The blocks are walked as one flat
+// sequence of 16-byte words.
+// ---------------------------------------------------------------------------
+constexpr int kAppendU = 2;  // words per thread per append batch (bounded by the slot's headroom)
+
+// pre[sj] = (keys, 16-byte words) of the pieces before sj; pre[nsplit] = totals.
+__device__ __noinline__ void piece_prefix(const Selector S, const int32_t* cnt, int nsplit,
+                                          int2* pre) {
+  if (S.tid < 32) {
+    uint32_t carry_c = 0, carry_4 = 0;
+    for (int b = 0; b < nsplit; b += 32) {
+      const int sj = b + S.tid;
+      const uint32_t c = sj < nsplit ? (uint32_t)__ldcg(cnt + sj) : 0u;
+      const uint32_t c4 = (c + 3u) >> 2;
+      const uint32_t ic = warp_inclusive_sum(c), i4 = warp_inclusive_sum(c4);
+      if (sj < nsplit) pre[sj] = make_int2((int)(carry_c + ic - c), (int)(carry_4 + i4 - c4));
+      carry_c += __shfl_sync(0xffffffffu, ic, 31);
+      carry_4 += __shfl_sync(0xffffffffu, i4, 31);
+    }
+    if (S.tid == 0) pre[nsplit] = make_int2((int)carry_c, (int)carry_4);
+  }
+  named_bar_sync(S.bar, S.nt);
+}
+
+// Piece of flat word q (walking forward from *sj), the word's first key index
+// inside the block, how many of its 4 keys are real, and its flat key index.
+struct WordPos {
+  int sj, e4, valid, dst;
+};
+__device__ __forceinline__ WordPos word_pos(const int2* pre, int nsplit, int q, int* sj) {
+  while (*sj + 1 < nsplit && pre[*sj + 1].y <= q) ++*sj;
+  WordPos w;
+  w.sj = *sj;
+  const int2 a = pre[*sj], b = pre[*sj + 1];
+  w.e4 = 4 * (q - a.y);
+  w.valid = min(4, (b.x - a.x) - w.e4);
+  w.dst = a.x + w.e4;
+  return w;
+}
+
+// All candidates into the slot buffer at their flat positions, counted in the
+// slot's histogram.  Four words per thread are loaded before any is stored.
+__device__ __noinline__ void gather_pieces(const Selector S, const uint32_t* gk0,
+                                           const int32_t* gi0, int cb, int nsplit,
+                                           const int2* pre, uint32_t ck_s, uint32_t ci_s,
+                                           uint32_t hist_s) {
+  const int total4 = pre[nsplit].y;
+  int sj = 0;
+  for (int q0 = 0; q0 < total4; q0 += 4 * S.nt) {
+    uint4 kv[4], iv[4];
+    int valid[4], dst[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = q0 + u * S.nt + S.tid;
+      valid[u] = 0;
+      dst[u] = 0;
+      kv[u] = make_uint4(0, 0, 0, 0);
+      iv[u] = make_uint4(0, 0, 0, 0);
+      if (q < total4) {
+        const WordPos wp = word_pos(pre, nsplit, q, &sj);
+        const int64_t off = (int64_t)wp.sj * cb + wp.e4;
+        valid[u] = wp.valid;
+        dst[u] = wp.dst;
+        kv[u] = __ldcg(reinterpret_cast<const uint4*>(gk0 + off));
+        iv[u] = __ldcg(reinterpret_cast<const uint4*>(gi0 + off));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool ok = e < valid[u];
+        const uint32_t key = u4_at(kv[u], e);
+        sts_u32_if(ok, ck_s + 4u * (uint32_t)(dst[u] + e), key);
+        sts_u32_if(ok, ci_s + 4u * (uint32_t)(dst[u] + e), u4_at(iv[u], e));
+        red_add_shared_if(ok, hist_s + 4u * (key >> kHistShift), 1u);
+      }
+  }
+}
+
+// Level-1 histogram of all candidate keys.
+__device__ __noinline__ void histogram_pieces(const Selector S, const uint32_t* gk0, int cb,
+                                              int nsplit, const int2* pre, uint32_t hist_s) {
+  const int total4 = pre[nsplit].y;
+  int sj = 0;
+#pragma unroll 4
+  for (int q = S.tid; q < total4; q += S.nt) {
+    const WordPos wp = word_pos(pre, nsplit, q, &sj);
+    const uint4 kv = __ldcg(reinterpret_cast<const uint4*>(gk0 + (int64_t)wp.sj * cb + wp.e4));
+    for (int e = 0; e < wp.valid; ++e)
+      red_add_shared(hist_s + 4u * (u4_at(kv, e) >> kHistShift), 1u);
+  }
+}
+
+// Append every candidate above the slot's threshold (ts->thr), shrinking the
+// slot whenever it could not take another batch.
+__device__ __noinline__ void append_pieces(const Selector S, const uint32_t* gk0,
+                                           const int32_t* gi0, int cb, int nsplit,
+                                           const int2* pre, TokSlot* ts, uint32_t* ck,
+                                           int32_t* ci, uint32_t hist_s, int C, int k) {
+  const int total4 = pre[nsplit].y;
+  const int batch = kAppendU * S.nt * 4;
+  int sj = 0;
+  for (int q0 = 0; q0 < total4; q0 += kAppendU * S.nt) {
+    const uint32_t thr = ts->thr;
+    uint4 kv[kAppendU], iv[kAppendU];
+    int valid[kAppendU];
+#pragma unroll
+    for (int u = 0; u < kAppendU; ++u) {
+      const int q = q0 + u * S.nt + S.tid;
+      valid[u] = 0;
+      kv[u] = make_uint4(0, 0, 0, 0);
+      iv[u] = make_uint4(0, 0, 0, 0);
+      if (q < total4) {
+        const WordPos wp = word_pos(pre, nsplit, q, &sj);
+        const int64_t off = (int64_t)wp.sj * cb + wp.e4;
+        valid[u] = wp.valid;
+        kv[u] = __ldcg(reinterpret_cast<const uint4*>(gk0 + off));
+        bool any = false;
+        for (int e = 0; e < wp.valid; ++e) any = any || u4_at(kv[u], e) > thr;
+        if (any) iv[u] = __ldcg(reinterpret_cast<const uint4*>(gi0 + off));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kAppendU; ++u)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        slot_append(e < valid[u] ? u4_at(kv[u], e) : 0u, (int32_t)u4_at(iv[u], e), thr, ts, ck,
+                    ci, hist_s);
+    named_bar_sync(S.bar, S.nt);
+    const int n = ts->count;
+    if (n > C - batch) {
+      uint32_t nthr = 0;
+      const int kept = slot_shrink(S, n, ck, ci, hist_s, k, C - batch, &nthr);
+      if (S.tid == 0) {
+        ts->count = kept;
+        ts->thr = nthr;
+      }
+      named_bar_sync(S.bar, S.nt);
+    }
   }
 }
 
@@ -380,6 +609,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int lane = threadIdx.x & 31;
 
   uint8_t* stage_base = smem + p.off_stage;
+  const uint32_t scale_ring_s = smem_u32(smem + p.off_scale);
   uint8_t* q_base = smem + p.off_q;
   uint32_t* ckeys_all = reinterpret_cast<uint32_t*>(smem + p.off_ckeys);
   int32_t* cidx_all = reinterpret_cast<int32_t*>(smem + p.off_cidx);
@@ -399,11 +629,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
+      // the producer's expect-tx arrival plus one cp.async arrival per producer lane
+      mbar_init(bar_full + 8 * s, 1 + 32);
       mbar_init(bar_empty + 8 * s, 1);  // freed by the MMA commit
     }
     for (int b = 0; b < p.NB; ++b) {
-      mbar_init(bar_tfull + 8 * b, 1);
+      // the MMA commit plus the issuing thread's own arrival (which publishes the
+      // tile's scales, observed through the full barrier, to the epilogue)
+      mbar_init(bar_tfull + 8 * b, 2);
       // decode layout: one warpgroup reads a tile; otherwise both do
       mbar_init(bar_tempty + 8 * b, p.G == 1 ? kEpiWarps / 2 : kEpiWarps);
     }
@@ -415,10 +648,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     misc->abort = 0;
     misc->epi_abort = 0;
     misc->merge_flag = 0;
-    for (int i = 0; i < 2; ++i) {
-      misc->sel[i].lo = 0xFFFFFFFFu;
-      misc->sel[i].hi = 0u;
-    }
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -433,22 +662,31 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = misc->tmem_base;
-  const int n_items = p.hdr->n_items;
+  const int it_begin = p.cta_start[blockIdx.x];
+  const int it_end = p.cta_start[blockIdx.x + 1];
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // The whole warp walks the tiles; lane 0 waits and issues the two key-page
-    // copies of each tile (each bulk-copy issue costs the thread ~100 cycles,
-    // so nothing else is issued here).  The page ids of 16 tiles (32 pages)
-    // come from one coalesced load, fetched one chunk ahead.
+    // The whole warp walks the tiles.  Per tile, lane 0 waits for the stage and
+    // issues the two key-page copies (each bulk-copy issue costs the thread
+    // ~100 cycles, so it issues nothing else); every lane copies 16 bytes of
+    // the two pages' scales (lanes 0-15 the first page, 16-31 the second) into
+    // the tile's slot of the scale ring with cp.async, zero-filled for a page
+    // outside the pool or the key range, and arrives on the stage's full
+    // barrier when its copy lands.  Tile s uses scale slot s % NR with
+    // NR >= NS + NB: the producer reaches tile s only after the epilogue has
+    // released tile s - NS - NB, so a slot is never overwritten while read.
+    // The page ids of 16 tiles (32 pages) come from one coalesced load,
+    // fetched one chunk ahead.
     int stage = 0;
     uint32_t sphase = 0;
     uint32_t issued_mask = 0;
     uint32_t last_par[kMaxStages];
     int q_last[kMaxQBufs] = {-1, -1};
     int item_i = 0;
+    long long seq = 0;  // tile sequence number of this CTA (all roles count alike)
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_i) {
+    for (int it = it_begin; it < it_end && ok; ++it, ++item_i) {
       const Item I = p.items[it];
       const int qb = item_i % p.NQ;
       const uint32_t qpar = (uint32_t)((item_i / p.NQ) & 1);
@@ -471,44 +709,52 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
       const int32_t* bt_row = p.block_table + (int64_t)I.r * p.max_blocks;
       const int page0 = I.k0 / kPageTokens;
-      auto load_pages = [&](int chunk) -> int64_t {  // this lane's page of a 32-page chunk
-        const int pidx = page0 + chunk * 32 + lane;
-        int64_t page = -1;
-        if (chunk * 16 < ntiles && pidx * kPageTokens < I.k1) {
-          page = __ldg(bt_row + pidx);
-          if (page < 0 || page >= p.num_pages) page = -1;
-        }
-        return page;
+      // a chunk's ids are loaded one chunk ahead and only checked when used, so
+      // the warp never waits for the load
+      auto in_range = [&](int chunk) {
+        return chunk * 16 < ntiles && (page0 + chunk * 32 + lane) * kPageTokens < I.k1;
       };
-      int64_t cur = load_pages(0);
+      auto fetch = [&](int chunk) -> int32_t {
+        return in_range(chunk) ? __ldg(bt_row + page0 + chunk * 32 + lane) : -1;
+      };
+      int32_t raw = fetch(0);
       for (int c = 0; c * 16 < ntiles && ok; ++c) {
-        const int64_t nxt = load_pages(c + 1);
+        int64_t cur = -1;  // this lane's page of the chunk, -1 if none or invalid
+        if (in_range(c)) {
+          if (raw >= 0 && (int64_t)raw < p.num_pages) cur = raw;
+          else raise_status(p.status, kStatusBadPage);
+        }
+        raw = fetch(c + 1);
         const int jend = min(16, ntiles - c * 16);
-        for (int jj = 0; jj < jend; ++jj) {
+        for (int jj = 0; jj < jend; ++jj, ++seq) {
           const int64_t pg0 = __shfl_sync(0xffffffffu, cur, 2 * jj);
           const int64_t pg1 = __shfl_sync(0xffffffffu, cur, 2 * jj + 1);
           okv = 1;
-          if (lane == 0) {
-            okv = mbar_wait(bar_empty + 8 * stage, sphase ^ 1, abort_flag);
-            if (okv) {
-              const uint32_t bytes = (pg0 >= 0 ? kPageTokens * kHeadDim : 0) +
-                                     (pg1 >= 0 ? kPageTokens * kHeadDim : 0);
-              mbar_arrive_expect_tx(bar_full + 8 * stage, bytes);
-              const uint32_t dst = smem_u32(stage_base + stage * kStageBytes);
-              if (pg0 >= 0)
-                tma_load_2d(dst, &tm_k, 0, (int32_t)(pg0 * (kPageBytes / kHeadDim)),
-                            bar_full + 8 * stage);
-              if (pg1 >= 0)
-                tma_load_2d(dst + kPageTokens * kHeadDim, &tm_k, 0,
-                            (int32_t)(pg1 * (kPageBytes / kHeadDim)), bar_full + 8 * stage);
-            }
-          }
+          if (lane == 0) okv = mbar_wait(bar_empty + 8 * stage, sphase ^ 1, abort_flag);
           if (!__shfl_sync(0xffffffffu, okv, 0)) { ok = false; break; }
+          const int64_t mine = lane < 16 ? pg0 : pg1;
+          const uint8_t* src =
+              mine >= 0 ? p.k_cache + mine * kPageBytes + kPageScaleOffset + (lane & 15) * 16
+                        : p.k_cache;
+          cp_async16(scale_ring_s + (uint32_t)(seq % p.NR) * kScaleSlotBytes + lane * 16, src,
+                     mine >= 0 ? 16u : 0u);
+          cp_async_arrive_noinc(bar_full + 8 * stage);
+          if (lane == 0) {
+            const uint32_t bytes = (pg0 >= 0 ? kPageTokens * kHeadDim : 0) +
+                                   (pg1 >= 0 ? kPageTokens * kHeadDim : 0);
+            mbar_arrive_expect_tx(bar_full + 8 * stage, bytes);
+            const uint32_t dst = smem_u32(stage_base + stage * kStageBytes);
+            if (pg0 >= 0)
+              tma_load_2d(dst, &tm_k, 0, (int32_t)(pg0 * (kPageBytes / kHeadDim)),
+                          bar_full + 8 * stage);
+            if (pg1 >= 0)
+              tma_load_2d(dst + kPageTokens * kHeadDim, &tm_k, 0,
+                          (int32_t)(pg1 * (kPageBytes / kHeadDim)), bar_full + 8 * stage);
+          }
           issued_mask |= 1u << stage;
           last_par[stage] = sphase;
           if (++stage == p.NS) { stage = 0; sphase ^= 1; }
         }
-        cur = nxt;
       }
     }
     if (lane == 0) {
@@ -529,7 +775,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       uint32_t sphase = 0, aphase = 0;
       int item_i = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++item_i) {
+      for (int it = it_begin; it < it_end && ok; ++it, ++item_i) {
         const Item I = p.items[it];
         const uint32_t N = (uint32_t)((I.gcount * H + 15) & ~15);
         const uint32_t idesc = idesc_e4m3_f32(128, N);
@@ -545,6 +791,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           if (!mbar_wait(bar_full + 8 * stage, sphase, abort_flag)) { ok = false; break; }
           if (!mbar_wait(bar_tempty + 8 * acc, aphase ^ 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
+          mbar_arrive(bar_tfull + 8 * acc);  // the tile's scales (seen via full) are ready
           const uint32_t aaddr = smem_u32(stage_base + stage * kStageBytes);
           const uint32_t d = tmem_base + (uint32_t)(acc * p.n_max);
 #pragma unroll
@@ -571,8 +818,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     // Thread = one key row of a tile (its TMEM lane).  With one query row per
     // item (decode) the two warpgroups take alternate tiles and share the
     // row's candidate buffer; otherwise each warpgroup owns alternate rows of
-    // the group and both read every tile.  Each thread fetches its key's scale
-    // and page id itself, a few tiles ahead of use.
+    // the group and both read every tile.  Each thread reads its key's scale
+    // from the tile's slot of the scale ring.
     const int epi = warp - 2;          // 0..7
     const int wg = epi >> 2;           // warpgroup 0/1
     const int tid = (epi & 3) * 32 + lane;
@@ -586,12 +833,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     // level-1 histogram of each row slot's candidates (2048 bins per slot)
     const uint32_t hist0_s = smem_u32(hist_all);
     auto hist_of = [&](int g) -> uint32_t { return hist0_s + (uint32_t)g * kBins * 4u; };
+    auto ck_of = [&](int g) -> uint32_t* { return ckeys_all + (size_t)g * p.C; };
+    auto ci_of = [&](int g) -> int32_t* { return cidx_all + (size_t)g * p.C; };
+    auto out_row = [&](int g) -> int32_t* { return p.topk + (int64_t)tok[g].t * p.k; };
     // buffer-fill checks every `chk` iterations, leaving room for what they append
     const int chk = alt ? 8 : 4;
     const int headroom = chk * kTileKeys * (alt ? 2 : 1);
     long long tile_base = 0;  // tiles of earlier items of this CTA (all roles count alike)
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    for (int it = it_begin; it < it_end && ok; ++it) {
       const Item I = p.items[it];
       const int qb0 = __ldg(p.qsl + I.r);
       const int q_len = __ldg(p.qsl + I.r + 1) - qb0;
@@ -614,50 +864,33 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           }
         }
       }
-      for (int g = g_first; g < I.gcount; g += 2) hist_clear(S, hist_of(g));
+      for (int g = g_first; g < I.gcount; g += 2) clear_bins(S, hist_of(g), kBins);
       named_bar_sync(3, 256);
       const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
       const bool may_fill = (I.k1 - I.k0) > p.C;
-      const int32_t* bt_row = p.block_table + (int64_t)I.r * p.max_blocks;
-      auto page_of = [&](int jj) -> int64_t {  // -1: beyond the range, -2: invalid id
-        const int key = I.k0 + jj * kTileKeys + row;
-        if (jj >= ntiles || key >= I.k1) return -1;
-        const int64_t pg = __ldg(bt_row + key / kPageTokens);
-        return (pg >= 0 && pg < p.num_pages) ? pg : -2;
-      };
-      auto scale_of = [&](int64_t pg, int jj) -> float {
-        if (pg < 0) return 0.f;
-        const int key = I.k0 + jj * kTileKeys + row;
-        return __ldg(reinterpret_cast<const float*>(p.k_cache + pg * kPageBytes +
-                                                    kPageScaleOffset) + (key % kPageTokens));
-      };
       const int j0 = alt ? wg : 0;
-      int64_t pg0 = page_of(j0), pg1 = page_of(j0 + step), pg2 = page_of(j0 + 2 * step),
-              pg3 = page_of(j0 + 3 * step), pg4 = page_of(j0 + 4 * step);
-      float sc0 = scale_of(pg0, j0), sc1 = scale_of(pg1, j0 + step), sc2 = scale_of(pg2, j0 + 2 * step);
       const int iters = alt ? (ntiles + 1) / 2 : ntiles;
       for (int m = 0; m < iters; ++m) {
         const int j = j0 + m * step;
-        // prefetch: scale three own tiles ahead, page id five ahead
-        const float sc3 = scale_of(pg3, j + 3 * step);
-        const int64_t pg5 = page_of(j + 5 * step);
         if (j < ntiles && ok) {
           const long long seq = tile_base + j;
           const int acc = (int)(seq % p.NB);
           const uint32_t aphase = (uint32_t)((seq / p.NB) & 1);
           const int key = I.k0 + j * kTileKeys + row;
-          const bool kvalid = pg0 >= 0;
-          if (pg0 == -2 && lane == 0) raise_status(p.status, kStatusBadPage);
           // no early exit on the abort flag here: the warps of a warpgroup must take
           // the same branch, so they all wait on the same phase with the same limit
           if (!mbar_wait(bar_tfull + 8 * acc, aphase, nullptr)) ok = false;
           if (ok) {
             tc_fence_after();
+            // the key's scale; zero (never a written scale) for a page outside the pool
+            const float sc = __uint_as_float(
+                lds_u32(scale_ring_s + (uint32_t)(seq % p.NR) * kScaleSlotBytes + row * 4));
+            const bool kvalid = sc > 0.f && key < I.k1;
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * p.n_max);
             for (int g = g_first; g < I.gcount; g += 2) {
-              const float s = relu_weighted_sum<H>(tbase + (uint32_t)(g * H), wq_all + g * H);
-              const float score = s * sc0;
+              const float sum = relu_weighted_sum<H>(tbase + (uint32_t)(g * H), wq_all + g * H);
+              const float score = sum * sc;
               const bool valid = kvalid && key <= tok[g].pos;
               if (p.scores_out && valid && key < p.scores_ld)
                 p.scores_out[(int64_t)tok[g].t * p.scores_ld + key] = score;
@@ -676,15 +909,21 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           if (misc->epi_abort) {
             ok = false;
           } else {
-            for (int g = g_first; g < I.gcount; g += 2)
-              if (tok[g].count > p.C - headroom)
-                slot_compress(S, &tok[g], ckeys_all + (size_t)g * p.C, cidx_all + (size_t)g * p.C,
-                              hist_of(g), p.k, p.C - headroom);
+            for (int g = g_first; g < I.gcount; g += 2) {
+              const int n = tok[g].count;
+              if (n > p.C - headroom) {
+                uint32_t thr = 0;
+                const int kept =
+                    slot_shrink(S, n, ck_of(g), ci_of(g), hist_of(g), p.k, p.C - headroom, &thr);
+                if (S.tid == 0) {
+                  tok[g].count = kept;
+                  tok[g].thr = thr;
+                }
+              }
+            }
           }
           named_bar_sync(3, 256);
         }
-        pg0 = pg1; pg1 = pg2; pg2 = pg3; pg3 = pg4; pg4 = pg5;
-        sc0 = sc1; sc1 = sc2; sc2 = sc3;
       }
       tile_base += ntiles;
       if (!ok) misc->epi_abort = 1;
@@ -692,21 +931,19 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (misc->epi_abort) { ok = false; break; }
       // finalize this item's rows
       for (int g = g_first; g < I.gcount; g += 2) {
-        uint32_t* ck = ckeys_all + (size_t)g * p.C;
-        int32_t* ci = cidx_all + (size_t)g * p.C;
+        const int n0 = tok[g].count;
         if (nsplit == 1) {
-          int32_t* out_row = p.topk + (int64_t)tok[g].t * p.k;
-          const int n = slot_emit(S, &tok[g], ck, ci, hist_of(g), p.k, nullptr, out_row);
-          for (int i = n + S.tid; i < p.k; i += S.nt) out_row[i] = -1;
+          slot_select_row(S, n0, ck_of(g), ci_of(g), hist_of(g), p.k, out_row(g));
         } else {
+          // a superset of the piece's top-k, at most one block
           const int64_t blk = (int64_t)I.cand_block + (int64_t)g * nsplit + split;
-          const int n = slot_emit(S, &tok[g], ck, ci, hist_of(g), p.k, p.cand_keys + blk * p.k,
-                                  p.cand_idx + blk * p.k);
-          if (S.tid == 0) p.cand_count[blk] = n;
+          const int n = slot_emit_block(S, n0, ck_of(g), ci_of(g), hist_of(g), p.k, p.CB,
+                                        p.cand_keys + blk * p.CB, p.cand_idx + blk * p.CB);
+          if (S.tid == 0) __stcg(p.cand_count + blk, n);
         }
       }
       if (nsplit > 1) {
-        // last split of the group to finish merges the candidates of all splits
+        // last piece of the group to finish merges the candidates of all pieces
         __threadfence();
         named_bar_sync(3, 256);
         if (epi == 0 && lane == 0) {
@@ -716,42 +953,39 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         named_bar_sync(3, 256);
         if (misc->merge_flag) {
           __threadfence();
-          const int batch = S.nt * kMergePer;
           for (int g = g_first; g < I.gcount; g += 2) {
-            uint32_t* ck = ckeys_all + (size_t)g * p.C;
-            int32_t* ci = cidx_all + (size_t)g * p.C;
-            if (S.tid == 0) {
-              tok[g].count = 0;
-              tok[g].thr = 0u;
-            }
-            hist_clear(S, hist_of(g));
+            const int64_t blk0 = (int64_t)I.cand_block + (int64_t)g * nsplit;
+            const uint32_t hs = hist_of(g);
+            int2* pre = misc->piece_pre + (alt ? 0 : wg * (kMaxCtas + 1));
+            piece_prefix(S, p.cand_count + blk0, nsplit, pre);  // ends with a barrier
+            const int total = pre[nsplit].x;
+            clear_bins(S, hs, kBins);
             named_bar_sync(S.bar, S.nt);
-            for (int sj = 0; sj < nsplit; ++sj) {
-              const int64_t blk = (int64_t)I.cand_block + (int64_t)g * nsplit + sj;
-              const int nb = __ldcg(p.cand_count + blk);
-              const uint32_t* gk = p.cand_keys + blk * p.k;
-              const int32_t* gi = p.cand_idx + blk * p.k;
-              for (int i0 = 0; i0 < nb; i0 += batch) {
-                uint32_t kk[kMergePer];
-                int32_t ix[kMergePer];
-#pragma unroll
-                for (int u = 0; u < kMergePer; ++u) {
-                  const int i = i0 + u * S.nt + S.tid;
-                  kk[u] = (i < nb) ? __ldcg(gk + i) : 0u;
-                  ix[u] = (i < nb) ? __ldcg(gi + i) : -1;
-                }
-                const uint32_t thr = tok[g].thr;
-#pragma unroll
-                for (int u = 0; u < kMergePer; ++u)
-                  slot_append(kk[u], ix[u], thr, &tok[g], ck, ci, hist_of(g));
-                named_bar_sync(S.bar, S.nt);
-                if (tok[g].count > p.C - batch)
-                  slot_compress(S, &tok[g], ck, ci, hist_of(g), p.k, p.C - batch);
+            const uint32_t* gk0 = p.cand_keys + blk0 * p.CB;
+            const int32_t* gi0 = p.cand_idx + blk0 * p.CB;
+            if (total <= p.C) {
+              // everything fits: gather the pieces' candidates into the slot
+              gather_pieces(S, gk0, gi0, p.CB, nsplit, pre, smem_u32(ck_of(g)), smem_u32(ci_of(g)),
+                            hs);
+              named_bar_sync(S.bar, S.nt);
+              slot_select_row(S, total, ck_of(g), ci_of(g), hs, p.k, out_row(g));
+            } else {
+              // level-1 histogram of all candidates: only keys in or above the bin
+              // of the k-th largest can be selected
+              histogram_pieces(S, gk0, p.CB, nsplit, pre, hs);
+              named_bar_sync(S.bar, S.nt);
+              const BinCut c = find_bin(S, hs, kBins, p.k);  // ends with a barrier
+              clear_bins(S, hs, kBins);
+              if (S.tid == 0) {
+                tok[g].count = 0;
+                tok[g].thr = c.bin > 0 ? ((uint32_t)c.bin << kHistShift) - 1u : 0u;
               }
+              named_bar_sync(S.bar, S.nt);
+              append_pieces(S, gk0, gi0, p.CB, nsplit, pre, &tok[g], ckeys_all + (size_t)g * p.C,
+                            cidx_all + (size_t)g * p.C, hs, p.C, p.k);
+              slot_select_row(S, tok[g].count, ck_of(g), ci_of(g), hs, p.k, out_row(g));
             }
-            int32_t* out_row = p.topk + (int64_t)tok[g].t * p.k;
-            const int n = slot_emit(S, &tok[g], ck, ci, hist_of(g), p.k, nullptr, out_row);
-            for (int i = n + S.tid; i < p.k; i += S.nt) out_row[i] = -1;
+            named_bar_sync(S.bar, S.nt);  // the slot is free for the next row
           }
           if (epi == 0 && lane == 0) p.done[I.sgroup] = 0;  // ready for the next layer
         }
