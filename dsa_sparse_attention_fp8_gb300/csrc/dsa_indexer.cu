@@ -306,6 +306,8 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   p.CB = L.cb;
   p.cand_keys = reinterpret_cast<uint32_t*>(ws + L.cand_keys);
   p.cand_idx = reinterpret_cast<int32_t*>(ws + L.cand_idx);
+  p.cand_hist = reinterpret_cast<uint16_t*>(ws + L.cand_hist);
+  p.cand_start = reinterpret_cast<uint16_t*>(ws + L.cand_start);
   p.cand_count = reinterpret_cast<int32_t*>(ws + L.cand_count);
   p.done = reinterpret_cast<int32_t*>(ws + L.done);
   p.topk = b.topk;

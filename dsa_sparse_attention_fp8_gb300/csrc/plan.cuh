@@ -54,21 +54,26 @@ __host__ __device__ inline int cand_block_capacity(int k) {
 }
 
 // Workspace carve-up; identical on host and device.
+constexpr int kBlockBins = 2048;  // level-1 bins published with every candidate block
+
 struct WsLayout {
-  size_t header, group_prefix, cta_start, items, done, cand_count, cand_keys, cand_idx, total;
+  size_t header, group_prefix, cta_start, items, done, cand_count, cand_keys, cand_idx, cand_hist,
+      cand_start, total;
   int max_items, max_split_groups, max_cand_blocks, cb;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // A piece boundary is a CTA boundary inside a group, so at most n_cta - 1 of
-// them: at most T + n_cta items, n_cta split groups and 2 n_cta pieces of
-// split groups (G candidate blocks each).
+// them: at most T + n_cta items, min(n_cta, groups) split groups and
+// (split groups + n_cta - 1) pieces of split groups, G candidate blocks each.
+// A request of q rows has ceil(q / G) groups, so groups <= min(T, T / G + R).
 __host__ __device__ inline WsLayout ws_layout(int T, int R, int G, int k, int n_cta) {
   WsLayout L;
   L.max_items = T + n_cta;
-  L.max_split_groups = n_cta;
-  L.max_cand_blocks = G * 2 * n_cta;
+  const long long groups = T < (T + G - 1) / G + R ? T : (T + G - 1) / G + R;
+  L.max_split_groups = (int)(groups < n_cta ? groups : n_cta);
+  L.max_cand_blocks = G * (L.max_split_groups + n_cta);
   L.cb = cand_block_capacity(k);
   size_t o = 0;
   L.header = o;       o = align256(o + sizeof(PlanHeader));
@@ -79,6 +84,8 @@ __host__ __device__ inline WsLayout ws_layout(int T, int R, int G, int k, int n_
   L.cand_count = o;   o = align256(o + sizeof(int32_t) * (size_t)L.max_cand_blocks);
   L.cand_keys = o;    o = align256(o + sizeof(uint32_t) * (size_t)L.max_cand_blocks * L.cb);
   L.cand_idx = o;     o = align256(o + sizeof(int32_t) * (size_t)L.max_cand_blocks * L.cb);
+  L.cand_hist = o;    o = align256(o + sizeof(uint16_t) * (size_t)L.max_cand_blocks * kBlockBins);
+  L.cand_start = o;   o = align256(o + sizeof(uint16_t) * (size_t)L.max_cand_blocks * kBlockBins);
   L.total = o;
   return L;
 }

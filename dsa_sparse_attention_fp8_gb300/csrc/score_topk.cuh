@@ -69,6 +69,8 @@ struct ScoreParams {
   int CB;                    // capacity of one candidate block
   uint32_t* cand_keys;
   int32_t* cand_idx;
+  uint16_t* cand_hist;   // per candidate block: level-1 histogram (kBlockBins; counts <= CB)
+  uint16_t* cand_start;  // per candidate block: start offset of every bin
   int32_t* cand_count;
   int32_t* done;
   int32_t* topk;
@@ -81,7 +83,7 @@ struct ScoreParams {
 };
 
 struct SelScratch {
-  int scan[8];                 // per-warp partials of a scan (up to 256 threads)
+  int scan[16];                // per-warp partials of a scan (up to 256 threads), 2 buffers
   int res[4];                  // a bin search's result (bin, above, count)
   uint32_t table[256];         // per-(chunk, warp) counts of a compaction, then their offsets
 };
@@ -154,15 +156,18 @@ __device__ __forceinline__ void clear_bins(const Selector S, uint32_t a, int nbi
 }
 
 // Exclusive scan of one value per selector thread (one barrier); *total gets
-// the sum.  The scratch is reused only after another barrier of the selector.
-__device__ __forceinline__ uint32_t sel_scan(const Selector S, uint32_t v, uint32_t* total) {
+// the sum.  Scratch buffer `buf` (0/1) is reused only after another barrier
+// of the selector.
+__device__ __forceinline__ uint32_t sel_scan(const Selector S, uint32_t v, uint32_t* total,
+                                             int buf = 0) {
   const int lane = S.tid & 31, w = S.tid >> 5, nw = S.nt >> 5;
+  int* sc = S.s->scan + 8 * buf;
   const uint32_t inc = warp_inclusive_sum(v);
-  if (lane == 31) S.s->scan[w] = (int)inc;
+  if (lane == 31) sc[w] = (int)inc;
   named_bar_sync(S.bar, S.nt);
   uint32_t off = inc - v, tot = 0;
   for (int u = 0; u < nw; ++u) {
-    const uint32_t c = (uint32_t)S.s->scan[u];
+    const uint32_t c = (uint32_t)sc[u];
     off += u < w ? c : 0u;
     tot += c;
   }
@@ -211,14 +216,28 @@ __device__ __noinline__ BinCut find_bin(const Selector S, uint32_t hist_s, int n
   return r;
 }
 
-// Exact threshold of the k-th largest of the slot's n candidates, starting
-// from the level-1 bin cut `c`: refine inside that bin on key bits 20..10,
-// then 9..0, with scratch_s (2048 ints of shared memory) holding the
-// sub-histograms.  Stops as soon as a whole sub-bin is taken.  The caller's
-// reads of scratch_s are complete (find_bin ends with a barrier).
-__device__ __noinline__ Thresh refine_in_bin(const Selector S, const uint32_t* ck, int n, BinCut c,
+__device__ __forceinline__ bool sel_above(uint32_t key, Thresh th) {
+  return key != 0u && (th.early ? key >= th.prefix : key > th.prefix);
+}
+__device__ __forceinline__ bool sel_tie(uint32_t key, Thresh th) {
+  return key != 0u && !th.early && key == th.prefix;
+}
+
+// Selection passes visit the slot's candidates in batches of kSelBatch per
+// thread (candidate i = (b * kSelBatch + u) * nt + tid): a rolled loop whose
+// body loads a whole batch before using it.  One-shot code that is unrolled
+// further runs at the instruction-fetch rate on this part, so the passes are
+// kept small and re-read shared memory instead of holding candidates in
+// registers.
+constexpr int kSelBatch = 8;
+
+// Exact threshold of the k-th largest of the slot's n keys, starting from the
+// level-1 bin cut `c`: refine inside that bin on key bits 20..10, then 9..0,
+// with scratch_s (2048 ints of shared memory) holding the sub-histograms.
+// Stops as soon as a whole sub-bin is taken.  The caller's reads of scratch_s
+// are complete (find_bin ends with a barrier).
+__device__ __noinline__ Thresh refine_in_bin(const Selector S, uint32_t ck_s, int n, BinCut c,
                                              int k, uint32_t scratch_s) {
-  const uint32_t ck_s = smem_u32(ck);
   Thresh th{(uint32_t)c.bin << kHistShift, k - c.above, 0};
   uint32_t mask = 0xFFFFFFFFu << kHistShift;
   if (c.cnt == th.need) {
@@ -231,15 +250,15 @@ __device__ __noinline__ Thresh refine_in_bin(const Selector S, const uint32_t* c
     const uint32_t dm = (uint32_t)nb - 1u;
     clear_bins(S, scratch_s, nb);
     named_bar_sync(S.bar, S.nt);
-    for (int i0 = 0; i0 < n; i0 += 4 * S.nt) {
-      uint32_t kk[4];
+    for (int i0 = S.tid; i0 < n; i0 += kSelBatch * S.nt) {
+      uint32_t kk[kSelBatch];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * S.nt + S.tid;
+      for (int u = 0; u < kSelBatch; ++u) {
+        const int i = i0 + u * S.nt;
         kk[u] = lds_u32_if(i < n, ck_s + 4u * (uint32_t)i);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < kSelBatch; ++u)
         red_add_shared_if(kk[u] != 0u && (kk[u] & mask) == th.prefix,
                           scratch_s + 4u * ((kk[u] >> shift) & dm), 1u);
     }
@@ -256,157 +275,109 @@ __device__ __noinline__ Thresh refine_in_bin(const Selector S, const uint32_t* c
   return th;
 }
 
-__device__ __forceinline__ bool sel_above(uint32_t key, Thresh th) {
-  return key != 0u && (th.early ? key >= th.prefix : key > th.prefix);
-}
-__device__ __forceinline__ bool sel_tie(uint32_t key, Thresh th) {
-  return key != 0u && !th.early && key == th.prefix;
-}
+enum SelMode {
+  kSelRow = 0,     // exact top-min(n, k) indices to a row of the top-k buffer, -1 after
+  kSelBlock = 1,   // a superset of the top-k of at most `limit` to a candidate block
+  kSelInPlace = 2  // the same superset kept in the slot; histogram and threshold follow
+};
 
-// Write the selected candidates (th) among the slot's n (ck, ci) to dk/di
-// (keys only if dk is not null; dk/di must not alias ck/ci) in thread-major
-// order: thread t's candidates t, t + nt, ... come after those of threads
-// before it, so the result is deterministic, and ties at an exact threshold
-// are taken in that order up to the quota.  One counting pass, one scan, one
-// writing pass.  Returns the number written, visible on return.
-__device__ __noinline__ int compact_selected(const Selector S, const uint32_t* ck, const int32_t* ci,
-                                             int n, Thresh th, uint32_t* dk, int32_t* di) {
-  const uint32_t ck_s = smem_u32(ck);
-  uint32_t cnt = 0;  // above | ties << 16
-  for (int i0 = 0; i0 < n; i0 += 4 * S.nt) {
-    uint32_t kk[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * S.nt + S.tid;
-      kk[u] = lds_u32_if(i < n, ck_s + 4u * (uint32_t)i);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      cnt += (sel_above(kk[u], th) ? 1u : 0u) + (sel_tie(kk[u], th) ? 0x10000u : 0u);
-  }
-  uint32_t tot;
-  const uint32_t off = sel_scan(S, cnt, &tot);
-  const uint32_t quota = th.early ? 0u : (uint32_t)th.need;
-  const uint32_t tie_off = off >> 16;
-  uint32_t pos = (off & 0xFFFFu) + min(quota, tie_off);
-  uint32_t take = min(quota - min(quota, tie_off), cnt >> 16);
-  if ((cnt & 0xFFFFu) + take > 0u) {
-    for (int i0 = 0; i0 < n; i0 += 4 * S.nt) {
-      uint32_t kk[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * S.nt + S.tid;
-        kk[u] = lds_u32_if(i < n, ck_s + 4u * (uint32_t)i);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const bool tie = sel_tie(kk[u], th) && take > 0u;
-        take -= tie ? 1u : 0u;
-        if (sel_above(kk[u], th) || tie) {
-          const int i = i0 + u * S.nt + S.tid;
-          if (dk) dk[pos] = kk[u];
-          di[pos] = ci[i];
-          ++pos;
-        }
-      }
-    }
-  }
-  named_bar_sync(S.bar, S.nt);
-  return (int)((tot & 0xFFFFu) + min(quota, tot >> 16));
-}
-
-// Exact top-min(n, k) of a slot's n candidates (buffer and level-1 histogram)
-// to a row of the top-k buffer, -1 after them.  The histogram is left
-// undefined.
-__device__ __noinline__ void slot_select_row(const Selector S, int n, const uint32_t* ck,
-                                             const int32_t* ci, uint32_t hist_s, int k,
-                                             int32_t* out_row) {
-  int m = n;
-  if (n <= k) {
-    for (int i = S.tid; i < n; i += S.nt) __stcg(out_row + i, ci[i]);
-  } else {
-    const BinCut c = find_bin(S, hist_s, kBins, k);
-    const Thresh th = refine_in_bin(S, ck, n, c, k, hist_s);
-    m = compact_selected(S, ck, ci, n, th, nullptr, out_row);
-  }
-  for (int i = m + S.tid; i < k; i += S.nt) __stcg(out_row + i, -1);
-}
-
-// Threshold for a superset of the slot's top-k of at most `limit` (>= k)
-// candidates: every candidate in or above the level-1 bin of the k-th
-// largest if that fits, else exactly k.  n > limit.
-__device__ __forceinline__ Thresh shrink_threshold(const Selector S, const uint32_t* ck, int n,
-                                                   uint32_t hist_s, int k, int limit) {
-  const BinCut c = find_bin(S, hist_s, kBins, k);
-  if (c.above + c.cnt <= limit) return Thresh{(uint32_t)c.bin << kHistShift, 0, 1};
-  return refine_in_bin(S, ck, n, c, k, hist_s);
-}
-
-// A superset of a piece's top-k of at most `limit` candidates to its global
-// candidate block (gk, gi): all n if n <= limit, else as shrink_threshold.
-// Returns the count.  The histogram is left undefined.
-__device__ __noinline__ int slot_emit_block(const Selector S, int n, const uint32_t* ck,
-                                            const int32_t* ci, uint32_t hist_s, int k, int limit,
-                                            uint32_t* gk, int32_t* gi) {
-  if (n <= limit) {
-    for (int i = S.tid; i < n; i += S.nt) {
-      __stcg(gk + i, ck[i]);
-      __stcg(gi + i, ci[i]);
-    }
+// One selection over a slot's n candidates (key buffer ck_s, index buffer
+// ci_s, level-1 histogram hist_s).  kSelBlock / kSelInPlace keep every
+// candidate if n <= limit, else every one in or above the level-1 bin of the
+// k-th largest if that fits, else exactly k.  Output order is thread-major
+// (thread t's candidates in visiting order after those of threads before
+// it): deterministic, ties at an exact threshold taken in that order up to
+// the quota.  Row output is staged in shared memory (hist_s, after its last
+// use) and copied out coalesced; in place, the kept candidates are staged in
+// registers one batch at a time behind a barrier per batch.  Returns the
+// number written; for kSelInPlace *thr gets the admission threshold of the
+// kept set.
+__device__ __noinline__ int slot_select(const Selector S, int mode, int n, uint32_t ck_s,
+                                        uint32_t ci_s, uint32_t hist_s, int k, int limit,
+                                        uint32_t* gk, int32_t* gi, uint32_t* thr) {
+  if (mode == kSelRow && n <= k) {
+    for (int i = S.tid; i < k; i += S.nt)
+      __stcg(gi + i, i < n ? (int32_t)lds_u32(ci_s + 4u * (uint32_t)i) : -1);
     return n;
   }
-  const Thresh th = shrink_threshold(S, ck, n, hist_s, k, limit);
-  return compact_selected(S, ck, ci, n, th, gk, gi);
-}
-
-// Shrink a slot in place to a superset of its top-k of at most `limit`
-// candidates (n > limit >= k), as shrink_threshold; the histogram is made to
-// match and *thr gets the admission threshold that goes with the kept set
-// (keys <= *thr may be dropped from now on).  Every thread first takes its
-// own candidates (at most kShrinkRegs) into registers, so the compaction
-// (thread-major, as compact_selected) can overwrite the buffer.  Returns the
-// new count.
-constexpr int kShrinkRegs = 32;
-__device__ __noinline__ int slot_shrink(const Selector S, int n, uint32_t* ck, int32_t* ci,
-                                        uint32_t hist_s, int k, int limit, uint32_t* thr) {
-  const Thresh th = shrink_threshold(S, ck, n, hist_s, k, limit);
-  const uint32_t ck_s = smem_u32(ck), ci_s = smem_u32(ci);
-  uint32_t kr[kShrinkRegs];
-  int32_t ir[kShrinkRegs];
-  uint32_t cnt = 0;
-#pragma unroll
-  for (int j = 0; j < kShrinkRegs; ++j) {
-    const int i = j * S.nt + S.tid;
-    kr[j] = lds_u32_if(i < n, ck_s + 4u * (uint32_t)i);
+  if (mode != kSelRow && n <= limit) {
+    if (mode == kSelBlock)
+      for (int i = S.tid; i < n; i += S.nt) {
+        __stcg(gk + i, lds_u32(ck_s + 4u * (uint32_t)i));
+        __stcg(gi + i, (int32_t)lds_u32(ci_s + 4u * (uint32_t)i));
+      }
+    return n;
   }
-#pragma unroll
-  for (int j = 0; j < kShrinkRegs; ++j) {
-    const int i = j * S.nt + S.tid;
-    const bool keep = sel_above(kr[j], th) || sel_tie(kr[j], th);
-    ir[j] = (int32_t)lds_u32_if(keep, ci_s + 4u * (uint32_t)i);
-    cnt += (sel_above(kr[j], th) ? 1u : 0u) + (sel_tie(kr[j], th) ? 0x10000u : 0u);
-  }
-  uint32_t tot;
-  const uint32_t off = sel_scan(S, cnt, &tot);  // every candidate is read
+  const BinCut c = find_bin(S, hist_s, kBins, k);
+  Thresh th;
+  if (mode != kSelRow && c.above + c.cnt <= limit)
+    th = Thresh{(uint32_t)c.bin << kHistShift, 0, 1};
+  else
+    th = refine_in_bin(S, ck_s, n, c, k, hist_s);
   const uint32_t quota = th.early ? 0u : (uint32_t)th.need;
-  const uint32_t tie_off = off >> 16;
-  uint32_t pos = (off & 0xFFFFu) + min(quota, tie_off);
-  uint32_t take = min(quota - min(quota, tie_off), cnt >> 16);
-  clear_bins(S, hist_s, kBins);
-  named_bar_sync(S.bar, S.nt);
-#pragma unroll
-  for (int j = 0; j < kShrinkRegs; ++j) {
-    const bool tie = sel_tie(kr[j], th) && take > 0u;
-    take -= tie ? 1u : 0u;
-    const bool wr = sel_above(kr[j], th) || tie;
-    sts_u32_if(wr, ck_s + 4u * pos, kr[j]);
-    sts_u32_if(wr, ci_s + 4u * pos, (uint32_t)ir[j]);
-    red_add_shared_if(wr, hist_s + 4u * (kr[j] >> kHistShift), 1u);
-    pos += wr ? 1u : 0u;
+  const bool in_place = mode == kSelInPlace;
+  if (in_place) {
+    clear_bins(S, hist_s, kBins);
+    named_bar_sync(S.bar, S.nt);
   }
-  *thr = th.early ? (th.prefix > 0u ? th.prefix - 1u : 0u) : th.prefix;
+  // Batch-major output order: batch b's candidates follow every kept one of
+  // earlier batches, so in place a batch's writes land at or below its own
+  // candidates; once every thread holds the batch it may be overwritten.
+  uint32_t carry_a = 0, carry_t = 0;  // kept-above / tie counts of earlier batches
+  const int batches = (n + kSelBatch * S.nt - 1) / (kSelBatch * S.nt);
+  for (int b = 0; b < batches; ++b) {
+    const int i0 = b * kSelBatch * S.nt + S.tid;
+    uint32_t kk[kSelBatch], ix[kSelBatch];
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {
+      const int i = i0 + u * S.nt;
+      kk[u] = lds_u32_if(i < n, ck_s + 4u * (uint32_t)i);
+    }
+    uint32_t cnt = 0;  // above | ties << 16
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u)
+      cnt += (sel_above(kk[u], th) ? 1u : 0u) + (sel_tie(kk[u], th) ? 0x10000u : 0u);
+    uint32_t tot;
+    const uint32_t off = sel_scan(S, cnt, &tot, b & 1);
+    uint32_t a = carry_a + (off & 0xFFFFu), t = carry_t + (off >> 16);
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {
+      const int i = i0 + u * S.nt;
+      ix[u] = lds_u32_if(sel_above(kk[u], th) || sel_tie(kk[u], th), ci_s + 4u * (uint32_t)i);
+    }
+    if (in_place) named_bar_sync(S.bar, S.nt);
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {
+      const bool above = sel_above(kk[u], th), tie = sel_tie(kk[u], th);
+      const bool wr = above || (tie && t < quota);
+      const uint32_t pos = a + min(quota, t);
+      if (mode == kSelRow) {
+        sts_u32_if(wr, hist_s + 4u * pos, ix[u]);
+      } else if (mode == kSelBlock) {
+        if (wr) {
+          __stcg(gk + pos, kk[u]);
+          __stcg(gi + pos, (int32_t)ix[u]);
+        }
+      } else {
+        sts_u32_if(wr, ck_s + 4u * pos, kk[u]);
+        sts_u32_if(wr, ci_s + 4u * pos, ix[u]);
+        red_add_shared_if(wr, hist_s + 4u * (kk[u] >> kHistShift), 1u);
+      }
+      a += above ? 1u : 0u;
+      t += tie ? 1u : 0u;
+    }
+    carry_a += tot & 0xFFFFu;
+    carry_t += tot >> 16;
+  }
+  const int total = (int)(carry_a + min(quota, carry_t));
   named_bar_sync(S.bar, S.nt);
-  return (int)((tot & 0xFFFFu) + min(quota, tot >> 16));
+  if (mode == kSelRow) {
+    for (int i = S.tid; i < k; i += S.nt)
+      __stcg(gi + i, i < total ? (int32_t)lds_u32(hist_s + 4u * (uint32_t)i) : -1);
+  } else if (in_place) {
+    *thr = th.early ? (th.prefix > 0u ? th.prefix - 1u : 0u) : th.prefix;
+  }
+  return total;
 }
 
 // Append one candidate per thread of a warp if its key beats the threshold,
@@ -428,142 +399,234 @@ __device__ __forceinline__ void slot_append(uint32_t key, int32_t idx, uint32_t 
 }
 
 // ---------------------------------------------------------------------------
-// Merging the candidate blocks of a group's pieces.  Piece sj of a row holds
-// cnt[sj] keys and indices at block sj (capacity cb, a multiple of 32, so a
-// block starts on a 16-byte boundary).  The blocks are walked as one flat
-// sequence of 16-byte words.
+// Pieces and their merge.  A piece of a split group writes, per row, a
+// candidate block: its candidates (keys, indices) sorted by level-1 bin from
+// the top, the block's level-1 histogram and each bin's start offset.  The
+// merger sums the pieces' histograms, finds the bin of the row's k-th largest
+// key, copies every candidate of the higher bins straight to the output row
+// (they are a prefix of every block), and selects exactly among the
+// candidates of that one bin.
 // ---------------------------------------------------------------------------
-constexpr int kAppendU = 2;  // words per thread per append batch (bounded by the slot's headroom)
 
-// pre[sj] = (keys, 16-byte words) of the pieces before sj; pre[nsplit] = totals.
-__device__ __noinline__ void piece_prefix(const Selector S, const int32_t* cnt, int nsplit,
-                                          int2* pre) {
-  if (S.tid < 32) {
-    uint32_t carry_c = 0, carry_4 = 0;
-    for (int b = 0; b < nsplit; b += 32) {
-      const int sj = b + S.tid;
-      const uint32_t c = sj < nsplit ? (uint32_t)__ldcg(cnt + sj) : 0u;
-      const uint32_t c4 = (c + 3u) >> 2;
-      const uint32_t ic = warp_inclusive_sum(c), i4 = warp_inclusive_sum(c4);
-      if (sj < nsplit) pre[sj] = make_int2((int)(carry_c + ic - c), (int)(carry_4 + i4 - c4));
-      carry_c += __shfl_sync(0xffffffffu, ic, 31);
-      carry_4 += __shfl_sync(0xffffffffu, i4, 31);
+// Publish a slot's n candidates as a bin-sorted block: histogram to ghist,
+// start offsets to gstart, candidates to gk/gi.  Positions inside a bin come
+// from shared atomics, so the order within a bin varies; the merger never
+// depends on it except to break exact ties.  The slot's histogram becomes
+// the bins' end offsets.
+__device__ __forceinline__ uint2 pack16(uint4 v) {
+  return make_uint2(v.x | (v.y << 16), v.z | (v.w << 16));
+}
+
+__device__ __noinline__ void slot_emit_sorted(const Selector S, int n, uint32_t ck_s, uint32_t ci_s,
+                                              uint32_t hist_s, uint32_t* gk, int32_t* gi,
+                                              uint16_t* ghist, uint16_t* gstart) {
+  const int per = kBins / S.nt;  // 8 or 16 consecutive bins per thread, the top first
+  const uint32_t lo = (uint32_t)(kBins - (S.tid + 1) * per);
+  uint4 q[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    q[i] = 4 * i < per ? lds_v4(hist_s + 4u * (lo + 4u * i)) : make_uint4(0, 0, 0, 0);
+  uint32_t local = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (4 * i < per) __stcg(reinterpret_cast<uint2*>(ghist + lo + 4 * i), pack16(q[i]));
+    local += q[i].x + q[i].y + q[i].z + q[i].w;
+  }
+  uint32_t tot;
+  uint32_t run = sel_scan(S, local, &tot);  // candidates in higher bins; every bin is read
+  uint4 st[4];
+#pragma unroll
+  for (int i = 3; i >= 0; --i) {
+    if (4 * i < per) {
+      st[i].w = run; run += q[i].w;
+      st[i].z = run; run += q[i].z;
+      st[i].y = run; run += q[i].y;
+      st[i].x = run; run += q[i].x;
+      sts_v4(hist_s + 4u * (lo + 4u * i), st[i]);
+      __stcg(reinterpret_cast<uint2*>(gstart + lo + 4 * i), pack16(st[i]));
     }
-    if (S.tid == 0) pre[nsplit] = make_int2((int)carry_c, (int)carry_4);
   }
   named_bar_sync(S.bar, S.nt);
+  for (int i0 = S.tid; i0 < n; i0 += kSelBatch * S.nt) {
+    uint32_t kk[kSelBatch], ix[kSelBatch];
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {
+      const int i = i0 + u * S.nt;
+      kk[u] = lds_u32_if(i < n, ck_s + 4u * (uint32_t)i);
+      ix[u] = lds_u32_if(i < n, ci_s + 4u * (uint32_t)i);
+    }
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {
+      if (i0 + u * S.nt < n) {
+        const uint32_t pos = atom_add_shared(hist_s + 4u * (kk[u] >> kHistShift), 1u);
+        __stcg(gk + pos, kk[u]);
+        __stcg(gi + pos, (int32_t)ix[u]);
+      }
+    }
+  }
 }
 
-// Piece of flat word q (walking forward from *sj), the word's first key index
-// inside the block, how many of its 4 keys are real, and its flat key index.
-struct WordPos {
-  int sj, e4, valid, dst;
+// One piece's share of a merge: (definite candidates, candidates of the cut
+// bin) and the running sums of both over the pieces before it.
+struct PieceCut {
+  int a_pre, c_pre;
 };
-__device__ __forceinline__ WordPos word_pos(const int2* pre, int nsplit, int q, int* sj) {
-  while (*sj + 1 < nsplit && pre[*sj + 1].y <= q) ++*sj;
-  WordPos w;
-  w.sj = *sj;
-  const int2 a = pre[*sj], b = pre[*sj + 1];
-  w.e4 = 4 * (q - a.y);
-  w.valid = min(4, (b.x - a.x) - w.e4);
-  w.dst = a.x + w.e4;
-  return w;
+
+// Candidate f of a flat concatenation (counts given by prefix sums pre[], the
+// .x or .y member) -> its piece, walking forward from *p.
+template <bool kY>
+__device__ __forceinline__ int piece_of(const PieceCut* pre, int nsplit, int f, int* p) {
+  while (*p + 1 < nsplit && (kY ? pre[*p + 1].c_pre : pre[*p + 1].a_pre) <= f) ++*p;
+  return *p;
 }
 
-// All candidates into the slot buffer at their flat positions, counted in the
-// slot's histogram.  Four words per thread are loaded before any is stored.
-__device__ __noinline__ void gather_pieces(const Selector S, const uint32_t* gk0,
-                                           const int32_t* gi0, int cb, int nsplit,
-                                           const int2* pre, uint32_t ck_s, uint32_t ci_s,
-                                           uint32_t hist_s) {
-  const int total4 = pre[nsplit].y;
-  int sj = 0;
-  for (int q0 = 0; q0 < total4; q0 += 4 * S.nt) {
-    uint4 kv[4], iv[4];
-    int valid[4], dst[4];
+// Merge the candidate blocks of one row's nsplit pieces (blocks blk0 ..
+// blk0 + nsplit - 1) into its output row: the exact top-min(total, k).
+// Shared memory: the row slot's buffers (ck_s, ci_s, capacity C, with the
+// slot's TokSlot for the rare streaming fallback), its histogram hist_s, and
+// pre (nsplit + 1 entries).
+__device__ __noinline__ void merge_pieces(const Selector S, const ScoreParams& p, int64_t blk0,
+                                          int nsplit, uint32_t ck_s, uint32_t ci_s,
+                                          uint32_t hist_s, TokSlot* ts, PieceCut* pre,
+                                          int32_t* out_row) {
+  const int k = p.k;
+  // summed histogram of all pieces (thread: 4-bin words tid, tid + nt, ...)
+  uint32_t local = 0;
+  for (int w = S.tid; w < kBins / 4; w += S.nt) {
+    uint4 acc = make_uint4(0, 0, 0, 0);
+    for (int sj0 = 0; sj0 < nsplit; sj0 += 8) {
+      uint2 v[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int q = q0 + u * S.nt + S.tid;
-      valid[u] = 0;
-      dst[u] = 0;
-      kv[u] = make_uint4(0, 0, 0, 0);
-      iv[u] = make_uint4(0, 0, 0, 0);
-      if (q < total4) {
-        const WordPos wp = word_pos(pre, nsplit, q, &sj);
-        const int64_t off = (int64_t)wp.sj * cb + wp.e4;
-        valid[u] = wp.valid;
-        dst[u] = wp.dst;
-        kv[u] = __ldcg(reinterpret_cast<const uint4*>(gk0 + off));
-        iv[u] = __ldcg(reinterpret_cast<const uint4*>(gi0 + off));
+      for (int u = 0; u < 8; ++u)
+        v[u] = sj0 + u < nsplit ? __ldcg(reinterpret_cast<const uint2*>(
+                                      p.cand_hist + (blk0 + sj0 + u) * kBlockBins + 4 * w))
+                                : make_uint2(0, 0);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc.x += v[u].x & 0xFFFFu; acc.y += v[u].x >> 16;
+        acc.z += v[u].y & 0xFFFFu; acc.w += v[u].y >> 16;
       }
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const bool ok = e < valid[u];
-        const uint32_t key = u4_at(kv[u], e);
-        sts_u32_if(ok, ck_s + 4u * (uint32_t)(dst[u] + e), key);
-        sts_u32_if(ok, ci_s + 4u * (uint32_t)(dst[u] + e), u4_at(iv[u], e));
-        red_add_shared_if(ok, hist_s + 4u * (key >> kHistShift), 1u);
+    sts_v4(hist_s + 16u * (uint32_t)w, acc);
+    local += acc.x + acc.y + acc.z + acc.w;
+  }
+  uint32_t total;
+  sel_scan(S, local, &total, 1);  // also: the summed histogram is complete
+  BinCut c{-1, 0, 0};
+  if ((int)total > k) c = find_bin(S, hist_s, kBins, k);
+  // per piece: definite = bins above the cut (a prefix of its block), then the cut bin
+  if (S.tid < 32) {
+    uint32_t ca = 0, cc = 0;
+    for (int b = 0; b < nsplit; b += 32) {
+      const int sj = b + S.tid;
+      uint32_t a = 0, cnt = 0;
+      if (sj < nsplit) {
+        const int64_t blk = blk0 + sj;
+        if (c.bin < 0) {
+          a = (uint32_t)__ldcg(p.cand_count + blk);
+        } else {
+          a = __ldcg(p.cand_start + blk * kBlockBins + c.bin);
+          cnt = __ldcg(p.cand_hist + blk * kBlockBins + c.bin);  // 16-bit counts
+        }
       }
+      const uint32_t ia = warp_inclusive_sum(a), ic = warp_inclusive_sum(cnt);
+      if (sj < nsplit) pre[sj] = PieceCut{(int)(ca + ia - a), (int)(cc + ic - cnt)};
+      ca += __shfl_sync(0xffffffffu, ia, 31);
+      cc += __shfl_sync(0xffffffffu, ic, 31);
+    }
+    if (S.tid == 0) pre[nsplit] = PieceCut{(int)ca, (int)cc};
   }
-}
-
-// Level-1 histogram of all candidate keys.
-__device__ __noinline__ void histogram_pieces(const Selector S, const uint32_t* gk0, int cb,
-                                              int nsplit, const int2* pre, uint32_t hist_s) {
-  const int total4 = pre[nsplit].y;
-  int sj = 0;
-#pragma unroll 4
-  for (int q = S.tid; q < total4; q += S.nt) {
-    const WordPos wp = word_pos(pre, nsplit, q, &sj);
-    const uint4 kv = __ldcg(reinterpret_cast<const uint4*>(gk0 + (int64_t)wp.sj * cb + wp.e4));
-    for (int e = 0; e < wp.valid; ++e)
-      red_add_shared(hist_s + 4u * (u4_at(kv, e) >> kHistShift), 1u);
+  named_bar_sync(S.bar, S.nt);
+  const int n_def = pre[nsplit].a_pre, n_cut = pre[nsplit].c_pre;
+  // definite candidates straight to the row
+  {
+    int sj = 0;
+    for (int f0 = S.tid; f0 < n_def; f0 += kSelBatch * S.nt) {
+      int32_t v[kSelBatch];
+#pragma unroll
+      for (int u = 0; u < kSelBatch; ++u) {
+        const int f = f0 + u * S.nt;
+        v[u] = 0;
+        if (f < n_def) {
+          const int q = piece_of<false>(pre, nsplit, f, &sj);
+          v[u] = __ldcg(p.cand_idx + (blk0 + q) * p.CB + (f - pre[q].a_pre));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kSelBatch; ++u)
+        if (f0 + u * S.nt < n_def) __stcg(out_row + f0 + u * S.nt, v[u]);
+    }
   }
-}
-
-// Append every candidate above the slot's threshold (ts->thr), shrinking the
-// slot whenever it could not take another batch.
-__device__ __noinline__ void append_pieces(const Selector S, const uint32_t* gk0,
-                                           const int32_t* gi0, int cb, int nsplit,
-                                           const int2* pre, TokSlot* ts, uint32_t* ck,
-                                           int32_t* ci, uint32_t hist_s, int C, int k) {
-  const int total4 = pre[nsplit].y;
-  const int batch = kAppendU * S.nt * 4;
+  if (c.bin < 0) {
+    for (int i = n_def + S.tid; i < k; i += S.nt) __stcg(out_row + i, -1);
+    return;
+  }
+  const int need = k - n_def;
+  // the cut bin's candidates: block q holds them at [definite_q, definite_q + cut_q)
+  auto cut_pos = [&](int q, int f) -> int64_t {
+    const int a_q = pre[q + 1].a_pre - pre[q].a_pre;
+    return (blk0 + q) * p.CB + a_q + (f - pre[q].c_pre);
+  };
+  if (n_cut <= p.C) {
+    int sj = 0;
+    for (int f0 = S.tid; f0 < n_cut; f0 += kSelBatch * S.nt) {
+      uint32_t kk[kSelBatch];
+      int32_t ix[kSelBatch];
+#pragma unroll
+      for (int u = 0; u < kSelBatch; ++u) {
+        const int f = f0 + u * S.nt;
+        kk[u] = 0u;
+        ix[u] = 0;
+        if (f < n_cut) {
+          const int64_t o = cut_pos(piece_of<true>(pre, nsplit, f, &sj), f);
+          kk[u] = __ldcg(p.cand_keys + o);
+          ix[u] = __ldcg(p.cand_idx + o);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kSelBatch; ++u) {
+        const int f = f0 + u * S.nt;
+        sts_u32_if(f < n_cut, ck_s + 4u * (uint32_t)f, kk[u]);
+        sts_u32_if(f < n_cut, ci_s + 4u * (uint32_t)f, (uint32_t)ix[u]);
+      }
+    }
+    // level-1 histogram of the gathered candidates: all in the cut bin
+    clear_bins(S, hist_s, kBins);
+    named_bar_sync(S.bar, S.nt);
+    if (S.tid == 0) sts_u32(hist_s + 4u * (uint32_t)c.bin, (uint32_t)n_cut);
+    named_bar_sync(S.bar, S.nt);
+    slot_select(S, kSelRow, n_cut, ck_s, ci_s, hist_s, need, 0, nullptr, out_row + n_def, nullptr);
+    return;
+  }
+  // Rare: more cut-bin candidates than the slot holds (heavily tied scores).
+  // Stream them through the slot, shrinking it to the top `need` as it fills.
+  clear_bins(S, hist_s, kBins);
+  if (S.tid == 0) {
+    ts->count = 0;
+    ts->thr = 0u;
+  }
+  named_bar_sync(S.bar, S.nt);
+  uint32_t* ck = reinterpret_cast<uint32_t*>(__cvta_shared_to_generic(ck_s));
+  int32_t* ci = reinterpret_cast<int32_t*>(__cvta_shared_to_generic(ci_s));
+  const int batch = S.nt;
   int sj = 0;
-  for (int q0 = 0; q0 < total4; q0 += kAppendU * S.nt) {
+  for (int f0 = 0; f0 < n_cut; f0 += batch) {
+    const int f = f0 + S.tid;
     const uint32_t thr = ts->thr;
-    uint4 kv[kAppendU], iv[kAppendU];
-    int valid[kAppendU];
-#pragma unroll
-    for (int u = 0; u < kAppendU; ++u) {
-      const int q = q0 + u * S.nt + S.tid;
-      valid[u] = 0;
-      kv[u] = make_uint4(0, 0, 0, 0);
-      iv[u] = make_uint4(0, 0, 0, 0);
-      if (q < total4) {
-        const WordPos wp = word_pos(pre, nsplit, q, &sj);
-        const int64_t off = (int64_t)wp.sj * cb + wp.e4;
-        valid[u] = wp.valid;
-        kv[u] = __ldcg(reinterpret_cast<const uint4*>(gk0 + off));
-        bool any = false;
-        for (int e = 0; e < wp.valid; ++e) any = any || u4_at(kv[u], e) > thr;
-        if (any) iv[u] = __ldcg(reinterpret_cast<const uint4*>(gi0 + off));
-      }
+    uint32_t key = 0u;
+    int32_t idx = 0;
+    if (f < n_cut) {
+      const int64_t o = cut_pos(piece_of<true>(pre, nsplit, f, &sj), f);
+      key = __ldcg(p.cand_keys + o);
+      idx = __ldcg(p.cand_idx + o);
     }
-#pragma unroll
-    for (int u = 0; u < kAppendU; ++u)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        slot_append(e < valid[u] ? u4_at(kv[u], e) : 0u, (int32_t)u4_at(iv[u], e), thr, ts, ck,
-                    ci, hist_s);
+    slot_append(key, idx, thr, ts, ck, ci, hist_s);
     named_bar_sync(S.bar, S.nt);
     const int n = ts->count;
-    if (n > C - batch) {
+    if (n > p.C - batch) {
       uint32_t nthr = 0;
-      const int kept = slot_shrink(S, n, ck, ci, hist_s, k, C - batch, &nthr);
+      const int kept =
+          slot_select(S, kSelInPlace, n, ck_s, ci_s, hist_s, need, p.C - batch, nullptr, nullptr, &nthr);
       if (S.tid == 0) {
         ts->count = kept;
         ts->thr = nthr;
@@ -571,6 +634,7 @@ __device__ __noinline__ void append_pieces(const Selector S, const uint32_t* gk0
       named_bar_sync(S.bar, S.nt);
     }
   }
+  slot_select(S, kSelRow, ts->count, ck_s, ci_s, hist_s, need, 0, nullptr, out_row + n_def, nullptr);
 }
 
 template <int H>
@@ -600,7 +664,8 @@ __device__ __forceinline__ float relu_weighted_sum(uint32_t taddr, const float* 
 template <int H>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_topk_kernel(const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_q, const ScoreParams p) {
+                      const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ ScoreParams p) {
   extern __shared__ uint8_t smem_raw[];
   // align to 1024 by pointer arithmetic on the shared array itself, so the
   // compiler keeps every access below in the shared address space
@@ -913,8 +978,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
               const int n = tok[g].count;
               if (n > p.C - headroom) {
                 uint32_t thr = 0;
-                const int kept =
-                    slot_shrink(S, n, ck_of(g), ci_of(g), hist_of(g), p.k, p.C - headroom, &thr);
+                const int kept = slot_select(S, kSelInPlace, n, smem_u32(ck_of(g)),
+                                             smem_u32(ci_of(g)), hist_of(g), p.k, p.C - headroom,
+                                             nullptr, nullptr, &thr);
                 if (S.tid == 0) {
                   tok[g].count = kept;
                   tok[g].thr = thr;
@@ -933,12 +999,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       for (int g = g_first; g < I.gcount; g += 2) {
         const int n0 = tok[g].count;
         if (nsplit == 1) {
-          slot_select_row(S, n0, ck_of(g), ci_of(g), hist_of(g), p.k, out_row(g));
+          slot_select(S, kSelRow, n0, smem_u32(ck_of(g)), smem_u32(ci_of(g)), hist_of(g), p.k, 0,
+                      nullptr, out_row(g), nullptr);
         } else {
           // a superset of the piece's top-k, at most one block
           const int64_t blk = (int64_t)I.cand_block + (int64_t)g * nsplit + split;
-          const int n = slot_emit_block(S, n0, ck_of(g), ci_of(g), hist_of(g), p.k, p.CB,
-                                        p.cand_keys + blk * p.CB, p.cand_idx + blk * p.CB);
+          int n = n0;
+          if (n > p.CB) {
+            uint32_t thr = 0;
+            n = slot_select(S, kSelInPlace, n, smem_u32(ck_of(g)), smem_u32(ci_of(g)), hist_of(g),
+                            p.k, p.CB, nullptr, nullptr, &thr);
+          }
+          slot_emit_sorted(S, n, smem_u32(ck_of(g)), smem_u32(ci_of(g)), hist_of(g),
+                           p.cand_keys + blk * p.CB, p.cand_idx + blk * p.CB,
+                           p.cand_hist + blk * kBlockBins, p.cand_start + blk * kBlockBins);
           if (S.tid == 0) __stcg(p.cand_count + blk, n);
         }
       }
@@ -955,36 +1029,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           __threadfence();
           for (int g = g_first; g < I.gcount; g += 2) {
             const int64_t blk0 = (int64_t)I.cand_block + (int64_t)g * nsplit;
-            const uint32_t hs = hist_of(g);
-            int2* pre = misc->piece_pre + (alt ? 0 : wg * (kMaxCtas + 1));
-            piece_prefix(S, p.cand_count + blk0, nsplit, pre);  // ends with a barrier
-            const int total = pre[nsplit].x;
-            clear_bins(S, hs, kBins);
-            named_bar_sync(S.bar, S.nt);
-            const uint32_t* gk0 = p.cand_keys + blk0 * p.CB;
-            const int32_t* gi0 = p.cand_idx + blk0 * p.CB;
-            if (total <= p.C) {
-              // everything fits: gather the pieces' candidates into the slot
-              gather_pieces(S, gk0, gi0, p.CB, nsplit, pre, smem_u32(ck_of(g)), smem_u32(ci_of(g)),
-                            hs);
-              named_bar_sync(S.bar, S.nt);
-              slot_select_row(S, total, ck_of(g), ci_of(g), hs, p.k, out_row(g));
-            } else {
-              // level-1 histogram of all candidates: only keys in or above the bin
-              // of the k-th largest can be selected
-              histogram_pieces(S, gk0, p.CB, nsplit, pre, hs);
-              named_bar_sync(S.bar, S.nt);
-              const BinCut c = find_bin(S, hs, kBins, p.k);  // ends with a barrier
-              clear_bins(S, hs, kBins);
-              if (S.tid == 0) {
-                tok[g].count = 0;
-                tok[g].thr = c.bin > 0 ? ((uint32_t)c.bin << kHistShift) - 1u : 0u;
-              }
-              named_bar_sync(S.bar, S.nt);
-              append_pieces(S, gk0, gi0, p.CB, nsplit, pre, &tok[g], ckeys_all + (size_t)g * p.C,
-                            cidx_all + (size_t)g * p.C, hs, p.C, p.k);
-              slot_select_row(S, tok[g].count, ck_of(g), ci_of(g), hs, p.k, out_row(g));
-            }
+            PieceCut* pre = reinterpret_cast<PieceCut*>(misc->piece_pre) + (alt ? 0 : wg * (kMaxCtas + 1));
+            merge_pieces(S, p, blk0, nsplit, smem_u32(ck_of(g)), smem_u32(ci_of(g)), hist_of(g),
+                         &tok[g], pre, out_row(g));
             named_bar_sync(S.bar, S.nt);  // the slot is free for the next row
           }
           if (epi == 0 && lane == 0) p.done[I.sgroup] = 0;  // ready for the next layer
