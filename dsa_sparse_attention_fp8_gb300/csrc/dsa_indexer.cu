@@ -89,9 +89,20 @@ int make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t b
   return DSA_OK;
 }
 
+// Tuning overrides read from the environment: DSA_MIN_SPLIT (keys, the
+// smallest per-CTA share of key tiles worth a piece of its own, default 1024)
+// and DSA_STAGE_KEYS (128 or 256, the decode layout's keys per pipeline
+// stage, default 256).
+int env_int(const char* name, int dflt, int lo, int hi) {
+  const char* v = getenv(name);
+  if (!v || !*v) return dflt;
+  const int x = atoi(v);
+  return x < lo ? lo : (x > hi ? hi : x);
+}
+
 // ---------------------------------------------------------------- launch shape
 struct ScoreShape {
-  int G, C, NS, NB, NQ, NR, n_max, q_box_per_token;
+  int G, C, NS, NB, NQ, NR, BPS, n_max, q_box_per_token;
   uint32_t q_bytes;
   size_t smem_bytes;
   dsa::ScoreParams offs;  // only the off_* fields are filled
@@ -99,19 +110,17 @@ struct ScoreShape {
 
 constexpr size_t kSmemLimit = 232448;  // 227 KB opt-in per block on sm_100-family
 
-// Candidate-buffer capacity per query row.  A decode layout (one row per
-// group) keeps whole splits of up to 8K keys without intermediate selection;
-// otherwise the buffer holds k plus room for at least one 512-candidate batch.
+// Candidate-buffer capacity per query row: k plus room for the candidates
+// appended between two fill checks.  A decode layout (one row per group)
+// takes more, so that long pieces shrink their buffer rarely, within the
+// shared memory left after four 256-key pipeline stages.
 int candidate_capacity(int k, bool decode) {
   int c = k + 1024;
-  if (decode && c < 8192) c = 8192;
+  if (decode && c < 6144) c = 6144;
   return (c + 127) / 128 * 128;
 }
-// A compaction's table holds one count per (chunk of nt candidates, warp), at
-// most 256 of them and at most one per selector thread: a buffer may hold at
-// most 32 * nt candidates (4096 for a warpgroup, 8192 for both).
-static_assert((DSA_MAX_TOPK + 1024 + 127) / 128 * 128 <= 32 * 128, "prefill buffer too large");
-static_assert(8192 <= 32 * 256, "decode buffer too large");
+// Candidate counts are packed in 16 bits during selection scans.
+static_assert(DSA_MAX_TOPK + 1024 + 6144 < 65536, "candidate buffer too large");
 
 // Rows per group: one row per decode batch (no request has more rows than
 // one), else as many rows as fill N = 256 of the MMA while each row's
@@ -132,7 +141,11 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   s->C = candidate_capacity(k, s->G == 1);
   s->q_box_per_token = (H % 8 == 0) ? 1 : 0;
   s->n_max = (s->G * H + 15) / 16 * 16;
-  s->NB = dsa::kTmemCols / s->n_max;
+  // decode layout: 256-key stages (two 128-key MMA blocks) when tensor memory
+  // still holds 4 stage accumulators; halves the per-key barrier and issue work
+  s->BPS = (s->G == 1 && dsa::kTmemCols / (2 * s->n_max) >= 4) ? 2 : 1;
+  if (env_int("DSA_STAGE_KEYS", 256, 128, 256) < 256) s->BPS = 1;
+  s->NB = dsa::kTmemCols / (s->BPS * s->n_max);
   if (s->NB > dsa::kMaxAccBufs) s->NB = dsa::kMaxAccBufs;
   if (s->NB < 2) return false;
   s->q_bytes = (uint32_t)up((size_t)s->G * H * 128, 1024);
@@ -145,16 +158,16 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   fixed += (size_t)s->G * dsa::kBins * 4;
   fixed += up(sizeof(dsa::Misc), 16);
   fixed += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 2 * dsa::kMaxQBufs + 1) * 8;
-  fixed += (size_t)s->NB * dsa::kScaleSlotBytes;  // scale ring: NS + NB slots
-  const size_t per_stage = dsa::kStageBytes + dsa::kScaleSlotBytes;
+  fixed += (size_t)s->NB * s->BPS * dsa::kScaleSlotBytes;  // scale ring: NS + NB slots
+  const size_t per_stage = (size_t)s->BPS * (dsa::kStageBytes + dsa::kScaleSlotBytes);
   const size_t budget = kSmemLimit - 1024 - 64;
   if (fixed + 2 * per_stage > budget) return false;
   s->NS = (int)((budget - fixed) / per_stage);
   if (s->NS > dsa::kMaxStages) s->NS = dsa::kMaxStages;
   s->NR = s->NS + s->NB;
   size_t o = 0;  // stages first: every key stage starts on a 1024-byte boundary
-  s->offs.off_stage = (uint32_t)o; o += (size_t)s->NS * dsa::kStageBytes;
-  s->offs.off_scale = (uint32_t)o; o += (size_t)s->NR * dsa::kScaleSlotBytes;
+  s->offs.off_stage = (uint32_t)o; o += (size_t)s->NS * s->BPS * dsa::kStageBytes;
+  s->offs.off_scale = (uint32_t)o; o += (size_t)s->NR * s->BPS * dsa::kScaleSlotBytes;
   s->offs.off_q = (uint32_t)o;     o += (size_t)s->NQ * s->q_bytes;
   s->offs.off_ckeys = (uint32_t)o; o += up((size_t)s->G * s->C * 4, 16);
   s->offs.off_cidx = (uint32_t)o;  o += up((size_t)s->G * s->C * 4, 16);
@@ -166,15 +179,6 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   o += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 2 * dsa::kMaxQBufs + 1) * 8;
   s->smem_bytes = o + 1024;  // slack for aligning the dynamic base to 1024
   return s->smem_bytes <= kSmemLimit;
-}
-
-// Balance policy: the smallest per-CTA share of key tiles worth a piece of
-// its own (DSA_MIN_SPLIT, in keys, overrides the default of 1024).
-int env_int(const char* name, int dflt, int lo, int hi) {
-  const char* v = getenv(name);
-  if (!v || !*v) return dflt;
-  const int x = atoi(v);
-  return x < lo ? lo : (x > hi ? hi : x);
 }
 
 template <int H>
@@ -298,6 +302,7 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   p.NB = s.NB;
   p.NQ = s.NQ;
   p.NR = s.NR;
+  p.BPS = s.BPS;
   p.q_bytes = s.q_bytes;
   p.n_max = s.n_max;
   p.q_box_per_token = s.q_box_per_token;

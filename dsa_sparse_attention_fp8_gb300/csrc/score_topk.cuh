@@ -62,6 +62,7 @@ struct ScoreParams {
   const float* q_scale;
   const float* w;
   int T, H, G, k, C, NS, NB, NQ, NR, n_max;
+  int BPS;           // 128-key MMA blocks per pipeline stage (1 or 2); a tile = one stage
   int q_box_per_token;
   uint32_t q_bytes;  // bytes of one query-tile buffer
   const Item* items;
@@ -702,8 +703,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       // the MMA commit plus the issuing thread's own arrival (which publishes the
       // tile's scales, observed through the full barrier, to the epilogue)
       mbar_init(bar_tfull + 8 * b, 2);
-      // decode layout: one warpgroup reads a tile; otherwise both do
-      mbar_init(bar_tempty + 8 * b, p.G == 1 ? kEpiWarps / 2 : kEpiWarps);
+      // decode layout with one block per tile: one warpgroup reads a tile;
+      // otherwise both do (each warp arrives once per tile)
+      mbar_init(bar_tempty + 8 * b, (p.G == 1 && p.BPS == 1) ? kEpiWarps / 2 : kEpiWarps);
     }
     for (int b = 0; b < p.NQ; ++b) {
       mbar_init(bar_qfull + 8 * b, 1);
@@ -745,8 +747,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     // fetched one chunk ahead.
     int stage = 0;
     uint32_t sphase = 0;
-    uint32_t issued_mask = 0;
-    uint32_t last_par[kMaxStages];
     int q_last[kMaxQBufs] = {-1, -1};
     int item_i = 0;
     long long seq = 0;  // tile sequence number of this CTA (all roles count alike)
@@ -771,53 +771,59 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           tma_load_2d(smem_u32(q_tile), &tm_q, 0, I.t0 * H, bar_qfull + 8 * qb);
         }
       }
-      const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
+      const int KS = kTileKeys * p.BPS;  // keys per tile
+      const int ppt = 2 * p.BPS;         // pages per tile
+      const int tpc = 32 / ppt;          // tiles per 32-page chunk
+      const uint32_t stage_bytes = (uint32_t)(p.BPS * kStageBytes);
+      const uint32_t slot_bytes = (uint32_t)(p.BPS * kScaleSlotBytes);
+      const int ntiles = (I.k1 - I.k0 + KS - 1) / KS;
       const int32_t* bt_row = p.block_table + (int64_t)I.r * p.max_blocks;
       const int page0 = I.k0 / kPageTokens;
       // a chunk's ids are loaded one chunk ahead and only checked when used, so
       // the warp never waits for the load
       auto in_range = [&](int chunk) {
-        return chunk * 16 < ntiles && (page0 + chunk * 32 + lane) * kPageTokens < I.k1;
+        return chunk * tpc < ntiles && (page0 + chunk * 32 + lane) * kPageTokens < I.k1;
       };
       auto fetch = [&](int chunk) -> int32_t {
         return in_range(chunk) ? __ldg(bt_row + page0 + chunk * 32 + lane) : -1;
       };
       int32_t raw = fetch(0);
-      for (int c = 0; c * 16 < ntiles && ok; ++c) {
-        int64_t cur = -1;  // this lane's page of the chunk, -1 if none or invalid
+      for (int c = 0; c * tpc < ntiles && ok; ++c) {
+        int32_t cur = -1;  // this lane's page of the chunk, -1 if none or invalid
         if (in_range(c)) {
           if (raw >= 0 && (int64_t)raw < p.num_pages) cur = raw;
           else raise_status(p.status, kStatusBadPage);
         }
         raw = fetch(c + 1);
-        const int jend = min(16, ntiles - c * 16);
+        const int jend = min(tpc, ntiles - c * tpc);
         for (int jj = 0; jj < jend; ++jj, ++seq) {
-          const int64_t pg0 = __shfl_sync(0xffffffffu, cur, 2 * jj);
-          const int64_t pg1 = __shfl_sync(0xffffffffu, cur, 2 * jj + 1);
+          // the tile's pages are held by chunk lanes first .. first + ppt - 1,
+          // and those lanes issue their own page copies
+          const int first = ppt * jj;
+          const bool my_page = lane >= first && lane < first + ppt && cur >= 0;
+          const uint32_t pages = __ballot_sync(0xffffffffu, my_page);
+          // scale chunk h*32 + lane (16 bytes) belongs to the tile's page 2h + lane/16
+          const int32_t sp0 = __shfl_sync(0xffffffffu, cur, first + (lane >> 4));
+          const int32_t sp1 = __shfl_sync(0xffffffffu, cur, (first + 2 + (lane >> 4)) & 31);
           okv = 1;
           if (lane == 0) okv = mbar_wait(bar_empty + 8 * stage, sphase ^ 1, abort_flag);
           if (!__shfl_sync(0xffffffffu, okv, 0)) { ok = false; break; }
-          const int64_t mine = lane < 16 ? pg0 : pg1;
-          const uint8_t* src =
-              mine >= 0 ? p.k_cache + mine * kPageBytes + kPageScaleOffset + (lane & 15) * 16
-                        : p.k_cache;
-          cp_async16(scale_ring_s + (uint32_t)(seq % p.NR) * kScaleSlotBytes + lane * 16, src,
-                     mine >= 0 ? 16u : 0u);
+          const uint32_t slot = scale_ring_s + (uint32_t)(seq % p.NR) * slot_bytes;
+          const uint8_t* scales = p.k_cache + kPageScaleOffset + (lane & 15) * 16;
+          cp_async16(slot + (uint32_t)lane * 16u, sp0 >= 0 ? scales + (int64_t)sp0 * kPageBytes : p.k_cache,
+                     sp0 >= 0 ? 16u : 0u);
+          if (p.BPS == 2)
+            cp_async16(slot + (uint32_t)(32 + lane) * 16u,
+                       sp1 >= 0 ? scales + (int64_t)sp1 * kPageBytes : p.k_cache, sp1 >= 0 ? 16u : 0u);
           cp_async_arrive_noinc(bar_full + 8 * stage);
-          if (lane == 0) {
-            const uint32_t bytes = (pg0 >= 0 ? kPageTokens * kHeadDim : 0) +
-                                   (pg1 >= 0 ? kPageTokens * kHeadDim : 0);
-            mbar_arrive_expect_tx(bar_full + 8 * stage, bytes);
-            const uint32_t dst = smem_u32(stage_base + stage * kStageBytes);
-            if (pg0 >= 0)
-              tma_load_2d(dst, &tm_k, 0, (int32_t)(pg0 * (kPageBytes / kHeadDim)),
-                          bar_full + 8 * stage);
-            if (pg1 >= 0)
-              tma_load_2d(dst + kPageTokens * kHeadDim, &tm_k, 0,
-                          (int32_t)(pg1 * (kPageBytes / kHeadDim)), bar_full + 8 * stage);
-          }
-          issued_mask |= 1u << stage;
-          last_par[stage] = sphase;
+          if (lane == 0)
+            mbar_arrive_expect_tx(bar_full + 8 * stage,
+                                  (uint32_t)__popc(pages) * (uint32_t)(kPageTokens * kHeadDim));
+          __syncwarp();
+          if (my_page)
+            tma_load_2d(smem_u32(stage_base) + (uint32_t)stage * stage_bytes +
+                            (uint32_t)((lane - first) * kPageTokens * kHeadDim),
+                        &tm_k, 0, cur * (kPageBytes / kHeadDim), bar_full + 8 * stage);
           if (++stage == p.NS) { stage = 0; sphase ^= 1; }
         }
       }
@@ -827,9 +833,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         *abort_flag = 1;
         raise_status(p.status, kStatusTimeout);
       }
-      // never leave with bulk copies in flight into this CTA's shared memory
-      for (int s = 0; s < p.NS; ++s)
-        if (issued_mask & (1u << s)) mbar_wait(bar_full + 8 * s, last_par[s], nullptr);
+      // never leave with bulk copies in flight into this CTA's shared memory:
+      // wait for the last tile issued on every stage (tiles 0 .. seq-1, tile t
+      // on stage t % NS in phase (t / NS) & 1)
+      for (int s = 0; s < p.NS; ++s) {
+        if (seq > s) {
+          const long long t_last = s + (long long)p.NS * ((seq - 1 - s) / p.NS);
+          mbar_wait(bar_full + 8 * s, (uint32_t)((t_last / p.NS) & 1), nullptr);
+        }
+      }
       for (int b = 0; b < p.NQ; ++b)
         if (q_last[b] >= 0) mbar_wait(bar_qfull + 8 * b, (uint32_t)((q_last[b] / p.NQ) & 1), nullptr);
     }
@@ -851,17 +863,21 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         tc_fence_after();
         const uint32_t qaddr = smem_u32(q_base + qb * p.q_bytes);
-        const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
+        const int ntiles = (I.k1 - I.k0 + kTileKeys * p.BPS - 1) / (kTileKeys * p.BPS);
         for (int j = 0; j < ntiles; ++j) {
           if (!mbar_wait(bar_full + 8 * stage, sphase, abort_flag)) { ok = false; break; }
           if (!mbar_wait(bar_tempty + 8 * acc, aphase ^ 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
           mbar_arrive(bar_tfull + 8 * acc);  // the tile's scales (seen via full) are ready
-          const uint32_t aaddr = smem_u32(stage_base + stage * kStageBytes);
-          const uint32_t d = tmem_base + (uint32_t)(acc * p.n_max);
+          const uint32_t aaddr = smem_u32(stage_base) + (uint32_t)(stage * p.BPS * kStageBytes);
+          const uint32_t d = tmem_base + (uint32_t)(acc * p.BPS * p.n_max);
+          for (int b = 0; b < p.BPS; ++b) {
 #pragma unroll
-          for (int kk = 0; kk < kHeadDim / 32; ++kk)
-            umma_f8(d, sw128_desc(aaddr + kk * 32), sw128_desc(qaddr + kk * 32), idesc, kk > 0);
+            for (int kk = 0; kk < kHeadDim / 32; ++kk)
+              umma_f8(d + (uint32_t)(b * p.n_max),
+                      sw128_desc(aaddr + (uint32_t)(b * kStageBytes) + kk * 32),
+                      sw128_desc(qaddr + kk * 32), idesc, kk > 0);
+          }
           umma_commit(bar_empty + 8 * stage);
           umma_commit(bar_tfull + 8 * acc);
           if (++stage == p.NS) { stage = 0; sphase ^= 1; }
@@ -931,17 +947,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
       for (int g = g_first; g < I.gcount; g += 2) clear_bins(S, hist_of(g), kBins);
       named_bar_sync(3, 256);
-      const int ntiles = (I.k1 - I.k0 + kTileKeys - 1) / kTileKeys;
+      const int KS = kTileKeys * p.BPS;
+      const int ntiles = (I.k1 - I.k0 + KS - 1) / KS;
+      const int units = ntiles * p.BPS;  // 128-key blocks of the item
       const bool may_fill = (I.k1 - I.k0) > p.C;
-      const int j0 = alt ? wg : 0;
-      const int iters = alt ? (ntiles + 1) / 2 : ntiles;
+      const int u0 = alt ? wg : 0;
+      const int iters = alt ? (units + 1) / 2 : units;
       for (int m = 0; m < iters; ++m) {
-        const int j = j0 + m * step;
-        if (j < ntiles && ok) {
+        const int u = u0 + m * step;  // block u = (tile j, block b of the tile)
+        const int j = u / p.BPS, b = u - j * p.BPS;
+        if (u < units && ok) {
           const long long seq = tile_base + j;
           const int acc = (int)(seq % p.NB);
           const uint32_t aphase = (uint32_t)((seq / p.NB) & 1);
-          const int key = I.k0 + j * kTileKeys + row;
+          const int key = I.k0 + j * KS + b * kTileKeys + row;
           // no early exit on the abort flag here: the warps of a warpgroup must take
           // the same branch, so they all wait on the same phase with the same limit
           if (!mbar_wait(bar_tfull + 8 * acc, aphase, nullptr)) ok = false;
@@ -949,10 +968,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             tc_fence_after();
             // the key's scale; zero (never a written scale) for a page outside the pool
             const float sc = __uint_as_float(
-                lds_u32(scale_ring_s + (uint32_t)(seq % p.NR) * kScaleSlotBytes + row * 4));
+                lds_u32(scale_ring_s + (uint32_t)(seq % p.NR) * (uint32_t)(p.BPS * kScaleSlotBytes) +
+                        (uint32_t)(b * kTileKeys + row) * 4u));
             const bool kvalid = sc > 0.f && key < I.k1;
-            const uint32_t tbase =
-                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * p.n_max);
+            const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) +
+                                   (uint32_t)((acc * p.BPS + b) * p.n_max);
             for (int g = g_first; g < I.gcount; g += 2) {
               const float sum = relu_weighted_sum<H>(tbase + (uint32_t)(g * H), wq_all + g * H);
               const float score = sum * sc;
