@@ -638,28 +638,41 @@ __device__ __noinline__ void merge_pieces(const Selector S, const ScoreParams& p
   slot_select(S, kSelRow, ts->count, ck_s, ci_s, hist_s, need, 0, nullptr, out_row + n_def, nullptr);
 }
 
+// sum_h wq[h] * ReLU(acc[h]) over the H accumulator columns at taddr (this
+// thread's TMEM lane); wq_s is the shared-memory address of the H weights.
+// The weights are read (explicit shared loads) before the tensor-memory
+// wait, and four partial sums keep the FMA chains short.
 template <int H>
-__device__ __forceinline__ float relu_weighted_sum(uint32_t taddr, const float* wq) {
+__device__ __forceinline__ float relu_weighted_sum(uint32_t taddr, uint32_t wq_s) {
   constexpr int CH = H >= 32 ? 32 : H;              // columns per tcgen05.ld
   constexpr int BATCH = H >= 64 ? 64 : H;           // columns loaded before one wait
-  float acc0 = 0.f, acc1 = 0.f;
+  constexpr int NA = BATCH >= 16 ? 4 : BATCH / 4;   // partial sums
+  float acc[NA];
+#pragma unroll
+  for (int i = 0; i < NA; ++i) acc[i] = 0.f;
 #pragma unroll
   for (int c0 = 0; c0 < H; c0 += BATCH) {
+    uint4 ww[BATCH / 4];
+#pragma unroll
+    for (int i = 0; i < BATCH / 4; ++i) ww[i] = lds_v4(wq_s + 4u * (uint32_t)(c0 + 4 * i));
     uint32_t v[BATCH];
 #pragma unroll
     for (int c = 0; c < BATCH; c += CH) tmem_ld<CH>(taddr + c0 + c, v + c);
     tmem_ld_wait();
-    const float4* w4 = reinterpret_cast<const float4*>(wq + c0);
 #pragma unroll
     for (int h = 0; h < BATCH; h += 4) {
-      const float4 ww = w4[h >> 2];
-      acc0 = fmaf(ww.x, fmaxf(__uint_as_float(v[h + 0]), 0.f), acc0);
-      acc1 = fmaf(ww.y, fmaxf(__uint_as_float(v[h + 1]), 0.f), acc1);
-      acc0 = fmaf(ww.z, fmaxf(__uint_as_float(v[h + 2]), 0.f), acc0);
-      acc1 = fmaf(ww.w, fmaxf(__uint_as_float(v[h + 3]), 0.f), acc1);
+      float& a = acc[(h / 4) % NA];
+      a = fmaf(__uint_as_float(ww[h / 4].x), fmaxf(__uint_as_float(v[h + 0]), 0.f), a);
+      a = fmaf(__uint_as_float(ww[h / 4].y), fmaxf(__uint_as_float(v[h + 1]), 0.f), a);
+      a = fmaf(__uint_as_float(ww[h / 4].z), fmaxf(__uint_as_float(v[h + 2]), 0.f), a);
+      a = fmaf(__uint_as_float(ww[h / 4].w), fmaxf(__uint_as_float(v[h + 3]), 0.f), a);
     }
   }
-  return acc0 + acc1;
+#pragma unroll
+  for (int s2 = NA / 2; s2 >= 1; s2 /= 2)
+#pragma unroll
+    for (int i = 0; i < s2; ++i) acc[i] += acc[i + s2];
+  return acc[0];
 }
 
 template <int H>
@@ -974,7 +987,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) +
                                    (uint32_t)((acc * p.BPS + b) * p.n_max);
             for (int g = g_first; g < I.gcount; g += 2) {
-              const float sum = relu_weighted_sum<H>(tbase + (uint32_t)(g * H), wq_all + g * H);
+              const float sum =
+                  relu_weighted_sum<H>(tbase + (uint32_t)(g * H), smem_u32(wq_all + g * H));
               const float score = sum * sc;
               const bool valid = kvalid && key <= tok[g].pos;
               if (p.scores_out && valid && key < p.scores_ld)
