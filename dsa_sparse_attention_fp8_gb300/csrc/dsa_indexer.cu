@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -110,27 +111,34 @@ struct ScoreShape {
 
 constexpr size_t kSmemLimit = 232448;  // 227 KB opt-in per block on sm_100-family
 
-// Candidate-buffer capacity per query row: k plus room for the candidates
-// appended between two fill checks.  A decode layout (one row per group)
-// takes more, so that long pieces shrink their buffer rarely, within the
-// shared memory left after four 256-key pipeline stages.
-int candidate_capacity(int k, bool decode) {
-  int c = k + 1024;
-  if (decode && c < 6144) c = 6144;
-  return (c + 127) / 128 * 128;
+// Shared memory for the rows' candidate buffers and histograms of a group.
+constexpr int kRowBudget = 128 * 1024;
+
+// Candidate-buffer capacity per query row: at least k plus room for the
+// candidates appended between two fill checks, and as much more as the rows'
+// budget allows (up to 8192), so that rows shrink their buffer rarely.  A
+// decode layout (one row per group) takes 6144, which leaves room for four
+// 256-key pipeline stages.
+int candidate_capacity(int k, int G, bool decode) {
+  if (decode) return std::max(6144, (k + 1024 + 127) / 128 * 128);
+  int c = ((kRowBudget / G - dsa::kBins * 4) / 8) / 128 * 128;
+  c = std::min(c, 8192);
+  return std::max(c, (k + 1024 + 127) / 128 * 128);
 }
-// Candidate counts are packed in 16 bits during selection scans.
-static_assert(DSA_MAX_TOPK + 1024 + 6144 < 65536, "candidate buffer too large");
 
 // Rows per group: one row per decode batch (no request has more rows than
-// one), else as many rows as fill N = 256 of the MMA while each row's
-// candidate buffer and histogram stay within 128 KB of shared memory.
+// one), else as many rows as fill N = 128 of the MMA while each row's
+// minimal candidate buffer and histogram fit the rows' budget.  Two rows of
+// 64 heads with 7K-candidate buffers measured faster than four with 3K
+// (fewer buffer shrinks outweigh the second read of each key tile, which
+// hits L2).  DSA_GROUP_ROWS lowers it further.
 int choose_group(int T, int R, int H, int k) {
   if (T <= R) return 1;
-  int g = 256 / H;
-  const int per_row = candidate_capacity(k, false) * 8 + dsa::kBins * 4;
-  const int by_smem = (128 * 1024) / per_row;
+  int g = H >= 128 ? 1 : 128 / H;
+  const int per_row = ((k + 1024 + 127) / 128 * 128) * 8 + dsa::kBins * 4;
+  const int by_smem = kRowBudget / per_row;
   if (g > by_smem) g = by_smem;
+  g = std::min(g, env_int("DSA_GROUP_ROWS", g, 1, 256));
   return g < 1 ? 1 : g;
 }
 
@@ -138,7 +146,7 @@ size_t up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   s->G = choose_group(T, R, H, k);
-  s->C = candidate_capacity(k, s->G == 1);
+  s->C = candidate_capacity(k, s->G, s->G == 1);
   s->q_box_per_token = (H % 8 == 0) ? 1 : 0;
   s->n_max = (s->G * H + 15) / 16 * 16;
   // decode layout: 256-key stages (two 128-key MMA blocks) when tensor memory
