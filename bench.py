@@ -297,7 +297,8 @@ def main():
     if not args.no_graph:
         step.capture()
     for _ in range(args.warmup):
-        step.run()
+        step.run(timed=False)
+        step.run(timed=True)
     torch.cuda.synchronize()
     assert step.status.item() == 0, f"device status {step.status.item()}"
     launches = step.launches_per_step
@@ -305,7 +306,8 @@ def main():
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     score_ms = []
-    kernel_timing = "events inside the captured step" if not args.no_graph else "events around each launch"
+    kernel_timing = ("events inside a second captured pass of the timed steps" if not args.no_graph
+                     else "events around each launch")
     timing_failed = False
     if world > 1:
         torch.distributed.barrier()
@@ -315,15 +317,21 @@ def main():
         for i in range(args.steps):
             flush.fill_(i & 0xFF)                 # evict L2 between timed steps
             ev0[i].record(stream)
-            step.run()
+            step.run(timed=False)
             ev1[i].record(stream)
             ev1[i].synchronize()
+        torch.cuda.synchronize()
+        # the same steps again with events around every scoring kernel (the
+        # roofline's per-launch durations)
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            step.run(timed=True)
+            torch.cuda.synchronize()
             if not timing_failed:
                 try:
                     score_ms.extend(step.score_kernel_ms())
                 except RuntimeError:
                     timing_failed = True
-        torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
     if world > 1:
         torch.distributed.barrier()

@@ -91,9 +91,10 @@ int make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t b
 }
 
 // Tuning overrides read from the environment: DSA_MIN_SPLIT (keys, the
-// smallest per-CTA share of key tiles worth a piece of its own, default 1024)
-// and DSA_STAGE_KEYS (128 or 256, the decode layout's keys per pipeline
-// stage, default 256).
+// smallest per-CTA share of key tiles worth a piece of its own, default 1024),
+// DSA_STAGE_KEYS (128 or 256, the decode layout's keys per pipeline stage,
+// default 256), DSA_GROUP_ROWS (cap on query rows per group) and DSA_PDL (0
+// turns off programmatic dependent launch of the scoring kernel).
 int env_int(const char* name, int dflt, int lo, int hi) {
   const char* v = getenv(name);
   if (!v || !*v) return dflt;
@@ -200,7 +201,21 @@ int launch_score_h(const CUtensorMap& tk, const CUtensorMap& tq, const dsa::Scor
   });
   if (attr_err != cudaSuccess)
     return fail(DSA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
-  dsa::score_topk_kernel<H><<<grid, dsa::kScoreThreads, smem, st>>>(tk, tq, p);
+  // programmatic stream serialisation: the kernel's prologue (TMEM
+  // allocation, barrier set-up) overlaps the preceding plan or cache-write
+  // kernel; it waits for that kernel's results before reading them
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(dsa::kScoreThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = env_int("DSA_PDL", 1, 0, 1);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, dsa::score_topk_kernel<H>, tk, tq, p);
+  if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "score_topk_kernel launch: %s", cudaGetErrorString(e));
   return check_launch("score_topk_kernel");
 }
 

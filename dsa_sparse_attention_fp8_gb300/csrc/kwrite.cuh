@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(256) write_k_kernel(
     const int32_t* __restrict__ seq_lens, int R, const int32_t* __restrict__ block_table,
     int max_blocks, uint8_t* __restrict__ k_cache, int64_t num_pages,
     int64_t* __restrict__ slot_mapping, int32_t* status) {
+  pdl_launch_dependents();  // the scoring kernel's prologue may overlap this write
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;

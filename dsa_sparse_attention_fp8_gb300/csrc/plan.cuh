@@ -137,6 +137,7 @@ __device__ __forceinline__ long long group_keys(long long P, int q, int G, int g
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
+  pdl_launch_dependents();  // the scoring kernel's prologue may overlap the plan
   __shared__ long long warp_sums[32];
   __shared__ long long s_Q;
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.L.header);

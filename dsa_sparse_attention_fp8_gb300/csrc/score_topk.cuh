@@ -741,6 +741,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // everything above overlaps the preceding kernel (plan or cache write) when
+  // launched with programmatic stream serialisation; its outputs are read below
+  pdl_wait();
   const uint32_t tmem_base = misc->tmem_base;
   const int it_begin = p.cta_start[blockIdx.x];
   const int it_end = p.cta_start[blockIdx.x + 1];

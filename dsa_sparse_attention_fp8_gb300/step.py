@@ -56,7 +56,8 @@ class IndexerStep:
                 io["score_begin"].record()
                 io["score_end"].record()
             self.layers.append(io)
-        self.graph: Optional[torch.cuda.CUDAGraph] = None
+        self.graph: Optional[torch.cuda.CUDAGraph] = None        # with the kernel-timing events
+        self.graph_plain: Optional[torch.cuda.CUDAGraph] = None  # without them
         self.launches_per_step = 0
 
     # -------------------------------------------------------------- inputs
@@ -73,28 +74,43 @@ class IndexerStep:
         io["w"].copy_(w, non_blocking=non_blocking)
 
     # -------------------------------------------------------------- running
-    def launch(self) -> None:
-        binding.layer_stack_run(self.layers, self.pattern, self.freq, self.offset, self.H,
+    def launch(self, timed: bool = True) -> None:
+        """One step.  timed=False leaves out the scoring kernels' timing events
+        (an event between the cache write and the scoring kernel would keep
+        the scoring kernel from overlapping the write's tail)."""
+        layers = self.layers
+        if not timed:
+            layers = [None if io is None else {k: v for k, v in io.items()
+                                               if k not in ("score_begin", "score_end")}
+                      for io in self.layers]
+        binding.layer_stack_run(layers, self.pattern, self.freq, self.offset, self.H,
                                 self.query_start_loc, self.seq_lens, self.block_table,
                                 self.num_pages, self.k, self.topk, self.workspace,
                                 status=self.status, T=self.T)
         self.launches_per_step = binding.last_launch_count()
 
     def capture(self) -> None:
-        """Record one step as a CUDA graph (after one eager step for warm-up)."""
+        """Record one step as two CUDA graphs, with and without the kernel-timing
+        events (after one eager step for warm-up)."""
         self.launch()
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.launch()
+            self.launch(timed=True)
         torch.cuda.synchronize()
         self.graph = g
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.launch(timed=False)
+        torch.cuda.synchronize()
+        self.graph_plain = g
 
-    def run(self) -> None:
-        if self.graph is not None:
-            self.graph.replay()
+    def run(self, timed: bool = True) -> None:
+        g = self.graph if timed else self.graph_plain
+        if g is not None:
+            g.replay()
         else:
-            self.launch()
+            self.launch(timed)
 
     def score_kernel_ms(self) -> list[float]:
         """Durations of the last step's scoring kernels (needs time_score_kernels)."""
