@@ -379,7 +379,10 @@ def main():
     peaks = read_peaks()
     k_ms = sum(score_ms) / len(score_ms)
     rows_bytes = wl.T * (wl.H * (128 + 4 + 4) + wl.index_topk * 4)   # q, q_scale, w in; top-k out
-    alg_bytes = wl.pairs_per_full_layer * BYTES_PER_PAIR + rows_bytes
+    # every key of a request is read once, whatever the number of its query rows
+    # (one row per request in a decode batch: one key per pair)
+    key_bytes = float(wl.seq_lens[wl.q_lens > 0].astype(np.int64).sum()) * BYTES_PER_PAIR
+    alg_bytes = key_bytes + rows_bytes
     achieved = alg_bytes / (k_ms * 1e-3) / 1e9
     traffic = profiled_traffic(wl.name)
     # FP8 tensor peak: the measured BF16 GEMM rate times the nominal FP8:BF16
@@ -392,9 +395,10 @@ def main():
     tensor = {"bound": "tensor", "achieved": tflops, "peak": fp8_peak, "unit": "TFLOP/s",
               "frac": tflops / fp8_peak, "traffic": traffic,
               "peak_note": f"{peaks['source']} bf16 x 2 (nominal fp8:bf16 dense ratio)"}
-    # decode batches (at most one query row per request) stream every key once:
-    # HBM-bound; prefill chunks reuse each key tile across rows: tensor-bound
-    prefill = wl.T > wl.R
+    # HBM-bound unless the work's FP8 FLOP per algorithmic byte exceed the
+    # machine balance (peak FLOP/s over peak bytes/s): prefill chunks reuse each
+    # key across many rows, decode batches (also with a few MTP rows) do not
+    prefill = alg_flops / alg_bytes > fp8_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     roof = dict(tensor if prefill else hbm)
     roof.update({"kernel": "score_topk_kernel", "kernel_ms": k_ms, "algorithmic_bytes": alg_bytes,
                  "algorithmic_flops": alg_flops, "kernel_timing": kernel_timing,

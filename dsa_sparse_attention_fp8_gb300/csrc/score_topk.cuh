@@ -232,11 +232,52 @@ __device__ __forceinline__ bool sel_tie(uint32_t key, Thresh th) {
 // registers.
 constexpr int kSelBatch = 8;
 
+// Warp-level search of a small histogram (nbins = 256 or 32, shared memory)
+// from the top for the bin where the running count reaches `need` (1 <= need
+// <= total): lane l sums the nbins/32 bins below the top l*nbins/32, a warp
+// scan finds the crossing lane, which walks its bins.  Every calling warp
+// computes the same answer, so no barrier is needed to share it.
+__device__ __forceinline__ BinCut find_bin_warp(uint32_t hist_s, int nbins, int need) {
+  const int lane = lane_id();
+  const int per = nbins >> 5;  // 8 or 1
+  const uint32_t lo = (uint32_t)(nbins - (lane + 1) * per);
+  uint32_t h[8];
+  if (per == 8) {
+    const uint4 a = lds_v4(hist_s + 4u * lo), b = lds_v4(hist_s + 4u * (lo + 4u));
+    h[0] = a.x; h[1] = a.y; h[2] = a.z; h[3] = a.w; h[4] = b.x; h[5] = b.y; h[6] = b.z; h[7] = b.w;
+  } else {
+    h[0] = lds_u32(hist_s + 4u * lo);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) h[i] = 0u;
+  }
+  uint32_t local = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) local += h[i];
+  const uint32_t inc = warp_inclusive_sum(local);
+  const uint32_t un = (uint32_t)need;
+  const int L = __ffs(__ballot_sync(0xffffffffu, inc - local < un && un <= inc)) - 1;
+  uint32_t above = inc - local, bin = lo, cnt = 0;
+  bool found = false;
+#pragma unroll
+  for (int i = 7; i >= 0; --i) {
+    const bool here = !found && i < per && un <= above + h[i];
+    bin = here ? lo + (uint32_t)i : bin;
+    cnt = here ? h[i] : cnt;
+    above += (!found && !here && i < per) ? h[i] : 0u;
+    found = found || here;
+  }
+  BinCut r;
+  r.bin = (int)__shfl_sync(0xffffffffu, bin, L);
+  r.above = (int)__shfl_sync(0xffffffffu, above, L);
+  r.cnt = (int)__shfl_sync(0xffffffffu, cnt, L);
+  return r;
+}
+
 // Exact threshold of the k-th largest of the slot's n keys, starting from the
-// level-1 bin cut `c`: refine inside that bin on key bits 20..10, then 9..0,
-// with scratch_s (2048 ints of shared memory) holding the sub-histograms.
-// Stops as soon as a whole sub-bin is taken.  The caller's reads of scratch_s
-// are complete (find_bin ends with a barrier).
+// level-1 bin cut `c`: refine inside that bin on key bits 20..13, 12..5 and
+// 4..0 (histograms of 256, 256 and 32 bins in scratch_s, each searched by
+// every warp on its own).  Stops as soon as a whole sub-bin is taken.  The
+// caller's reads of scratch_s are complete.
 __device__ __noinline__ Thresh refine_in_bin(const Selector S, uint32_t ck_s, int n, BinCut c,
                                              int k, uint32_t scratch_s) {
   Thresh th{(uint32_t)c.bin << kHistShift, k - c.above, 0};
@@ -245,11 +286,11 @@ __device__ __noinline__ Thresh refine_in_bin(const Selector S, uint32_t ck_s, in
     th.early = 1;
     return th;
   }
-  for (int level = 0; level < 2; ++level) {
-    const int shift = level == 0 ? 10 : 0;
-    const int nb = level == 0 ? 2048 : 1024;
+  for (int level = 0; level < 3; ++level) {
+    const int shift = level == 0 ? 13 : (level == 1 ? 5 : 0);
+    const int nb = level == 2 ? 32 : 256;
     const uint32_t dm = (uint32_t)nb - 1u;
-    clear_bins(S, scratch_s, nb);
+    for (int b = S.tid; b < nb; b += S.nt) sts_u32(scratch_s + 4u * (uint32_t)b, 0u);
     named_bar_sync(S.bar, S.nt);
     for (int i0 = S.tid; i0 < n; i0 += kSelBatch * S.nt) {
       uint32_t kk[kSelBatch];
@@ -264,7 +305,7 @@ __device__ __noinline__ Thresh refine_in_bin(const Selector S, uint32_t ck_s, in
                           scratch_s + 4u * ((kk[u] >> shift) & dm), 1u);
     }
     named_bar_sync(S.bar, S.nt);
-    const BinCut c2 = find_bin(S, scratch_s, nb, th.need);
+    const BinCut c2 = find_bin_warp(scratch_s, nb, th.need);
     th.need -= c2.above;
     th.prefix |= (uint32_t)c2.bin << shift;
     mask |= dm << shift;
@@ -272,6 +313,7 @@ __device__ __noinline__ Thresh refine_in_bin(const Selector S, uint32_t ck_s, in
       th.early = 1;
       break;
     }
+    named_bar_sync(S.bar, S.nt);  // every warp has read the scratch before it is cleared
   }
   return th;
 }
@@ -288,14 +330,16 @@ enum SelMode {
 // k-th largest if that fits, else exactly k.  Output order is thread-major
 // (thread t's candidates in visiting order after those of threads before
 // it): deterministic, ties at an exact threshold taken in that order up to
-// the quota.  Row output is staged in shared memory (hist_s, after its last
-// use) and copied out coalesced; in place, the kept candidates are staged in
+// the quota.  `known`, if given, is the level-1 cut of the k-th largest
+// (hist_s is then only scratch).  Row output is staged in shared memory
+// (hist_s, after its last use) and copied out coalesced; in place, the kept candidates are staged in
 // registers one batch at a time behind a barrier per batch.  Returns the
 // number written; for kSelInPlace *thr gets the admission threshold of the
 // kept set.
 __device__ __noinline__ int slot_select(const Selector S, int mode, int n, uint32_t ck_s,
                                         uint32_t ci_s, uint32_t hist_s, int k, int limit,
-                                        uint32_t* gk, int32_t* gi, uint32_t* thr) {
+                                        uint32_t* gk, int32_t* gi, uint32_t* thr,
+                                        const BinCut* known = nullptr) {
   if (mode == kSelRow && n <= k) {
     for (int i = S.tid; i < k; i += S.nt)
       __stcg(gi + i, i < n ? (int32_t)lds_u32(ci_s + 4u * (uint32_t)i) : -1);
@@ -309,7 +353,8 @@ __device__ __noinline__ int slot_select(const Selector S, int mode, int n, uint3
       }
     return n;
   }
-  const BinCut c = find_bin(S, hist_s, kBins, k);
+  // the level-1 cut, found in the histogram unless the caller knows it
+  const BinCut c = known ? *known : find_bin(S, hist_s, kBins, k);
   Thresh th;
   if (mode != kSelRow && c.above + c.cnt <= limit)
     th = Thresh{(uint32_t)c.bin << kHistShift, 0, 1};
@@ -591,12 +636,11 @@ __device__ __noinline__ void merge_pieces(const Selector S, const ScoreParams& p
         sts_u32_if(f < n_cut, ci_s + 4u * (uint32_t)f, (uint32_t)ix[u]);
       }
     }
-    // level-1 histogram of the gathered candidates: all in the cut bin
-    clear_bins(S, hist_s, kBins);
-    named_bar_sync(S.bar, S.nt);
-    if (S.tid == 0) sts_u32(hist_s + 4u * (uint32_t)c.bin, (uint32_t)n_cut);
-    named_bar_sync(S.bar, S.nt);
-    slot_select(S, kSelRow, n_cut, ck_s, ci_s, hist_s, need, 0, nullptr, out_row + n_def, nullptr);
+    named_bar_sync(S.bar, S.nt);  // the gathered candidates are visible
+    // all of them lie in the cut bin: start the selection from that cut
+    const BinCut cut{c.bin, 0, n_cut};
+    slot_select(S, kSelRow, n_cut, ck_s, ci_s, hist_s, need, 0, nullptr, out_row + n_def, nullptr,
+                &cut);
     return;
   }
   // Rare: more cut-bin candidates than the slot holds (heavily tied scores).

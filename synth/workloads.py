@@ -44,6 +44,7 @@ WORKLOAD_NAMES = {
     2: "prefix_hit_chunked_prefill",
     3: "mixed_batch",
     4: "long_context_decode",
+    5: "mtp_decode",
 }
 
 
@@ -267,4 +268,18 @@ def make_workload(workload_id: int, seed: int = 0, scale: float = 1.0) -> Worklo
                         pattern="".join(chars), freq=1, offset=2, q_lens=q_lens,
                         seq_lens=seq_lens, block_table=bt, num_pages=pool,
                         max_num_batched_tokens=R)
+    if wid == 5:
+        # 64 decode requests with one speculative (MTP) token each: 2 query rows per
+        # request, the second seeing one more key; context ~ U[1024, 8192], H=64,
+        # k=2048, 4 layers all F
+        R, q = 64, 2
+        lo, hi = 1024, 8192
+        ctx = _rng(seed, wid, 0, _T_CTX).integers(lo, hi, size=R, endpoint=True)
+        ctx = np.maximum(q + 1, np.round(ctx * scale)).astype(np.int32)
+        q_lens = np.full(R, q, np.int32)
+        pool = int(_pages_for(ctx).sum())
+        bt = _scatter_pages(seed, wid, ctx, pool, int(_pages_for(np.array([max(q + 1, round(hi * scale))]))[0]))
+        return Workload(wid, name, seed, H=64, index_topk=2048, num_layers=4, pattern=None,
+                        freq=1, offset=2, q_lens=q_lens, seq_lens=ctx, block_table=bt,
+                        num_pages=pool, max_num_batched_tokens=R * q)
     raise ValueError(f"unknown workload {workload_id}")

@@ -140,6 +140,8 @@ def test_cache_write_bit_exact(B, wid, scale):
     (1, 0.2, {"index_topk": 100}),                  # decode with selection + compaction
     (3, 1 / 64, {"index_topk": 64}),                # mixed prefill + decode rows
     (2, 1 / 32, {"index_topk": 128}),               # prefix-hit chunked prefill
+    (5, 0.25, {}),                                  # MTP decode: 2 rows per request
+    (5, 1.0, {"index_topk": 300}),                  # MTP decode, full contexts, selection
 ])
 def test_scores_and_topk(B, wid, scale, over):
     wl = _wl(wid, scale, **over)

@@ -145,6 +145,13 @@ def test_full_mixed_batch(B):
     _check_shared(full, outs)
 
 
+def test_full_mtp_decode_stack(B):
+    wl = synth.make_workload(5)                       # 64 requests x 2 rows, ctx 1024..8192
+    full, layers, outs, _ = _run_stack(B, wl, None, 1, 2, 2)
+    _check_rows(wl, 0, layers[0], outs[0], range(wl.T))
+    _check_rows(wl, 1, layers[1], outs[1], _sample_rows(wl, 8))
+
+
 def test_full_long_context_decode(B):
     wl = synth.make_workload(4)                       # 4 x (1,048,576 cached + 1) tokens
     full, layers, outs, _ = _run_stack(B, wl, "FS", 1, 2, 2)
