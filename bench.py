@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bf16", action="store_true",
+                    help="BF16 keys and queries, quantised by the cache-write launch")
     return ap.parse_args()
 
 
@@ -272,12 +274,17 @@ def main():
             continue
         io = staging.stage_layer(wl, l, meta, dev)
         caches.append(io["k_cache"])
-        host_layers[l] = tuple(t.cpu().pin_memory() for t in (io["k"], io["q_fp8"], io["q_scale"], io["w"]))
+        if args.bf16:
+            q16 = torch.from_numpy(wl.q(l)).to(dev).bfloat16()
+            ins = (io["k"].bfloat16(), q16, io["w"])
+        else:
+            ins = (io["k"], io["q_fp8"], io["q_scale"], io["w"])
+        host_layers[l] = tuple(t.cpu().pin_memory() for t in ins)
     step = IndexerStep(num_layers=wl.num_layers, pattern=wl.pattern, freq=wl.freq,
                        offset=wl.offset, H=wl.H, index_topk=wl.index_topk, T=wl.T, R=wl.R,
                        max_blocks=wl.max_blocks, num_pages=wl.num_pages,
                        max_num_batched_tokens=wl.max_num_batched_tokens, k_caches=caches,
-                       device=dev, time_score_kernels=True)
+                       device=dev, time_score_kernels=True, bf16=args.bf16)
     host_meta = tuple(torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in
                       (wl.query_start_loc, wl.seq_lens.astype(np.int32), wl.block_table))
     host = {"meta": host_meta, "layers": host_layers}
@@ -414,6 +421,8 @@ def main():
         "config": {"workload": wl.name, **{k: v for k, v in wl.describe().items() if k != "workload"},
                    "pairs_per_step": pairs_per_step, "full_layers": n_full,
                    "cuda_graph": not args.no_graph, "l2": "flushed between timed steps",
+                   "inputs": ("bf16 keys and queries, quantised in the cache-write launch"
+                              if args.bf16 else "fp32 keys, e4m3 queries + fp32 scales"),
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": wl.T * n_full * world / (ms * 1e-3),
         "roofline": roof,

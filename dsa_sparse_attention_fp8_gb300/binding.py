@@ -40,6 +40,7 @@ EXPORTS = (
     "dsa_last_error",
     "dsa_last_launch_count",
     "dsa_indexer_write_k",
+    "dsa_indexer_write_k_bf16",
     "dsa_quantize_fp8_blocks",
     "dsa_indexer_workspace_bytes",
     "dsa_indexer_score_topk",
@@ -47,6 +48,7 @@ EXPORTS = (
     "dsa_indexer_no_alloc_workspace_bytes",
     "dsa_layer_is_full",
     "dsa_layer_stack_run",
+    "dsa_layer_stack_run_bf16",
 )
 
 
@@ -63,6 +65,19 @@ class LayerIO(ctypes.Structure):
         ("q_scale", ctypes.c_void_p),
         ("w", ctypes.c_void_p),
         ("k_cache", ctypes.c_void_p),
+        ("score_begin", ctypes.c_void_p),
+        ("score_end", ctypes.c_void_p),
+    ]
+
+
+class LayerIOBf16(ctypes.Structure):
+    _fields_ = [
+        ("k", ctypes.c_void_p),
+        ("q", ctypes.c_void_p),
+        ("w", ctypes.c_void_p),
+        ("k_cache", ctypes.c_void_p),
+        ("q_fp8", ctypes.c_void_p),
+        ("q_scale", ctypes.c_void_p),
         ("score_begin", ctypes.c_void_p),
         ("score_end", ctypes.c_void_p),
     ]
@@ -85,6 +100,9 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.dsa_last_launch_count.argtypes = []
     lib.dsa_indexer_write_k.restype = _I
     lib.dsa_indexer_write_k.argtypes = [_P, _I, _P, _P, _I, _P, _I, _P, _I64, _P, _P, _P]
+    lib.dsa_indexer_write_k_bf16.restype = _I
+    lib.dsa_indexer_write_k_bf16.argtypes = [
+        _P, _I, _P, _P, _I, _P, _I, _P, _I64, _P, _I, _P, _P, _P, _P, _P]
     lib.dsa_quantize_fp8_blocks.restype = _I
     lib.dsa_quantize_fp8_blocks.argtypes = [_P, _I64, _P, _P, _P]
     lib.dsa_indexer_workspace_bytes.restype = _SZ
@@ -103,6 +121,10 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.dsa_layer_stack_run.argtypes = [
         _I, ctypes.c_char_p, _I, _I, ctypes.POINTER(LayerIO), _I, _I, _P, _P, _I, _P, _I, _I64,
         _I, _P, _I, ctypes.POINTER(ctypes.c_void_p), _P, _P, _SZ, _P, _P]
+    lib.dsa_layer_stack_run_bf16.restype = _I
+    lib.dsa_layer_stack_run_bf16.argtypes = [
+        _I, ctypes.c_char_p, _I, _I, ctypes.POINTER(LayerIOBf16), _I, _I, _P, _P, _I, _P, _I,
+        _I64, _I, _P, _I, ctypes.POINTER(ctypes.c_void_p), _P, _P, _SZ, _P, _P]
 
 
 def load() -> ctypes.CDLL:
@@ -221,6 +243,38 @@ def write_k(k: torch.Tensor, query_start_loc: torch.Tensor, seq_lens: torch.Tens
         _stream(stream)))
 
 
+def write_k_bf16(k: torch.Tensor, query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
+                 block_table: torch.Tensor, k_cache: torch.Tensor,
+                 q: Optional[torch.Tensor] = None, q_fp8: Optional[torch.Tensor] = None,
+                 q_scale: Optional[torch.Tensor] = None,
+                 slot_mapping: Optional[torch.Tensor] = None,
+                 status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Cache write of BF16 keys; with ``q`` [T, H, 128] BF16 the same launch
+    quantises the query rows into ``q_fp8`` [T, H, 128] uint8 and ``q_scale``
+    [T, H] float32."""
+    T = k.shape[0]
+    R = seq_lens.shape[0]
+    _need(k, "k", torch.bfloat16, (T, HEAD_DIM))
+    _need(query_start_loc, "query_start_loc", torch.int32, (R + 1,))
+    _need(seq_lens, "seq_lens", torch.int32, (R,))
+    _need(block_table, "block_table", torch.int32, (R, None))
+    _need(k_cache, "k_cache", torch.uint8, (None, PAGE_BYTES))
+    H = 0
+    if q is not None:
+        H = q.shape[1]
+        _need(q, "q", torch.bfloat16, (T, H, HEAD_DIM))
+        _need(q_fp8, "q_fp8", torch.uint8, (T, H, HEAD_DIM))
+        _need(q_scale, "q_scale", torch.float32, (T, H))
+    if slot_mapping is not None:
+        _need(slot_mapping, "slot_mapping", torch.int64, (T,))
+    if status is not None:
+        _need(status, "status", torch.int32)
+    _check(load().dsa_indexer_write_k_bf16(
+        _ptr(k), T, _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table),
+        block_table.shape[1], _ptr(k_cache), k_cache.shape[0], _ptr(q), H, _ptr(q_fp8),
+        _ptr(q_scale), _ptr(slot_mapping), _ptr(status), _stream(stream)))
+
+
 def score_topk(q_fp8: torch.Tensor, q_scale: torch.Tensor, w: torch.Tensor,
                k_cache: torch.Tensor, query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
                block_table: torch.Tensor, index_topk: int, topk_buffer: torch.Tensor,
@@ -327,6 +381,63 @@ def layer_stack_run(layers: Sequence[Optional[dict]], pattern: Optional[str], fr
     if status is not None:
         _need(status, "status", torch.int32)
     _check(load().dsa_layer_stack_run(
+        L, None if pattern is None else pattern.encode(), freq, offset, arr, T, H,
+        _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table), block_table.shape[1],
+        num_pages, index_topk, _ptr(topk_buffer), topk_buffer.shape[0], outs, _ptr(slot_mapping),
+        _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)))
+
+
+def layer_stack_run_bf16(layers: Sequence[Optional[dict]], pattern: Optional[str], freq: int,
+                         offset: int, H: int, query_start_loc: torch.Tensor,
+                         seq_lens: torch.Tensor, block_table: torch.Tensor, num_pages: int,
+                         index_topk: int, topk_buffer: torch.Tensor, workspace: torch.Tensor,
+                         per_layer_out: Optional[Sequence[Optional[torch.Tensor]]] = None,
+                         slot_mapping: Optional[torch.Tensor] = None,
+                         status: Optional[torch.Tensor] = None, T: Optional[int] = None,
+                         stream=None) -> None:
+    """The F/S layer stack with BF16 inputs.  ``layers[l]`` is a dict with keys
+    k [T, 128] and q [T, H, 128] (BF16), w, k_cache, and the scratch q_fp8 /
+    q_scale that the cache-write launch fills, for F layers; None for S
+    layers."""
+    R = seq_lens.shape[0]
+    _need(query_start_loc, "query_start_loc", torch.int32, (R + 1,))
+    _need(seq_lens, "seq_lens", torch.int32, (R,))
+    _need(block_table, "block_table", torch.int32, (R, None))
+    _need(topk_buffer, "topk_buffer", torch.int32, (None, index_topk))
+    _need(workspace, "workspace", torch.uint8)
+    L = len(layers)
+    arr = (LayerIOBf16 * L)()
+    for i, io in enumerate(layers):
+        if io is None:
+            continue
+        if T is None:
+            T = io["k"].shape[0]
+        _need(io["k"], f"layers[{i}].k", torch.bfloat16, (T, HEAD_DIM))
+        _need(io["q"], f"layers[{i}].q", torch.bfloat16, (T, H, HEAD_DIM))
+        _need(io["w"], f"layers[{i}].w", torch.float32, (T, H))
+        _need(io["k_cache"], f"layers[{i}].k_cache", torch.uint8, (num_pages, PAGE_BYTES))
+        _need(io["q_fp8"], f"layers[{i}].q_fp8", torch.uint8, (T, H, HEAD_DIM))
+        _need(io["q_scale"], f"layers[{i}].q_scale", torch.float32, (T, H))
+        ev0, ev1 = io.get("score_begin"), io.get("score_end")
+        arr[i] = LayerIOBf16(io["k"].data_ptr(), io["q"].data_ptr(), io["w"].data_ptr(),
+                             io["k_cache"].data_ptr(), io["q_fp8"].data_ptr(),
+                             io["q_scale"].data_ptr(),
+                             None if ev0 is None else ev0.cuda_event,
+                             None if ev1 is None else ev1.cuda_event)
+    if T is None:
+        raise ValueError("no F layer given")
+    outs = None
+    if per_layer_out is not None:
+        outs = (ctypes.c_void_p * L)()
+        for i, o in enumerate(per_layer_out):
+            if o is not None:
+                _need(o, f"per_layer_out[{i}]", torch.int32, (T, index_topk))
+                outs[i] = o.data_ptr()
+    if slot_mapping is not None:
+        _need(slot_mapping, "slot_mapping", torch.int64, (T,))
+    if status is not None:
+        _need(status, "status", torch.int32)
+    _check(load().dsa_layer_stack_run_bf16(
         L, None if pattern is None else pattern.encode(), freq, offset, arr, T, H,
         _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table), block_table.shape[1],
         num_pages, index_topk, _ptr(topk_buffer), topk_buffer.shape[0], outs, _ptr(slot_mapping),

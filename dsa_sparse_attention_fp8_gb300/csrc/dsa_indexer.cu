@@ -359,15 +359,26 @@ cudaError_t record_event(void* ev, cudaStream_t st) {
   return cudaEventRecord((cudaEvent_t)ev, st);
 }
 
-int launch_write(const float* k, const Batch& b, uint8_t* k_cache, int64_t* slot_mapping,
-                 int* launches) {
+// Cache write of T new keys (FP32 or BF16); with q given (BF16 only) the same
+// launch also quantises the T*H query blocks into q_fp8 / q_scale.
+template <typename TIn>
+int launch_write_t(const TIn* k, const Batch& b, uint8_t* k_cache, int64_t* slot_mapping,
+                   const TIn* q, int H, uint8_t* q_fp8, float* q_scale, int* launches) {
   const int warps_per_block = 8;
-  const int grid = (b.T + warps_per_block - 1) / warps_per_block;
-  dsa::write_k_kernel<<<grid, 32 * warps_per_block, 0, b.st>>>(
+  const int64_t warps = (int64_t)b.T + (q ? (int64_t)b.T * H : 0);
+  const int64_t grid = (warps + warps_per_block - 1) / warps_per_block;
+  if (grid > INT32_MAX) return fail(DSA_ERR_INVALID_ARG, "too many rows for one cache-write launch");
+  dsa::write_k_kernel<TIn><<<(unsigned)grid, 32 * warps_per_block, 0, b.st>>>(
       k, b.T, b.qsl, b.seq_lens, b.R, b.block_table, b.max_blocks, k_cache, b.num_pages,
-      slot_mapping, b.status);
+      slot_mapping, b.status, q, H, q_fp8, q_scale);
   ++*launches;
   return check_launch("write_k_kernel");
+}
+
+int launch_write(const float* k, const Batch& b, uint8_t* k_cache, int64_t* slot_mapping,
+                 int* launches) {
+  return launch_write_t<float>(k, b, k_cache, slot_mapping, nullptr, 0, nullptr, nullptr,
+                               launches);
 }
 
 __global__ void copy_rows_kernel(const int4* __restrict__ src, int4* __restrict__ dst, int64_t n16) {
@@ -406,6 +417,95 @@ int static_workspace(void** out) {
   }
   *out = g_static_ws_ptr[dev];
   return DSA_OK;
+}
+
+// ---------------------------------------------------------------- layer stacks
+// The two layer-input forms (FP32 keys + quantised queries, or BF16 keys and
+// queries quantised by the cache-write launch) share one stack driver.
+int check_layer(const dsa_layer_io& io, int l) {
+  if (!io.k || !io.q_fp8 || !io.q_scale || !io.w || !io.k_cache)
+    return fail(DSA_ERR_INVALID_ARG, "F layer %d has a null input", l);
+  if (!aligned(io.k, 16) || !aligned(io.q_fp8, 16) || !aligned(io.k_cache, 16))
+    return fail(DSA_ERR_INVALID_ARG, "F layer %d: k, q_fp8, k_cache must be 16-byte aligned", l);
+  return DSA_OK;
+}
+int check_layer(const dsa_layer_io_bf16& io, int l) {
+  if (!io.k || !io.q || !io.w || !io.k_cache || !io.q_fp8 || !io.q_scale)
+    return fail(DSA_ERR_INVALID_ARG, "F layer %d has a null input", l);
+  if (!aligned(io.k, 16) || !aligned(io.q, 16) || !aligned(io.q_fp8, 16) || !aligned(io.k_cache, 16))
+    return fail(DSA_ERR_INVALID_ARG, "F layer %d: k, q, q_fp8, k_cache must be 16-byte aligned", l);
+  return DSA_OK;
+}
+int write_layer(const dsa_layer_io& io, const Batch& b, int64_t* slot_mapping, int* launches) {
+  return launch_write(io.k, b, io.k_cache, slot_mapping, launches);
+}
+int write_layer(const dsa_layer_io_bf16& io, const Batch& b, int64_t* slot_mapping, int* launches) {
+  return launch_write_t<uint16_t>(static_cast<const uint16_t*>(io.k), b, io.k_cache, slot_mapping,
+                                  static_cast<const uint16_t*>(io.q), b.H, io.q_fp8, io.q_scale,
+                                  launches);
+}
+
+template <typename IO>
+int stack_run(int num_layers, const char* pattern, int freq, int offset, const IO* layers,
+              const Batch& b, int32_t* const* per_layer_topk_out, int64_t* slot_mapping) {
+  g_last_launches = 0;
+  if (num_layers < 1) return fail(DSA_ERR_INVALID_ARG, "num_layers=%d < 1", num_layers);
+  if (!layers) return fail(DSA_ERR_INVALID_ARG, "null layers array");
+  int rc = check_batch(b);
+  if (rc) return rc;
+  // schedule and per-layer inputs are checked before anything is launched
+  for (int l = 0; l < num_layers; ++l) {
+    const int full = dsa_layer_is_full(l, pattern, freq, offset);
+    if (full < 0) return full;
+    if (l == 0 && !full)
+      return fail(DSA_ERR_INVALID_ARG,
+                  "layer 0 is S: no F layer has written the top-k buffer in this pass");
+    if (full && (rc = check_layer(layers[l], l)) != DSA_OK) return rc;
+  }
+  if (b.T == 0) return DSA_OK;
+  ScoreShape s;
+  if (!score_shape(b.T, b.R, b.H, b.k, &s))
+    return fail(DSA_ERR_UNSUPPORTED, "no shared-memory configuration for H=%d, index_topk=%d", b.H,
+                b.k);
+  int launches = 0;
+  rc = launch_plan(b, s.G, &launches);
+  bool first_full = true;
+  for (int l = 0; l < num_layers && rc == DSA_OK; ++l) {
+    const int full = dsa_layer_is_full(l, pattern, freq, offset);
+    if (full) {
+      const IO& io = layers[l];
+      rc = write_layer(io, b, first_full ? slot_mapping : nullptr, &launches);
+      first_full = false;
+      if (rc) break;
+      LayerQ lq{io.q_fp8, io.q_scale, io.w, io.k_cache, nullptr, 0};
+      if (io.score_begin && record_event(io.score_begin, b.st) != cudaSuccess) {
+        rc = fail(DSA_ERR_CUDA, "recording score_begin of layer %d failed", l);
+        break;
+      }
+      rc = launch_score_layer(b, s, lq, &launches);
+      if (rc) break;
+      if (io.score_end && record_event(io.score_end, b.st) != cudaSuccess) {
+        rc = fail(DSA_ERR_CUDA, "recording score_end of layer %d failed", l);
+        break;
+      }
+    }
+    if (per_layer_topk_out && per_layer_topk_out[l]) {
+      const int64_t bytes = (int64_t)b.T * b.k * 4;
+      if (bytes % 16 == 0 && aligned(per_layer_topk_out[l], 16) && aligned(b.topk, 16)) {
+        copy_rows_kernel<<<256, 256, 0, b.st>>>(reinterpret_cast<const int4*>(b.topk),
+                                                reinterpret_cast<int4*>(per_layer_topk_out[l]),
+                                                bytes / 16);
+        ++launches;
+        rc = check_launch("copy_rows_kernel");
+      } else {
+        if (cudaMemcpyAsync(per_layer_topk_out[l], b.topk, (size_t)bytes,
+                            cudaMemcpyDeviceToDevice, b.st) != cudaSuccess)
+          rc = fail(DSA_ERR_CUDA, "snapshot copy of layer %d failed", l);
+      }
+    }
+  }
+  g_last_launches = launches;
+  return rc;
 }
 
 }  // namespace
@@ -560,71 +660,58 @@ int dsa_layer_stack_run(int num_layers, const char* pattern, int freq, int offse
                         int32_t* const* per_layer_topk_out, int64_t* slot_mapping,
                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
                         dsa_stream_t stream) {
+  const Batch b{T, H, R, max_blocks, index_topk, max_num_batched_tokens, num_pages,
+                query_start_loc, seq_lens, block_table, topk_buffer, workspace, workspace_bytes,
+                dev_status, (cudaStream_t)stream};
+  return stack_run(num_layers, pattern, freq, offset, layers, b, per_layer_topk_out, slot_mapping);
+}
+
+int dsa_layer_stack_run_bf16(int num_layers, const char* pattern, int freq, int offset,
+                             const dsa_layer_io_bf16* layers, int T, int H,
+                             const int32_t* query_start_loc, const int32_t* seq_lens, int R,
+                             const int32_t* block_table, int max_blocks, int64_t num_pages,
+                             int index_topk, int32_t* topk_buffer, int max_num_batched_tokens,
+                             int32_t* const* per_layer_topk_out, int64_t* slot_mapping,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             dsa_stream_t stream) {
+  const Batch b{T, H, R, max_blocks, index_topk, max_num_batched_tokens, num_pages,
+                query_start_loc, seq_lens, block_table, topk_buffer, workspace, workspace_bytes,
+                dev_status, (cudaStream_t)stream};
+  return stack_run(num_layers, pattern, freq, offset, layers, b, per_layer_topk_out, slot_mapping);
+}
+
+int dsa_indexer_write_k_bf16(const void* k, int T, const int32_t* query_start_loc,
+                             const int32_t* seq_lens, int R, const int32_t* block_table,
+                             int max_blocks, uint8_t* k_cache, int64_t num_pages,
+                             const void* q, int H, uint8_t* q_fp8, float* q_scale,
+                             int64_t* slot_mapping, int32_t* dev_status, dsa_stream_t stream) {
   g_last_launches = 0;
-  if (num_layers < 1) return fail(DSA_ERR_INVALID_ARG, "num_layers=%d < 1", num_layers);
-  if (!layers) return fail(DSA_ERR_INVALID_ARG, "null layers array");
-  Batch b{T, H, R, max_blocks, index_topk, max_num_batched_tokens, num_pages, query_start_loc,
-          seq_lens, block_table, topk_buffer, workspace, workspace_bytes, dev_status,
-          (cudaStream_t)stream};
-  int rc = check_batch(b);
-  if (rc) return rc;
-  // schedule and per-layer inputs are checked before anything is launched
-  for (int l = 0; l < num_layers; ++l) {
-    const int full = dsa_layer_is_full(l, pattern, freq, offset);
-    if (full < 0) return full;
-    if (l == 0 && !full)
-      return fail(DSA_ERR_INVALID_ARG,
-                  "layer 0 is S: no F layer has written the top-k buffer in this pass");
-    if (full) {
-      const dsa_layer_io& io = layers[l];
-      if (!io.k || !io.q_fp8 || !io.q_scale || !io.w || !io.k_cache)
-        return fail(DSA_ERR_INVALID_ARG, "F layer %d has a null input", l);
-      if (!aligned(io.k, 16) || !aligned(io.q_fp8, 16) || !aligned(io.k_cache, 16))
-        return fail(DSA_ERR_INVALID_ARG, "F layer %d: k, q_fp8, k_cache must be 16-byte aligned", l);
-    }
-  }
+  if (T < 0) return fail(DSA_ERR_INVALID_ARG, "T=%d < 0", T);
+  if (R < 1) return fail(DSA_ERR_INVALID_ARG, "R=%d < 1", R);
+  if (max_blocks < 1) return fail(DSA_ERR_INVALID_ARG, "max_blocks < 1");
+  if (num_pages < 1) return fail(DSA_ERR_INVALID_ARG, "num_pages < 1");
+  if (q && (H < 1 || !q_fp8 || !q_scale))
+    return fail(DSA_ERR_INVALID_ARG, "with q: H >= 1 and q_fp8, q_scale outputs are required");
   if (T == 0) return DSA_OK;
-  ScoreShape s;
-  if (!score_shape(T, R, H, index_topk, &s))
-    return fail(DSA_ERR_UNSUPPORTED, "no shared-memory configuration for H=%d, index_topk=%d", H,
-                index_topk);
+  if (!k || !query_start_loc || !seq_lens || !block_table || !k_cache)
+    return fail(DSA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(k, 16) || !aligned(k_cache, 16) || (q && (!aligned(q, 16) || !aligned(q_fp8, 16))))
+    return fail(DSA_ERR_INVALID_ARG, "k, q, q_fp8 and k_cache must be 16-byte aligned");
+  Batch b{};
+  b.T = T;
+  b.H = H;
+  b.R = R;
+  b.max_blocks = max_blocks;
+  b.num_pages = num_pages;
+  b.qsl = query_start_loc;
+  b.seq_lens = seq_lens;
+  b.block_table = block_table;
+  b.status = dev_status;
+  b.st = (cudaStream_t)stream;
   int launches = 0;
-  rc = launch_plan(b, s.G, &launches);
-  bool first_full = true;
-  for (int l = 0; l < num_layers && rc == DSA_OK; ++l) {
-    const int full = dsa_layer_is_full(l, pattern, freq, offset);
-    if (full) {
-      const dsa_layer_io& io = layers[l];
-      rc = launch_write(io.k, b, io.k_cache, first_full ? slot_mapping : nullptr, &launches);
-      first_full = false;
-      if (rc) break;
-      LayerQ lq{io.q_fp8, io.q_scale, io.w, io.k_cache, nullptr, 0};
-      if (io.score_begin && record_event(io.score_begin, b.st) != cudaSuccess) {
-        rc = fail(DSA_ERR_CUDA, "recording score_begin of layer %d failed", l);
-        break;
-      }
-      rc = launch_score_layer(b, s, lq, &launches);
-      if (rc) break;
-      if (io.score_end && record_event(io.score_end, b.st) != cudaSuccess) {
-        rc = fail(DSA_ERR_CUDA, "recording score_end of layer %d failed", l);
-        break;
-      }
-    }
-    if (per_layer_topk_out && per_layer_topk_out[l]) {
-      const int64_t bytes = (int64_t)T * index_topk * 4;
-      if (bytes % 16 == 0 && aligned(per_layer_topk_out[l], 16) && aligned(topk_buffer, 16)) {
-        copy_rows_kernel<<<256, 256, 0, b.st>>>(reinterpret_cast<const int4*>(topk_buffer),
-                                                reinterpret_cast<int4*>(per_layer_topk_out[l]),
-                                                bytes / 16);
-        ++launches;
-        rc = check_launch("copy_rows_kernel");
-      } else {
-        if (cudaMemcpyAsync(per_layer_topk_out[l], topk_buffer, (size_t)bytes,
-                            cudaMemcpyDeviceToDevice, b.st) != cudaSuccess)
-          rc = fail(DSA_ERR_CUDA, "snapshot copy of layer %d failed", l);
-      }
-    }
-  }
+  const int rc = launch_write_t<uint16_t>(static_cast<const uint16_t*>(k), b, k_cache, slot_mapping,
+                                          static_cast<const uint16_t*>(q), H, q_fp8, q_scale,
+                                          &launches);
   g_last_launches = launches;
   return rc;
 }

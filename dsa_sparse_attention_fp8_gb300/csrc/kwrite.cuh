@@ -59,18 +59,43 @@ __device__ __forceinline__ int find_request(const int32_t* __restrict__ qsl, int
   return lo;
 }
 
+// One lane's 4 consecutive elements of 128-element block `blk` as FP32
+// (BF16 widens exactly: its bits are the upper half of the FP32 value).
+__device__ __forceinline__ float4 load_lane4(const float* x, int64_t blk, int lane) {
+  return __ldg(reinterpret_cast<const float4*>(x + blk * kHeadDim) + lane);
+}
+__device__ __forceinline__ float4 load_lane4(const uint16_t* x, int64_t blk, int lane) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(x + blk * kHeadDim) + lane);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+}
+
+// Warps [0, T): the new tokens' keys (quantise, slot mapping, write into the
+// page pool).  Warps [T, T + T*H) when q is given: the query rows' H blocks
+// each, quantised to q_codes [T, H, 128] and q_scales [T, H] with the same
+// rule, so one launch performs the whole per-token quantisation of a layer.
+template <typename TIn>
 __global__ void __launch_bounds__(256) write_k_kernel(
-    const float* __restrict__ k, int T, const int32_t* __restrict__ qsl,
+    const TIn* __restrict__ k, int T, const int32_t* __restrict__ qsl,
     const int32_t* __restrict__ seq_lens, int R, const int32_t* __restrict__ block_table,
     int max_blocks, uint8_t* __restrict__ k_cache, int64_t num_pages,
-    int64_t* __restrict__ slot_mapping, int32_t* status) {
+    int64_t* __restrict__ slot_mapping, int32_t* status, const TIn* __restrict__ q, int H,
+    uint8_t* __restrict__ q_codes, float* __restrict__ q_scales) {
   pdl_launch_dependents();  // the scoring kernel's prologue may overlap this write
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp >= T) return;
-  const int t = warp;
+  if (warp >= T) {
+    const int64_t b = warp - T;
+    if (q == nullptr || b >= (int64_t)T * H) return;
+    float s;
+    const uint32_t c = quantize_lane4(load_lane4(q, b, lane), &s);
+    reinterpret_cast<uint32_t*>(q_codes + b * kHeadDim)[lane] = c;
+    if (lane == 0) q_scales[b] = s;
+    return;
+  }
+  const int t = (int)warp;
 
-  const float4 v = __ldg(reinterpret_cast<const float4*>(k + (int64_t)t * kHeadDim) + lane);
+  const float4 v = load_lane4(k, t, lane);
   float s;
   const uint32_t codes = quantize_lane4(v, &s);
 

@@ -21,11 +21,13 @@ class IndexerStep:
     def __init__(self, *, num_layers: int, pattern: Optional[str], freq: int, offset: int,
                  H: int, index_topk: int, T: int, R: int, max_blocks: int, num_pages: int,
                  max_num_batched_tokens: int, k_caches: Sequence[Optional[torch.Tensor]],
-                 device="cuda", time_score_kernels: bool = False):
+                 device="cuda", time_score_kernels: bool = False, bf16: bool = False):
         self.num_layers, self.pattern, self.freq, self.offset = num_layers, pattern, freq, offset
         self.H, self.k, self.T, self.R = H, index_topk, T, R
         self.max_blocks, self.num_pages = max_blocks, num_pages
         self.device = torch.device(device)
+        self.bf16 = bf16   # BF16 keys and queries, quantised by the cache-write launch
+        self.input_keys = ("k", "q", "w") if bf16 else ("k", "q_fp8", "q_scale", "w")
         self.full = [binding.layer_is_full(l, pattern, freq, offset) for l in range(num_layers)]
         dev = self.device
         self.query_start_loc = torch.zeros(R + 1, dtype=torch.int32, device=dev)
@@ -43,12 +45,15 @@ class IndexerStep:
             cache = k_caches[l]
             assert cache is not None and cache.shape == (num_pages, binding.PAGE_BYTES)
             io = {
-                "k": torch.zeros((T, binding.HEAD_DIM), dtype=torch.float32, device=dev),
+                "k": torch.zeros((T, binding.HEAD_DIM),
+                                 dtype=torch.bfloat16 if bf16 else torch.float32, device=dev),
                 "q_fp8": torch.zeros((T, H, binding.HEAD_DIM), dtype=torch.uint8, device=dev),
                 "q_scale": torch.ones((T, H), dtype=torch.float32, device=dev),
                 "w": torch.zeros((T, H), dtype=torch.float32, device=dev),
                 "k_cache": cache,
             }
+            if bf16:
+                io["q"] = torch.zeros((T, H, binding.HEAD_DIM), dtype=torch.bfloat16, device=dev)
             if time_score_kernels:
                 io["score_begin"] = torch.cuda.Event(enable_timing=True)
                 io["score_end"] = torch.cuda.Event(enable_timing=True)
@@ -66,12 +71,13 @@ class IndexerStep:
         self.seq_lens.copy_(seq_lens, non_blocking=non_blocking)
         self.block_table.copy_(block_table, non_blocking=non_blocking)
 
-    def set_layer(self, layer: int, k, q_fp8, q_scale, w, non_blocking=False) -> None:
+    def set_layer(self, layer: int, *inputs, non_blocking=False) -> None:
+        """This step's inputs of F layer `layer`: (k, q_fp8, q_scale, w), or
+        (k, q, w) in BF16 mode."""
         io = self.layers[layer]
-        io["k"].copy_(k, non_blocking=non_blocking)
-        io["q_fp8"].copy_(q_fp8, non_blocking=non_blocking)
-        io["q_scale"].copy_(q_scale, non_blocking=non_blocking)
-        io["w"].copy_(w, non_blocking=non_blocking)
+        assert len(inputs) == len(self.input_keys)
+        for key, t in zip(self.input_keys, inputs):
+            io[key].copy_(t, non_blocking=non_blocking)
 
     # -------------------------------------------------------------- running
     def launch(self, timed: bool = True) -> None:
@@ -83,7 +89,8 @@ class IndexerStep:
             layers = [None if io is None else {k: v for k, v in io.items()
                                                if k not in ("score_begin", "score_end")}
                       for io in self.layers]
-        binding.layer_stack_run(layers, self.pattern, self.freq, self.offset, self.H,
+        run = binding.layer_stack_run_bf16 if self.bf16 else binding.layer_stack_run
+        run(layers, self.pattern, self.freq, self.offset, self.H,
                                 self.query_start_loc, self.seq_lens, self.block_table,
                                 self.num_pages, self.k, self.topk, self.workspace,
                                 status=self.status, T=self.T)
@@ -128,12 +135,13 @@ class IndexerStep:
         """H2D of this step's inputs, the stack, D2H of rows [0, T) of the top-k buffer.
 
         ``host["meta"]`` = (query_start_loc, seq_lens, block_table) and
-        ``host["layers"][l]`` = (k, q_fp8, q_scale, w), pinned CPU tensors;
+        ``host["layers"][l]`` = the layer's inputs as set_layer takes them, pinned
+        CPU tensors;
         ``out`` is a pinned int32 [T, index_topk] CPU tensor.  Asynchronous on
         the current stream.
         """
         self.set_metadata(*host["meta"], non_blocking=True)
         for l, io in host["layers"].items():
             self.set_layer(l, *io, non_blocking=True)
-        self.run()
+        self.run(timed=False)
         out.copy_(self.topk[: self.T], non_blocking=True)

@@ -106,6 +106,24 @@ int dsa_indexer_write_k(const float* k, int T, const int32_t* query_start_loc,
                         int64_t* slot_mapping, int32_t* dev_status, dsa_stream_t stream);
 
 /*
+ * Step 1 with BF16 inputs, and the upstream query quantisation fused into the
+ * same launch (the cache write of the page "GLM-5.3 推理全链路(十二)" takes the
+ * key already quantised; here one kernel quantises both the new keys and the
+ * layer's query rows with the rule of the cache write).  The pages print no
+ * BF16 interface; BF16 widens to FP32 exactly, so the results equal
+ * dsa_indexer_write_k / dsa_quantize_fp8_blocks on the widened values.
+ *   k          [T, 128] BF16 (16-byte aligned) new-token keys.
+ *   q          [T, H, 128] BF16 query rows, or NULL (keys only).
+ *   q_fp8      [T, H, 128] E4M3 out, q_scale [T, H] FP32 out (when q != NULL).
+ * Other arguments and errors as dsa_indexer_write_k; H must be >= 1 with q.
+ */
+int dsa_indexer_write_k_bf16(const void* k, int T, const int32_t* query_start_loc,
+                             const int32_t* seq_lens, int R, const int32_t* block_table,
+                             int max_blocks, uint8_t* k_cache, int64_t num_pages,
+                             const void* q, int H, uint8_t* q_fp8, float* q_scale,
+                             int64_t* slot_mapping, int32_t* dev_status, dsa_stream_t stream);
+
+/*
  * Per-block FP8 quantiser used for keys, exposed for queries: x [n_blocks, 128]
  * FP32 -> codes [n_blocks, 128] E4M3 bytes + scales [n_blocks] FP32, same rule
  * as the cache write ([KV] byte-accounting table: 128 FP8 bytes + one FP32
@@ -226,6 +244,33 @@ int dsa_layer_stack_run(int num_layers, const char* pattern, int freq, int offse
                         int32_t* const* per_layer_topk_out, int64_t* slot_mapping,
                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
                         dsa_stream_t stream);
+
+/* Per-layer inputs of dsa_layer_stack_run_bf16 (BF16 keys and queries). */
+typedef struct dsa_layer_io_bf16 {
+  const void* k;          /* [T, 128] BF16 new-token keys of this layer */
+  const void* q;          /* [T, H, 128] BF16 query rows */
+  const float* w;         /* [T, H] head weights */
+  uint8_t* k_cache;       /* [num_pages, 8448] this layer's page pool */
+  uint8_t* q_fp8;         /* [T, H, 128] scratch: this layer's quantised queries */
+  float* q_scale;         /* [T, H] scratch: their scales */
+  void* score_begin;      /* cudaEvent_t or NULL */
+  void* score_end;        /* cudaEvent_t or NULL */
+} dsa_layer_io_bf16;
+
+/*
+ * dsa_layer_stack_run with BF16 keys and queries: each F layer's cache write
+ * also quantises its query rows into the layer's q_fp8 / q_scale scratch (one
+ * launch, dsa_indexer_write_k_bf16), which its scoring kernel then reads.
+ * Arguments, schedule and errors as dsa_layer_stack_run.
+ */
+int dsa_layer_stack_run_bf16(int num_layers, const char* pattern, int freq, int offset,
+                             const dsa_layer_io_bf16* layers, int T, int H,
+                             const int32_t* query_start_loc, const int32_t* seq_lens, int R,
+                             const int32_t* block_table, int max_blocks, int64_t num_pages,
+                             int index_topk, int32_t* topk_buffer, int max_num_batched_tokens,
+                             int32_t* const* per_layer_topk_out, int64_t* slot_mapping,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             dsa_stream_t stream);
 
 /*
  * Number of kernel launches the last successful call of each entry point on
