@@ -165,10 +165,10 @@ def oracle_sample_setup(wl, layer=0):
     import oracle as O
     cache = np.zeros((wl.num_pages, O.PAGE_BYTES), np.uint8)
     for r in range(wl.R):
-        P = int(wl.prefix_lens[r])
-        if P:
+        E = int(wl.prefix_entries[r])
+        if E:
             O.write_k_cache(cache, wl.k_prefix(layer, r),
-                            O.slot_mapping(np.array([0, P]), np.array([P]), wl.block_table[r:r + 1]))
+                            O.slot_mapping(np.array([0, E]), np.array([E]), wl.block_table[r:r + 1]))
     qc, qs = O.quantize_blocks(wl.q(layer))
     return cache, wl.k_new(layer), qc, qs, wl.w(layer)
 
@@ -181,10 +181,10 @@ def oracle_time_rows(wl, state, rows):
     c = cache.copy()
     t0 = time.perf_counter()
     O.indexer_layer(c, k_new, qc, qs, w, wl.query_start_loc, wl.seq_lens, wl.block_table,
-                    wl.index_topk, buf, rows=rows)
+                    wl.index_topk, buf, rows=rows, compress_ratio=wl.compress_ratio)
     dt = time.perf_counter() - t0
     _, pos = O.token_positions(wl.query_start_loc, wl.seq_lens)
-    pairs = int(sum(int(pos[t]) + 1 for t in rows))
+    pairs = int(sum(int(O.visible_entries(pos[t], wl.compress_ratio)) for t in rows))
     return pairs, dt
 
 

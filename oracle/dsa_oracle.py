@@ -21,7 +21,10 @@ Sources (page title, then section):
   int32) and the write-path section (``store_quantized`` writes the FP8 key and
   its scale at the token's in-page offset).
 * [HBM] "HBM 索引架构设计" -- §2.3 物理公式 (slot = block_table[req, pos // bs]
-  * bs + pos % bs).
+  * bs + pos % bs); §5.1 (a compressed cache stores one entry per
+  ``compress_ratio`` tokens: storage block = block size // ratio) and §5.2
+  (compressed slot mapping: only a token with (pos + 1) % ratio == 0 gets a
+  slot, at entry pos // ratio; every other token gets -1 and is not written).
 * [DSA] the DeepSeek-V3.2 report (arXiv:2512.02556), which the [KV] page lists
   among its references for the DSA structure: the lightning-indexer score
   ``I(t, s) = sum_h w[t,h] * ReLU(q[t,h] . k[s])``.  The pages themselves print
@@ -38,6 +41,15 @@ Readings where the pages leave a step open:
 * Causality: key s is visible to query token t iff s <= pos(t) (itself
   included); its key is written before scoring.
 * Returned indices are logical token positions within the request.
+* Compressed indexer (ratio N > 1): the key row of the token that completes a
+  state (position (c + 1) * N - 1) is the state's key c -- the compressor that
+  produces it runs upstream and is not part of this step.  The indexer page
+  still holds 64 entries ([KV] 64-token page section: with ``index_kpool`` = N
+  the indexer page stays 64 entries and its numbering is divided by N), so the
+  indexer block table maps entry blocks c // 64.  Entry c becomes visible to
+  the query at pos once its writer has run (the causality rule above), i.e.
+  iff (c + 1) * N - 1 <= pos: a row sees (pos + 1) // N entries, and its
+  returned indices are entry numbers c.
 * Within a row the order is unspecified; this oracle orders by (score desc,
   position asc) and pads with -1 after min(ctx, k) entries.
 """
@@ -60,7 +72,7 @@ E4M3_MAX = 448.0
 __all__ = [
     "PAGE_TOKENS", "HEAD_DIM", "TOKEN_BYTES", "PAGE_BYTES", "PAGE_SCALE_OFFSET",
     "E4M3_MAX", "e4m3_decode", "e4m3_encode", "quantize_blocks", "token_positions",
-    "slot_mapping", "write_k_cache", "gather_request_keys", "dequant_keys",
+    "slot_mapping", "compressed_slot_mapping", "visible_entries", "write_k_cache", "gather_request_keys", "dequant_keys",
     "index_scores", "topk_row", "layer_is_full", "layer_schedule",
     "indexer_layer", "run_layer_stack", "cache_bytes_per_token",
 ]
@@ -166,15 +178,42 @@ def slot_mapping(query_start_loc, seq_lens, block_table) -> np.ndarray:
     return page * PAGE_TOKENS + pos % PAGE_TOKENS
 
 
+def compressed_slot_mapping(query_start_loc, seq_lens, block_table, compress_ratio) -> np.ndarray:
+    """[HBM] §5.2: int64 slot per token; -1 unless (pos + 1) % ratio == 0.
+
+    A token that completes a state writes entry c = pos // ratio at
+    block_table[r, c // 64] * 64 + c % 64 (64-entry indexer pages).  With
+    ratio 1 every token is valid and this is ``slot_mapping``.
+    """
+    n = int(compress_ratio)
+    if n < 1:
+        raise ValueError("compress_ratio must be >= 1")
+    bt = np.asarray(block_table, dtype=np.int64)
+    req, pos = token_positions(query_start_loc, seq_lens)
+    slots = np.full(pos.shape[0], -1, dtype=np.int64)
+    valid = (pos + 1) % n == 0
+    c = pos[valid] // n
+    slots[valid] = bt[req[valid], c // PAGE_TOKENS] * PAGE_TOKENS + c % PAGE_TOKENS
+    return slots
+
+
+def visible_entries(pos, compress_ratio: int = 1):
+    """Cache entries a query at ``pos`` sees: (pos + 1) // ratio (ratio 1: pos + 1)."""
+    return (np.asarray(pos, dtype=np.int64) + 1) // int(compress_ratio)
+
+
 def write_k_cache(cache: np.ndarray, k: np.ndarray, slots: np.ndarray) -> np.ndarray:
     """[KV] write path: FP8 key bytes and FP32 scale at each token's page offset.
 
     ``cache`` is uint8 [num_pages, 8448]; page ``p`` holds the 64 keys at
     bytes [off*128, off*128+128) and their scales at 8192 + off*4 ([KV],
-    ``IndexKeyCache.move`` comment).  Returns ``cache`` (modified in place).
+    ``IndexKeyCache.move`` comment).  Rows whose slot is -1 are not written
+    ([HBM] §5.2).  Returns ``cache`` (modified in place).
     """
-    codes, scales = quantize_blocks(k)
     slots = np.asarray(slots, dtype=np.int64)
+    keep = slots >= 0
+    codes, scales = quantize_blocks(np.asarray(k)[keep])
+    slots = slots[keep]
     page = (slots // PAGE_TOKENS)[:, None]
     off = (slots % PAGE_TOKENS)[:, None]
     sbytes = scales.astype("<f4").view(np.uint8).reshape(-1, 4)
@@ -258,14 +297,16 @@ def layer_schedule(num_layers: int, pattern: str | None, freq: int = 1, offset: 
 # --------------------------------------------------------------------------
 
 def indexer_layer(cache, k_new, q_codes, q_scale, w, query_start_loc, seq_lens,
-                  block_table, index_topk, topk_buffer, rows=None):
+                  block_table, index_topk, topk_buffer, rows=None, compress_ratio=1):
     """One F layer: write this step's keys, then top-k rows into ``topk_buffer``.
 
     ``rows`` limits scoring to a subset of query tokens (the whole step's keys
     are still written).  Rows [0, T) of the buffer are rewritten; rows beyond
-    T are untouched.  Returns (slot_mapping, {row: scores}).
+    T are untouched.  With ``compress_ratio`` N > 1 only the tokens that
+    complete a state are written ([HBM] §5.2) and row t ranks the
+    (pos + 1) // N entries it sees.  Returns (slot_mapping, {row: scores}).
     """
-    slots = slot_mapping(query_start_loc, seq_lens, block_table)
+    slots = compressed_slot_mapping(query_start_loc, seq_lens, block_table, compress_ratio)
     write_k_cache(cache, k_new, slots)
     req, pos = token_positions(query_start_loc, seq_lens)
     T = req.shape[0]
@@ -273,9 +314,10 @@ def indexer_layer(cache, k_new, q_codes, q_scale, w, query_start_loc, seq_lens,
     scores_out = {}
     per_req = {}
     for t in rows:
-        r, ctx = int(req[t]), int(pos[t]) + 1
+        r, ctx = int(req[t]), int(visible_entries(pos[t], compress_ratio))
         if r not in per_req:
-            per_req[r] = gather_request_keys(cache, block_table[r], int(seq_lens[r]))
+            per_req[r] = gather_request_keys(cache, block_table[r],
+                                             int(seq_lens[r]) // int(compress_ratio))
         kc, ks = per_req[r]
         s = index_scores(q_codes[t], q_scale[t], w[t], kc[:ctx], ks[:ctx])
         topk_buffer[t] = topk_row(s, index_topk)
@@ -285,7 +327,7 @@ def indexer_layer(cache, k_new, q_codes, q_scale, w, query_start_loc, seq_lens,
 
 def run_layer_stack(num_layers, pattern, freq, offset, layer_inputs, caches,
                     query_start_loc, seq_lens, block_table, index_topk,
-                    max_num_batched_tokens):
+                    max_num_batched_tokens, compress_ratio=1):
     """[IC] §二: F layers write the shared buffer, S layers read what the last F
     layer wrote in this pass.  Returns the buffer contents each layer consumes
     (a copy per layer) and the schedule.
@@ -302,6 +344,6 @@ def run_layer_stack(num_layers, pattern, freq, offset, layer_inputs, caches,
         if sched[layer]:
             k_new, qc, qs, w = layer_inputs[layer]
             indexer_layer(caches[layer], k_new, qc, qs, w, query_start_loc, seq_lens,
-                          block_table, index_topk, buf)
+                          block_table, index_topk, buf, compress_ratio=compress_ratio)
         consumed.append(buf.copy())
     return consumed, sched

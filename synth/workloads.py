@@ -14,7 +14,10 @@ Shapes follow the serving setups the pages describe:
   ("GLM-5.3 推理全链路(十二)", top-k / logits workspace section);
 * IndexCache F/S stacks given either by ``index_topk_freq`` with offset 2 or
   by an explicit pattern ("vLLM IndexCache 实战指南", parameter table and CLI
-  section).
+  section);
+* a compressed indexer cache holding one entry per ``compress_ratio`` tokens
+  ("HBM 索引架构设计", §5.1 ratio 4 and §5.3 indexer cache), for contexts of
+  16K-128K tokens (the range §5.6 names).
 
 Distributions: q and k ~ N(0, 1) FP32; w ~ N(0, 1) / sqrt(H) FP32; pages of
 each request are placed by a random permutation of a pool sized to fit.
@@ -45,6 +48,7 @@ WORKLOAD_NAMES = {
     3: "mixed_batch",
     4: "long_context_decode",
     5: "mtp_decode",
+    6: "compressed_decode",
 }
 
 
@@ -92,6 +96,7 @@ class Workload:
     max_num_batched_tokens: int
     outlier_channels: np.ndarray = field(default_factory=lambda: np.zeros(0, np.int64))
     outlier_scale: float = 1.0
+    compress_ratio: int = 1     # tokens per indexer cache entry
 
     # ---- derived metadata -------------------------------------------------
     @property
@@ -114,6 +119,16 @@ class Workload:
         return (self.seq_lens - self.q_lens).astype(np.int32)
 
     @property
+    def prefix_entries(self) -> np.ndarray:
+        """Cache entries written before this step: one per compress_ratio tokens."""
+        return (self.prefix_lens // self.compress_ratio).astype(np.int32)
+
+    @property
+    def entries(self) -> np.ndarray:
+        """Cache entries of each request after this step."""
+        return (self.seq_lens // self.compress_ratio).astype(np.int32)
+
+    @property
     def max_blocks(self) -> int:
         return int(self.block_table.shape[1])
 
@@ -129,8 +144,9 @@ class Workload:
         return self._apply_outliers(k)
 
     def k_prefix(self, layer: int, request: int) -> np.ndarray:
-        """FP32 [prefix_len, 128]: keys of the tokens cached before this step."""
-        n = int(self.prefix_lens[request])
+        """FP32 [prefix_entries, 128]: keys of the cache entries written before
+        this step (one per token, or one per compress_ratio tokens)."""
+        n = int(self.prefix_entries[request])
         k = _normal_rows((self.seed, self.workload_id, layer, _T_KPREFIX, request), n, HEAD_DIM)
         return self._apply_outliers(k)
 
@@ -147,11 +163,15 @@ class Workload:
 
     @property
     def pairs_per_full_layer(self) -> int:
-        """Sum over query tokens of the keys each one sees (causal, itself included)."""
+        """Sum over query tokens of the keys each one sees (causal, itself
+        included; with compress_ratio N, the (pos + 1) // N entries)."""
         pre = self.prefix_lens.astype(np.int64)
         ql = self.q_lens.astype(np.int64)
-        # token j (0-based) of request r sees pre[r] + j + 1 keys
-        return int(np.sum(ql * pre + ql * (ql + 1) // 2))
+        if self.compress_ratio == 1:
+            # token j (0-based) of request r sees pre[r] + j + 1 keys
+            return int(np.sum(ql * pre + ql * (ql + 1) // 2))
+        pos = np.repeat(pre, ql) + (np.arange(int(ql.sum())) - np.repeat(np.cumsum(ql) - ql, ql))
+        return int(np.sum((pos + 1) // self.compress_ratio))
 
     def describe(self) -> dict:
         return {
@@ -167,6 +187,7 @@ class Workload:
             "offset": self.offset,
             "max_num_batched_tokens": self.max_num_batched_tokens,
             "pages_per_layer": self.num_pages,
+            "compress_ratio": self.compress_ratio,
             "pairs_per_full_layer": self.pairs_per_full_layer,
             "seed": self.seed,
         }
@@ -282,4 +303,18 @@ def make_workload(workload_id: int, seed: int = 0, scale: float = 1.0) -> Worklo
         return Workload(wid, name, seed, H=64, index_topk=2048, num_layers=4, pattern=None,
                         freq=1, offset=2, q_lens=q_lens, seq_lens=ctx, block_table=bt,
                         num_pages=pool, max_num_batched_tokens=R * q)
+    if wid == 6:
+        # 64 decode requests, context log-uniform [16384, 131072], compressed indexer
+        # cache (one entry per 4 tokens), H=64, k=2048, 4 layers all F
+        R, ratio = 64, 4
+        ctx = np.exp(_rng(seed, wid, 0, _T_CTX).uniform(math.log(16384), math.log(131072), size=R))
+        ctx = np.maximum(ratio, np.round(ctx * scale)).astype(np.int32)
+        q_lens = np.ones(R, np.int32)
+        ent = ctx // ratio
+        pool = int(_pages_for(ent).sum())
+        mb = int(_pages_for(np.array([max(1, round(131072 * scale) // ratio)]))[0])
+        bt = _scatter_pages(seed, wid, ent, pool, max(mb, int(_pages_for(ent).max())))
+        return Workload(wid, name, seed, H=64, index_topk=2048, num_layers=4, pattern=None,
+                        freq=1, offset=2, q_lens=q_lens, seq_lens=ctx, block_table=bt,
+                        num_pages=pool, max_num_batched_tokens=R, compress_ratio=ratio)
     raise ValueError(f"unknown workload {workload_id}")

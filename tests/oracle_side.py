@@ -12,27 +12,33 @@ SCORE_RTOL = 2e-3   # scores within 2e-3 x the row's max |score|
 
 
 def oracle_cache(wl, layer: int, with_new: bool = True) -> np.ndarray:
-    """The oracle's page pool for `layer`: cached prefix (+ this step's keys)."""
+    """The oracle's page pool for `layer`: cached prefix (+ this step's keys).
+    Prefix entries sit at entry positions 0 .. prefix_entries-1."""
     cache = np.zeros((wl.num_pages, O.PAGE_BYTES), np.uint8)
     for r in range(wl.R):
-        P = int(wl.prefix_lens[r])
-        if P:
-            slots = O.slot_mapping(np.array([0, P]), np.array([P]), wl.block_table[r:r + 1])
+        E = int(wl.prefix_entries[r])
+        if E:
+            slots = O.slot_mapping(np.array([0, E]), np.array([E]), wl.block_table[r:r + 1])
             O.write_k_cache(cache, wl.k_prefix(layer, r), slots)
     if with_new:
         O.write_k_cache(cache, wl.k_new(layer),
-                        O.slot_mapping(wl.query_start_loc, wl.seq_lens, wl.block_table))
+                        O.compressed_slot_mapping(wl.query_start_loc, wl.seq_lens, wl.block_table,
+                                                  wl.compress_ratio))
     return cache
 
 
 def request_keys(wl, layer: int, r: int, k_new=None):
-    """Codes/scales of request r by logical position, straight from its FP32 keys."""
+    """Codes/scales of request r by entry position, straight from its FP32
+    keys: the prefix entries, then the new tokens that complete an entry."""
     qsl = wl.query_start_loc
     kn = wl.k_new(layer) if k_new is None else k_new
+    n = wl.compress_ratio
     parts = []
-    if wl.prefix_lens[r]:
+    if wl.prefix_entries[r]:
         parts.append(wl.k_prefix(layer, r))
-    parts.append(kn[qsl[r]:qsl[r + 1]])
+    new = kn[qsl[r]:qsl[r + 1]]
+    pos = int(wl.prefix_lens[r]) + np.arange(new.shape[0])
+    parts.append(new[(pos + 1) % n == 0])
     return O.quantize_blocks(np.concatenate(parts, axis=0))
 
 
@@ -46,7 +52,7 @@ def oracle_rows(wl, layer: int, rows, q_codes, q_scale, w, k_new=None):
     for r, ts in by_req.items():
         kc, ks = request_keys(wl, layer, r, k_new)
         for t in ts:
-            ctx = int(pos[t]) + 1
+            ctx = int(O.visible_entries(pos[t], wl.compress_ratio))
             out[t] = O.index_scores(q_codes[t], q_scale[t], w[t], kc[:ctx], ks[:ctx])
     return out
 

@@ -207,6 +207,109 @@ def test_slot_mapping_brute_force_inverse():
 
 
 # ----------------------------------------------------------------------------
+# compressed slot mapping (one cache entry per compress_ratio tokens)
+# ----------------------------------------------------------------------------
+
+def test_compressed_slot_mapping_example():
+    g = golden("compressed_slot_mapping.json")
+    for case in g["cases"]:
+        row = np.array(case["block_table_row"], np.int32)[None, :]
+        n = int(case["ratio"])
+        for pos, want in zip(case["positions"], case["slots"]):
+            got = O.compressed_slot_mapping(np.array([0, 1]), np.array([pos + 1]), row, n)
+            assert got.tolist() == [want], (n, pos)
+
+
+def test_compressed_entries_per_256_token_block():
+    """A 256-token prefill keeps 64 entries at ratio 4 and 2 at ratio 128, in
+    entry order at the front of the request's first indexer page."""
+    g = golden("compressed_slot_mapping.json")
+    bt = np.array([[9, 4, 6, 1]], np.int32)
+    for ratio, want in g["entries_per_256_token_block"].items():
+        slots = O.compressed_slot_mapping(np.array([0, 256]), np.array([256]), bt, int(ratio))
+        kept = slots[slots >= 0]
+        assert kept.size == want
+        assert kept.tolist() == [9 * 64 + i for i in range(want)]
+
+
+def test_compressed_ratio_one_is_the_plain_mapping():
+    rng = np.random.default_rng(21)
+    seq = np.array([1, 77, 300, 64])
+    ql = np.array([1, 5, 300, 0])
+    qsl = np.concatenate([[0], np.cumsum(ql)])
+    bt = rng.permutation(40).astype(np.int32)[:20].reshape(4, 5)
+    assert np.array_equal(O.compressed_slot_mapping(qsl, seq, bt, 1), O.slot_mapping(qsl, seq, bt))
+    with pytest.raises(ValueError):
+        O.compressed_slot_mapping(qsl, seq, bt, 0)
+
+
+def test_compressed_write_leaves_unmapped_tokens_out():
+    """Rows with slot -1 change no byte; the others land as an uncompressed
+    write of just those rows would put them."""
+    rng = np.random.default_rng(22)
+    k = rng.standard_normal((200, 128)).astype(np.float32)
+    bt = np.array([[3, 0]], np.int32)
+    slots = O.compressed_slot_mapping(np.array([0, 200]), np.array([200]), bt, 4)
+    got = O.write_k_cache(np.full((5, O.PAGE_BYTES), 0x3C, np.uint8), k, slots)
+    keep = np.nonzero(slots >= 0)[0]
+    assert keep.tolist() == list(range(3, 200, 4))
+    want = np.full((5, O.PAGE_BYTES), 0x3C, np.uint8)
+    for i in keep:          # one row at a time, at the page offset worked out by hand
+        c = i // 4
+        O.write_k_cache(want, k[i:i + 1], np.array([3 * 64 + c]))
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("ratio", [2, 3, 4, 7])
+def test_compressed_rows_brute_force(ratio):
+    """Every row against an enumeration of the states its request holds: walk
+    the request's tokens in order, let each token that completes a state append
+    its key, and rank the states appended by tokens at or before the row."""
+    rng = np.random.default_rng(300 + ratio)
+    seq = np.array([5 * ratio + 3, ratio - 1, 2 * ratio, 9 * ratio + 1])
+    ql = np.array([4 * ratio, ratio - 1, 2, 1])
+    R, H, k = len(seq), 4, 5
+    tokens = [rng.standard_normal((int(s), 128)).astype(np.float32) for s in seq]
+    entries = [int(s) // ratio for s in seq]
+    pages = [max(1, (e + 63) // 64) for e in entries]
+    pool = sum(pages) + 2
+    perm = rng.permutation(pool).astype(np.int32)
+    bt = np.full((R, max(pages)), -1, np.int32)
+    at = 0
+    for r, n in enumerate(pages):
+        bt[r, :n] = perm[at:at + n]
+        at += n
+    cache = np.zeros((pool, O.PAGE_BYTES), np.uint8)
+    for r in range(R):                       # the cached prefix, written by an earlier step
+        P = int(seq[r] - ql[r])
+        if P:
+            sl = O.compressed_slot_mapping(np.array([0, P]), np.array([P]), bt[r:r + 1], ratio)
+            O.write_k_cache(cache, tokens[r][:P], sl)
+    qsl = np.concatenate([[0], np.cumsum(ql)])
+    T = int(qsl[-1])
+    k_new = np.concatenate([tokens[r][int(seq[r] - ql[r]):] for r in range(R)])
+    qc, qs = O.quantize_blocks(rng.standard_normal((T, H, 128)).astype(np.float32))
+    w = rng.standard_normal((T, H)).astype(np.float32)
+    buf = np.full((T + 1, k), 7, np.int32)
+    O.indexer_layer(cache, k_new, qc, qs, w, qsl, seq, bt, k, buf, compress_ratio=ratio)
+    assert np.all(buf[T] == 7)
+    for r in range(R):
+        for j in range(int(ql[r])):
+            t = int(qsl[r]) + j
+            pos = int(seq[r] - ql[r]) + j
+            states = [tokens[r][p] for p in range(pos + 1) if (p + 1) % ratio == 0]
+            if states:
+                kc, ks = O.quantize_blocks(np.stack(states))
+                s = np.array([sum(float(w[t, h]) * max(float(np.dot(
+                    O.e4m3_decode(qc[t, h]) * float(qs[t, h]), O.e4m3_decode(kc[i]) * float(ks[i]))), 0.0)
+                    for h in range(H)) for i in range(len(states))])
+                want = O.topk_row(s, k)
+            else:
+                want = np.full(k, -1, np.int32)
+            assert np.array_equal(buf[t], want), (ratio, r, j)
+
+
+# ----------------------------------------------------------------------------
 # scores
 # ----------------------------------------------------------------------------
 
