@@ -284,7 +284,8 @@ def main():
                        offset=wl.offset, H=wl.H, index_topk=wl.index_topk, T=wl.T, R=wl.R,
                        max_blocks=wl.max_blocks, num_pages=wl.num_pages,
                        max_num_batched_tokens=wl.max_num_batched_tokens, k_caches=caches,
-                       device=dev, time_score_kernels=True, bf16=args.bf16)
+                       device=dev, time_score_kernels=True, bf16=args.bf16,
+                       compress_ratio=wl.compress_ratio)
     host_meta = tuple(torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in
                       (wl.query_start_loc, wl.seq_lens.astype(np.int32), wl.block_table))
     host = {"meta": host_meta, "layers": host_layers}
@@ -386,9 +387,9 @@ def main():
     peaks = read_peaks()
     k_ms = sum(score_ms) / len(score_ms)
     rows_bytes = wl.T * (wl.H * (128 + 4 + 4) + wl.index_topk * 4)   # q, q_scale, w in; top-k out
-    # every key of a request is read once, whatever the number of its query rows
-    # (one row per request in a decode batch: one key per pair)
-    key_bytes = float(wl.seq_lens[wl.q_lens > 0].astype(np.int64).sum()) * BYTES_PER_PAIR
+    # every key (cache entry) of a request is read once, whatever the number of
+    # its query rows (one row per request in a decode batch: one key per pair)
+    key_bytes = float(wl.entries[wl.q_lens > 0].astype(np.int64).sum()) * BYTES_PER_PAIR
     alg_bytes = key_bytes + rows_bytes
     achieved = alg_bytes / (k_ms * 1e-3) / 1e9
     traffic = profiled_traffic(wl.name)

@@ -41,14 +41,17 @@ EXPORTS = (
     "dsa_last_launch_count",
     "dsa_indexer_write_k",
     "dsa_indexer_write_k_bf16",
+    "dsa_indexer_write_k_compressed",
     "dsa_quantize_fp8_blocks",
     "dsa_indexer_workspace_bytes",
     "dsa_indexer_score_topk",
     "dsa_indexer_score_topk_no_alloc",
+    "dsa_indexer_score_topk_compressed",
     "dsa_indexer_no_alloc_workspace_bytes",
     "dsa_layer_is_full",
     "dsa_layer_stack_run",
     "dsa_layer_stack_run_bf16",
+    "dsa_layer_stack_run_compressed",
 )
 
 
@@ -103,6 +106,9 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.dsa_indexer_write_k_bf16.restype = _I
     lib.dsa_indexer_write_k_bf16.argtypes = [
         _P, _I, _P, _P, _I, _P, _I, _P, _I64, _P, _I, _P, _P, _P, _P, _P]
+    lib.dsa_indexer_write_k_compressed.restype = _I
+    lib.dsa_indexer_write_k_compressed.argtypes = [
+        _P, _I, _P, _P, _I, _P, _I, _P, _I64, _I, _P, _P, _P]
     lib.dsa_quantize_fp8_blocks.restype = _I
     lib.dsa_quantize_fp8_blocks.argtypes = [_P, _I64, _P, _P, _P]
     lib.dsa_indexer_workspace_bytes.restype = _SZ
@@ -113,6 +119,10 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.dsa_indexer_score_topk_no_alloc.restype = _I
     lib.dsa_indexer_score_topk_no_alloc.argtypes = [
         _P, _P, _P, _I, _I, _P, _I64, _P, _P, _I, _P, _I, _I, _P, _I, _P, _P]
+    lib.dsa_indexer_score_topk_compressed.restype = _I
+    lib.dsa_indexer_score_topk_compressed.argtypes = [
+        _P, _P, _P, _I, _I, _P, _I64, _P, _P, _I, _P, _I, _I, _I, _P, _I, _P, _I64, _P, _SZ, _P,
+        _P]
     lib.dsa_indexer_no_alloc_workspace_bytes.restype = _SZ
     lib.dsa_indexer_no_alloc_workspace_bytes.argtypes = []
     lib.dsa_layer_is_full.restype = _I
@@ -121,6 +131,10 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.dsa_layer_stack_run.argtypes = [
         _I, ctypes.c_char_p, _I, _I, ctypes.POINTER(LayerIO), _I, _I, _P, _P, _I, _P, _I, _I64,
         _I, _P, _I, ctypes.POINTER(ctypes.c_void_p), _P, _P, _SZ, _P, _P]
+    lib.dsa_layer_stack_run_compressed.restype = _I
+    lib.dsa_layer_stack_run_compressed.argtypes = [
+        _I, ctypes.c_char_p, _I, _I, ctypes.POINTER(LayerIO), _I, _I, _P, _P, _I, _P, _I, _I64,
+        _I, _I, _P, _I, ctypes.POINTER(ctypes.c_void_p), _P, _P, _SZ, _P, _P]
     lib.dsa_layer_stack_run_bf16.restype = _I
     lib.dsa_layer_stack_run_bf16.argtypes = [
         _I, ctypes.c_char_p, _I, _I, ctypes.POINTER(LayerIOBf16), _I, _I, _P, _P, _I, _P, _I,
@@ -226,6 +240,23 @@ def write_k(k: torch.Tensor, query_start_loc: torch.Tensor, seq_lens: torch.Tens
             block_table: torch.Tensor, k_cache: torch.Tensor,
             slot_mapping: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
             stream=None) -> None:
+    _check(load().dsa_indexer_write_k(*_write_k_args(
+        k, query_start_loc, seq_lens, block_table, k_cache, slot_mapping, status, stream)))
+
+
+def write_k_compressed(k: torch.Tensor, query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
+                       block_table: torch.Tensor, k_cache: torch.Tensor, compress_ratio: int,
+                       slot_mapping: Optional[torch.Tensor] = None,
+                       status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Cache write into a compressed cache: only tokens with
+    (pos + 1) % compress_ratio == 0 are stored, as entry pos // compress_ratio."""
+    a = _write_k_args(k, query_start_loc, seq_lens, block_table, k_cache, slot_mapping, status,
+                      stream)
+    _check(load().dsa_indexer_write_k_compressed(*a[:9], int(compress_ratio), *a[9:]))
+
+
+def _write_k_args(k, query_start_loc, seq_lens, block_table, k_cache, slot_mapping, status,
+                  stream):
     T = k.shape[0]
     R = seq_lens.shape[0]
     _need(k, "k", torch.float32, (T, HEAD_DIM))
@@ -237,10 +268,9 @@ def write_k(k: torch.Tensor, query_start_loc: torch.Tensor, seq_lens: torch.Tens
         _need(slot_mapping, "slot_mapping", torch.int64, (T,))
     if status is not None:
         _need(status, "status", torch.int32)
-    _check(load().dsa_indexer_write_k(
-        _ptr(k), T, _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table),
-        block_table.shape[1], _ptr(k_cache), k_cache.shape[0], _ptr(slot_mapping), _ptr(status),
-        _stream(stream)))
+    return (_ptr(k), T, _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table),
+            block_table.shape[1], _ptr(k_cache), k_cache.shape[0], _ptr(slot_mapping),
+            _ptr(status), _stream(stream))
 
 
 def write_k_bf16(k: torch.Tensor, query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
@@ -280,6 +310,26 @@ def score_topk(q_fp8: torch.Tensor, q_scale: torch.Tensor, w: torch.Tensor,
                block_table: torch.Tensor, index_topk: int, topk_buffer: torch.Tensor,
                workspace: torch.Tensor, scores_out: Optional[torch.Tensor] = None,
                status: Optional[torch.Tensor] = None, stream=None) -> None:
+    _check(load().dsa_indexer_score_topk(*_score_args(
+        q_fp8, q_scale, w, k_cache, query_start_loc, seq_lens, block_table, index_topk,
+        topk_buffer, workspace, scores_out, status, stream)))
+
+
+def score_topk_compressed(q_fp8: torch.Tensor, q_scale: torch.Tensor, w: torch.Tensor,
+                          k_cache: torch.Tensor, query_start_loc: torch.Tensor,
+                          seq_lens: torch.Tensor, block_table: torch.Tensor, compress_ratio: int,
+                          index_topk: int, topk_buffer: torch.Tensor, workspace: torch.Tensor,
+                          scores_out: Optional[torch.Tensor] = None,
+                          status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """score_topk over a compressed cache: row t ranks the entries
+    c < (pos + 1) // compress_ratio; indices (and scores_out columns) are entries."""
+    a = _score_args(q_fp8, q_scale, w, k_cache, query_start_loc, seq_lens, block_table,
+                    index_topk, topk_buffer, workspace, scores_out, status, stream)
+    _check(load().dsa_indexer_score_topk_compressed(*a[:12], int(compress_ratio), *a[12:]))
+
+
+def _score_args(q_fp8, q_scale, w, k_cache, query_start_loc, seq_lens, block_table, index_topk,
+                topk_buffer, workspace, scores_out, status, stream):
     T, H = q_fp8.shape[0], q_fp8.shape[1]
     R = seq_lens.shape[0]
     _need(q_fp8, "q_fp8", torch.uint8, (T, H, HEAD_DIM))
@@ -297,11 +347,10 @@ def score_topk(q_fp8: torch.Tensor, q_scale: torch.Tensor, w: torch.Tensor,
         ld = scores_out.shape[1]
     if status is not None:
         _need(status, "status", torch.int32)
-    _check(load().dsa_indexer_score_topk(
-        _ptr(q_fp8), _ptr(q_scale), _ptr(w), T, H, _ptr(k_cache), k_cache.shape[0],
-        _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table), block_table.shape[1],
-        index_topk, _ptr(topk_buffer), topk_buffer.shape[0], _ptr(scores_out), ld,
-        _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)))
+    return (_ptr(q_fp8), _ptr(q_scale), _ptr(w), T, H, _ptr(k_cache), k_cache.shape[0],
+            _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table), block_table.shape[1],
+            index_topk, _ptr(topk_buffer), topk_buffer.shape[0], _ptr(scores_out), ld,
+            _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
 
 
 def score_topk_no_alloc(q_fp8: torch.Tensor, q_scale: torch.Tensor, w: torch.Tensor,
@@ -340,10 +389,12 @@ def layer_stack_run(layers: Sequence[Optional[dict]], pattern: Optional[str], fr
                     per_layer_out: Optional[Sequence[Optional[torch.Tensor]]] = None,
                     slot_mapping: Optional[torch.Tensor] = None,
                     status: Optional[torch.Tensor] = None, T: Optional[int] = None,
-                    stream=None) -> None:
+                    stream=None, compress_ratio: int = 1) -> None:
     """Run the F/S layer stack.  ``layers[l]`` is a dict with keys k, q_fp8,
     q_scale, w, k_cache (and optionally score_begin / score_end, torch.cuda.Event
-    objects created with enable_timing=True) for F layers, or None for S layers."""
+    objects created with enable_timing=True) for F layers, or None for S layers.
+    ``compress_ratio`` > 1 runs dsa_layer_stack_run_compressed (compressed
+    caches, one entry per compress_ratio tokens)."""
     R = seq_lens.shape[0]
     _need(query_start_loc, "query_start_loc", torch.int32, (R + 1,))
     _need(seq_lens, "seq_lens", torch.int32, (R,))
@@ -380,11 +431,20 @@ def layer_stack_run(layers: Sequence[Optional[dict]], pattern: Optional[str], fr
         _need(slot_mapping, "slot_mapping", torch.int64, (T,))
     if status is not None:
         _need(status, "status", torch.int32)
-    _check(load().dsa_layer_stack_run(
-        L, None if pattern is None else pattern.encode(), freq, offset, arr, T, H,
-        _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table), block_table.shape[1],
-        num_pages, index_topk, _ptr(topk_buffer), topk_buffer.shape[0], outs, _ptr(slot_mapping),
-        _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)))
+    head = (L, None if pattern is None else pattern.encode(), freq, offset, arr, T, H,
+            _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table), block_table.shape[1],
+            num_pages)
+    tail = (index_topk, _ptr(topk_buffer), topk_buffer.shape[0], outs, _ptr(slot_mapping),
+            _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
+    if compress_ratio == 1:
+        _check(load().dsa_layer_stack_run(*head, *tail))
+    else:
+        _check(load().dsa_layer_stack_run_compressed(*head, int(compress_ratio), *tail))
+
+
+def layer_stack_run_compressed(*args, compress_ratio: int, **kw) -> None:
+    """dsa_layer_stack_run_compressed: layer_stack_run's arguments plus the ratio."""
+    layer_stack_run(*args, compress_ratio=compress_ratio, **kw)
 
 
 def layer_stack_run_bf16(layers: Sequence[Optional[dict]], pattern: Optional[str], freq: int,

@@ -242,11 +242,13 @@ struct Batch {
   size_t ws_bytes;
   int32_t* status;
   cudaStream_t st;
+  int ratio = 1;  // tokens per cache entry (compressed indexer cache when > 1)
 };
 
 int check_batch(const Batch& b) {
   if (b.T < 0) return fail(DSA_ERR_INVALID_ARG, "T=%d < 0", b.T);
   if (b.R < 1) return fail(DSA_ERR_INVALID_ARG, "R=%d < 1", b.R);
+  if (b.ratio < 1) return fail(DSA_ERR_INVALID_ARG, "compress_ratio=%d < 1", b.ratio);
   if (!supported_heads(b.H)) return fail(DSA_ERR_UNSUPPORTED, "H=%d not in {4,8,16,32,64,128}", b.H);
   if (b.k < 1 || b.k > DSA_MAX_TOPK)
     return fail(DSA_ERR_UNSUPPORTED, "index_topk=%d outside [1, %d]", b.k, DSA_MAX_TOPK);
@@ -276,6 +278,7 @@ int launch_plan(const Batch& b, int G, int* launches) {
   pp.G = G;
   pp.max_blocks = b.max_blocks;
   pp.index_topk = b.k;
+  pp.ratio = b.ratio;
   if (sm_count() <= 0) return fail(DSA_ERR_CUDA, "no CUDA device");
   pp.n_cta = grid_ctas();
   pp.min_tiles = env_int("DSA_MIN_SPLIT", 1024, 128, 1 << 20) / 128;
@@ -326,6 +329,7 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   p.NQ = s.NQ;
   p.NR = s.NR;
   p.BPS = s.BPS;
+  p.ratio = b.ratio;
   p.q_bytes = s.q_bytes;
   p.n_max = s.n_max;
   p.q_box_per_token = s.q_box_per_token;
@@ -370,7 +374,7 @@ int launch_write_t(const TIn* k, const Batch& b, uint8_t* k_cache, int64_t* slot
   if (grid > INT32_MAX) return fail(DSA_ERR_INVALID_ARG, "too many rows for one cache-write launch");
   dsa::write_k_kernel<TIn><<<(unsigned)grid, 32 * warps_per_block, 0, b.st>>>(
       k, b.T, b.qsl, b.seq_lens, b.R, b.block_table, b.max_blocks, k_cache, b.num_pages,
-      slot_mapping, b.status, q, H, q_fp8, q_scale);
+      b.ratio, slot_mapping, b.status, q, H, q_fp8, q_scale);
   ++*launches;
   return check_launch("write_k_kernel");
 }
@@ -567,7 +571,18 @@ int dsa_indexer_write_k(const float* k, int T, const int32_t* query_start_loc,
                         const int32_t* seq_lens, int R, const int32_t* block_table,
                         int max_blocks, uint8_t* k_cache, int64_t num_pages,
                         int64_t* slot_mapping, int32_t* dev_status, dsa_stream_t stream) {
+  return dsa_indexer_write_k_compressed(k, T, query_start_loc, seq_lens, R, block_table,
+                                        max_blocks, k_cache, num_pages, 1, slot_mapping,
+                                        dev_status, stream);
+}
+
+int dsa_indexer_write_k_compressed(const float* k, int T, const int32_t* query_start_loc,
+                                   const int32_t* seq_lens, int R, const int32_t* block_table,
+                                   int max_blocks, uint8_t* k_cache, int64_t num_pages,
+                                   int compress_ratio, int64_t* slot_mapping,
+                                   int32_t* dev_status, dsa_stream_t stream) {
   g_last_launches = 0;
+  if (compress_ratio < 1) return fail(DSA_ERR_INVALID_ARG, "compress_ratio=%d < 1", compress_ratio);
   if (T < 0) return fail(DSA_ERR_INVALID_ARG, "T=%d < 0", T);
   if (R < 1) return fail(DSA_ERR_INVALID_ARG, "R=%d < 1", R);
   if (max_blocks < 1) return fail(DSA_ERR_INVALID_ARG, "max_blocks < 1");
@@ -587,6 +602,7 @@ int dsa_indexer_write_k(const float* k, int T, const int32_t* query_start_loc,
   b.block_table = block_table;
   b.status = dev_status;
   b.st = (cudaStream_t)stream;
+  b.ratio = compress_ratio;
   int launches = 0;
   const int rc = launch_write(k, b, k_cache, slot_mapping, &launches);
   g_last_launches = launches;
@@ -600,10 +616,25 @@ int dsa_indexer_score_topk(const uint8_t* q_fp8, const float* q_scale, const flo
                            int32_t* topk_buffer, int max_num_batched_tokens, float* scores_out,
                            int64_t scores_ld, void* workspace, size_t workspace_bytes,
                            int32_t* dev_status, dsa_stream_t stream) {
+  return dsa_indexer_score_topk_compressed(q_fp8, q_scale, w, T, H, k_cache, num_pages,
+                                           query_start_loc, seq_lens, R, block_table, max_blocks,
+                                           1, index_topk, topk_buffer, max_num_batched_tokens,
+                                           scores_out, scores_ld, workspace, workspace_bytes,
+                                           dev_status, stream);
+}
+
+int dsa_indexer_score_topk_compressed(const uint8_t* q_fp8, const float* q_scale, const float* w,
+                                      int T, int H, const uint8_t* k_cache, int64_t num_pages,
+                                      const int32_t* query_start_loc, const int32_t* seq_lens,
+                                      int R, const int32_t* block_table, int max_blocks,
+                                      int compress_ratio, int index_topk, int32_t* topk_buffer,
+                                      int max_num_batched_tokens, float* scores_out,
+                                      int64_t scores_ld, void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_status, dsa_stream_t stream) {
   g_last_launches = 0;
   Batch b{T, H, R, max_blocks, index_topk, max_num_batched_tokens, num_pages, query_start_loc,
           seq_lens, block_table, topk_buffer, workspace, workspace_bytes, dev_status,
-          (cudaStream_t)stream};
+          (cudaStream_t)stream, compress_ratio};
   int rc = check_batch(b);
   if (rc) return rc;
   if (T == 0) return DSA_OK;
@@ -663,6 +694,20 @@ int dsa_layer_stack_run(int num_layers, const char* pattern, int freq, int offse
   const Batch b{T, H, R, max_blocks, index_topk, max_num_batched_tokens, num_pages,
                 query_start_loc, seq_lens, block_table, topk_buffer, workspace, workspace_bytes,
                 dev_status, (cudaStream_t)stream};
+  return stack_run(num_layers, pattern, freq, offset, layers, b, per_layer_topk_out, slot_mapping);
+}
+
+int dsa_layer_stack_run_compressed(int num_layers, const char* pattern, int freq, int offset,
+                                   const dsa_layer_io* layers, int T, int H,
+                                   const int32_t* query_start_loc, const int32_t* seq_lens, int R,
+                                   const int32_t* block_table, int max_blocks, int64_t num_pages,
+                                   int compress_ratio, int index_topk, int32_t* topk_buffer,
+                                   int max_num_batched_tokens, int32_t* const* per_layer_topk_out,
+                                   int64_t* slot_mapping, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_status, dsa_stream_t stream) {
+  const Batch b{T, H, R, max_blocks, index_topk, max_num_batched_tokens, num_pages,
+                query_start_loc, seq_lens, block_table, topk_buffer, workspace, workspace_bytes,
+                dev_status, (cudaStream_t)stream, compress_ratio};
   return stack_run(num_layers, pattern, freq, offset, layers, b, per_layer_topk_out, slot_mapping);
 }
 

@@ -74,11 +74,16 @@ __device__ __forceinline__ float4 load_lane4(const uint16_t* x, int64_t blk, int
 // page pool).  Warps [T, T + T*H) when q is given: the query rows' H blocks
 // each, quantised to q_codes [T, H, 128] and q_scales [T, H] with the same
 // rule, so one launch performs the whole per-token quantisation of a layer.
+//
+// Compressed cache ("HBM 索引架构设计" §5.2), ratio > 1: only a token with
+// (pos + 1) % ratio == 0 holds an entry, number pos / ratio, stored through
+// the block table like a token position; the others get slot -1 and write
+// nothing.  ratio 1 is the plain cache.
 template <typename TIn>
 __global__ void __launch_bounds__(256) write_k_kernel(
     const TIn* __restrict__ k, int T, const int32_t* __restrict__ qsl,
     const int32_t* __restrict__ seq_lens, int R, const int32_t* __restrict__ block_table,
-    int max_blocks, uint8_t* __restrict__ k_cache, int64_t num_pages,
+    int max_blocks, uint8_t* __restrict__ k_cache, int64_t num_pages, int ratio,
     int64_t* __restrict__ slot_mapping, int32_t* status, const TIn* __restrict__ q, int H,
     uint8_t* __restrict__ q_codes, float* __restrict__ q_scales) {
   pdl_launch_dependents();  // the scoring kernel's prologue may overlap this write
@@ -105,15 +110,16 @@ __global__ void __launch_bounds__(256) write_k_kernel(
   const int seq_len = __ldg(seq_lens + r);
   const int pos = seq_len - q_len + (t - q_begin);
   int64_t slot = -1;
+  const int entry = pos / ratio;  // cache entry of a token that completes one
   if (q_len < 0 || seq_len < q_len || pos < 0 || pos >= seq_len ||
-      pos / kPageTokens >= max_blocks) {
+      ((pos + 1) % ratio == 0 && entry / kPageTokens >= max_blocks)) {
     if (lane == 0) raise_status(status, kStatusBadMetadata);
-  } else {
-    const int64_t page = __ldg(block_table + (int64_t)r * max_blocks + pos / kPageTokens);
+  } else if ((pos + 1) % ratio == 0) {
+    const int64_t page = __ldg(block_table + (int64_t)r * max_blocks + entry / kPageTokens);
     if (page < 0 || page >= num_pages) {
       if (lane == 0) raise_status(status, kStatusBadPage);
     } else {
-      const int off = pos % kPageTokens;
+      const int off = entry % kPageTokens;
       uint8_t* pg = k_cache + page * kPageBytes;
       reinterpret_cast<uint32_t*>(pg + off * kHeadDim)[lane] = codes;
       if (lane == 0) *reinterpret_cast<float*>(pg + kPageScaleOffset + off * 4) = s;

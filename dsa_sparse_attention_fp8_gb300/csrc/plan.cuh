@@ -122,6 +122,7 @@ struct PlanParams {
   const int32_t* qsl;
   const int32_t* seq_lens;
   int R, T, G, max_blocks, index_topk;
+  int ratio;       // tokens per cache entry (1: plain cache)
   int n_cta;       // CTAs of the scoring launch (<= kMaxCtas)
   int min_tiles;   // smallest per-CTA share worth a piece of its own
   int32_t* topk_buffer;  // for -1 rows of malformed requests
@@ -130,16 +131,19 @@ struct PlanParams {
   int32_t* status;
 };
 
-// Keys visible to the last row of group g of a request with prefix P and q new rows.
-__device__ __forceinline__ long long group_keys(long long P, int q, int G, int g) {
+// Cache entries visible to the last row of group g of a request with prefix P
+// and q new rows: the row at position pos sees (pos + 1) / ratio entries.
+__device__ __forceinline__ long long group_keys(long long P, int q, int G, int g, int ratio) {
   const int last = min((g + 1) * G, q);
-  return P + last;
+  return (P + last) / ratio;
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   pdl_launch_dependents();  // the scoring kernel's prologue may overlap the plan
   __shared__ long long warp_sums[32];
   __shared__ long long s_Q;
+  __shared__ int2 s_empty[kPlanThreads];  // (first row, rows) of groups that see no entry
+  __shared__ int s_n_empty;
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.L.header);
   int32_t* group_prefix = reinterpret_cast<int32_t*>(p.ws + p.L.group_prefix);
   int32_t* cta_start = reinterpret_cast<int32_t*>(p.ws + p.L.cta_start);
@@ -155,7 +159,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     if (r < p.R) {
       const int qb = p.qsl[r], qe = p.qsl[r + 1];
       const int q = qe - qb, seq = p.seq_lens[r];
-      const bool bad = q < 0 || seq < q || (long long)seq > (long long)p.max_blocks * kPageTokens ||
+      const bool bad = q < 0 || seq < q ||
+                       (long long)(seq / p.ratio) > (long long)p.max_blocks * kPageTokens ||
                        qb < 0 || qe > p.T;
       if (bad) {
         raise_status(p.status, kStatusBadMetadata);
@@ -186,7 +191,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     const int qb = p.qsl[r], q = p.qsl[r + 1] - qb;
     t0 = qb + g * G;
     gcount = min(G, q - g * G);
-    keys = group_keys((long long)p.seq_lens[r] - q, q, G, g);
+    keys = group_keys((long long)p.seq_lens[r] - q, q, G, g, p.ratio);
   };
 
   // Phase B: total tiles W, the per-CTA share Q and the number of items.
@@ -208,6 +213,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     if (Q < p.min_tiles) Q = p.min_tiles;
     if (Q < 1) Q = 1;
     s_Q = Q;
+    s_n_empty = 0;
   }
   __syncthreads();
   const long long Q = s_Q;
@@ -256,6 +262,24 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     item_carry += t_items;
     sg_carry += t_sg;
     cb_carry += t_cb;
+    if (p.ratio > 1) {
+      // a compressed cache leaves the first rows of a request without a visible
+      // entry: no item covers them, so their rows are all -1, written here a
+      // warp per group
+      if (gi < total_groups && keys == 0) s_empty[atomicAdd(&s_n_empty, 1)] = make_int2(t0, gc);
+      __syncthreads();
+      const int n_empty = s_n_empty;
+      const int lane = threadIdx.x & 31;
+      for (int e = threadIdx.x >> 5; e < n_empty; e += kPlanThreads / 32) {
+        const int2 ge = s_empty[e];
+        for (int t = ge.x; t < ge.x + ge.y; ++t)
+          for (int i = lane; i < p.index_topk; i += 32)
+            p.topk_buffer[(size_t)t * p.index_topk + i] = -1;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) s_n_empty = 0;
+      __syncthreads();
+    }
   }
   const int any_overflow = __syncthreads_or(overflow ? 1 : 0);
   if (any_overflow) raise_status(p.status, kStatusBadMetadata);

@@ -48,7 +48,7 @@ constexpr int kTmemCols = 512;
 struct TokSlot {
   int32_t count;   // candidates held
   uint32_t thr;    // keys <= thr are not admitted
-  int32_t pos;     // position of the query row in its request
+  int32_t pos;     // last cache entry the query row sees (its position when uncompressed)
   int32_t t;       // query row
 };
 
@@ -63,6 +63,7 @@ struct ScoreParams {
   const float* w;
   int T, H, G, k, C, NS, NB, NQ, NR, n_max;
   int BPS;           // 128-key MMA blocks per pipeline stage (1 or 2); a tile = one stage
+  int ratio;         // tokens per cache entry: a row at pos sees entries < (pos + 1) / ratio
   int q_box_per_token;
   uint32_t q_bytes;  // bytes of one query-tile buffer
   const Item* items;
@@ -1000,7 +1001,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           if (tid == 0) {
             tok[g].count = 0;
             tok[g].thr = 0u;
-            tok[g].pos = seq_len - q_len + (t - qb0);
+            tok[g].pos = (seq_len - q_len + (t - qb0) + 1) / p.ratio - 1;  // last visible entry
             tok[g].t = t;
           }
         }

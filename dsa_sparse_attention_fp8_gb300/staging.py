@@ -52,11 +52,13 @@ def fill_prefix(wl, layer: int, meta: DeviceMeta, k_cache: torch.Tensor,
                 chunk_tokens: int = 1 << 22) -> None:
     """Write every request's cached-prefix keys of `layer` into `k_cache`.
 
-    Requests are written in batches of at most `chunk_tokens` tokens, each
-    batch as one cache-write call whose "new tokens" are the prefix tokens.
+    Requests are written in batches of at most `chunk_tokens` entries, each
+    batch as one cache-write call whose "new tokens" are the prefix entries
+    (for a compressed cache, the entries completed before this step, stored
+    at entry positions 0 .. prefix_entries-1).
     """
     dev = k_cache.device
-    pre = wl.prefix_lens.astype(np.int64)
+    pre = wl.prefix_entries.astype(np.int64)
     r = 0
     while r < wl.R:
         rs, tot = [], 0

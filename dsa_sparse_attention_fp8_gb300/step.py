@@ -21,12 +21,16 @@ class IndexerStep:
     def __init__(self, *, num_layers: int, pattern: Optional[str], freq: int, offset: int,
                  H: int, index_topk: int, T: int, R: int, max_blocks: int, num_pages: int,
                  max_num_batched_tokens: int, k_caches: Sequence[Optional[torch.Tensor]],
-                 device="cuda", time_score_kernels: bool = False, bf16: bool = False):
+                 device="cuda", time_score_kernels: bool = False, bf16: bool = False,
+                 compress_ratio: int = 1):
         self.num_layers, self.pattern, self.freq, self.offset = num_layers, pattern, freq, offset
         self.H, self.k, self.T, self.R = H, index_topk, T, R
         self.max_blocks, self.num_pages = max_blocks, num_pages
         self.device = torch.device(device)
         self.bf16 = bf16   # BF16 keys and queries, quantised by the cache-write launch
+        self.compress_ratio = compress_ratio  # tokens per cache entry (compressed caches)
+        if bf16 and compress_ratio != 1:
+            raise ValueError("the BF16 layer stack has no compressed form")
         self.input_keys = ("k", "q", "w") if bf16 else ("k", "q_fp8", "q_scale", "w")
         self.full = [binding.layer_is_full(l, pattern, freq, offset) for l in range(num_layers)]
         dev = self.device
@@ -89,11 +93,14 @@ class IndexerStep:
             layers = [None if io is None else {k: v for k, v in io.items()
                                                if k not in ("score_begin", "score_end")}
                       for io in self.layers]
-        run = binding.layer_stack_run_bf16 if self.bf16 else binding.layer_stack_run
-        run(layers, self.pattern, self.freq, self.offset, self.H,
-                                self.query_start_loc, self.seq_lens, self.block_table,
-                                self.num_pages, self.k, self.topk, self.workspace,
-                                status=self.status, T=self.T)
+        args = (layers, self.pattern, self.freq, self.offset, self.H, self.query_start_loc,
+                self.seq_lens, self.block_table, self.num_pages, self.k, self.topk,
+                self.workspace)
+        if self.bf16:
+            binding.layer_stack_run_bf16(*args, status=self.status, T=self.T)
+        else:
+            binding.layer_stack_run(*args, status=self.status, T=self.T,
+                                    compress_ratio=self.compress_ratio)
         self.launches_per_step = binding.last_launch_count()
 
     def capture(self) -> None:

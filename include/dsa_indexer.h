@@ -21,7 +21,9 @@
  *         (all key bytes of a page, then all scale bytes), the
  *         topk_indices_buffer passage, the write-path section
  *         (store_quantized), and "64 token 页的由来" (64-token pages).
- *   [HBM] "HBM 索引架构设计" -- §2.3 (slot = block_table[req, pos/bs]*bs + pos%bs).
+ *   [HBM] "HBM 索引架构设计" -- §2.3 (slot = block_table[req, pos/bs]*bs + pos%bs);
+ *         §5.1-5.3 (compressed caches: one entry per compress_ratio tokens,
+ *         slot only for a token with (pos+1) % ratio == 0, -1 otherwise).
  *   [DSA] DeepSeek-V3.2 report (arXiv:2512.02556, in [KV]'s references):
  *         score(t,s) = sum_h w[t,h] * ReLU(q[t,h] . k[s]).
  *
@@ -46,6 +48,14 @@
  *   - Returned top-k indices are logical token positions inside the request
  *     (0 .. ctx-1), in no particular order; row t holds min(ctx(t), index_topk)
  *     valid indices followed by -1, ctx(t) = pos(t)+1 (causal, self included).
+ *   - Compressed cache (the *_compressed entry points, compress_ratio N >= 1;
+ *     N = 1 is the plain cache): entry c of a request holds the key of its
+ *     token at position (c+1)*N - 1, the token that completes the entry; the
+ *     block table maps 64-entry pages (entry c in block c/64, offset c%64),
+ *     so a request needs ceil((seq_len/N) / 64) blocks.  Row t sees the
+ *     entries c < ctx(t) = (pos(t)+1)/N (integer division: those whose
+ *     completing token is at or before it) and its indices are entry numbers.
+ *     Rows that see no entry are all -1.
  *   - Return value: DSA_OK or a negative DSA_ERR_*; the message of the last
  *     failing call on this thread is dsa_last_error().  Faults in device-side
  *     metadata (e.g. a block id outside [0, num_pages)) do not trap: the
@@ -124,6 +134,21 @@ int dsa_indexer_write_k_bf16(const void* k, int T, const int32_t* query_start_lo
                              int64_t* slot_mapping, int32_t* dev_status, dsa_stream_t stream);
 
 /*
+ * Step 1 for a compressed cache ([HBM] §5.2): like dsa_indexer_write_k, but
+ * only a token with (pos+1) % compress_ratio == 0 is stored, as entry
+ * pos / compress_ratio (see the conventions above); the other tokens write
+ * nothing and get slot -1.  k holds one row per new token (the rows of tokens
+ * that complete no entry are read but not stored).
+ *   slot_mapping  [T] int64 or NULL: page*64 + entry%64, or -1.
+ * Errors: as dsa_indexer_write_k, plus INVALID_ARG for compress_ratio < 1.
+ */
+int dsa_indexer_write_k_compressed(const float* k, int T, const int32_t* query_start_loc,
+                                   const int32_t* seq_lens, int R, const int32_t* block_table,
+                                   int max_blocks, uint8_t* k_cache, int64_t num_pages,
+                                   int compress_ratio, int64_t* slot_mapping,
+                                   int32_t* dev_status, dsa_stream_t stream);
+
+/*
  * Per-block FP8 quantiser used for keys, exposed for queries: x [n_blocks, 128]
  * FP32 -> codes [n_blocks, 128] E4M3 bytes + scales [n_blocks] FP32, same rule
  * as the cache write ([KV] byte-accounting table: 128 FP8 bytes + one FP32
@@ -164,6 +189,23 @@ int dsa_indexer_score_topk(const uint8_t* q_fp8, const float* q_scale, const flo
                            int32_t* topk_buffer, int max_num_batched_tokens, float* scores_out,
                            int64_t scores_ld, void* workspace, size_t workspace_bytes,
                            int32_t* dev_status, dsa_stream_t stream);
+
+/*
+ * Steps 2-3 over a compressed cache: as dsa_indexer_score_topk, with row t
+ * ranking the entries c < (pos(t)+1) / compress_ratio and returning entry
+ * numbers; scores_out[t, c] is indexed by entry.  compress_ratio = 1 is
+ * dsa_indexer_score_topk.  DSA_STATUS_BAD_METADATA also flags
+ * seq_len / compress_ratio > 64 * max_blocks.
+ * Errors: as dsa_indexer_score_topk, plus INVALID_ARG for compress_ratio < 1.
+ */
+int dsa_indexer_score_topk_compressed(const uint8_t* q_fp8, const float* q_scale, const float* w,
+                                      int T, int H, const uint8_t* k_cache, int64_t num_pages,
+                                      const int32_t* query_start_loc, const int32_t* seq_lens,
+                                      int R, const int32_t* block_table, int max_blocks,
+                                      int compress_ratio, int index_topk, int32_t* topk_buffer,
+                                      int max_num_batched_tokens, float* scores_out,
+                                      int64_t scores_ld, void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_status, dsa_stream_t stream);
 
 /*
  * Same computation and arguments as dsa_indexer_score_topk (without the debug
@@ -244,6 +286,21 @@ int dsa_layer_stack_run(int num_layers, const char* pattern, int freq, int offse
                         int32_t* const* per_layer_topk_out, int64_t* slot_mapping,
                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
                         dsa_stream_t stream);
+
+/*
+ * dsa_layer_stack_run over compressed caches: every F layer writes its keys
+ * as dsa_indexer_write_k_compressed and scores as
+ * dsa_indexer_score_topk_compressed, with one compress_ratio for the stack.
+ * Arguments, schedule and errors otherwise as dsa_layer_stack_run.
+ */
+int dsa_layer_stack_run_compressed(int num_layers, const char* pattern, int freq, int offset,
+                                   const dsa_layer_io* layers, int T, int H,
+                                   const int32_t* query_start_loc, const int32_t* seq_lens, int R,
+                                   const int32_t* block_table, int max_blocks, int64_t num_pages,
+                                   int compress_ratio, int index_topk, int32_t* topk_buffer,
+                                   int max_num_batched_tokens, int32_t* const* per_layer_topk_out,
+                                   int64_t* slot_mapping, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_status, dsa_stream_t stream);
 
 /* Per-layer inputs of dsa_layer_stack_run_bf16 (BF16 keys and queries). */
 typedef struct dsa_layer_io_bf16 {

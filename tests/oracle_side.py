@@ -11,10 +11,11 @@ import oracle as O
 SCORE_RTOL = 2e-3   # scores within 2e-3 x the row's max |score|
 
 
-def oracle_cache(wl, layer: int, with_new: bool = True) -> np.ndarray:
-    """The oracle's page pool for `layer`: cached prefix (+ this step's keys).
-    Prefix entries sit at entry positions 0 .. prefix_entries-1."""
-    cache = np.zeros((wl.num_pages, O.PAGE_BYTES), np.uint8)
+def oracle_cache(wl, layer: int, with_new: bool = True, fill: int = 0) -> np.ndarray:
+    """The oracle's page pool for `layer` (bytes never written hold `fill`):
+    cached prefix (+ this step's keys).  Prefix entries sit at entry
+    positions 0 .. prefix_entries-1."""
+    cache = np.full((wl.num_pages, O.PAGE_BYTES), fill, np.uint8)
     for r in range(wl.R):
         E = int(wl.prefix_entries[r])
         if E:
