@@ -7,3 +7,4 @@ shares no code with it.
 """
 
 from .dsa_oracle import *  # noqa: F401,F403
+from .sparse_mla import *  # noqa: F401,F403
