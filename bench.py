@@ -62,6 +62,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bf16", action="store_true",
                     help="BF16 keys and queries, quantised by the cache-write launch")
+    ap.add_argument("--sparse-mla", action="store_true",
+                    help="time the consumer instead: sparse MLA attention of every query row over "
+                         "its top-k tokens (record write + attention per F layer)")
+    ap.add_argument("--mla-heads", type=int, default=128)
     return ap.parse_args()
 
 
@@ -240,6 +244,208 @@ def run_reference(args, wl):
 
 
 # ----------------------------------------------------------------------------
+# Sparse MLA leg (the consumer of the top-k rows)
+# ----------------------------------------------------------------------------
+
+MLA_METRIC = "sparse MLA attention (row, selected token) pairs/s; % of BF16 tensor roofline"
+MLA_UNIT = "pairs/s"
+
+
+def mla_oracle_rows(wl, heads, scale, budget_s):
+    """The FP64 oracle on layer 0's rows in order until about budget_s seconds."""
+    import oracle as O
+    cache = np.zeros((wl.num_pages, O.MLA_PAGE_BYTES), np.uint8)
+    for r in range(wl.R):
+        P = int(wl.prefix_lens[r])
+        if P:
+            O.mla_write_kv_cache(cache, wl.mla_kv_prefix(0, r),
+                                 O.slot_mapping(np.array([0, P]), np.array([P]),
+                                                wl.block_table[r:r + 1]))
+    O.mla_write_kv_cache(cache, wl.mla_kv_new(0),
+                         O.slot_mapping(wl.query_start_loc, wl.seq_lens, wl.block_table))
+    q = wl.mla_q(0, heads).astype(np.float64)
+    topk = wl.selection_rows(0)
+    pairs, secs, n = 0, 0.0, 0
+    while secs < budget_s:
+        t = n % wl.T
+        t0 = time.perf_counter()
+        O.sparse_mla_attention(q, cache, wl.query_start_loc, wl.seq_lens, wl.block_table, topk,
+                               scale, rows=[t])
+        secs += time.perf_counter() - t0
+        pairs += int(np.sum(topk[t] >= 0))
+        n += 1
+    return pairs, secs, n
+
+
+def run_sparse_mla(args, wl):
+    import math
+    import torch
+    from dsa_sparse_attention_fp8_gb300 import _build, binding, staging
+
+    rank, world, local = dist_env()
+    heads, scale = args.mla_heads, 1.0 / math.sqrt(192.0)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        pairs, secs, n = mla_oracle_rows(wl, heads, scale, args.cpu_budget_s)
+        value = pairs / secs
+        line = {"impl": "reference", "metric": MLA_METRIC, "value": value, "unit": MLA_UNIT,
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": wl.name + "+sparse_mla", "heads": heads},
+                "cpu_baseline": {"value": value, "unit": MLA_UNIT, "cores": cpu_cores(),
+                                 "kind": "oracle", "sample": f"{n} query rows of layer 0"},
+                "e2e": {"value": value, "unit": MLA_UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    _build.build_library(quiet=True)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    meta = staging.stage_metadata(wl, dev)
+    full = [binding.layer_is_full(l, wl.pattern, wl.freq, wl.offset) for l in range(wl.num_layers)]
+    layers = []
+    for l in range(wl.num_layers):
+        if full[l]:
+            io = staging.stage_mla(wl, l, meta, heads, dev)
+            io["kv_new"] = torch.from_numpy(wl.mla_kv_new(l)).to(dev)
+            io["out"] = torch.empty((wl.T, heads, 512), dtype=torch.bfloat16, device=dev)
+            io["lse"] = torch.empty((wl.T, heads), dtype=torch.float32, device=dev)
+            layers.append(io)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    selected = sum(int((io["topk"][:wl.T] >= 0).sum().item()) for io in layers)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def one_step(events=None):
+        for j, io in enumerate(layers):
+            binding.mla_write_kv(io["kv_new"], meta.query_start_loc, meta.seq_lens,
+                                 meta.block_table, io["kv_cache"], status=status)
+            if events:
+                events[j][0].record(stream)
+            binding.sparse_mla_attention(io["q"], io["kv_cache"], meta.query_start_loc,
+                                         meta.seq_lens, meta.block_table, io["topk"], scale,
+                                         out=io["out"], lse=io["lse"], status=status)
+            if events:
+                events[j][1].record(stream)
+
+    one_step()
+    torch.cuda.synchronize()
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            one_step()
+    run = graph.replay if graph is not None else one_step
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    assert status.item() == 0, f"device status {status.item()}"
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ev0[i].record(stream)
+            run()
+            ev1[i].record(stream)
+            ev1[i].synchronize()
+        torch.cuda.synchronize()
+        k_ms = []
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in layers]
+            one_step(evs)
+            torch.cuda.synchronize()
+            k_ms.extend(a.elapsed_time(b) for a, b in evs)
+    if world > 1:
+        torch.distributed.barrier()
+    ms = sum(a.elapsed_time(b) for a, b in zip(ev0, ev1)) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = t.item()
+    kms = sum(k_ms) / len(k_ms)
+
+    # end to end: this step's q, top-k rows and new records from pinned host
+    # memory, the outputs back
+    host = [{k: io[k].cpu().pin_memory() for k in ("q", "topk", "kv_new")} for io in layers]
+    outs = [torch.empty_like(io["out"], device="cpu").pin_memory() for io in layers]
+    h2d = sum(v.numel() * v.element_size() for h in host for v in h.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def e2e_step():
+        for io, h in zip(layers, host):
+            for k, v in h.items():
+                io[k].copy_(v, non_blocking=True)
+        run()
+        for io, o in zip(layers, outs):
+            o.copy_(io["out"], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e0[i].record(stream)
+        e2e_step()
+        e1[i].record(stream)
+        e1[i].synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / args.steps
+
+    peaks = read_peaks()
+    per_layer_sel = selected / len(layers)
+    flops = per_layer_sel * heads * 2.0 * (576 + 512)          # QK^T and PV, useful work
+    bytes_ = per_layer_sel * 656 + wl.T * heads * (576 * 2 + 512 * 2 + 4)
+    tflops = flops / (kms * 1e-3) / 1e12
+    gbs = bytes_ / (kms * 1e-3) / 1e9
+    roof = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": tflops / peaks["bf16_tflops"], "traffic": None,
+            "kernel": "sparse_mla_kernel", "kernel_ms": kms, "algorithmic_flops": flops,
+            "algorithmic_bytes": bytes_, "peak_source": peaks["source"] + " bf16",
+            "executed_flops_note": "each of the 4 CTAs of a row recomputes QK^T: executed tensor "
+                                   "work is (4*576 + 512) / (576 + 512) = 2.59x the algorithmic",
+            "other_bound": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                            "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}}
+    line = {
+        "metric": MLA_METRIC, "value": selected * world / (ms * 1e-3), "unit": MLA_UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (fp8 e4m3 records dequantised; fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": wl.name + "+sparse_mla", "heads": heads, "index_topk": wl.index_topk,
+                   "layers": len(layers), "requests": wl.R, "query_rows": wl.T,
+                   "selected_per_step": selected, "softmax_scale": scale,
+                   "cuda_graph": graph is not None, "l2": "flushed between timed steps",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "e2e": {"value": selected * world / (e2e_ms * 1e-3), "unit": MLA_UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "clocks": clocks.summary(),
+        "gpu_launches": 2 * len(layers) * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pairs, secs, n = mla_oracle_rows(wl, heads, scale, args.cpu_budget_s)
+        line["cpu_baseline"] = {"value": pairs / secs, "unit": MLA_UNIT, "cores": cpu_cores(),
+                                "kind": "oracle", "sample": f"{n} query rows of layer 0 in order "
+                                f"({pairs} pairs, {secs:.1f} s; numpy FP64)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
 # GPU leg
 # ----------------------------------------------------------------------------
 
@@ -247,6 +453,9 @@ def main():
     args = parse()
     rank, world, local = dist_env()
     wl = synth.make_workload(args.workload, seed=args.seed + rank, scale=args.scale)
+    if args.sparse_mla:
+        run_sparse_mla(args, wl)
+        return
     if args.impl == "reference":
         run_reference(args, wl)
         return

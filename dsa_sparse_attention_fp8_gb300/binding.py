@@ -52,6 +52,8 @@ EXPORTS = (
     "dsa_layer_stack_run",
     "dsa_layer_stack_run_bf16",
     "dsa_layer_stack_run_compressed",
+    "dsa_mla_write_kv",
+    "dsa_sparse_mla_attention",
 )
 
 
@@ -135,6 +137,11 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.dsa_layer_stack_run_compressed.argtypes = [
         _I, ctypes.c_char_p, _I, _I, ctypes.POINTER(LayerIO), _I, _I, _P, _P, _I, _P, _I, _I64,
         _I, _I, _P, _I, ctypes.POINTER(ctypes.c_void_p), _P, _P, _SZ, _P, _P]
+    lib.dsa_mla_write_kv.restype = _I
+    lib.dsa_mla_write_kv.argtypes = [_P, _I, _P, _P, _I, _P, _I, _P, _I64, _P, _P, _P]
+    lib.dsa_sparse_mla_attention.restype = _I
+    lib.dsa_sparse_mla_attention.argtypes = [
+        _P, _I, _I, _P, _I64, _P, _P, _I, _P, _I, _P, _I, ctypes.c_float, _P, _P, _P, _P]
     lib.dsa_layer_stack_run_bf16.restype = _I
     lib.dsa_layer_stack_run_bf16.argtypes = [
         _I, ctypes.c_char_p, _I, _I, ctypes.POINTER(LayerIOBf16), _I, _I, _P, _P, _I, _P, _I,
@@ -502,3 +509,67 @@ def layer_stack_run_bf16(layers: Sequence[Optional[dict]], pattern: Optional[str
         _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table), block_table.shape[1],
         num_pages, index_topk, _ptr(topk_buffer), topk_buffer.shape[0], outs, _ptr(slot_mapping),
         _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)))
+
+
+# ---------------------------------------------------------------- sparse MLA
+MLA_DIM = 576
+MLA_LATENT = 512
+MLA_RECORD_BYTES = 656
+MLA_PAGE_BYTES = 41984
+
+
+def mla_write_kv(kv: torch.Tensor, query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
+                 block_table: torch.Tensor, kv_cache: torch.Tensor,
+                 slot_mapping: Optional[torch.Tensor] = None,
+                 status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Store each new token's [latent | RoPE] (FP32 [T, 576]) as its 656-byte
+    record in kv_cache [num_pages, 41984] (dsa_mla_write_kv)."""
+    T = kv.shape[0]
+    R = seq_lens.shape[0]
+    _need(kv, "kv", torch.float32, (T, MLA_DIM))
+    _need(query_start_loc, "query_start_loc", torch.int32, (R + 1,))
+    _need(seq_lens, "seq_lens", torch.int32, (R,))
+    _need(block_table, "block_table", torch.int32, (R, None))
+    _need(kv_cache, "kv_cache", torch.uint8, (None, MLA_PAGE_BYTES))
+    if slot_mapping is not None:
+        _need(slot_mapping, "slot_mapping", torch.int64, (T,))
+    if status is not None:
+        _need(status, "status", torch.int32)
+    _check(load().dsa_mla_write_kv(
+        _ptr(kv), T, _ptr(query_start_loc), _ptr(seq_lens), R, _ptr(block_table),
+        block_table.shape[1], _ptr(kv_cache), kv_cache.shape[0], _ptr(slot_mapping),
+        _ptr(status), _stream(stream)))
+
+
+def sparse_mla_attention(q: torch.Tensor, kv_cache: torch.Tensor, query_start_loc: torch.Tensor,
+                         seq_lens: torch.Tensor, block_table: torch.Tensor,
+                         topk_indices: torch.Tensor, softmax_scale: float,
+                         out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                         status: Optional[torch.Tensor] = None, stream=None):
+    """Attention of each query row (q [T, Hq, 576] BF16) over the tokens its
+    top-k row selects (dsa_sparse_mla_attention).  Returns (out [T, Hq, 512]
+    BF16, lse [T, Hq] FP32)."""
+    T, Hq = q.shape[0], q.shape[1]
+    R = seq_lens.shape[0]
+    _need(q, "q", torch.bfloat16, (T, Hq, MLA_DIM))
+    _need(kv_cache, "kv_cache", torch.uint8, (None, MLA_PAGE_BYTES))
+    _need(query_start_loc, "query_start_loc", torch.int32, (R + 1,))
+    _need(seq_lens, "seq_lens", torch.int32, (R,))
+    _need(block_table, "block_table", torch.int32, (R, None))
+    _need(topk_indices, "topk_indices", torch.int32, (None, None))
+    if topk_indices.shape[0] < T:
+        raise ValueError("topk_indices has fewer rows than q")
+    if out is None:
+        out = torch.empty((T, Hq, MLA_LATENT), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, (T, Hq, MLA_LATENT))
+    _need(lse, "lse", torch.float32, (T, Hq))
+    if status is not None:
+        _need(status, "status", torch.int32)
+    _check(load().dsa_sparse_mla_attention(
+        _ptr(q), T, Hq, _ptr(kv_cache), kv_cache.shape[0], _ptr(query_start_loc),
+        _ptr(seq_lens), R, _ptr(block_table), block_table.shape[1], _ptr(topk_indices),
+        topk_indices.shape[1], float(softmax_scale), _ptr(out), _ptr(lse), _ptr(status),
+        _stream(stream)))
+    return out, lse

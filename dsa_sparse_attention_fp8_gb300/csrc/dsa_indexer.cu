@@ -15,6 +15,7 @@
 
 #include "dsa_indexer.h"
 #include "kwrite.cuh"
+#include "mla.cuh"
 #include "plan.cuh"
 #include "score_topk.cuh"
 
@@ -759,6 +760,85 @@ int dsa_indexer_write_k_bf16(const void* k, int T, const int32_t* query_start_lo
                                           &launches);
   g_last_launches = launches;
   return rc;
+}
+
+int dsa_mla_write_kv(const float* kv, int T, const int32_t* query_start_loc,
+                     const int32_t* seq_lens, int R, const int32_t* block_table, int max_blocks,
+                     uint8_t* kv_cache, int64_t num_pages, int64_t* slot_mapping,
+                     int32_t* dev_status, dsa_stream_t stream) {
+  g_last_launches = 0;
+  if (T < 0) return fail(DSA_ERR_INVALID_ARG, "T=%d < 0", T);
+  if (R < 1) return fail(DSA_ERR_INVALID_ARG, "R=%d < 1", R);
+  if (max_blocks < 1) return fail(DSA_ERR_INVALID_ARG, "max_blocks < 1");
+  if (num_pages < 1) return fail(DSA_ERR_INVALID_ARG, "num_pages < 1");
+  if (T == 0) return DSA_OK;
+  if (!kv || !query_start_loc || !seq_lens || !block_table || !kv_cache)
+    return fail(DSA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(kv, 16) || !aligned(kv_cache, 16))
+    return fail(DSA_ERR_INVALID_ARG, "kv and kv_cache must be 16-byte aligned");
+  const int64_t grid = ((int64_t)T * 32 + 255) / 256;
+  if (grid > INT32_MAX) return fail(DSA_ERR_INVALID_ARG, "too many rows");
+  dsa::mla_write_kernel<<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(
+      kv, T, query_start_loc, seq_lens, R, block_table, max_blocks, kv_cache, num_pages,
+      slot_mapping, dev_status);
+  g_last_launches = 1;
+  return check_launch("mla_write_kernel");
+}
+
+int dsa_sparse_mla_attention(const void* q, int T, int Hq, const uint8_t* kv_cache,
+                             int64_t num_pages, const int32_t* query_start_loc,
+                             const int32_t* seq_lens, int R, const int32_t* block_table,
+                             int max_blocks, const int32_t* topk_indices, int index_topk,
+                             float softmax_scale, void* out, float* lse, int32_t* dev_status,
+                             dsa_stream_t stream) {
+  g_last_launches = 0;
+  if (T < 0) return fail(DSA_ERR_INVALID_ARG, "T=%d < 0", T);
+  if (R < 1) return fail(DSA_ERR_INVALID_ARG, "R=%d < 1", R);
+  if (Hq < 1 || Hq > dsa::kMlaMaxHeads)
+    return fail(DSA_ERR_UNSUPPORTED, "Hq=%d outside [1, %d]", Hq, dsa::kMlaMaxHeads);
+  if (index_topk < 1 || index_topk > dsa::kMlaMaxTopk)
+    return fail(DSA_ERR_UNSUPPORTED, "index_topk=%d outside [1, %d]", index_topk,
+                dsa::kMlaMaxTopk);
+  if (max_blocks < 1) return fail(DSA_ERR_INVALID_ARG, "max_blocks < 1");
+  if (num_pages < 1) return fail(DSA_ERR_INVALID_ARG, "num_pages < 1");
+  if (!(softmax_scale > 0.0f) || !(softmax_scale < 1e30f))
+    return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
+  if (T == 0) return DSA_OK;
+  if (!q || !kv_cache || !query_start_loc || !seq_lens || !block_table || !topk_indices || !out)
+    return fail(DSA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16))
+    return fail(DSA_ERR_INVALID_ARG, "q, kv_cache and out must be 16-byte aligned");
+  if ((int64_t)T * 4 > INT32_MAX) return fail(DSA_ERR_INVALID_ARG, "too many rows");
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(dsa::sparse_mla_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)dsa::kMlaSmemBytes);
+  });
+  if (attr_err != cudaSuccess)
+    return fail(DSA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+  dsa::MlaParams p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.cache = kv_cache;
+  p.num_pages = num_pages;
+  p.qsl = query_start_loc;
+  p.seq_lens = seq_lens;
+  p.R = R;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks;
+  p.topk = topk_indices;
+  p.k = index_topk;
+  p.T = T;
+  p.Hq = Hq;
+  p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.status = dev_status;
+  dsa::sparse_mla_kernel<<<(unsigned)(T * 4), dsa::kMlaThreads, dsa::kMlaSmemBytes,
+                           (cudaStream_t)stream>>>(p);
+  g_last_launches = 1;
+  return check_launch("sparse_mla_kernel");
 }
 
 }  // extern "C"

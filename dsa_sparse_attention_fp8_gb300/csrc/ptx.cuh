@@ -237,6 +237,83 @@ __device__ __forceinline__ uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
   return d;
 }
 
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16 (A and B both BF16 here), one CTA.
+// A (M x K) sits in tensor memory: row m in lane m, two 16-bit elements per
+// 32-bit column (the even element in the low half).  Issued by one thread.
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory descriptor of an MN-major operand in the 128-byte swizzle
+// layout: rows of 128 bytes hold 64 consecutive M/N elements (16-bit), one
+// row per K index; 8-row atoms are `k_group_bytes` apart along K and the next
+// 64 M/N elements start `mn_block_bytes` further on.
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr, uint32_t mn_block_bytes,
+                                                  uint32_t k_group_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);          // start address
+  d |= (uint64_t)(mn_block_bytes >> 4) << 16;         // leading byte offset: next 64 M/N
+  d |= (uint64_t)(k_group_bytes >> 4) << 32;          // stride byte offset: next 8 K rows
+  d |= (uint64_t)1 << 46;                             // descriptor version (sm_100 family)
+  d |= (uint64_t)2 << 61;                             // swizzle mode: 128 B
+  return d;
+}
+
+// Instruction descriptor: kind::f16, A = B = BF16, D = F32; A K-major, B
+// K-major or (b_mn_major) MN-major.
+__device__ __forceinline__ uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool b_mn_major) {
+  uint32_t d = 0;
+  d |= 1u << 4;                 // D format F32
+  d |= 1u << 7;                 // A format BF16
+  d |= 1u << 10;                // B format BF16
+  d |= (b_mn_major ? 1u : 0u) << 16;
+  d |= (N >> 3) << 17;          // N / 8
+  d |= (M >> 4) << 24;          // M / 16
+  return d;
+}
+
+// tcgen05.st: 32 lanes x 32 bit, repeated N times along columns.
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t* r);
+
+template <>
+__device__ __forceinline__ void tmem_st<16>(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st<32>(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]),
+      "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),
+      "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (the tensor core reads its shared-memory operands through it).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // tcgen05.ld: 32 lanes x 32 bit, repeated N times along columns.
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t* r);

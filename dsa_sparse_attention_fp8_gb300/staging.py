@@ -92,3 +92,27 @@ def stage_layer(wl, layer: int, meta: DeviceMeta, device="cuda", fill: bool = Tr
     q_fp8, q_scale = binding.quantize_fp8_blocks(q)
     w = torch.from_numpy(wl.w(layer)).to(dev)
     return {"k": k_new, "q_fp8": q_fp8, "q_scale": q_scale, "w": w, "k_cache": k_cache}
+
+
+def stage_mla(wl, layer: int, meta: DeviceMeta, heads: int, device="cuda",
+              cache_fill_byte: int = 0) -> dict:
+    """Sparse-MLA inputs of one layer on the device: the main-KV pool holding
+    every cached prefix and this step's records (written by the library's
+    record write), BF16 queries and the stand-in top-k rows."""
+    dev = torch.device(device)
+    cache = torch.full((wl.num_pages, binding.MLA_PAGE_BYTES), cache_fill_byte, dtype=torch.uint8,
+                       device=dev)
+    pre = wl.prefix_lens.astype(np.int64)
+    for r in range(wl.R):
+        if pre[r] == 0:
+            continue
+        qsl = torch.tensor([0, int(pre[r])], dtype=torch.int32, device=dev)
+        seq = torch.tensor([int(pre[r])], dtype=torch.int32, device=dev)
+        bt = torch.from_numpy(np.ascontiguousarray(wl.block_table[r:r + 1])).to(dev)
+        binding.mla_write_kv(torch.from_numpy(wl.mla_kv_prefix(layer, r)).to(dev), qsl, seq, bt,
+                             cache)
+    binding.mla_write_kv(torch.from_numpy(wl.mla_kv_new(layer)).to(dev), meta.query_start_loc,
+                         meta.seq_lens, meta.block_table, cache)
+    q = torch.from_numpy(wl.mla_q(layer, heads)).to(dev).bfloat16()
+    topk = torch.from_numpy(wl.selection_rows(layer)).to(dev)
+    return {"kv_cache": cache, "q": q, "topk": topk}

@@ -330,6 +330,66 @@ int dsa_layer_stack_run_bf16(int num_layers, const char* pattern, int freq, int 
                              dsa_stream_t stream);
 
 /*
+ * ---------------------------------------------------------------------------
+ * Sparse MLA attention over the top-k buffer (the consumer of steps 1-4).
+ *
+ * Sources: [KV] the list above the byte-accounting table (the main KV of a
+ * token in one layer is an fp8_ds_mla record of 656 B: a 512-d KV latent and
+ * a 64-d RoPE part as 576 FP8 bytes plus 16 B of FP32 scales for each of five
+ * 128-element blocks; 656 x 64 = 41,984 B per page) and its page-table passage
+ * (the indexer cache and the main KV share slot numbers); [RFC] "RFC:
+ * DeepseekV32 模型适配支持" §2.1.3 (the top-k is a 0 / -inf mask on the q.k
+ * scores, i.e. attention over the selected tokens only).
+ *
+ * Record layout (DSA_MLA_RECORD_BYTES per token, 64 records per page row of
+ * DSA_MLA_PAGE_BYTES, record of position p at (p % 64) * 656 of page
+ * block_table[r, p / 64]): bytes [0, 576) E4M3 codes of [latent | RoPE];
+ * bytes [576, 656) 20 FP32 scales, scale j for elements [32 j, 32 j + 32),
+ * slots 18 and 19 zero.  Each 32-element group is quantised with the rule of
+ * the indexer cache (s = amax / 448, codes E4M3(x / s) RNE, saturating).
+ * ---------------------------------------------------------------------------
+ */
+#define DSA_MLA_DIM 576
+#define DSA_MLA_LATENT 512
+#define DSA_MLA_RECORD_BYTES 656
+#define DSA_MLA_PAGE_BYTES 41984
+
+/*
+ * Quantise each new token's 576-vector [latent | RoPE] (FP32 [T, 576], 16-byte
+ * aligned) into its record of kv_cache [num_pages, 41984] (this layer's main
+ * KV pool), at the slot of the indexer's slot mapping (same block table).
+ * slot_mapping [T] int64 or NULL.  Bad pages / metadata: as
+ * dsa_indexer_write_k.  Errors: INVALID_ARG, CUDA.
+ */
+int dsa_mla_write_kv(const float* kv, int T, const int32_t* query_start_loc,
+                     const int32_t* seq_lens, int R, const int32_t* block_table, int max_blocks,
+                     uint8_t* kv_cache, int64_t num_pages, int64_t* slot_mapping,
+                     int32_t* dev_status, dsa_stream_t stream);
+
+/*
+ * For every query row t in [0, T) and head h < Hq (absorbed MLA):
+ *   out[t, h, :] = sum_s softmax_s(softmax_scale * q[t,h] . key_s) * key_s[0:512]
+ *   lse[t, h]    = ln sum_s exp(softmax_scale * q[t,h] . key_s)
+ * over the tokens s of row t of topk_indices (entries >= 0 and < seq_len of
+ * the row's request; -1 selects nothing), key_s = the dequantised 576-vector
+ * of s's record.  A row selecting nothing gives out = 0, lse = -inf.
+ *   q            [T, Hq, 576] BF16 (16-byte aligned), 1 <= Hq <= 128.
+ *   topk_indices [>= T, index_topk] int32 (the indexer's buffer), index_topk <= 2048.
+ *   out          [T, Hq, 512] BF16 (16-byte aligned); lse [T, Hq] FP32 or NULL.
+ * Entries >= seq_len set DSA_STATUS_BAD_METADATA and are skipped; tokens on a
+ * page outside the pool set DSA_STATUS_BAD_PAGE and contribute zero keys.
+ * Computation: keys dequantised to BF16, tensor-core products with FP32
+ * accumulation, probabilities rounded to BF16.  Errors: INVALID_ARG,
+ * UNSUPPORTED, CUDA.
+ */
+int dsa_sparse_mla_attention(const void* q, int T, int Hq, const uint8_t* kv_cache,
+                             int64_t num_pages, const int32_t* query_start_loc,
+                             const int32_t* seq_lens, int R, const int32_t* block_table,
+                             int max_blocks, const int32_t* topk_indices, int index_topk,
+                             float softmax_scale, void* out, float* lse, int32_t* dev_status,
+                             dsa_stream_t stream);
+
+/*
  * Number of kernel launches the last successful call of each entry point on
  * this thread enqueued (for launch accounting by benchmarks).
  */

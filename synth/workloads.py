@@ -38,6 +38,9 @@ PAGE_TOKENS = 64
 # tensor ids of the random streams
 _T_KNEW, _T_Q, _T_W, _T_KPREFIX = 0, 1, 2, 3
 _T_CTX, _T_PERM, _T_OUTLIER, _T_PATTERN = 10, 11, 12, 13
+_T_MLA_KVNEW, _T_MLA_KVPREFIX, _T_MLA_Q, _T_MLA_SEL = 20, 21, 22, 23
+
+MLA_DIM = 576   # fp8_ds_mla record: 512-d latent + 64-d RoPE
 
 _CHUNK_TOKENS = 16384  # tokens per independent stream chunk (x 128 values)
 
@@ -160,6 +163,39 @@ class Workload:
         w = _rng(self.seed, self.workload_id, layer, _T_W).standard_normal(
             (self.T, self.H), dtype=np.float32)
         return (w / np.float32(math.sqrt(self.H))).astype(np.float32)
+
+    # ---- sparse-MLA inputs (the consumer of the top-k rows) ---------------
+    def mla_kv_new(self, layer: int) -> np.ndarray:
+        """FP32 [T, 576]: [latent | RoPE] of every token of this step, N(0, 1)."""
+        return _normal_rows((self.seed, self.workload_id, layer, _T_MLA_KVNEW), self.T, MLA_DIM)
+
+    def mla_kv_prefix(self, layer: int, request: int) -> np.ndarray:
+        """FP32 [prefix_len, 576]: [latent | RoPE] of the cached tokens, N(0, 1)."""
+        n = int(self.prefix_lens[request])
+        return _normal_rows((self.seed, self.workload_id, layer, _T_MLA_KVPREFIX, request), n,
+                            MLA_DIM)
+
+    def mla_q(self, layer: int, heads: int) -> np.ndarray:
+        """FP32 [T, heads, 576] absorbed MLA queries, N(0, 1)."""
+        q = _normal_rows((self.seed, self.workload_id, layer, _T_MLA_Q, heads), self.T,
+                         heads * MLA_DIM)
+        return q.reshape(self.T, heads, MLA_DIM)
+
+    def selection_rows(self, layer: int, k: int | None = None) -> np.ndarray:
+        """int32 [T, k] stand-in top-k rows: row t holds min(ctx, k) distinct
+        positions of [0, ctx) in random order, then -1 (ctx = pos(t) + 1)."""
+        k = self.index_topk if k is None else k
+        qsl = self.query_start_loc
+        out = np.full((self.T, k), -1, np.int32)
+        for r in range(self.R):
+            pre = int(self.prefix_lens[r])
+            for j in range(int(self.q_lens[r])):
+                t = int(qsl[r]) + j
+                ctx = pre + j + 1
+                g = _rng(self.seed, self.workload_id, layer, _T_MLA_SEL, t)
+                n = min(ctx, k)
+                out[t, :n] = g.choice(ctx, n, replace=False) if n < ctx else g.permutation(ctx)
+        return out
 
     @property
     def pairs_per_full_layer(self) -> int:
