@@ -800,7 +800,9 @@ int dsa_sparse_mla_attention(const void* q, int T, int Hq, const uint8_t* kv_cac
     return fail(DSA_ERR_UNSUPPORTED, "index_topk=%d outside [1, %d]", index_topk,
                 dsa::kMlaMaxTopk);
   if (max_blocks < 1) return fail(DSA_ERR_INVALID_ARG, "max_blocks < 1");
-  if (num_pages < 1) return fail(DSA_ERR_INVALID_ARG, "num_pages < 1");
+  if (num_pages < 1 || num_pages > INT32_MAX / DSA_PAGE_TOKENS)
+    return fail(DSA_ERR_INVALID_ARG, "num_pages=%lld outside [1, %d]", (long long)num_pages,
+                INT32_MAX / DSA_PAGE_TOKENS);
   if (!(softmax_scale > 0.0f) || !(softmax_scale < 1e30f))
     return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
   if (T == 0) return DSA_OK;
@@ -835,8 +837,21 @@ int dsa_sparse_mla_attention(const void* q, int T, int Hq, const uint8_t* kv_cac
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   p.status = dev_status;
-  dsa::sparse_mla_kernel<<<(unsigned)(T * 4), dsa::kMlaThreads, dsa::kMlaSmemBytes,
-                           (cudaStream_t)stream>>>(p);
+  // the four quarter CTAs of a row form one cluster
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(T * dsa::kMlaCluster));
+  cfg.blockDim = dim3(dsa::kMlaThreads);
+  cfg.dynamicSmemBytes = dsa::kMlaSmemBytes;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = dsa::kMlaCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, dsa::sparse_mla_kernel, p);
+  if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "sparse_mla_kernel launch: %s", cudaGetErrorString(e));
   g_last_launches = 1;
   return check_launch("sparse_mla_kernel");
 }

@@ -17,20 +17,34 @@
 //
 // One CTA per (query row, 128-wide quarter of the 512 output dimensions): the
 // FP32 output of 128 heads x 512 dimensions alone would fill all 512 columns
-// of tensor memory, so each CTA keeps a quarter of it, next to the row's
-// queries (the MMA's A operand, held in tensor memory so that it is not
-// re-read from shared memory for every key tile) and the score and
-// probability tiles.  The four CTAs of a row compute the same scores.
-//   warps 0-3   softmax: thread = head; online softmax over 32-token tiles
+// of tensor memory, so each CTA keeps a quarter of it (128 columns), next to
+// the row's queries (288 columns: the MMA's A operand, held in tensor memory
+// so that it is not re-read from shared memory for every key tile), one
+// 64-token score tile (64) and its BF16 probabilities (32).  The four CTAs
+// of a row compute the same scores.  A tcgen05.mma costs its issuing thread
+// ~45 cycles however small N is, and an M128 x N64 x K16 BF16 product takes
+// the tensor core about as long, so key tiles are 64 tokens wide (the widest
+// that fits next to the output quarter) and the 36 QK^T instructions of a
+// tile are issued back to back from precomputed descriptors.
+//   warps 0-3   softmax: thread = head; online softmax over 64-token tiles
 //               (rescaling the output only when the running maximum grows by
 //               more than 2^8), probabilities to tensor memory as BF16,
 //               final normalisation and the BF16 output rows;
-//   warps 4-11  producers: compact the top-k row, then gather each tile's
-//               records and dequantise them to BF16 in shared memory
-//               (128-byte-swizzled rows, the K-major layout of the QK^T B
-//               operand and the MN-major layout of the PV B operand at once);
-//   warp 12     MMA issuer: S = Q K^T (M = 128 heads, N = 32 tokens, K = 576)
-//               and O += P V (N = 128 dimensions, K = 32 tokens).
+//   warps 4-9   converters: compact the top-k row and resolve its slots;
+//               then dequantise each 32-token half tile of records to BF16
+//               in shared memory (128-byte-swizzled rows, the K-major layout
+//               of the QK^T B operand and the MN-major layout of the PV B
+//               operand at once);
+//   warp 10     MMA issuer: S = Q K^T (M = 128 heads, N = 64 tokens, K = 576)
+//               and O += P V (N = 128 dimensions, K = 64 tokens);
+//   warp 11     loader: the selected records into a ring of raw half tiles.
+//
+// Gathering 656-byte records from random pages runs at ~8 bytes per cycle
+// per SM however the copies are issued, so the four CTAs of a row form a
+// thread-block cluster and gather each record once: CTA c copies the records
+// n = c (mod 4) of every half tile with a bulk copy multicast to all four,
+// and a raw slot is refilled only after every CTA of the cluster has
+// converted it (each one arrives on the slot's empty barrier in every CTA).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -103,18 +117,23 @@ __global__ void __launch_bounds__(256) mla_write_kernel(
 }
 
 // ---------------------------------------------------------------- attention
-constexpr int kMlaTile = 32;                     // tokens per pipeline stage
-constexpr int kMlaStages = 4;
-constexpr int kMlaChunkBytes = kMlaTile * 128;   // 64 dimensions x 32 tokens, BF16
-constexpr int kMlaStageBytes = 9 * kMlaChunkBytes;
-constexpr int kMlaSoftmaxWarps = 4, kMlaProducerWarps = 8;
-constexpr int kMlaThreads = (kMlaSoftmaxWarps + kMlaProducerWarps + 1) * 32;
+constexpr int kMlaTile = 64;                       // tokens per key tile (N of QK^T)
+constexpr int kMlaHalf = 32;                       // tokens per raw half tile
+constexpr int kMlaStages = 2;
+constexpr int kMlaChunkBytes = kMlaTile * 128;     // 64 dimensions x 64 tokens, BF16
+constexpr int kMlaStageBytes = 9 * kMlaChunkBytes; // 73,728
+constexpr int kMlaRawStages = 3;
+constexpr int kMlaRawBytes = kMlaHalf * kMlaRecBytes;  // 20,992: 32 records
+constexpr int kMlaSoftmaxWarps = 4, kMlaProducerWarps = 6;  // 12 warps: 170 registers each
+constexpr int kMlaThreads = (kMlaSoftmaxWarps + kMlaProducerWarps + 2) * 32;
 constexpr int kMlaProducers = kMlaProducerWarps * 32;
 constexpr int kMlaMmaWarp = kMlaSoftmaxWarps + kMlaProducerWarps;
+constexpr int kMlaLoaderWarp = kMlaMmaWarp + 1;
+constexpr int kMlaCluster = 4;                       // the four quarter CTAs of a query row
 // tensor-memory columns
 constexpr uint32_t kMlaColO = 0;       // 128 FP32: this CTA's quarter of the output
-constexpr uint32_t kMlaColS = 128;     // 2 x 32 FP32 score tiles
-constexpr uint32_t kMlaColP = 192;     // 2 x 16: BF16 probability tiles (A of PV)
+constexpr uint32_t kMlaColS = 128;     // 64 FP32: the score tile
+constexpr uint32_t kMlaColP = 192;     // 32: the tile's BF16 probabilities (A of PV)
 constexpr uint32_t kMlaColQ = 224;     // 288: BF16 queries (A of QK^T)
 constexpr float kMlaRescaleLog2 = 8.0f;  // rescale the output when the max grows by > 2^8
 
@@ -137,13 +156,16 @@ struct MlaParams {
 };
 
 struct MlaSmem {
-  int32_t idx[kMlaMaxTopk];     // the row's selected positions, compacted
+  int32_t slot[kMlaMaxTopk];    // the row's selected tokens, compacted: page * 64 + offset, or -1
   int32_t warp_count[kMlaProducerWarps];
   int32_t n_valid;
   int32_t abort;
+  int32_t conv_fail;            // set by a converter whose wait gave up; read after a barrier
   uint32_t tmem_base;
+  uint32_t raw_live[kMlaRawStages];  // per raw half tile: bit n = record n is being copied
   uint64_t kfull[kMlaStages], kempty[kMlaStages];
-  uint64_t sfull[2], pfull[2], pvdone[2];
+  uint64_t rfull[kMlaRawStages], rempty[kMlaRawStages];
+  uint64_t sfull, sfree, pfull, pvdone;
   uint64_t qfull, drain;
 };
 
@@ -170,9 +192,11 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
   extern __shared__ __align__(1024) unsigned char mla_smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(mla_smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* stages = base;                                   // kMlaStages x 36,864 B
-  MlaSmem* sm = reinterpret_cast<MlaSmem*>(base + kMlaStages * kMlaStageBytes);
+  unsigned char* stages = base;                                   // kMlaStages x 73,728 B
+  unsigned char* raw = base + kMlaStages * kMlaStageBytes;        // kMlaRawStages x 20,992 B
+  MlaSmem* sm = reinterpret_cast<MlaSmem*>(raw + kMlaRawStages * kMlaRawBytes);
   const uint32_t stage_s = smem_u32(stages);
+  const uint32_t raw_s = smem_u32(raw);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x >> 2, qd = blockIdx.x & 3;
@@ -185,14 +209,18 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
       mbar_init(smem_u32(&sm->kfull[i]), kMlaProducers);
       mbar_init(smem_u32(&sm->kempty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&sm->sfull[i]), 1);
-      mbar_init(smem_u32(&sm->pfull[i]), 128);
-      mbar_init(smem_u32(&sm->pvdone[i]), 1);
+    for (int i = 0; i < kMlaRawStages; ++i) {
+      mbar_init(smem_u32(&sm->rfull[i]), 1);
+      mbar_init(smem_u32(&sm->rempty[i]), kMlaCluster);
     }
+    mbar_init(smem_u32(&sm->sfull), 1);
+    mbar_init(smem_u32(&sm->sfree), 128);
+    mbar_init(smem_u32(&sm->pfull), 128);
+    mbar_init(smem_u32(&sm->pvdone), 1);
     mbar_init(smem_u32(&sm->qfull), 128);
     mbar_init(smem_u32(&sm->drain), 1);
     sm->abort = 0;
+    sm->conv_fail = 0;
     fence_barrier_init();
   }
   if (warp == kMlaMmaWarp) {
@@ -200,8 +228,11 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
     tmem_relinquish();
   }
   if (warp >= kMlaSoftmaxWarps && warp < kMlaMmaWarp) {
-    // compaction: entries >= 0 in row order; entries beyond the context are dropped
+    // compaction: entries >= 0 in row order (entries beyond the context are
+    // dropped), each resolved through the block table to its slot here, all
+    // lookups in flight at once, so the loader's loop never waits on memory
     const int pt = threadIdx.x - kMlaSoftmaxWarps * 32;
+    const int32_t* bt_row = p.block_table + (int64_t)r * p.max_blocks;
     const int per = (p.k + kMlaProducers - 1) / kMlaProducers;
     const int32_t* row = p.topk + (int64_t)t * p.k;
     int cnt = 0;
@@ -229,7 +260,13 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
       const int j = pt * per + i;
       if (j < p.k) {
         const int e = __ldg(row + j);
-        if (e >= 0 && e < seq_len) sm->idx[off++] = e;
+        if (e >= 0 && e < seq_len) {
+          const int blk = e / kPageTokens;
+          const int64_t page = blk < p.max_blocks ? (int64_t)__ldg(bt_row + blk) : -1;
+          const bool good = page >= 0 && page < p.num_pages;
+          if (!good) raise_status(p.status, kStatusBadPage);
+          sm->slot[off++] = good ? (int32_t)(page * kPageTokens + e % kPageTokens) : -1;
+        }
       }
     }
     if (pt == kMlaProducers - 1) sm->n_valid = off;
@@ -237,9 +274,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_sync();  // every CTA's barriers exist before any multicast copy targets them
+  const uint32_t crank = cluster_ctarank();
   const uint32_t tmem = sm->tmem_base;
   const int n_valid = sm->n_valid;
   const int n_tiles = (n_valid + kMlaTile - 1) / kMlaTile;
+  const int n_halves = (n_valid + kMlaHalf - 1) / kMlaHalf;
   volatile int* abort_flag = &sm->abort;
 
   if (warp < kMlaSoftmaxWarps) {
@@ -247,6 +287,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
     const int h = threadIdx.x;  // head = tensor-memory lane
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     const bool head_ok = h < p.Hq;
+    // waits are taken warp-uniformly: the tensor-memory loads and stores that
+    // follow them are warp-collective
+    auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      const bool ok = mbar_wait(smem_u32(bar), parity, abort_flag);
+      return __all_sync(0xffffffffu, ok);
+    };
     // queries into tensor memory (zero rows for heads beyond Hq)
     {
       const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)t * p.Hq + h) * kMlaDim);
@@ -263,38 +309,45 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
       tc_fence_before();
       mbar_arrive(smem_u32(&sm->qfull));
     }
-    // waits are taken warp-uniformly: the tensor-memory loads and stores that
-    // follow them are warp-collective
-    auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      const bool r = mbar_wait(smem_u32(bar), parity, abort_flag);
-      return __all_sync(0xffffffffu, r);
-    };
     float m_run = -INFINITY, l_run = 0.0f;
     bool ok = true;
     for (int i = 0; i < n_tiles && ok; ++i) {
-      const int b = i & 1;
-      if (!wwait(&sm->sfull[b], (uint32_t)((i >> 1) & 1))) { ok = false; break; }
+      const uint32_t ph = (uint32_t)(i & 1);
+      if (!wwait(&sm->sfull, ph)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sv[32];
-      tmem_ld<32>(lane_base + kMlaColS + 32 * b, sv);
-      tmem_ld_wait();
-      const int left = n_valid - i * kMlaTile;  // valid tokens of this tile
-      float x[32];
-      float mt = -INFINITY;
+      float x[64];
+      {
+        uint32_t sv[32];
+        tmem_ld<32>(lane_base + kMlaColS, sv);
+        tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        x[j] = j < left ? __uint_as_float(sv[j]) * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, x[j]);
+        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(sv[j]);
+        tmem_ld<32>(lane_base + kMlaColS + 32, sv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[32 + j] = __uint_as_float(sv[j]);
       }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm->sfree));  // the next QK^T may overwrite the score tile
+      const int left = n_valid - i * kMlaTile;  // valid tokens of this tile
+#pragma unroll
+      for (int j = 0; j < 64; ++j) x[j] = j < left ? x[j] * p.scale_log2 : -INFINITY;
+      // maximum as a tree (the four softmax warps are one per scheduler:
+      // nothing hides a 64-long dependent chain)
+      float mx[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) mx[j] = fmaxf(fmaxf(x[j], x[j + 16]), fmaxf(x[j + 32], x[j + 48]));
+#pragma unroll
+      for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
+      const float mt = mx[0];
+      // the previous PV has read the probability tile and written the output
+      if (i > 0 && !wwait(&sm->pvdone, (uint32_t)((i - 1) & 1))) { ok = false; break; }
+      tc_fence_after();
       const bool grow = mt > m_run + kMlaRescaleLog2;
       const float m_new = grow ? mt : m_run;
       if (__any_sync(0xffffffffu, grow && i > 0)) {
-        // rescale this warp's rows of the output once the previous PV has landed
-        if (!wwait(&sm->pvdone[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
         const float alpha = (grow && i > 0) ? exp2f(m_run - m_new) : 1.0f;
         for (int c = 0; c < 4; ++c) {
           uint32_t ov[32];
@@ -304,35 +357,26 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
           for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
           tmem_st<32>(lane_base + kMlaColO + 32 * c, ov);
         }
-        tmem_st_wait();
         l_run *= alpha;
       }
       m_run = m_new;
-      uint32_t pw[16];
-      float lsum = 0.f;
+      uint32_t pw[32];
+      float ls[8];  // the sum of the probabilities the MMA multiplies, in 8 partial sums
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float p0 = exp2f(x[2 * j] - m_run), p1 = exp2f(x[2 * j + 1] - m_run);
-        pw[j] = pack_bf16x2(p0, p1);
-        const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162*>(&pw[j]);
-        const float2 pf = __bfloat1622float2(pb);
-        lsum += pf.x + pf.y;  // the sum of the probabilities the MMA multiplies
+      for (int j = 0; j < 8; ++j) ls[j] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        pw[j] = pack_bf16x2(exp2f(x[2 * j] - m_run), exp2f(x[2 * j + 1] - m_run));
+        const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pw[j]));
+        ls[j & 7] += pf.x + pf.y;
       }
-      l_run += lsum;
-      if (i >= 2 && !wwait(&sm->pvdone[b], (uint32_t)(((i - 2) >> 1) & 1))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      tmem_st<16>(lane_base + kMlaColP + 16 * b, pw);
+      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      tmem_st<32>(lane_base + kMlaColP, pw);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&sm->pfull[b]));
+      mbar_arrive(smem_u32(&sm->pfull));
     }
-    if (ok && n_tiles > 0) {
-      const int last = n_tiles - 1;
-      if (!wwait(&sm->pvdone[last & 1], (uint32_t)((last >> 1) & 1))) ok = false;
-    }
+    if (ok && n_tiles > 0 && !wwait(&sm->pvdone, (uint32_t)((n_tiles - 1) & 1))) ok = false;
     if (!ok) {
       sm->abort = 1;
       raise_status(p.status, kStatusTimeout);
@@ -364,100 +408,135 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
             l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
     }
   } else if (warp < kMlaMmaWarp) {
-    // ================================================================ producers
+    // ================================================================ converters
     const int pt = threadIdx.x - kMlaSoftmaxWarps * 32;
-    const int32_t* bt_row = p.block_table + (int64_t)r * p.max_blocks;
+    // Every converter reaches every named barrier, also after a wait gave up:
+    // a failure is published in conv_fail and acted on, by all of them at
+    // once, after the barrier.
     bool ok = true;
     for (int i = 0; i < n_tiles && ok; ++i) {
       const int b = i % kMlaStages;
-      if (i >= kMlaStages &&
-          !mbar_wait(smem_u32(&sm->kempty[b]), (uint32_t)((i / kMlaStages - 1) & 1), abort_flag)) {
-        ok = false;
-        break;
-      }
-      // 32 tokens x 36 sixteen-element pieces; piece (n, cc) holds elements [16 cc, 16 cc + 16)
-      uint4 code[5];
-      float scl[5];
-      bool live[5];
-#pragma unroll
-      for (int u = 0; u < 5; ++u) {
-        const int job = pt + kMlaProducers * u;
-        const int n = job / 36, cc = job - n * 36;
-        live[u] = false;
-        code[u] = make_uint4(0u, 0u, 0u, 0u);
-        scl[u] = 0.f;
-        if (job < kMlaTile * 36) {
-          const int ti = i * kMlaTile + n;
-          if (ti < n_valid) {
-            const int s = sm->idx[ti];
-            const int blk = s / kPageTokens;
-            const int64_t page = blk < p.max_blocks ? (int64_t)__ldg(bt_row + blk) : -1;
-            if (page >= 0 && page < p.num_pages) {
-              const uint8_t* rec = p.cache + page * kMlaPageBytes + (int64_t)(s % kPageTokens) * kMlaRecBytes;
-              code[u] = __ldg(reinterpret_cast<const uint4*>(rec) + cc);
-              scl[u] = __ldg(reinterpret_cast<const float*>(rec + kMlaDim) + (cc >> 1));
-              live[u] = true;
-            } else if (cc == 0) {
-              raise_status(p.status, kStatusBadPage);
-            }
-          }
-        }
-      }
+      bool good = i < kMlaStages ||
+                  mbar_wait(smem_u32(&sm->kempty[b]), (uint32_t)((i / kMlaStages - 1) & 1), abort_flag);
       const uint32_t sbase = stage_s + (uint32_t)(b * kMlaStageBytes);
+      for (int hf = 0; hf < 2; ++hf) {
+        const int g = 2 * i + hf;  // half tile
+        const int rb = g % kMlaRawStages;
+        const bool got = good && (g >= n_halves ||
+                                  mbar_wait(smem_u32(&sm->rfull[rb]),
+                                            (uint32_t)((g / kMlaRawStages) & 1), abort_flag));
+        if (!got) sm->conv_fail = 1;
+        const uint32_t live = (got && g < n_halves) ? sm->raw_live[rb] : 0u;
+        const uint32_t rbase = raw_s + (uint32_t)(rb * kMlaRawBytes);
+        // 32 tokens x 36 sixteen-element pieces; piece (n, cc) holds elements [16 cc, 16 cc + 16)
 #pragma unroll
-      for (int u = 0; u < 5; ++u) {
-        const int job = pt + kMlaProducers * u;
-        if (job < kMlaTile * 36) {
-          const int n = job / 36, cc = job - n * 36;
-          uint32_t o[8];
-          if (live[u]) {
-            dequant16(code[u], scl[u], o);
-          } else {
+        for (int u = 0; u < (kMlaHalf * 36 + kMlaProducers - 1) / kMlaProducers; ++u) {
+          const int job = pt + kMlaProducers * u;
+          if (job < kMlaHalf * 36) {
+            const int n = job / 36, cc = job - n * 36;
+            uint32_t o[8];
+            if ((live >> n) & 1u) {
+              const uint32_t rec = rbase + (uint32_t)(n * kMlaRecBytes);
+              dequant16(lds_v4(rec + 16u * (uint32_t)cc),
+                        __uint_as_float(lds_u32(rec + (uint32_t)kMlaDim + 4u * (uint32_t)(cc >> 1))), o);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) o[j] = 0u;
+              for (int j = 0; j < 8; ++j) o[j] = 0u;
+            }
+            // element 16 cc + j of tile row nn: chunk cc / 4, 16-byte units 2 (cc % 4) and +1
+            const int nn = hf * kMlaHalf + n;
+            const uint32_t row = sbase + (uint32_t)((cc >> 2) * kMlaChunkBytes + nn * 128);
+            const uint32_t u0 = (uint32_t)(2 * (cc & 3));
+            sts_v4(row + (((u0) ^ (uint32_t)(nn & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+            sts_v4(row + (((u0 + 1) ^ (uint32_t)(nn & 7)) << 4), make_uint4(o[4], o[5], o[6], o[7]));
           }
-          // element 16 cc + j of token n: chunk cc / 4, 16-byte units 2 (cc % 4) and +1
-          const uint32_t row = sbase + (uint32_t)((cc >> 2) * kMlaChunkBytes + n * 128);
-          const uint32_t u0 = (uint32_t)(2 * (cc & 3));
-          sts_v4(row + (((u0) ^ (uint32_t)(n & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
-          sts_v4(row + (((u0 + 1) ^ (uint32_t)(n & 7)) << 4), make_uint4(o[4], o[5], o[6], o[7]));
+        }
+        named_bar_sync(2, kMlaProducers);  // every converter is done with raw slot rb
+        good = sm->conv_fail == 0;
+        if (pt < kMlaCluster && g < n_halves && good) {
+          // the slot may be refilled: tell the loader of every CTA of the
+          // cluster (one thread each; the slot's reads are complete, nothing
+          // to publish)
+          mbar_arrive_cluster_relaxed(cluster_map(smem_u32(&sm->rempty[rb]), (uint32_t)pt));
         }
       }
+      if (!good) { ok = false; break; }
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&sm->kfull[b]));
     }
     if (!ok) sm->abort = 1;
+  } else if (warp == kMlaLoaderWarp) {
+    // ================================================================ loader
+    // Each CTA expects every record of a half tile (all four copy into it)
+    // and copies its own share, records n = rank (mod 4), to all four.
+    bool ok = true;
+    int issued = 0;
+    for (int g = 0; g < n_halves && ok; ++g) {
+      const int rb = g % kMlaRawStages;
+      if (g >= kMlaRawStages) {
+        const bool got = mbar_wait(smem_u32(&sm->rempty[rb]),
+                                   (uint32_t)((g / kMlaRawStages - 1) & 1), abort_flag);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+      }
+      const int ti = g * kMlaHalf + lane;
+      const int sl = ti < n_valid ? sm->slot[ti] : -1;
+      const uint32_t live = __ballot_sync(0xffffffffu, sl >= 0);
+      const uint32_t bar = smem_u32(&sm->rfull[rb]);
+      if (lane == 0) {
+        sm->raw_live[rb] = live;
+        mbar_arrive_expect_tx(bar, (uint32_t)__popc(live) * (uint32_t)kMlaRecBytes);
+      }
+      __syncwarp();
+      if (sl >= 0 && (uint32_t)(lane % kMlaCluster) == crank)
+        bulk_load_multicast(raw_s + (uint32_t)(rb * kMlaRawBytes + lane * kMlaRecBytes),
+                            p.cache + (int64_t)(sl / kPageTokens) * kMlaPageBytes +
+                                (int64_t)(sl % kPageTokens) * kMlaRecBytes,
+                            (uint32_t)kMlaRecBytes, bar, (uint16_t)((1u << kMlaCluster) - 1u));
+      issued = g + 1;
+    }
+    if (!ok) sm->abort = 1;
+    // the latest phase of every raw slot this CTA expected has landed
+    for (int j = issued > kMlaRawStages ? issued - kMlaRawStages : 0; j < issued; ++j)
+      mbar_wait(smem_u32(&sm->rfull[j % kMlaRawStages]), (uint32_t)((j / kMlaRawStages) & 1), nullptr);
   } else if (lane == 0) {
     // ================================================================ MMA issuer
     const uint32_t id_qk = idesc_bf16_f32(128, kMlaTile, false);
     const uint32_t id_pv = idesc_bf16_f32(128, 128, true);
     bool ok = n_tiles == 0 || mbar_wait(smem_u32(&sm->qfull), 0, abort_flag);
-    auto pv = [&](int j) -> bool {  // O += P_j V_j
-      const int b = j & 1, st = j % kMlaStages;
-      if (!mbar_wait(smem_u32(&sm->pfull[b]), (uint32_t)((j >> 1) & 1), abort_flag)) return false;
+    auto qk = [&](int i) -> bool {  // S = Q K_i^T, 36 instructions back to back
+      const int st = i % kMlaStages;
+      if (!mbar_wait(smem_u32(&sm->kfull[st]), (uint32_t)((i / kMlaStages) & 1), abort_flag)) return false;
+      if (i > 0 && !mbar_wait(smem_u32(&sm->sfree), (uint32_t)((i - 1) & 1), abort_flag)) return false;
       tc_fence_after();
-      const uint32_t vbase = stage_s + (uint32_t)(st * kMlaStageBytes + (2 * qd) * kMlaChunkBytes);
+      const uint64_t d0 = sw128_desc(stage_s + (uint32_t)(st * kMlaStageBytes));
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk)
-        umma_f16_ta(tmem + kMlaColO, tmem + kMlaColP + 16 * b + 8 * kk,
-                    sw128_desc_mn(vbase + kk * 16 * 128, kMlaChunkBytes, 1024), id_pv,
-                    (j > 0 || kk > 0) ? 1u : 0u);
-      umma_commit(smem_u32(&sm->pvdone[b]));
+      for (int s = 0; s < kMlaDim / 16; ++s)
+        umma_f16_ta(tmem + kMlaColS, tmem + kMlaColQ + 8 * s,
+                    d0 + (uint64_t)(((s >> 2) * kMlaChunkBytes + (s & 3) * 32) >> 4), id_qk,
+                    s > 0 ? 1u : 0u);
+      umma_commit(smem_u32(&sm->sfull));
+      return true;
+    };
+    auto pv = [&](int j) -> bool {  // O += P_j V_j
+      const int st = j % kMlaStages;
+      if (!mbar_wait(smem_u32(&sm->pfull), (uint32_t)(j & 1), abort_flag)) return false;
+      tc_fence_after();
+      const uint64_t v0 = sw128_desc_mn(stage_s + (uint32_t)(st * kMlaStageBytes + (2 * qd) * kMlaChunkBytes),
+                                        kMlaChunkBytes, 1024);
+#pragma unroll
+      for (int kk = 0; kk < kMlaTile / 16; ++kk)
+        umma_f16_ta(tmem + kMlaColO, tmem + kMlaColP + 8 * kk, v0 + (uint64_t)((kk * 16 * 128) >> 4),
+                    id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(smem_u32(&sm->pvdone));
       umma_commit(smem_u32(&sm->kempty[st]));
       return true;
     };
-    for (int i = 0; i < n_tiles && ok; ++i) {
-      const int st = i % kMlaStages;
-      if (!mbar_wait(smem_u32(&sm->kfull[st]), (uint32_t)((i / kMlaStages) & 1), abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t kbase = stage_s + (uint32_t)(st * kMlaStageBytes);
-      const uint32_t dS = tmem + kMlaColS + 32 * (i & 1);
-      for (int s = 0; s < kMlaDim / 16; ++s)
-        umma_f16_ta(dS, tmem + kMlaColQ + 8 * s,
-                    sw128_desc(kbase + (uint32_t)((s >> 2) * kMlaChunkBytes + (s & 3) * 32)), id_qk,
-                    s > 0 ? 1u : 0u);
-      umma_commit(smem_u32(&sm->sfull[i & 1]));
-      if (i > 0 && !pv(i - 1)) { ok = false; break; }
+    // PV of tile i-1 goes first: it releases tile i-1's stage to the
+    // converters as soon as its probabilities are ready (measured faster than
+    // issuing QK^T of tile i first, or interleaving the two).
+    if (ok && n_tiles > 0) ok = qk(0);
+    for (int i = 1; i < n_tiles && ok; ++i) {
+      if (!pv(i - 1) || !qk(i)) ok = false;
     }
     if (ok && n_tiles > 0 && !pv(n_tiles - 1)) ok = false;
     // every MMA issued has completed before tensor memory is released
@@ -472,10 +551,23 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // No CTA leaves while a peer may still copy into it or arrive on its
+  // barriers.  After a wait gave up anywhere in the cluster, copies a peer
+  // issued before giving up may still be landing: wait ~100 us for them.
+  cluster_sync();
+  {
+    bool any_abort = false;
+    for (uint32_t c = 0; c < kMlaCluster; ++c)
+      any_abort |= ld_cluster_u32(cluster_map(smem_u32(&sm->abort), c)) != 0;
+    if (any_abort)
+      for (int k = 0; k < 100; ++k) __nanosleep(1000);
+  }
+  cluster_sync();
   if (warp == kMlaMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 // Dynamic shared memory of the attention kernel (plus 1 KB for alignment).
-constexpr size_t kMlaSmemBytes = (size_t)kMlaStages * kMlaStageBytes + sizeof(MlaSmem) + 1024;
+constexpr size_t kMlaSmemBytes =
+    (size_t)kMlaStages * kMlaStageBytes + (size_t)kMlaRawStages * kMlaRawBytes + sizeof(MlaSmem) + 1024;
 
 }  // namespace dsa
