@@ -351,6 +351,7 @@ def run_sparse_mla(args, wl):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed_steps")
     with ClockSampler(dev.index) as clocks:
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
@@ -359,6 +360,7 @@ def run_sparse_mla(args, wl):
             ev1[i].record(stream)
             ev1[i].synchronize()
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
         k_ms = []
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
