@@ -76,6 +76,23 @@ def dist_env():
     return rank, world, local
 
 
+def reduce_over_ranks(times_ms, units, world: int, device=None):
+    """Whole-job figures of a replicated run: each time is the maximum over
+    the ranks (the job ends with its slowest replica), the units processed are
+    summed over the ranks.  With one rank the inputs come back unchanged.  Works
+    on any initialised process group (NCCL on GPUs, gloo on CPUs)."""
+    times_ms = [float(x) for x in times_ms]
+    if world == 1:
+        return times_ms, float(units)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(times_ms, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    dist.all_reduce(u)
+    return t.tolist(), u.item()
+
+
 def read_peaks() -> dict:
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -372,10 +389,6 @@ def run_sparse_mla(args, wl):
     if world > 1:
         torch.distributed.barrier()
     ms = sum(a.elapsed_time(b) for a, b in zip(ev0, ev1)) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = t.item()
     kms = sum(k_ms) / len(k_ms)
 
     # end to end: this step's q, top-k rows and new records from pinned host
@@ -405,6 +418,7 @@ def run_sparse_mla(args, wl):
         e1[i].record(stream)
         e1[i].synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / args.steps
+    (ms, e2e_ms), total_selected = reduce_over_ranks([ms, e2e_ms], selected, world, dev)
 
     peaks = read_peaks()
     per_layer_sel = selected / len(layers)
@@ -421,7 +435,7 @@ def run_sparse_mla(args, wl):
             "other_bound": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
                             "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}}
     line = {
-        "metric": MLA_METRIC, "value": selected * world / (ms * 1e-3), "unit": MLA_UNIT,
+        "metric": MLA_METRIC, "value": total_selected / (ms * 1e-3), "unit": MLA_UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 (fp8 e4m3 records dequantised; fp32 accumulate)", "data": "synthetic",
@@ -431,7 +445,7 @@ def run_sparse_mla(args, wl):
                    "cuda_graph": graph is not None, "l2": "flushed between timed steps",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
-        "e2e": {"value": selected * world / (e2e_ms * 1e-3), "unit": MLA_UNIT,
+        "e2e": {"value": total_selected / (e2e_ms * 1e-3), "unit": MLA_UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "clocks": clocks.summary(),
         "gpu_launches": 2 * len(layers) * args.steps,
@@ -583,15 +597,7 @@ def main():
         e1[i].synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / args.steps
 
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = t.tolist()
-        pr = torch.tensor([pairs_per_step], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(pr)
-        total_pairs = pr.item()
-    else:
-        total_pairs = pairs_per_step
+    (ms, e2e_ms), total_pairs = reduce_over_ranks([ms, e2e_ms], pairs_per_step, world, dev)
     clk = clocks.summary()
 
     # ---- roofline of the dominant kernel (scoring + top-k), per launch

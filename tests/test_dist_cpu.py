@@ -1,0 +1,68 @@
+"""The multi-rank (torchrun) path of bench.py on CPU, with gloo (no GPU).
+
+The indexer path shards by request with no exchange step, so N ranks run N
+independent replicas; the only cross-rank logic is the whole-job reduction
+(slowest rank's time, summed units) and "rank 0 alone prints, the others
+exit 0".  Both are checked here with world size 2 on 127.0.0.1.
+"""
+
+import json
+import os
+import socket
+import subprocess
+import sys
+from pathlib import Path
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    import torch.distributed as dist
+    sys.path.insert(0, str(ROOT))
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r: step times 1.5 + r and 10 - r ms, 100 * (r + 1) units
+        times, units = bench.reduce_over_ranks([1.5 + rank, 10.0 - rank], 100 * (rank + 1), world,
+                                               "cpu")
+        Path(out_dir, f"r{rank}.json").write_text(json.dumps({"times": times, "units": units}))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_reduce_over_ranks_gloo_world_2(tmp_path):
+    world = 2
+    mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world,
+                       join=True, start_method="spawn")
+    got = [json.loads((tmp_path / f"r{r}.json").read_text()) for r in range(world)]
+    for g in got:          # every rank holds the same whole-job figures
+        assert g["times"] == [2.5, 10.0]
+        assert g["units"] == 300.0
+
+
+def test_reduce_over_ranks_single_rank_is_identity():
+    sys.path.insert(0, str(ROOT))
+    import bench
+    assert bench.reduce_over_ranks([3.0, 4.0], 7, 1) == ([3.0, 4.0], 7.0)
+
+
+@pytest.mark.parametrize("extra", [[], ["--sparse-mla"]])
+def test_non_zero_ranks_print_nothing_and_exit_0(extra):
+    """Under torchrun the reference arm runs on rank 0 only: rank 1 exits 0
+    without work and without output."""
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1", MASTER_ADDR="127.0.0.1")
+    res = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "0", "--scale", "0.05", *extra],
+                         env=env, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    assert res.stdout.strip() == ""
