@@ -221,8 +221,12 @@ def workspace_bytes(T: int, H: int, R: int, index_topk: int, max_ctx: int = 0) -
     return int(n)
 
 
-def alloc_workspace(T: int, H: int, R: int, index_topk: int, device="cuda") -> torch.Tensor:
-    n = workspace_bytes(T, H, R, index_topk)
+def alloc_workspace(T: int, H: int, R: int, index_topk: int, device="cuda",
+                    max_ctx: int = 0) -> torch.Tensor:
+    """Workspace for score_topk / layer_stack_run.  0 < max_ctx <= 8192 (a bound on
+    the keys any row sees) also makes room for decode rows to be scored into the
+    workspace and selected by a second kernel (see dsa_indexer_workspace_bytes)."""
+    n = workspace_bytes(T, H, R, index_topk, max_ctx)
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 

@@ -246,6 +246,31 @@ struct Batch {
   int ratio = 1;  // tokens per cache entry (compressed indexer cache when > 1)
 };
 
+// Keys per workspace score row for a decode layout (G = 1) sized for
+// contexts up to max_ctx: max_ctx rounded up to a multiple of 128 when that
+// is at most kScoreRowMax (every row of such a batch then fits, so the plan
+// always takes the row path and the row kernel is never launched for
+// nothing); 0 otherwise, or when the rows would take more than 256 MB.
+int score_stride_for(int T, int G, int64_t max_ctx) {
+  if (G != 1 || max_ctx <= 0 || T <= 0 || max_ctx > dsa::kScoreRowMax) return 0;
+  const int64_t s = (max_ctx + 127) / 128 * 128;
+  if ((int64_t)T * s * 4 > (int64_t(256) << 20)) return 0;
+  return (int)s;
+}
+
+// The score-row stride a caller's workspace holds: the largest stride whose
+// layout fits in ws_bytes (the stride dsa_indexer_workspace_bytes sized it
+// for, when the caller passed exactly that many bytes).
+int score_stride_in(const Batch& b, int G, int n_cta) {
+  if (G != 1 || b.T <= 0) return 0;
+  const size_t base = dsa::ws_layout(b.T, b.R, G, b.k, n_cta, 0).total;
+  if (b.ws_bytes <= base) return 0;
+  int64_t s = (int64_t)((b.ws_bytes - base) / (4 * (size_t)b.T)) / 128 * 128;
+  s = std::min<int64_t>(s, dsa::kScoreRowMax);
+  while (s > 0 && dsa::ws_layout(b.T, b.R, G, b.k, n_cta, (int)s).total > b.ws_bytes) s -= 128;
+  return s > 0 ? (int)s : 0;
+}
+
 int check_batch(const Batch& b) {
   if (b.T < 0) return fail(DSA_ERR_INVALID_ARG, "T=%d < 0", b.T);
   if (b.R < 1) return fail(DSA_ERR_INVALID_ARG, "R=%d < 1", b.R);
@@ -285,7 +310,7 @@ int launch_plan(const Batch& b, int G, int* launches) {
   pp.min_tiles = env_int("DSA_MIN_SPLIT", 1024, 128, 1 << 20) / 128;
   pp.topk_buffer = b.topk;
   pp.ws = static_cast<unsigned char*>(b.ws);
-  pp.L = dsa::ws_layout(b.T, b.R, G, b.k, pp.n_cta);
+  pp.L = dsa::ws_layout(b.T, b.R, G, b.k, pp.n_cta, score_stride_in(b, G, pp.n_cta));
   pp.status = b.status;
   dsa::plan_kernel<<<1, dsa::kPlanThreads, 0, b.st>>>(pp);
   ++*launches;
@@ -309,7 +334,7 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
                         s.q_box_per_token ? (uint32_t)b.H : (uint32_t)(s.G * b.H));
   if (rc) return rc;
   const int grid = grid_ctas();
-  const dsa::WsLayout L = dsa::ws_layout(b.T, b.R, s.G, b.k, grid);
+  const dsa::WsLayout L = dsa::ws_layout(b.T, b.R, s.G, b.k, grid, score_stride_in(b, s.G, grid));
   unsigned char* ws = static_cast<unsigned char*>(b.ws);
   dsa::ScoreParams p = s.offs;
   p.qsl = b.qsl;
@@ -346,10 +371,39 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   p.topk = b.topk;
   p.scores_out = lq.scores_out;
   p.scores_ld = lq.scores_ld;
+  p.score_rows = reinterpret_cast<uint32_t*>(ws + L.score_rows);
+  p.score_stride = L.score_stride;
   p.status = b.status;
   rc = launch_score(b.H, tk, tq, p, s.smem_bytes, grid, b.st);
   if (rc == DSA_OK) ++*launches;
   return rc;
+}
+
+// The top-k of the rows the scoring kernel wrote into the workspace (decode
+// layouts whose workspace has room for them; nothing to do otherwise).
+int launch_rows_topk(const Batch& b, const ScoreShape& s, int* launches) {
+  const int grid = grid_ctas();
+  const dsa::WsLayout L = dsa::ws_layout(b.T, b.R, s.G, b.k, grid, score_stride_in(b, s.G, grid));
+  if (L.score_stride <= 0) return DSA_OK;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(dsa::rows_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)dsa::rows_topk_smem(dsa::kScoreRowMax));
+  });
+  if (attr_err != cudaSuccess)
+    return fail(DSA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+  unsigned char* ws = static_cast<unsigned char*>(b.ws);
+  dsa::RowsTopkParams rp;
+  rp.score_rows = reinterpret_cast<const uint32_t*>(ws + L.score_rows);
+  rp.row_keys = reinterpret_cast<const int32_t*>(ws + L.row_keys);
+  rp.score_stride = L.score_stride;
+  rp.k = b.k;
+  rp.topk = b.topk;
+  dsa::rows_topk_kernel<<<(unsigned)b.T, dsa::kRowsThreads, dsa::rows_topk_smem(L.score_stride),
+                          b.st>>>(rp);
+  ++*launches;
+  return check_launch("rows_topk_kernel");
 }
 
 // Record a caller's timing event on the stream; inside stream capture it must
@@ -493,6 +547,8 @@ int stack_run(int num_layers, const char* pattern, int freq, int offset, const I
         rc = fail(DSA_ERR_CUDA, "recording score_end of layer %d failed", l);
         break;
       }
+      rc = launch_rows_topk(b, s, &launches);
+      if (rc) break;
     }
     if (per_layer_topk_out && per_layer_topk_out[l]) {
       const int64_t bytes = (int64_t)b.T * b.k * 4;
@@ -544,11 +600,10 @@ int dsa_layer_is_full(int layer_id, const char* pattern, int freq, int offset) {
 }
 
 size_t dsa_indexer_workspace_bytes(int T, int H, int R, int64_t max_ctx, int index_topk) {
-  (void)max_ctx;
   if (T < 0 || R < 1 || !supported_heads(H) || index_topk < 1 || index_topk > DSA_MAX_TOPK)
     return 0;
   const int G = choose_group(T, R, H, index_topk);
-  return dsa::ws_layout(T, R, G, index_topk, grid_ctas()).total;
+  return dsa::ws_layout(T, R, G, index_topk, grid_ctas(), score_stride_for(T, G, max_ctx)).total;
 }
 
 int dsa_quantize_fp8_blocks(const float* x, int64_t n_blocks, uint8_t* codes, float* scales,
@@ -652,6 +707,7 @@ int dsa_indexer_score_topk_compressed(const uint8_t* q_fp8, const float* q_scale
   if (rc == DSA_OK) {
     LayerQ lq{q_fp8, q_scale, w, k_cache, scores_out, scores_ld};
     rc = launch_score_layer(b, s, lq, &launches);
+    if (rc == DSA_OK) rc = launch_rows_topk(b, s, &launches);
   }
   g_last_launches = launches;
   return rc;

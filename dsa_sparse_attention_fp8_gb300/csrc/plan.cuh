@@ -27,8 +27,9 @@ struct Item {
   int32_t k0, k1;      // key range [k0, k1) (logical positions); k0 % 128 == 0
   int32_t split;       // piece index | (number of pieces << 16)
   int32_t cand_block;  // first candidate block of the group (split groups), else -1
-  int32_t sgroup;      // split-group id (index of its done counter), else -1
+  int32_t sgroup;      // split-group id (index of its done counter), -1, or kSgroupRows
 };
+constexpr int32_t kSgroupRows = -2;  // the item's row is scored into the workspace
 static_assert(sizeof(Item) == 32, "Item must stay 32 bytes");
 
 constexpr int kMaxCtas = 320;       // upper bound on the scoring grid (one CTA per SM)
@@ -56,10 +57,17 @@ __host__ __device__ inline int cand_block_capacity(int k) {
 // Workspace carve-up; identical on host and device.
 constexpr int kBlockBins = 2048;  // level-1 bins published with every candidate block
 
+// Decode batches (one query row per group) may score their rows into the
+// workspace instead and select each row's top-k with a second kernel: the
+// scoring kernel then streams keys without selecting, splitting or merging.
+// A row takes that path when it sees at most score_stride keys (a multiple of
+// 128, at most kScoreRowMax; 0 = never).
+constexpr int kScoreRowMax = 8192;   // longer rows merge faster across SMs (measured)
+
 struct WsLayout {
   size_t header, group_prefix, cta_start, items, done, cand_count, cand_keys, cand_idx, cand_hist,
-      cand_start, total;
-  int max_items, max_split_groups, max_cand_blocks, cb;
+      cand_start, row_keys, score_rows, total;
+  int max_items, max_split_groups, max_cand_blocks, cb, score_stride;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -68,8 +76,10 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 // them: at most T + n_cta items, min(n_cta, groups) split groups and
 // (split groups + n_cta - 1) pieces of split groups, G candidate blocks each.
 // A request of q rows has ceil(q / G) groups, so groups <= min(T, T / G + R).
-__host__ __device__ inline WsLayout ws_layout(int T, int R, int G, int k, int n_cta) {
+__host__ __device__ inline WsLayout ws_layout(int T, int R, int G, int k, int n_cta,
+                                               int score_stride = 0) {
   WsLayout L;
+  L.score_stride = score_stride;
   L.max_items = T + n_cta;
   const long long groups = T < (T + G - 1) / G + R ? T : (T + G - 1) / G + R;
   L.max_split_groups = (int)(groups < n_cta ? groups : n_cta);
@@ -86,6 +96,8 @@ __host__ __device__ inline WsLayout ws_layout(int T, int R, int G, int k, int n_
   L.cand_idx = o;     o = align256(o + sizeof(int32_t) * (size_t)L.max_cand_blocks * L.cb);
   L.cand_hist = o;    o = align256(o + sizeof(uint16_t) * (size_t)L.max_cand_blocks * kBlockBins);
   L.cand_start = o;   o = align256(o + sizeof(uint16_t) * (size_t)L.max_cand_blocks * kBlockBins);
+  L.row_keys = o;     o = align256(o + (score_stride > 0 ? sizeof(int32_t) * (size_t)T : 0));
+  L.score_rows = o;   o = align256(o + sizeof(uint32_t) * (size_t)T * (size_t)score_stride);
   L.total = o;
   return L;
 }
@@ -140,8 +152,12 @@ __device__ __forceinline__ long long group_keys(long long P, int q, int G, int g
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   pdl_launch_dependents();  // the scoring kernel's prologue may overlap the plan
+  int32_t* row_keys = reinterpret_cast<int32_t*>(p.ws + p.L.row_keys);
+  if (p.L.score_stride > 0)
+    for (int t = threadIdx.x; t < p.T; t += kPlanThreads) row_keys[t] = 0;
   __shared__ long long warp_sums[32];
   __shared__ long long s_Q;
+  __shared__ unsigned long long s_max_keys;
   __shared__ int2 s_empty[kPlanThreads];  // (first row, rows) of groups that see no entry
   __shared__ int s_n_empty;
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.L.header);
@@ -195,6 +211,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   };
 
   // Phase B: total tiles W, the per-CTA share Q and the number of items.
+  if (threadIdx.x == 0) s_max_keys = 0ull;
+  __syncthreads();
   long long W = 0;
   for (int base = 0; base < total_groups; base += kPlanThreads) {
     const int gi = base + threadIdx.x;
@@ -203,6 +221,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
       int r, t0, gc; long long keys;
       describe(gi, r, t0, gc, keys);
       my = (keys + kTileKeysPlan - 1) / kTileKeysPlan;
+      atomicMax(&s_max_keys, (unsigned long long)keys);
     }
     long long tot;
     block_exclusive_scan(my, &tot, warp_sums);
@@ -217,6 +236,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   }
   __syncthreads();
   const long long Q = s_Q;
+  // rows go to the workspace only when every row of the batch fits there: a
+  // batch that still merges long rows inside the scoring kernel gains nothing
+  // from a second kernel for the short ones
+  const bool rows_ok = G == 1 && p.L.score_stride > 0 && s_max_keys <= (unsigned long long)p.L.score_stride;
   const int n_used = (int)((W + Q - 1) / Q);
 
   // Phase C: emit the pieces in tile order; CTA c's items are contiguous.
@@ -230,10 +253,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
       describe(gi, r, t0, gc, keys);
       tiles = (keys + kTileKeysPlan - 1) / kTileKeysPlan;
     }
+    // a decode row short enough is scored into the workspace (no merge)
+    const bool to_rows = rows_ok && keys > 0;
+    if (to_rows) row_keys[t0] = (int32_t)keys;
     long long t_tiles;
     const long long P = tile_carry + block_exclusive_scan(tiles, &t_tiles, warp_sums);
     if (tiles > 0) pieces = (P + tiles - 1) / Q - P / Q + 1;
-    const bool is_split = pieces > 1;
+    const bool is_split = pieces > 1 && !to_rows;
     long long t_items, t_sg, t_cb;
     const long long my_item = item_carry + block_exclusive_scan(pieces, &t_items, warp_sums);
     const long long my_sg = sg_carry + block_exclusive_scan(is_split ? 1 : 0, &t_sg, warp_sums);
@@ -254,7 +280,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
       it.k1 = (int)min((s1 - P) * kTileKeysPlan, keys);
       it.split = (int)j | ((int)pieces << 16);
       it.cand_block = is_split ? (int)my_cb : -1;
-      it.sgroup = is_split ? (int)my_sg : -1;
+      it.sgroup = to_rows ? kSgroupRows : (is_split ? (int)my_sg : -1);
       items[my_item + j] = it;
       if (s0 == c * Q) cta_start[c] = (int)(my_item + j);  // the piece that opens CTA c
     }
@@ -283,6 +309,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   }
   const int any_overflow = __syncthreads_or(overflow ? 1 : 0);
   if (any_overflow) raise_status(p.status, kStatusBadMetadata);
+  if (any_overflow && p.L.score_stride > 0)
+    for (int t = threadIdx.x; t < p.T; t += kPlanThreads) row_keys[t] = 0;
   const int n_items = any_overflow ? 0 : (int)item_carry;
   for (int c = threadIdx.x; c <= p.n_cta; c += kPlanThreads)
     if (any_overflow || c >= n_used) cta_start[c] = n_items;

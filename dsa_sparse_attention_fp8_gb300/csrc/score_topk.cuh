@@ -78,6 +78,8 @@ struct ScoreParams {
   int32_t* topk;
   float* scores_out;
   int64_t scores_ld;
+  uint32_t* score_rows;      // [T, score_stride] keys of rows scored into the workspace
+  int score_stride;
   int32_t* status;
   // dynamic shared memory offsets (from a 1024-aligned base)
   uint32_t off_stage, off_scale, off_q, off_ckeys, off_cidx, off_wq, off_tok, off_hist, off_misc,
@@ -990,6 +992,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const int seq_len = __ldg(p.seq_lens + I.r);
       const int nsplit = I.split >> 16;
       const int split = I.split & 0xFFFF;
+      const bool to_rows = I.sgroup == kSgroupRows;  // keys to the workspace, selected later
       const int g_first = alt ? 0 : wg;  // this thread's rows: g_first, g_first + 2, ...
       // per-row setup (warpgroup 0 for the shared decode row)
       for (int g = g_first; g < I.gcount; g += 2) {
@@ -1042,8 +1045,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
               if (p.scores_out && valid && key < p.scores_ld)
                 p.scores_out[(int64_t)tok[g].t * p.scores_ld + key] = score;
               const uint32_t kk = valid ? score_key(score) : 0u;
-              slot_append(kk, key, tok[g].thr, &tok[g], ckeys_all + (size_t)g * p.C,
-                          cidx_all + (size_t)g * p.C, hist_of(g));
+              if (to_rows) {
+                if (key < I.k1) p.score_rows[(int64_t)tok[g].t * p.score_stride + key] = kk;
+              } else {
+                slot_append(kk, key, tok[g].thr, &tok[g], ckeys_all + (size_t)g * p.C,
+                            cidx_all + (size_t)g * p.C, hist_of(g));
+              }
             }
             tc_fence_before();
             __syncwarp();
@@ -1077,8 +1084,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (!ok) misc->epi_abort = 1;
       named_bar_sync(3, 256);  // every append of the item is done
       if (misc->epi_abort) { ok = false; break; }
-      // finalize this item's rows
-      for (int g = g_first; g < I.gcount; g += 2) {
+      // finalize this item's rows (rows scored into the workspace are
+      // selected by the row kernel)
+      for (int g = g_first; g < I.gcount && !to_rows; g += 2) {
         const int n0 = tok[g].count;
         if (nsplit == 1) {
           slot_select(S, kSelRow, n0, smem_u32(ck_of(g)), smem_u32(ci_of(g)), hist_of(g), p.k, 0,
@@ -1098,7 +1106,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           if (S.tid == 0) __stcg(p.cand_count + blk, n);
         }
       }
-      if (nsplit > 1) {
+      if (nsplit > 1 && !to_rows) {
         // last piece of the group to finish merges the candidates of all pieces
         __threadfence();
         named_bar_sync(3, 256);
@@ -1131,6 +1139,311 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// Top-k of the rows a decode batch scored into the workspace: one CTA of
+// 1024 threads per query row, an exact radix select over the row's keys held
+// in shared memory.  The first level bins the scores linearly over the row's
+// own value range (scores crowd into few exponent values, so bins by the top
+// bits of the key would collide), emits every key above the bin holding the
+// k-th largest and gathers that bin's keys, normally a few dozen, which are
+// then ranked directly (one thread each; ties by position).  A cut bin of
+// more than 1024 keys (heavily tied scores) is resolved instead by levels
+// that bin the keys still in play by (key - lo) >> shift over their own key
+// range [lo, hi]; keys all equal to lo = hi are taken in position order.  Key 0 marks a key that is not
+// visible (bad page) and is never selected.
+// ---------------------------------------------------------------------------
+constexpr int kRowsThreads = 1024;
+constexpr int kRowsBins = 2048;
+
+struct RowsTopkParams {
+  const uint32_t* score_rows;
+  const int32_t* row_keys;   // keys of row t, 0 = not a workspace row
+  int score_stride;
+  int k;
+  int32_t* topk;
+};
+
+struct RowsScratch {
+  uint32_t hist[kRowsBins];
+  uint32_t cand_key[kRowsThreads];   // the first level's cut bin
+  int32_t cand_pos[kRowsThreads];
+  float vmin, vmax;
+  uint32_t cut_lo, cut_hi;           // key range of the cut bin
+  uint32_t warp_part[32];
+  uint32_t lo, hi;           // key range of the level
+  int cut_bin, above, total;
+  int base;                  // outputs written so far
+};
+
+__host__ __device__ inline size_t rows_topk_smem(int score_stride) {
+  return (size_t)score_stride * 4 + sizeof(RowsScratch) + 64;
+}
+
+// Exclusive block-wide prefix sum of one count per thread; *total = the sum.
+__device__ __forceinline__ uint32_t rows_scan(uint32_t v, RowsScratch* sc, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sc->warp_part[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = sc->warp_part[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    sc->warp_part[lane] = w;  // inclusive
+  }
+  __syncthreads();
+  *total = sc->warp_part[31];
+  const uint32_t ex = (warp > 0 ? sc->warp_part[warp - 1] : 0u) + x - v;
+  __syncthreads();
+  return ex;
+}
+
+// The score a key encodes (inverse of score_key).
+__device__ __forceinline__ float key_score(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// Shift that maps [lo, hi] onto at most kRowsBins bins: (key - lo) >> shift.
+__device__ __forceinline__ int rows_shift(uint32_t lo, uint32_t hi) {
+  const int bits = 32 - __clz(hi - lo);  // bit length of hi - lo
+  return bits > 11 ? bits - 11 : 0;
+}
+
+__global__ void __launch_bounds__(kRowsThreads, 1) rows_topk_kernel(const __grid_constant__ RowsTopkParams p) {
+  const int t = blockIdx.x;
+  const int n = __ldg(p.row_keys + t);
+  if (n <= 0) return;
+  extern __shared__ __align__(16) unsigned char rows_smem[];
+  uint32_t* keys = reinterpret_cast<uint32_t*>(rows_smem);
+  RowsScratch* sc = reinterpret_cast<RowsScratch*>(keys + p.score_stride);
+  int32_t* out = p.topk + (int64_t)t * p.k;
+  const int tid = threadIdx.x;
+  // keys to shared memory, with the range of the visible ones
+  const uint32_t* row = p.score_rows + (int64_t)t * p.score_stride;
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  for (int i = tid; i < n; i += kRowsThreads) {
+    const uint32_t kk = __ldcg(row + i);
+    keys[i] = kk;
+    if (kk != 0u) {
+      kmin = min(kmin, kk);
+      kmax = max(kmax, kk);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  if (tid == 0) { sc->lo = 0xFFFFFFFFu; sc->hi = 0u; sc->base = 0; }
+  __syncthreads();
+  if ((tid & 31) == 0) { atomicMin(&sc->lo, kmin); atomicMax(&sc->hi, kmax); }
+  __syncthreads();
+  uint32_t lo = sc->lo, hi = sc->hi;
+  int need = p.k;
+  bool done = lo > hi;  // no visible key
+  if (!done) {
+    // ---- first level: 2048 bins linear in the score over [vmin, vmax]
+    const float vmin = key_score(lo), vmax = key_score(hi);
+    const float scale = vmax > vmin ? (float)kRowsBins / (vmax - vmin) : 0.f;
+    auto vbin = [&](uint32_t kk) -> int {  // monotone in the score
+      const float b = (key_score(kk) - vmin) * scale;
+      return b >= (float)(kRowsBins - 1) ? kRowsBins - 1 : (b > 0.f ? (int)b : 0);
+    };
+    for (int b = tid; b < kRowsBins; b += kRowsThreads) sc->hist[b] = 0u;
+    if (tid == 0) { sc->cut_lo = 0xFFFFFFFFu; sc->cut_hi = 0u; }
+    __syncthreads();
+    for (int i = tid; i < n; i += kRowsThreads) {
+      const uint32_t kk = keys[i];
+      if (kk != 0u) atomicAdd(&sc->hist[vbin(kk)], 1u);
+    }
+    __syncthreads();
+    const int b1 = kRowsBins - 2 * tid - 1, b0 = b1 - 1;
+    const uint32_t c1 = sc->hist[b1], c0 = sc->hist[b0];
+    uint32_t total;
+    const uint32_t above = rows_scan(c1 + c0, sc, &total);
+    if ((int)total <= need) {
+      if (tid == 0) sc->cut_bin = -1;
+    } else if ((int)above < need && need <= (int)(above + c1 + c0)) {
+      const bool in1 = need <= (int)(above + c1);
+      sc->cut_bin = in1 ? b1 : b0;
+      sc->above = (int)(in1 ? above : above + c1);
+      sc->total = (int)(in1 ? c1 : c0);
+    }
+    __syncthreads();
+    const int cut = sc->cut_bin;
+    // emit the keys above the cut bin (every visible key when there is none)
+    // and gather the cut bin's keys
+    uint32_t mine = 0, mc = 0;
+    for (int i = tid; i < n; i += kRowsThreads) {
+      const uint32_t kk = keys[i];
+      if (kk == 0u) continue;
+      const int b = vbin(kk);
+      mine += (cut < 0 || b > cut) ? 1u : 0u;
+      mc += (b == cut) ? 1u : 0u;
+    }
+    uint32_t emitted, m;
+    uint32_t pos = rows_scan(mine, sc, &emitted);
+    uint32_t cpos = rows_scan(mc, sc, &m);
+    uint32_t clo = 0xFFFFFFFFu, chi = 0u;
+    for (int i = tid; i < n; i += kRowsThreads) {
+      const uint32_t kk = keys[i];
+      if (kk == 0u) continue;
+      const int b = vbin(kk);
+      if (cut < 0 || b > cut) out[pos++] = i;
+      if (b == cut) {
+        if (cpos < (uint32_t)kRowsThreads) {
+          sc->cand_key[cpos] = kk;
+          sc->cand_pos[cpos] = i;
+        }
+        ++cpos;
+        clo = min(clo, kk);
+        chi = max(chi, kk);
+      }
+    }
+    if (cut < 0) {
+      if (tid == 0) sc->base = (int)emitted;
+      done = true;
+    } else {
+      need -= sc->above;
+      if (m <= (uint32_t)kRowsThreads) {
+        __syncthreads();  // the gathered candidates are visible
+        // rank of candidate tid among the cut bin: larger keys first, ties by position
+        if (tid < (int)m) {
+          const uint32_t kj = sc->cand_key[tid];
+          const int pj = sc->cand_pos[tid];
+          int rank = 0;
+          for (int i = 0; i < (int)m; ++i) {
+            const uint32_t ki = sc->cand_key[i];
+            rank += (ki > kj || (ki == kj && sc->cand_pos[i] < pj)) ? 1 : 0;
+          }
+          if (rank < need) out[emitted + rank] = pj;
+        }
+        if (tid == 0) sc->base = (int)emitted + min((int)m, need);
+        done = true;
+      } else {
+        // heavily tied: resolve the cut bin by key-range levels
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          clo = min(clo, __shfl_xor_sync(0xffffffffu, clo, o));
+          chi = max(chi, __shfl_xor_sync(0xffffffffu, chi, o));
+        }
+        if ((tid & 31) == 0) { atomicMin(&sc->cut_lo, clo); atomicMax(&sc->cut_hi, chi); }
+        if (tid == 0) sc->base = (int)emitted;
+        __syncthreads();
+        lo = sc->cut_lo;
+        hi = sc->cut_hi;
+        if (lo == hi) {
+          // every key of the cut bin is equal: the first `need` in position order
+          const int per = (n + kRowsThreads - 1) / kRowsThreads;
+          uint32_t eq = 0;
+          for (int i = tid * per, e = 0; e < per && i < n; ++i, ++e) eq += keys[i] == lo ? 1u : 0u;
+          const uint32_t base1 = (uint32_t)sc->base;
+          uint32_t all;
+          uint32_t rank = rows_scan(eq, sc, &all);
+          uint32_t w = base1 + rank;
+          for (int i = tid * per, e = 0; e < per && i < n; ++i, ++e)
+            if (keys[i] == lo) {
+              if (rank < (uint32_t)need) out[w] = i;
+              ++rank;
+              ++w;
+            }
+          __syncthreads();
+          if (tid == 0) sc->base += min((int)all, need);
+          done = true;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  while (!done) {
+    const int sh = rows_shift(lo, hi);
+    // keys in play: lo <= key <= hi; count them per bin
+    for (int b = tid; b < kRowsBins; b += kRowsThreads) sc->hist[b] = 0u;
+    __syncthreads();
+    for (int i = tid; i < n; i += kRowsThreads) {
+      const uint32_t kk = keys[i];
+      if (kk != 0u && kk >= lo && kk <= hi) atomicAdd(&sc->hist[(kk - lo) >> sh], 1u);
+    }
+    __syncthreads();
+    // bins from the top: thread tid owns bins [kRowsBins - 2 (tid + 1), kRowsBins - 2 tid)
+    const int b1 = kRowsBins - 2 * tid - 1, b0 = b1 - 1;
+    const uint32_t c1 = sc->hist[b1], c0 = sc->hist[b0];
+    uint32_t total;
+    const uint32_t above = rows_scan(c1 + c0, sc, &total);
+    if ((int)total <= need) {
+      // every key in play is taken
+      if (tid == 0) sc->cut_bin = -1;
+    } else if ((int)above < need && need <= (int)(above + c1 + c0)) {
+      // exactly one thread holds the bin of the need-th largest key
+      const bool in1 = need <= (int)(above + c1);
+      sc->cut_bin = in1 ? b1 : b0;
+      sc->above = (int)(in1 ? above : above + c1);
+      sc->total = (int)(in1 ? c1 : c0);
+    }
+    __syncthreads();
+    const int cut = sc->cut_bin;
+    // emit the keys above the cut bin (all keys in play when there is no cut)
+    const uint32_t base0 = (uint32_t)sc->base;  // thread 0 updates it after the scan's barriers
+    uint32_t mine = 0;
+    for (int i = tid; i < n; i += kRowsThreads) {
+      const uint32_t kk = keys[i];
+      mine += (kk != 0u && kk >= lo && kk <= hi && (cut < 0 || (int)((kk - lo) >> sh) > cut)) ? 1u : 0u;
+    }
+    uint32_t emitted;
+    uint32_t pos = base0 + rows_scan(mine, sc, &emitted);
+    for (int i = tid; i < n; i += kRowsThreads) {
+      const uint32_t kk = keys[i];
+      if (kk != 0u && kk >= lo && kk <= hi && (cut < 0 || (int)((kk - lo) >> sh) > cut)) out[pos++] = i;
+    }
+    if (cut < 0) {
+      if (tid == 0) sc->base += (int)emitted;
+      done = true;
+    } else {
+      need -= sc->above;
+      // the cut bin's key range
+      const uint32_t nlo = lo + ((uint32_t)cut << sh);
+      const uint32_t nhi = (uint32_t)min((uint64_t)hi, (uint64_t)nlo + ((uint64_t)1 << sh) - 1u);
+      if (tid == 0) sc->base += (int)emitted;
+      lo = nlo;
+      hi = nhi;
+      if (lo == hi) {
+        // every remaining key equals lo: the first `need` in position order
+        __syncthreads();
+        uint32_t eq = 0;
+        for (int i = tid * ((n + kRowsThreads - 1) / kRowsThreads), e = 0;
+             e < (n + kRowsThreads - 1) / kRowsThreads && i < n; ++i, ++e)
+          eq += keys[i] == lo ? 1u : 0u;
+        const uint32_t base1 = (uint32_t)sc->base;
+        uint32_t all;
+        uint32_t rank = rows_scan(eq, sc, &all);
+        uint32_t w = base1 + rank;
+        for (int i = tid * ((n + kRowsThreads - 1) / kRowsThreads), e = 0;
+             e < (n + kRowsThreads - 1) / kRowsThreads && i < n; ++i, ++e)
+          if (keys[i] == lo) {
+            if (rank < (uint32_t)need) out[w] = i;
+            ++rank;
+            ++w;
+          }
+        __syncthreads();
+        if (tid == 0) sc->base += min((int)all, need);
+        done = true;
+      }
+    }
+    __syncthreads();
+  }
+  // -1 after the selected keys
+  const int filled = sc->base;
+  for (int i = filled + tid; i < p.k; i += kRowsThreads) out[i] = -1;
 }
 
 }  // namespace dsa

@@ -39,7 +39,9 @@ class IndexerStep:
         self.block_table = torch.zeros((R, max_blocks), dtype=torch.int32, device=dev)
         self.topk = torch.full((max_num_batched_tokens, index_topk), -1, dtype=torch.int32,
                                device=dev)
-        self.workspace = binding.alloc_workspace(T, H, R, index_topk, device=dev)
+        # the keys a row sees are bounded by the block table: max_blocks pages of 64
+        self.workspace = binding.alloc_workspace(T, H, R, index_topk, device=dev,
+                                                 max_ctx=max_blocks * 64)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.layers: list[Optional[dict]] = []
         for l in range(num_layers):

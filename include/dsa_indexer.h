@@ -159,9 +159,20 @@ int dsa_quantize_fp8_blocks(const float* x, int64_t n_blocks, uint8_t* codes, fl
 
 /*
  * Bytes of device workspace that dsa_indexer_score_topk / dsa_layer_stack_run
- * need for a batch of T query rows with H heads and this index_topk.  R and
- * max_ctx are accepted for forward compatibility.  Returns 0 for invalid
- * arguments.  Pure host function.
+ * need for a batch of T query rows with H heads and this index_topk.  Returns
+ * 0 for invalid arguments.  Pure host function.
+ *   max_ctx  0, or a bound on the keys any query row sees (its request's
+ *            seq_len; seq_len / compress_ratio for a compressed cache; 64 x
+ *            max_blocks always bounds it).  For a decode batch (no
+ *            request with more than one query row), 0 < max_ctx <= 8192 adds
+ *            room for per-row key areas: the rows are then scored into the
+ *            workspace and their top-k selected by a second kernel, instead
+ *            of being selected (and, when cut across SMs, merged) inside the
+ *            scoring kernel (should a row exceed the bound after all, the
+ *            whole batch takes the in-kernel path).  The results are
+ *            the same (exact top-k; ties at the k-th score may be broken
+ *            differently).  The scoring calls detect the room from their
+ *            workspace_bytes argument; the rows take at most 256 MB.
  */
 size_t dsa_indexer_workspace_bytes(int T, int H, int R, int64_t max_ctx, int index_topk);
 
