@@ -1167,8 +1167,9 @@ struct RowsTopkParams {
 
 struct RowsScratch {
   uint32_t hist[kRowsBins];
-  uint32_t cand_key[kRowsThreads];   // the first level's cut bin
-  int32_t cand_pos[kRowsThreads];
+  uint32_t cand_key[1024];           // the first level's cut bin
+  int32_t cand_pos[1024];
+  uint32_t n_out, n_cand;            // warp-aggregated output and gather counters
   float vmin, vmax;
   uint32_t cut_lo, cut_hi;           // key range of the cut bin
   uint32_t warp_part[32];
@@ -1176,6 +1177,18 @@ struct RowsScratch {
   int cut_bin, above, total;
   int base;                  // outputs written so far
 };
+
+// Warp-aggregated slot in a shared counter for every lane whose flag is set
+// (all 32 lanes call it).
+__device__ __forceinline__ uint32_t warp_take(bool flag, uint32_t* counter) {
+  const uint32_t m = __ballot_sync(0xffffffffu, flag);
+  uint32_t base = 0;
+  if ((threadIdx.x & 31) == 0 && m) base = atomicAdd(counter, (uint32_t)__popc(m));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  uint32_t lt;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+  return base + (uint32_t)__popc(m & lt);
+}
 
 __host__ __device__ inline size_t rows_topk_smem(int score_stride) {
   return (size_t)score_stride * 4 + sizeof(RowsScratch) + 64;
@@ -1192,21 +1205,28 @@ __device__ __forceinline__ uint32_t rows_scan(uint32_t v, RowsScratch* sc, uint3
   }
   if (lane == 31) sc->warp_part[warp] = x;
   __syncthreads();
+  constexpr int kWarps = kRowsThreads / 32;
   if (warp == 0) {
-    uint32_t w = sc->warp_part[lane];
+    uint32_t w = lane < kWarps ? sc->warp_part[lane] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    sc->warp_part[lane] = w;  // inclusive
+    if (lane < kWarps) sc->warp_part[lane] = w;  // inclusive
   }
   __syncthreads();
-  *total = sc->warp_part[31];
+  *total = sc->warp_part[kWarps - 1];
   const uint32_t ex = (warp > 0 ? sc->warp_part[warp - 1] : 0u) + x - v;
   __syncthreads();
   return ex;
 }
+
+// The bin holding the need-th largest key of sc->hist (bins from the top;
+// each thread owns kRowsBins / kRowsThreads of them): sets sc->cut_bin (-1 when the bins hold at most
+// `need` keys), sc->above (keys in higher bins) and sc->total (the bin's).
+// Every thread calls it; it ends without a barrier.
+__device__ __forceinline__ void rows_find_cut(RowsScratch* sc, int need);
 
 // The score a key encodes (inverse of score_key).
 __device__ __forceinline__ float key_score(uint32_t key) {
@@ -1217,6 +1237,34 @@ __device__ __forceinline__ float key_score(uint32_t key) {
 __device__ __forceinline__ int rows_shift(uint32_t lo, uint32_t hi) {
   const int bits = 32 - __clz(hi - lo);  // bit length of hi - lo
   return bits > 11 ? bits - 11 : 0;
+}
+
+__device__ __forceinline__ void rows_find_cut(RowsScratch* sc, int need) {
+  constexpr int kPer = kRowsBins / kRowsThreads;
+  const int tid = threadIdx.x;
+  const int bt = kRowsBins - kPer * tid - 1;
+  uint32_t cs[kPer], mine = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    cs[j] = sc->hist[bt - j];
+    mine += cs[j];
+  }
+  uint32_t total;
+  const uint32_t above = rows_scan(mine, sc, &total);
+  if ((int)total <= need) {
+    if (tid == 0) sc->cut_bin = -1;
+  } else if ((int)above < need && need <= (int)(above + mine)) {
+    uint32_t a = above;
+    for (int j = 0; j < kPer; ++j) {
+      if (need <= (int)(a + cs[j])) {
+        sc->cut_bin = bt - j;
+        sc->above = (int)a;
+        sc->total = (int)cs[j];
+        break;
+      }
+      a += cs[j];
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kRowsThreads, 1) rows_topk_kernel(const __grid_constant__ RowsTopkParams p) {
@@ -1267,60 +1315,44 @@ __global__ void __launch_bounds__(kRowsThreads, 1) rows_topk_kernel(const __grid
       if (kk != 0u) atomicAdd(&sc->hist[vbin(kk)], 1u);
     }
     __syncthreads();
-    const int b1 = kRowsBins - 2 * tid - 1, b0 = b1 - 1;
-    const uint32_t c1 = sc->hist[b1], c0 = sc->hist[b0];
-    uint32_t total;
-    const uint32_t above = rows_scan(c1 + c0, sc, &total);
-    if ((int)total <= need) {
-      if (tid == 0) sc->cut_bin = -1;
-    } else if ((int)above < need && need <= (int)(above + c1 + c0)) {
-      const bool in1 = need <= (int)(above + c1);
-      sc->cut_bin = in1 ? b1 : b0;
-      sc->above = (int)(in1 ? above : above + c1);
-      sc->total = (int)(in1 ? c1 : c0);
-    }
+    rows_find_cut(sc, need);
+    if (tid == 0) { sc->n_out = 0u; sc->n_cand = 0u; }
     __syncthreads();
     const int cut = sc->cut_bin;
     // emit the keys above the cut bin (every visible key when there is none)
-    // and gather the cut bin's keys
-    uint32_t mine = 0, mc = 0;
-    for (int i = tid; i < n; i += kRowsThreads) {
-      const uint32_t kk = keys[i];
-      if (kk == 0u) continue;
-      const int b = vbin(kk);
-      mine += (cut < 0 || b > cut) ? 1u : 0u;
-      mc += (b == cut) ? 1u : 0u;
-    }
-    uint32_t emitted, m;
-    uint32_t pos = rows_scan(mine, sc, &emitted);
-    uint32_t cpos = rows_scan(mc, sc, &m);
+    // and gather the cut bin's keys; positions from warp-aggregated counters
+    // (the order inside the output row is free)
     uint32_t clo = 0xFFFFFFFFu, chi = 0u;
-    for (int i = tid; i < n; i += kRowsThreads) {
-      const uint32_t kk = keys[i];
-      if (kk == 0u) continue;
-      const int b = vbin(kk);
-      if (cut < 0 || b > cut) out[pos++] = i;
-      if (b == cut) {
-        if (cpos < (uint32_t)kRowsThreads) {
-          sc->cand_key[cpos] = kk;
-          sc->cand_pos[cpos] = i;
+    for (int c0i = 0; c0i < n; c0i += kRowsThreads) {  // same bound for every thread
+      const int i = c0i + tid;
+      const uint32_t kk = i < n ? keys[i] : 0u;
+      const int b = kk != 0u ? vbin(kk) : -2;
+      const bool emit = kk != 0u && (cut < 0 || b > cut);
+      const bool gather = kk != 0u && b == cut;
+      const uint32_t po = warp_take(emit, &sc->n_out);
+      if (emit) out[po] = i;
+      const uint32_t pc = warp_take(gather, &sc->n_cand);
+      if (gather) {
+        if (pc < 1024u) {
+          sc->cand_key[pc] = kk;
+          sc->cand_pos[pc] = i;
         }
-        ++cpos;
         clo = min(clo, kk);
         chi = max(chi, kk);
       }
     }
+    __syncthreads();
+    const uint32_t emitted = sc->n_out, m = sc->n_cand;
     if (cut < 0) {
       if (tid == 0) sc->base = (int)emitted;
       done = true;
     } else {
       need -= sc->above;
-      if (m <= (uint32_t)kRowsThreads) {
-        __syncthreads();  // the gathered candidates are visible
-        // rank of candidate tid among the cut bin: larger keys first, ties by position
-        if (tid < (int)m) {
-          const uint32_t kj = sc->cand_key[tid];
-          const int pj = sc->cand_pos[tid];
+      if (m <= 1024u) {
+        // rank of each gathered candidate: larger keys first, ties by position
+        for (int j = tid; j < (int)m; j += kRowsThreads) {
+          const uint32_t kj = sc->cand_key[j];
+          const int pj = sc->cand_pos[j];
           int rank = 0;
           for (int i = 0; i < (int)m; ++i) {
             const uint32_t ki = sc->cand_key[i];
@@ -1375,21 +1407,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1) rows_topk_kernel(const __grid
       if (kk != 0u && kk >= lo && kk <= hi) atomicAdd(&sc->hist[(kk - lo) >> sh], 1u);
     }
     __syncthreads();
-    // bins from the top: thread tid owns bins [kRowsBins - 2 (tid + 1), kRowsBins - 2 tid)
-    const int b1 = kRowsBins - 2 * tid - 1, b0 = b1 - 1;
-    const uint32_t c1 = sc->hist[b1], c0 = sc->hist[b0];
-    uint32_t total;
-    const uint32_t above = rows_scan(c1 + c0, sc, &total);
-    if ((int)total <= need) {
-      // every key in play is taken
-      if (tid == 0) sc->cut_bin = -1;
-    } else if ((int)above < need && need <= (int)(above + c1 + c0)) {
-      // exactly one thread holds the bin of the need-th largest key
-      const bool in1 = need <= (int)(above + c1);
-      sc->cut_bin = in1 ? b1 : b0;
-      sc->above = (int)(in1 ? above : above + c1);
-      sc->total = (int)(in1 ? c1 : c0);
-    }
+    rows_find_cut(sc, need);
     __syncthreads();
     const int cut = sc->cut_bin;
     // emit the keys above the cut bin (all keys in play when there is no cut)
