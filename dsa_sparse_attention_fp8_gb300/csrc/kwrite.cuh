@@ -59,6 +59,20 @@ __device__ __forceinline__ int find_request(const int32_t* __restrict__ qsl, int
   return lo;
 }
 
+// The same search over a copy of query_start_loc in shared memory.
+__device__ __forceinline__ int find_request_smem(const int32_t* qsl_s, int R, int t) {
+  int lo = 0, hi = R - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (qsl_s[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// query_start_loc entries staged in shared memory by the cache-write kernel
+// (its binary search would otherwise be a chain of dependent global loads)
+constexpr int kQslSmem = 4096;
+
 // One lane's 4 consecutive elements of 128-element block `blk` as FP32
 // (BF16 widens exactly: its bits are the upper half of the FP32 value).
 __device__ __forceinline__ float4 load_lane4(const float* x, int64_t blk, int lane) {
@@ -89,6 +103,14 @@ __global__ void __launch_bounds__(256) write_k_kernel(
   pdl_launch_dependents();  // the scoring kernel's prologue may overlap this write
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  // the key's load is in flight while the block stages query_start_loc
+  const float4 v = warp < T ? load_lane4(k, warp, lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+  __shared__ int32_t qsl_s[kQslSmem];
+  const bool staged = R + 1 <= kQslSmem;
+  if (staged) {
+    for (int i = threadIdx.x; i <= R; i += blockDim.x) qsl_s[i] = __ldg(qsl + i);
+    __syncthreads();
+  }
   if (warp >= T) {
     const int64_t b = warp - T;
     if (q == nullptr || b >= (int64_t)T * H) return;
@@ -99,14 +121,12 @@ __global__ void __launch_bounds__(256) write_k_kernel(
     return;
   }
   const int t = (int)warp;
-
-  const float4 v = load_lane4(k, t, lane);
   float s;
   const uint32_t codes = quantize_lane4(v, &s);
 
-  const int r = find_request(qsl, R, t);
-  const int q_begin = __ldg(qsl + r);
-  const int q_len = __ldg(qsl + r + 1) - q_begin;
+  const int r = staged ? find_request_smem(qsl_s, R, t) : find_request(qsl, R, t);
+  const int q_begin = staged ? qsl_s[r] : __ldg(qsl + r);
+  const int q_len = (staged ? qsl_s[r + 1] : __ldg(qsl + r + 1)) - q_begin;
   const int seq_len = __ldg(seq_lens + r);
   const int pos = seq_len - q_len + (t - q_begin);
   int64_t slot = -1;
