@@ -400,8 +400,20 @@ int launch_rows_topk(const Batch& b, const ScoreShape& s, int* launches) {
   rp.score_stride = L.score_stride;
   rp.k = b.k;
   rp.topk = b.topk;
-  dsa::rows_topk_kernel<<<(unsigned)b.T, dsa::kRowsThreads, dsa::rows_topk_smem(L.score_stride),
-                          b.st>>>(rp);
+  // programmatic stream serialisation: the row kernel's blocks are placed
+  // while the scoring kernel drains; they wait for its keys before reading
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)b.T);
+  cfg.blockDim = dim3(dsa::kRowsThreads);
+  cfg.dynamicSmemBytes = dsa::rows_topk_smem(L.score_stride);
+  cfg.stream = b.st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = env_int("DSA_PDL", 1, 0, 1);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, dsa::rows_topk_kernel, rp);
+  if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "rows_topk_kernel launch: %s", cudaGetErrorString(e));
   ++*launches;
   return check_launch("rows_topk_kernel");
 }

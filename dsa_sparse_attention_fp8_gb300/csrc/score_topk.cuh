@@ -791,6 +791,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   // everything above overlaps the preceding kernel (plan or cache write) when
   // launched with programmatic stream serialisation; its outputs are read below
   pdl_wait();
+  // every block of this persistent grid is resident: the row kernel's blocks
+  // may be placed as SMs free up (they wait for this grid's completion)
+  pdl_launch_dependents();
   const uint32_t tmem_base = misc->tmem_base;
   const int it_begin = p.cta_start[blockIdx.x];
   const int it_end = p.cta_start[blockIdx.x + 1];
@@ -1268,20 +1271,24 @@ __device__ __forceinline__ void rows_find_cut(RowsScratch* sc, int need) {
 }
 
 __global__ void __launch_bounds__(kRowsThreads, 1) rows_topk_kernel(const __grid_constant__ RowsTopkParams p) {
+  // launched while the scoring kernel runs; its keys are complete after this
+  pdl_wait();
   const int t = blockIdx.x;
-  const int n = __ldg(p.row_keys + t);
-  if (n <= 0) return;
   extern __shared__ __align__(16) unsigned char rows_smem[];
   uint32_t* keys = reinterpret_cast<uint32_t*>(rows_smem);
   RowsScratch* sc = reinterpret_cast<RowsScratch*>(keys + p.score_stride);
   int32_t* out = p.topk + (int64_t)t * p.k;
   const int tid = threadIdx.x;
-  // keys to shared memory, with the range of the visible ones
+  // the whole row area to shared memory while the row's key count loads
+  // (entries beyond it are not used)
   const uint32_t* row = p.score_rows + (int64_t)t * p.score_stride;
+  const int n = __ldg(p.row_keys + t);
+  for (int i = tid; i < p.score_stride; i += kRowsThreads) keys[i] = __ldcg(row + i);
+  if (n <= 0) return;  // not a workspace row (uniform: every thread leaves)
+  __syncthreads();
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   for (int i = tid; i < n; i += kRowsThreads) {
-    const uint32_t kk = __ldcg(row + i);
-    keys[i] = kk;
+    const uint32_t kk = keys[i];
     if (kk != 0u) {
       kmin = min(kmin, kk);
       kmax = max(kmax, kk);
