@@ -308,6 +308,7 @@ int launch_plan(const Batch& b, int G, int* launches) {
   if (sm_count() <= 0) return fail(DSA_ERR_CUDA, "no CUDA device");
   pp.n_cta = grid_ctas();
   pp.min_tiles = env_int("DSA_MIN_SPLIT", 1024, 128, 1 << 20) / 128;
+  pp.item_cost = env_int("DSA_ITEM_TILES", 3, 0, 64);
   pp.topk_buffer = b.topk;
   pp.ws = static_cast<unsigned char*>(b.ws);
   pp.L = dsa::ws_layout(b.T, b.R, G, b.k, pp.n_cta, score_stride_in(b, G, pp.n_cta));
@@ -326,7 +327,13 @@ struct LayerQ {
   int64_t scores_ld;
 };
 
-int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, int* launches) {
+// meta_ready: the launch right before this one is the layer's cache write, a
+// plain launch issued after the plan, so the plan completed before it started:
+// the scoring kernel may read the plan's outputs, and the cache entries below
+// each request's first new entry, before its programmatic-launch wait.
+// q_ready: that cache write does not produce q_fp8 (FP32-input layers).
+int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, int* launches,
+                       bool meta_ready, bool q_ready) {
   CUtensorMap tk, tq;
   int rc = make_rows128_map(&tk, lq.k_cache, (uint64_t)b.num_pages * (DSA_PAGE_BYTES / 128), 64);
   if (rc) return rc;
@@ -359,6 +366,8 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   p.q_bytes = s.q_bytes;
   p.n_max = s.n_max;
   p.q_box_per_token = s.q_box_per_token;
+  p.meta_ready = meta_ready ? 1 : 0;
+  p.q_ready = q_ready ? 1 : 0;
   p.items = reinterpret_cast<const dsa::Item*>(ws + L.items);
   p.cta_start = reinterpret_cast<const int32_t*>(ws + L.cta_start);
   p.CB = L.cb;
@@ -439,6 +448,8 @@ int launch_write_t(const TIn* k, const Batch& b, uint8_t* k_cache, int64_t* slot
   const int64_t warps = (int64_t)b.T + (q ? (int64_t)b.T * H : 0);
   const int64_t grid = (warps + warps_per_block - 1) / warps_per_block;
   if (grid > INT32_MAX) return fail(DSA_ERR_INVALID_ARG, "too many rows for one cache-write launch");
+  // a plain launch (no programmatic serialisation): a layer stack's scoring
+  // launch relies on it to read the plan's outputs before its own wait
   dsa::write_k_kernel<TIn><<<(unsigned)grid, 32 * warps_per_block, 0, b.st>>>(
       k, b.T, b.qsl, b.seq_lens, b.R, b.block_table, b.max_blocks, k_cache, b.num_pages,
       b.ratio, slot_mapping, b.status, q, H, q_fp8, q_scale);
@@ -516,6 +527,12 @@ int write_layer(const dsa_layer_io_bf16& io, const Batch& b, int64_t* slot_mappi
                                   launches);
 }
 
+// FP32-input layers take q_fp8 as an input; BF16-input layers have the cache
+// write quantise it.
+template <typename IO> struct QueriesAreInputs;
+template <> struct QueriesAreInputs<dsa_layer_io> { static constexpr bool value = true; };
+template <> struct QueriesAreInputs<dsa_layer_io_bf16> { static constexpr bool value = false; };
+
 template <typename IO>
 int stack_run(int num_layers, const char* pattern, int freq, int offset, const IO* layers,
               const Batch& b, int32_t* const* per_layer_topk_out, int64_t* slot_mapping) {
@@ -553,7 +570,8 @@ int stack_run(int num_layers, const char* pattern, int freq, int offset, const I
         rc = fail(DSA_ERR_CUDA, "recording score_begin of layer %d failed", l);
         break;
       }
-      rc = launch_score_layer(b, s, lq, &launches);
+      // the cache write, a plain launch, lies between the plan and this launch
+      rc = launch_score_layer(b, s, lq, &launches, true, QueriesAreInputs<IO>::value);
       if (rc) break;
       if (io.score_end && record_event(io.score_end, b.st) != cudaSuccess) {
         rc = fail(DSA_ERR_CUDA, "recording score_end of layer %d failed", l);
@@ -718,7 +736,7 @@ int dsa_indexer_score_topk_compressed(const uint8_t* q_fp8, const float* q_scale
   rc = launch_plan(b, s.G, &launches);
   if (rc == DSA_OK) {
     LayerQ lq{q_fp8, q_scale, w, k_cache, scores_out, scores_ld};
-    rc = launch_score_layer(b, s, lq, &launches);
+    rc = launch_score_layer(b, s, lq, &launches, false, true);
     if (rc == DSA_OK) rc = launch_rows_topk(b, s, &launches);
   }
   g_last_launches = launches;

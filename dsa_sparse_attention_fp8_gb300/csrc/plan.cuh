@@ -137,6 +137,10 @@ struct PlanParams {
   int ratio;       // tokens per cache entry (1: plain cache)
   int n_cta;       // CTAs of the scoring launch (<= kMaxCtas)
   int min_tiles;   // smallest per-CTA share worth a piece of its own
+  // tiles charged for starting a group's first piece: a CTA's item switch
+  // costs its producer about this much streaming time, so the balance counts
+  // it and a CTA that holds several items gets fewer keys (< min_tiles)
+  int item_cost;
   int32_t* topk_buffer;  // for -1 rows of malformed requests
   unsigned char* ws;
   WsLayout L;
@@ -221,6 +225,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
       int r, t0, gc; long long keys;
       describe(gi, r, t0, gc, keys);
       my = (keys + kTileKeysPlan - 1) / kTileKeysPlan;
+      if (my > 0) my += p.item_cost;
       atomicMax(&s_max_keys, (unsigned long long)keys);
     }
     long long tot;
@@ -230,6 +235,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   if (threadIdx.x == 0) {
     long long Q = (W + p.n_cta - 1) / p.n_cta;
     if (Q < p.min_tiles) Q = p.min_tiles;
+    if (Q <= p.item_cost) Q = p.item_cost + 1;  // every used CTA keeps tiles of its own
     if (Q < 1) Q = 1;
     s_Q = Q;
     s_n_empty = 0;
@@ -243,6 +249,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   const int n_used = (int)((W + Q - 1) / Q);
 
   // Phase C: emit the pieces in tile order; CTA c's items are contiguous.
+  // Group g takes stream positions [P, P + item_cost + tiles): the charged
+  // tiles first, then its own from V = P + item_cost on.
   long long tile_carry = 0, item_carry = 0, sg_carry = 0, cb_carry = 0;
   bool overflow = false;
   for (int base = 0; base < total_groups; base += kPlanThreads) {
@@ -257,8 +265,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     const bool to_rows = rows_ok && keys > 0;
     if (to_rows) row_keys[t0] = (int32_t)keys;
     long long t_tiles;
-    const long long P = tile_carry + block_exclusive_scan(tiles, &t_tiles, warp_sums);
-    if (tiles > 0) pieces = (P + tiles - 1) / Q - P / Q + 1;
+    const long long cost = tiles > 0 ? tiles + p.item_cost : 0;
+    const long long P = tile_carry + block_exclusive_scan(cost, &t_tiles, warp_sums);
+    const long long V = P + (tiles > 0 ? p.item_cost : 0);
+    if (tiles > 0) pieces = (V + tiles - 1) / Q - V / Q + 1;
     const bool is_split = pieces > 1 && !to_rows;
     long long t_items, t_sg, t_cb;
     const long long my_item = item_carry + block_exclusive_scan(pieces, &t_items, warp_sums);
@@ -270,19 +280,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
                                      my_cb + (long long)gc * pieces <= p.L.max_cand_blocks));
     if (!fits) overflow = true;
     for (long long j = 0; j < pieces && fits; ++j) {
-      const long long c = P / Q + j;  // CTA of this piece
-      const long long s0 = max(P, c * Q), s1 = min(P + tiles, (c + 1) * Q);
+      const long long c = V / Q + j;  // CTA of this piece
+      const long long s0 = max(V, c * Q), s1 = min(V + tiles, (c + 1) * Q);
       Item it;
       it.r = r;
       it.t0 = t0;
       it.gcount = gc;
-      it.k0 = (int)((s0 - P) * kTileKeysPlan);
-      it.k1 = (int)min((s1 - P) * kTileKeysPlan, keys);
+      it.k0 = (int)((s0 - V) * kTileKeysPlan);
+      it.k1 = (int)min((s1 - V) * kTileKeysPlan, keys);
       it.split = (int)j | ((int)pieces << 16);
       it.cand_block = is_split ? (int)my_cb : -1;
       it.sgroup = to_rows ? kSgroupRows : (is_split ? (int)my_sg : -1);
       items[my_item + j] = it;
-      if (s0 == c * Q) cta_start[c] = (int)(my_item + j);  // the piece that opens CTA c
+      // the piece that opens CTA c: its range starts at c * Q, or CTA c
+      // starts among the tiles charged to this group
+      if (s0 == c * Q || (j == 0 && c * Q >= P)) cta_start[c] = (int)(my_item + j);
     }
     tile_carry += t_tiles;
     item_carry += t_items;

@@ -414,6 +414,23 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// A read-only global load issued where it stands: the compiler may neither
+// move it nor re-issue it at the value's use (it may do both with __ldg), so a
+// value loaded ahead of time stays loaded ahead of time.
+__device__ __forceinline__ int32_t ld_ahead(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ int4 ld_ahead_v4(const void* p) {
+  int4 v;
+  asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 // Programmatic dependent launch.  A kernel lets the next kernel of its stream
 // start (that kernel's prologue then overlaps this one) ...
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -65,6 +65,13 @@ struct ScoreParams {
   int BPS;           // 128-key MMA blocks per pipeline stage (1 or 2); a tile = one stage
   int ratio;         // tokens per cache entry: a row at pos sees entries < (pos + 1) / ratio
   int q_box_per_token;
+  // 1 when the kernel that precedes this one in the stream is this layer's
+  // cache write, launched after the plan completed: the plan's outputs (items,
+  // cta_start) and every cache entry below a request's first new entry may
+  // then be read before the programmatic-launch wait, overlapping the write
+  int meta_ready;
+  // 1 when q_fp8 is not written by the preceding kernel (may be loaded before the wait)
+  int q_ready;
   uint32_t q_bytes;  // bytes of one query-tile buffer
   const Item* items;
   const int32_t* cta_start;  // CTA c walks items [cta_start[c], cta_start[c+1])
@@ -685,6 +692,22 @@ __device__ __noinline__ void merge_pieces(const Selector S, const ScoreParams& p
   slot_select(S, kSelRow, ts->count, ck_s, ci_s, hist_s, need, 0, nullptr, out_row + n_def, nullptr);
 }
 
+// An Item loaded where the call stands (see ld_ahead).
+__device__ __forceinline__ Item load_item(const Item* items, int i) {
+  const int4 a = ld_ahead_v4(items + i);
+  const int4 b = ld_ahead_v4(reinterpret_cast<const int4*>(items + i) + 1);
+  Item I;
+  I.r = a.x;
+  I.t0 = a.y;
+  I.gcount = a.z;
+  I.k0 = a.w;
+  I.k1 = b.x;
+  I.split = b.y;
+  I.cand_block = b.z;
+  I.sgroup = b.w;
+  return I;
+}
+
 // sum_h wq[h] * ReLU(acc[h]) over the H accumulator columns at taddr (this
 // thread's TMEM lane); wq_s is the shared-memory address of the H weights.
 // The weights are read (explicit shared loads) before the tensor-memory
@@ -785,18 +808,74 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_q);
   }
+  // Keys per tile and the producer's view of a chunk of an item's page ids:
+  // lane l holds page 32 * chunk + l of the item, -1 where the item has none.
+  const int KS = kTileKeys * p.BPS;
+  const int ppt = 2 * p.BPS;  // pages per tile
+  const int tpc = 32 / ppt;   // tiles per 32-page chunk
+  auto tiles_of = [&](const Item& J) { return (J.k1 - J.k0 + KS - 1) / KS; };
+  auto in_range = [&](const Item& J, int chunk) {
+    return chunk * tpc < tiles_of(J) && (J.k0 / kPageTokens + chunk * 32 + lane) * kPageTokens < J.k1;
+  };
+  auto fetch = [&](const Item& J, int chunk) -> int32_t {
+    return in_range(J, chunk)
+               ? ld_ahead(p.block_table + (int64_t)J.r * p.max_blocks + J.k0 / kPageTokens + chunk * 32 + lane)
+               : -1;
+  };
+  // Entries below stable_end of an item's request are not written by the
+  // preceding cache write: its new tokens sit at positions >= seq_len - q_len,
+  // and an entry e is written only by a position >= e * ratio.
+  const bool early = p.meta_ready != 0;
+  auto stable_end_of = [&](const Item& J) -> int {
+    if (!early) return 0;
+    const int q_len = ld_ahead(p.qsl + J.r + 1) - ld_ahead(p.qsl + J.r);
+    return (ld_ahead(p.seq_lens + J.r) - q_len) / p.ratio;
+  };
+  // The producer's first three items with the page ids of their first chunks
+  // and their stable ends.  Inputs (block table, query_start_loc, seq_lens)
+  // and, with meta_ready, the plan's outputs are complete before this kernel
+  // starts, so these loads overlap the preceding kernel.  (Once the page copies
+  // of every SM are in flight, any load takes microseconds, so nothing the
+  // producer needs for a decode CTA's items is loaded later.)
+  int it_begin = 0, it_end = 0;
+  Item I_cur{}, I_next{}, I_after{};
+  int32_t raw_cur = -1, raw_next = -1, raw_after = -1;
+  int se_cur = 0, se_next = 0, se_after = 0;
+  auto load_meta = [&] {
+    it_begin = p.cta_start[blockIdx.x];
+    it_end = p.cta_start[blockIdx.x + 1];
+    if (warp == 0) {
+      if (it_begin < it_end) I_cur = load_item(p.items, it_begin);
+      if (it_begin + 1 < it_end) I_next = load_item(p.items, it_begin + 1);
+      if (it_begin + 2 < it_end) I_after = load_item(p.items, it_begin + 2);
+      if (it_begin < it_end) {
+        raw_cur = fetch(I_cur, 0);
+        se_cur = stable_end_of(I_cur);
+      }
+      if (it_begin + 1 < it_end) {
+        raw_next = fetch(I_next, 0);
+        se_next = stable_end_of(I_next);
+      }
+      if (it_begin + 2 < it_end) {
+        raw_after = fetch(I_after, 0);
+        se_after = stable_end_of(I_after);
+      }
+    }
+  };
+  if (early) load_meta();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   // everything above overlaps the preceding kernel (plan or cache write) when
-  // launched with programmatic stream serialisation; its outputs are read below
-  pdl_wait();
+  // launched with programmatic stream serialisation; its outputs are read
+  // below.  With meta_ready the producer waits later, only before what the
+  // preceding kernel may write.
+  if (!(early && warp == 0)) pdl_wait();
   // every block of this persistent grid is resident: the row kernel's blocks
   // may be placed as SMs free up (they wait for this grid's completion)
   pdl_launch_dependents();
+  if (!early) load_meta();
   const uint32_t tmem_base = misc->tmem_base;
-  const int it_begin = p.cta_start[blockIdx.x];
-  const int it_end = p.cta_start[blockIdx.x + 1];
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -811,56 +890,66 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     // released tile s - NS - NB, so a slot is never overwritten while read.
     // The page ids of 16 tiles (32 pages) come from one coalesced load,
     // fetched one chunk ahead.
+    // Items are pipelined three deep: the current item and the next two are
+    // held with their first chunk's page ids; the item three ahead is loaded
+    // once the current item's first tile is issued, and its page ids when the
+    // current item ends.
+    // With meta_ready the warp streams the tiles whose pages are stable before
+    // the programmatic-launch wait, and waits before the first tile that may
+    // hold a new entry or may have to wait for a free stage (seq >= NS), and,
+    // unless q_ready, before the first query load (deferred until then).
     int stage = 0;
     uint32_t sphase = 0;
     int q_last[kMaxQBufs] = {-1, -1};
     int item_i = 0;
     long long seq = 0;  // tile sequence number of this CTA (all roles count alike)
     bool ok = true;
+    bool waited = !early;
+    auto ensure_wait = [&] {
+      if (!waited) {
+        pdl_wait();
+        waited = true;
+      }
+    };
+    const uint32_t stage_bytes = (uint32_t)(p.BPS * kStageBytes);
+    const uint32_t slot_bytes = (uint32_t)(p.BPS * kScaleSlotBytes);
+    Item I_far{};
     for (int it = it_begin; it < it_end && ok; ++it, ++item_i) {
-      const Item I = p.items[it];
+      const Item I = I_cur;
+      const int stable_end = se_cur;
       const int qb = item_i % p.NQ;
       const uint32_t qpar = (uint32_t)((item_i / p.NQ) & 1);
       int okv = 1;
       if (lane == 0) okv = mbar_wait(bar_qempty + 8 * qb, qpar ^ 1, abort_flag);
       if (!__shfl_sync(0xffffffffu, okv, 0)) { ok = false; break; }
-      q_last[qb] = item_i;
-      if (lane == 0) {
-        uint8_t* q_tile = q_base + qb * p.q_bytes;
-        if (p.q_box_per_token) {
-          mbar_arrive_expect_tx(bar_qfull + 8 * qb, (uint32_t)(I.gcount * H * kHeadDim));
-          for (int g = 0; g < I.gcount; ++g)
-            tma_load_2d(smem_u32(q_tile + g * H * kHeadDim), &tm_q, 0, (I.t0 + g) * H,
-                        bar_qfull + 8 * qb);
-        } else {
-          mbar_arrive_expect_tx(bar_qfull + 8 * qb, (uint32_t)(p.G * H * kHeadDim));
-          tma_load_2d(smem_u32(q_tile), &tm_q, 0, I.t0 * H, bar_qfull + 8 * qb);
+      bool q_pending = true;
+      auto issue_q = [&] {
+        q_pending = false;
+        q_last[qb] = item_i;
+        if (lane == 0) {
+          uint8_t* q_tile = q_base + qb * p.q_bytes;
+          if (p.q_box_per_token) {
+            mbar_arrive_expect_tx(bar_qfull + 8 * qb, (uint32_t)(I.gcount * H * kHeadDim));
+            for (int g = 0; g < I.gcount; ++g)
+              tma_load_2d(smem_u32(q_tile + g * H * kHeadDim), &tm_q, 0, (I.t0 + g) * H,
+                          bar_qfull + 8 * qb);
+          } else {
+            mbar_arrive_expect_tx(bar_qfull + 8 * qb, (uint32_t)(p.G * H * kHeadDim));
+            tma_load_2d(smem_u32(q_tile), &tm_q, 0, I.t0 * H, bar_qfull + 8 * qb);
+          }
         }
-      }
-      const int KS = kTileKeys * p.BPS;  // keys per tile
-      const int ppt = 2 * p.BPS;         // pages per tile
-      const int tpc = 32 / ppt;          // tiles per 32-page chunk
-      const uint32_t stage_bytes = (uint32_t)(p.BPS * kStageBytes);
-      const uint32_t slot_bytes = (uint32_t)(p.BPS * kScaleSlotBytes);
-      const int ntiles = (I.k1 - I.k0 + KS - 1) / KS;
-      const int32_t* bt_row = p.block_table + (int64_t)I.r * p.max_blocks;
-      const int page0 = I.k0 / kPageTokens;
-      // a chunk's ids are loaded one chunk ahead and only checked when used, so
-      // the warp never waits for the load
-      auto in_range = [&](int chunk) {
-        return chunk * tpc < ntiles && (page0 + chunk * 32 + lane) * kPageTokens < I.k1;
       };
-      auto fetch = [&](int chunk) -> int32_t {
-        return in_range(chunk) ? __ldg(bt_row + page0 + chunk * 32 + lane) : -1;
-      };
-      int32_t raw = fetch(0);
+      if (p.q_ready || waited) issue_q();
+      const int ntiles = tiles_of(I);
+      int32_t raw = raw_cur;
+      bool ahead = false;  // the next items' loads were issued
       for (int c = 0; c * tpc < ntiles && ok; ++c) {
         int32_t cur = -1;  // this lane's page of the chunk, -1 if none or invalid
-        if (in_range(c)) {
+        if (in_range(I, c)) {
           if (raw >= 0 && (int64_t)raw < p.num_pages) cur = raw;
           else raise_status(p.status, kStatusBadPage);
         }
-        raw = fetch(c + 1);
+        raw = fetch(I, c + 1);
         const int jend = min(tpc, ntiles - c * tpc);
         for (int jj = 0; jj < jend; ++jj, ++seq) {
           // the tile's pages are held by chunk lanes first .. first + ppt - 1,
@@ -871,6 +960,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           // scale chunk h*32 + lane (16 bytes) belongs to the tile's page 2h + lane/16
           const int32_t sp0 = __shfl_sync(0xffffffffu, cur, first + (lane >> 4));
           const int32_t sp1 = __shfl_sync(0xffffffffu, cur, (first + 2 + (lane >> 4)) & 31);
+          if (!waited) {
+            // the tile's pages end at a page boundary: all of them below stable_end?
+            const int tile_end = min(I.k0 + (c * tpc + jj + 1) * KS, I.k1);
+            const int page_end = (tile_end + kPageTokens - 1) / kPageTokens * kPageTokens;
+            if (seq >= p.NS || page_end > stable_end) ensure_wait();
+          }
+          if (q_pending && waited) issue_q();
           okv = 1;
           if (lane == 0) okv = mbar_wait(bar_empty + 8 * stage, sphase ^ 1, abort_flag);
           if (!__shfl_sync(0xffffffffu, okv, 0)) { ok = false; break; }
@@ -891,9 +987,30 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                             (uint32_t)((lane - first) * kPageTokens * kHeadDim),
                         &tm_k, 0, cur * (kPageBytes / kHeadDim), bar_full + 8 * stage);
           if (++stage == p.NS) { stage = 0; sphase ^= 1; }
+          if (!ahead) {
+            ahead = true;
+            if (it + 3 < it_end) I_far = load_item(p.items, it + 3);
+          }
         }
       }
+      if (!ahead && it + 3 < it_end) I_far = load_item(p.items, it + 3);  // an item without tiles
+      if (q_pending && ok) {  // an item whose tiles all went out before the wait
+        ensure_wait();
+        issue_q();
+      }
+      I_cur = I_next;
+      raw_cur = raw_next;
+      se_cur = se_next;
+      I_next = I_after;
+      raw_next = raw_after;
+      se_next = se_after;
+      I_after = I_far;
+      if (it + 3 < it_end) {
+        raw_after = fetch(I_far, 0);
+        se_after = stable_end_of(I_far);
+      }
     }
+    ensure_wait();
     if (lane == 0) {
       if (!ok) {
         *abort_flag = 1;
@@ -988,22 +1105,52 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int headroom = chk * kTileKeys * (alt ? 2 : 1);
     long long tile_base = 0;  // tiles of earlier items of this CTA (all roles count alike)
     bool ok = true;
+    const int g_first = alt ? 0 : wg;  // this thread's rows: g_first, g_first + 2, ...
+    const bool sets_up = !alt || wg == 0;  // per-row setup: warpgroup 0 for the shared decode row
+    // Items are read ahead so that starting one never waits on memory: the
+    // item after the current one is loaded one item early, and its request's
+    // metadata and first row's weight and query scale (head tid) when the
+    // current item starts.
+    struct ItemMeta {
+      int qb0, qe, seq_len;
+      float w, qs;
+    };
+    auto load_meta_of = [&](const Item& J) {
+      ItemMeta m;
+      m.qb0 = ld_ahead(p.qsl + J.r);
+      m.qe = ld_ahead(p.qsl + J.r + 1);
+      m.seq_len = ld_ahead(p.seq_lens + J.r);
+      m.w = 0.f;
+      m.qs = 0.f;
+      if (sets_up && tid < H && g_first < J.gcount) {
+        const int64_t o = (int64_t)(J.t0 + g_first) * H + tid;
+        m.w = __int_as_float(ld_ahead(reinterpret_cast<const int32_t*>(p.w + o)));
+        m.qs = __int_as_float(ld_ahead(reinterpret_cast<const int32_t*>(p.q_scale + o)));
+      }
+      return m;
+    };
+    Item I_nx{}, I_af{};
+    ItemMeta M_cur{}, M_nx{};
+    if (it_begin < it_end) I_nx = load_item(p.items, it_begin);
+    if (it_begin + 1 < it_end) I_af = load_item(p.items, it_begin + 1);
+    if (it_begin < it_end) M_nx = load_meta_of(I_nx);
     for (int it = it_begin; it < it_end && ok; ++it) {
-      const Item I = p.items[it];
-      const int qb0 = __ldg(p.qsl + I.r);
-      const int q_len = __ldg(p.qsl + I.r + 1) - qb0;
-      const int seq_len = __ldg(p.seq_lens + I.r);
+      const Item I = I_nx;
+      M_cur = M_nx;
+      I_nx = I_af;
+      const int qb0 = M_cur.qb0;
+      const int q_len = M_cur.qe - qb0;
+      const int seq_len = M_cur.seq_len;
       const int nsplit = I.split >> 16;
       const int split = I.split & 0xFFFF;
       const bool to_rows = I.sgroup == kSgroupRows;  // keys to the workspace, selected later
-      const int g_first = alt ? 0 : wg;  // this thread's rows: g_first, g_first + 2, ...
-      // per-row setup (warpgroup 0 for the shared decode row)
       for (int g = g_first; g < I.gcount; g += 2) {
         const int t = I.t0 + g;
-        if (!alt || wg == 0) {
+        if (sets_up) {
           for (int h = tid; h < H; h += 128)
-            wq_all[g * H + h] =
-                __ldg(p.w + (int64_t)t * H + h) * __ldg(p.q_scale + (int64_t)t * H + h);
+            wq_all[g * H + h] = g == g_first && h == tid
+                                    ? M_cur.w * M_cur.qs
+                                    : __ldg(p.w + (int64_t)t * H + h) * __ldg(p.q_scale + (int64_t)t * H + h);
           if (tid == 0) {
             tok[g].count = 0;
             tok[g].thr = 0u;
@@ -1014,7 +1161,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
       for (int g = g_first; g < I.gcount; g += 2) clear_bins(S, hist_of(g), kBins);
       named_bar_sync(3, 256);
-      const int KS = kTileKeys * p.BPS;
+      // read ahead: the next item's metadata (its Item arrived one item ago),
+      // the Item after it
+      if (it + 1 < it_end) M_nx = load_meta_of(I_nx);
+      if (it + 2 < it_end) I_af = load_item(p.items, it + 2);
       const int ntiles = (I.k1 - I.k0 + KS - 1) / KS;
       const int units = ntiles * p.BPS;  // 128-key blocks of the item
       const bool may_fill = (I.k1 - I.k0) > p.C;

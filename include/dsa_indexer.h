@@ -286,6 +286,11 @@ typedef struct dsa_layer_io {
  *                         receives rows [0, T) of the buffer as layer l
  *                         consumes it (a copy made after layer l).
  *   slot_mapping          [T] int64 or NULL, from the first F layer.
+ * Within an F layer the scoring kernel starts streaming cache pages while the
+ * layer's cache write still runs, but only pages whose entries all lie below
+ * the request's first new position (seq_len - q_len); so a physical page that
+ * receives a new key in this call must hold no earlier position of another
+ * request (the paged-cache convention: only full pages are shared).
  * Errors: as dsa_indexer_score_topk, plus INVALID_ARG for a bad pattern,
  * freq <= 0, a first layer that is S, or an F layer with a NULL field.
  */
