@@ -308,7 +308,7 @@ int launch_plan(const Batch& b, int G, int* launches) {
   if (sm_count() <= 0) return fail(DSA_ERR_CUDA, "no CUDA device");
   pp.n_cta = grid_ctas();
   pp.min_tiles = env_int("DSA_MIN_SPLIT", 1024, 128, 1 << 20) / 128;
-  pp.item_cost = env_int("DSA_ITEM_TILES", 3, 0, 64);
+  pp.item_cost = env_int("DSA_ITEM_TILES", 2, 0, 64);
   pp.topk_buffer = b.topk;
   pp.ws = static_cast<unsigned char*>(b.ws);
   pp.L = dsa::ws_layout(b.T, b.R, G, b.k, pp.n_cta, score_stride_in(b, G, pp.n_cta));
@@ -370,6 +370,7 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   p.q_ready = q_ready ? 1 : 0;
   p.items = reinterpret_cast<const dsa::Item*>(ws + L.items);
   p.cta_start = reinterpret_cast<const int32_t*>(ws + L.cta_start);
+  p.heads = reinterpret_cast<const dsa::CtaHead*>(ws + L.heads);
   p.CB = L.cb;
   p.cand_keys = reinterpret_cast<uint32_t*>(ws + L.cand_keys);
   p.cand_idx = reinterpret_cast<int32_t*>(ws + L.cand_idx);

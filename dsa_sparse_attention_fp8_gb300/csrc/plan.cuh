@@ -32,6 +32,16 @@ struct Item {
 constexpr int32_t kSgroupRows = -2;  // the item's row is scored into the workspace
 static_assert(sizeof(Item) == 32, "Item must stay 32 bytes");
 
+// Per scoring CTA: its item range and a copy of its first item, so that the
+// kernel reaches its first item's pages in two dependent loads, not three.
+struct CtaHead {
+  Item first;        // valid when it_begin < it_end
+  int32_t it_begin;  // = cta_start[c]
+  int32_t it_end;    // = cta_start[c + 1]
+  int32_t pad[2];
+};
+static_assert(sizeof(CtaHead) == 48, "CtaHead must stay 48 bytes");
+
 constexpr int kMaxCtas = 320;       // upper bound on the scoring grid (one CTA per SM)
 constexpr int kPlanThreads = 1024;
 constexpr int kTileKeysPlan = 128;  // keys per tile, the unit of the balance
@@ -65,8 +75,8 @@ constexpr int kBlockBins = 2048;  // level-1 bins published with every candidate
 constexpr int kScoreRowMax = 8192;   // longer rows merge faster across SMs (measured)
 
 struct WsLayout {
-  size_t header, group_prefix, cta_start, items, done, cand_count, cand_keys, cand_idx, cand_hist,
-      cand_start, row_keys, score_rows, total;
+  size_t header, group_prefix, cta_start, heads, items, done, cand_count, cand_keys, cand_idx,
+      cand_hist, cand_start, row_keys, score_rows, total;
   int max_items, max_split_groups, max_cand_blocks, cb, score_stride;
 };
 
@@ -89,6 +99,7 @@ __host__ __device__ inline WsLayout ws_layout(int T, int R, int G, int k, int n_
   L.header = o;       o = align256(o + sizeof(PlanHeader));
   L.group_prefix = o; o = align256(o + sizeof(int32_t) * (size_t)(R + 1));
   L.cta_start = o;    o = align256(o + sizeof(int32_t) * (size_t)(n_cta + 1));
+  L.heads = o;        o = align256(o + sizeof(CtaHead) * (size_t)n_cta);
   L.items = o;        o = align256(o + sizeof(Item) * (size_t)L.max_items);
   L.done = o;         o = align256(o + sizeof(int32_t) * (size_t)L.max_split_groups);
   L.cand_count = o;   o = align256(o + sizeof(int32_t) * (size_t)L.max_cand_blocks);
@@ -326,6 +337,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   const int n_items = any_overflow ? 0 : (int)item_carry;
   for (int c = threadIdx.x; c <= p.n_cta; c += kPlanThreads)
     if (any_overflow || c >= n_used) cta_start[c] = n_items;
+  __syncthreads();  // every CTA's range and items are written
+  CtaHead* heads = reinterpret_cast<CtaHead*>(p.ws + p.L.heads);
+  for (int c = threadIdx.x; c < p.n_cta; c += kPlanThreads) {
+    CtaHead h;
+    h.it_begin = cta_start[c];
+    h.it_end = cta_start[c + 1];
+    h.first = h.it_begin < h.it_end ? items[h.it_begin] : Item{};
+    h.pad[0] = h.pad[1] = 0;
+    heads[c] = h;
+  }
   for (int i = threadIdx.x; i < (int)min(sg_carry, (long long)p.L.max_split_groups); i += kPlanThreads)
     done[i] = 0;
   if (threadIdx.x == 0) {

@@ -75,6 +75,7 @@ struct ScoreParams {
   uint32_t q_bytes;  // bytes of one query-tile buffer
   const Item* items;
   const int32_t* cta_start;  // CTA c walks items [cta_start[c], cta_start[c+1])
+  const CtaHead* heads;      // per CTA: that range and its first item
   int CB;                    // capacity of one candidate block
   uint32_t* cand_keys;
   int32_t* cand_idx;
@@ -693,9 +694,7 @@ __device__ __noinline__ void merge_pieces(const Selector S, const ScoreParams& p
 }
 
 // An Item loaded where the call stands (see ld_ahead).
-__device__ __forceinline__ Item load_item(const Item* items, int i) {
-  const int4 a = ld_ahead_v4(items + i);
-  const int4 b = ld_ahead_v4(reinterpret_cast<const int4*>(items + i) + 1);
+__device__ __forceinline__ Item item_of(int4 a, int4 b) {
   Item I;
   I.r = a.x;
   I.t0 = a.y;
@@ -706,6 +705,9 @@ __device__ __forceinline__ Item load_item(const Item* items, int i) {
   I.cand_block = b.z;
   I.sgroup = b.w;
   return I;
+}
+__device__ __forceinline__ Item load_item(const Item* items, int i) {
+  return item_of(ld_ahead_v4(items + i), ld_ahead_v4(reinterpret_cast<const int4*>(items + i) + 1));
 }
 
 // sum_h wq[h] * ReLU(acc[h]) over the H accumulator columns at taddr (this
@@ -842,10 +844,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   int32_t raw_cur = -1, raw_next = -1, raw_after = -1;
   int se_cur = 0, se_next = 0, se_after = 0;
   auto load_meta = [&] {
-    it_begin = p.cta_start[blockIdx.x];
-    it_end = p.cta_start[blockIdx.x + 1];
+    const int4* head = reinterpret_cast<const int4*>(p.heads + blockIdx.x);
+    const int4 range = ld_ahead_v4(head + 2);
+    it_begin = range.x;
+    it_end = range.y;
     if (warp == 0) {
-      if (it_begin < it_end) I_cur = load_item(p.items, it_begin);
+      if (it_begin < it_end) I_cur = item_of(ld_ahead_v4(head), ld_ahead_v4(head + 1));
       if (it_begin + 1 < it_end) I_next = load_item(p.items, it_begin + 1);
       if (it_begin + 2 < it_end) I_after = load_item(p.items, it_begin + 2);
       if (it_begin < it_end) {
@@ -920,7 +924,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const int qb = item_i % p.NQ;
       const uint32_t qpar = (uint32_t)((item_i / p.NQ) & 1);
       int okv = 1;
-      if (lane == 0) okv = mbar_wait(bar_qempty + 8 * qb, qpar ^ 1, abort_flag);
+      // the first NQ query buffers are free from the start
+      if (lane == 0 && item_i >= p.NQ) okv = mbar_wait(bar_qempty + 8 * qb, qpar ^ 1, abort_flag);
       if (!__shfl_sync(0xffffffffu, okv, 0)) { ok = false; break; }
       bool q_pending = true;
       auto issue_q = [&] {
@@ -939,7 +944,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           }
         }
       };
-      if (p.q_ready || waited) issue_q();
+      // item 0's first tile is issued before its queries (the tile's pages
+      // take longer to arrive than the queries)
+      if (item_i > 0 && (p.q_ready || waited)) issue_q();
       const int ntiles = tiles_of(I);
       int32_t raw = raw_cur;
       bool ahead = false;  // the next items' loads were issued
@@ -966,9 +973,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             const int page_end = (tile_end + kPageTokens - 1) / kPageTokens * kPageTokens;
             if (seq >= p.NS || page_end > stable_end) ensure_wait();
           }
-          if (q_pending && waited) issue_q();
+          if (q_pending && (p.q_ready || waited) && (item_i > 0 || seq > 0)) issue_q();
           okv = 1;
-          if (lane == 0) okv = mbar_wait(bar_empty + 8 * stage, sphase ^ 1, abort_flag);
+          // the first NS stages are free from the start
+          if (lane == 0 && seq >= p.NS) okv = mbar_wait(bar_empty + 8 * stage, sphase ^ 1, abort_flag);
           if (!__shfl_sync(0xffffffffu, okv, 0)) { ok = false; break; }
           const uint32_t slot = scale_ring_s + (uint32_t)(seq % p.NR) * slot_bytes;
           const uint8_t* scales = p.k_cache + kPageScaleOffset + (lane & 15) * 16;
@@ -994,8 +1002,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
       }
       if (!ahead && it + 3 < it_end) I_far = load_item(p.items, it + 3);  // an item without tiles
-      if (q_pending && ok) {  // an item whose tiles all went out before the wait
-        ensure_wait();
+      if (q_pending && ok) {  // an item whose tiles all went out before its queries
+        if (!p.q_ready) ensure_wait();
         issue_q();
       }
       I_cur = I_next;
