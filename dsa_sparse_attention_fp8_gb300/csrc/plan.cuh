@@ -44,6 +44,7 @@ static_assert(sizeof(CtaHead) == 48, "CtaHead must stay 48 bytes");
 
 constexpr int kMaxCtas = 320;       // upper bound on the scoring grid (one CTA per SM)
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanSmemRequests = 4096;  // group prefix held in shared memory up to this many requests
 constexpr int kTileKeysPlan = 128;  // keys per tile, the unit of the balance
 
 struct PlanHeader {
@@ -175,6 +176,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   __shared__ unsigned long long s_max_keys;
   __shared__ int2 s_empty[kPlanThreads];  // (first row, rows) of groups that see no entry
   __shared__ int s_n_empty;
+  // the group prefix of a batch of at most kPlanSmemRequests requests, for the
+  // per-group binary search (a search over global memory is a chain of
+  // dependent loads, about half a microsecond each)
+  __shared__ int32_t s_gp[kPlanSmemRequests + 1];
+  const bool gp_in_smem = p.R <= kPlanSmemRequests;
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.L.header);
   int32_t* group_prefix = reinterpret_cast<int32_t*>(p.ws + p.L.group_prefix);
   int32_t* cta_start = reinterpret_cast<int32_t*>(p.ws + p.L.cta_start);
@@ -204,21 +210,28 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     }
     long long tot;
     const long long ex = block_exclusive_scan(groups, &tot, warp_sums);
-    if (r < p.R) group_prefix[r] = (int32_t)(groups_carry + ex);
+    if (r < p.R) {
+      group_prefix[r] = (int32_t)(groups_carry + ex);
+      if (gp_in_smem) s_gp[r] = (int32_t)(groups_carry + ex);
+    }
     groups_carry += tot;
   }
-  if (threadIdx.x == 0) group_prefix[p.R] = (int32_t)groups_carry;
+  if (threadIdx.x == 0) {
+    group_prefix[p.R] = (int32_t)groups_carry;
+    if (gp_in_smem) s_gp[p.R] = (int32_t)groups_carry;
+  }
   __syncthreads();
+  const int32_t* gp = gp_in_smem ? s_gp : group_prefix;
   const int total_groups = (int)groups_carry;
 
   auto describe = [&](int gi, int& r, int& t0, int& gcount, long long& keys) {
     int lo = 0, hi = p.R - 1;  // last r with group_prefix[r] <= gi
     while (lo < hi) {
       int mid = (lo + hi + 1) >> 1;
-      if (group_prefix[mid] <= gi) lo = mid; else hi = mid - 1;
+      if (gp[mid] <= gi) lo = mid; else hi = mid - 1;
     }
     r = lo;
-    const int g = gi - group_prefix[r];
+    const int g = gi - gp[r];
     const int qb = p.qsl[r], q = p.qsl[r + 1] - qb;
     t0 = qb + g * G;
     gcount = min(G, q - g * G);

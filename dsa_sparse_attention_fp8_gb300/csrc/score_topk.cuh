@@ -1115,40 +1115,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     bool ok = true;
     const int g_first = alt ? 0 : wg;  // this thread's rows: g_first, g_first + 2, ...
     const bool sets_up = !alt || wg == 0;  // per-row setup: warpgroup 0 for the shared decode row
-    // Items are read ahead so that starting one never waits on memory: the
-    // item after the current one is loaded one item early, and its request's
-    // metadata and first row's weight and query scale (head tid) when the
-    // current item starts.
-    struct ItemMeta {
-      int qb0, qe, seq_len;
-      float w, qs;
-    };
-    auto load_meta_of = [&](const Item& J) {
-      ItemMeta m;
-      m.qb0 = ld_ahead(p.qsl + J.r);
-      m.qe = ld_ahead(p.qsl + J.r + 1);
-      m.seq_len = ld_ahead(p.seq_lens + J.r);
-      m.w = 0.f;
-      m.qs = 0.f;
-      if (sets_up && tid < H && g_first < J.gcount) {
-        const int64_t o = (int64_t)(J.t0 + g_first) * H + tid;
-        m.w = __int_as_float(ld_ahead(reinterpret_cast<const int32_t*>(p.w + o)));
-        m.qs = __int_as_float(ld_ahead(reinterpret_cast<const int32_t*>(p.q_scale + o)));
-      }
-      return m;
-    };
-    Item I_nx{}, I_af{};
-    ItemMeta M_cur{}, M_nx{};
-    if (it_begin < it_end) I_nx = load_item(p.items, it_begin);
-    if (it_begin + 1 < it_end) I_af = load_item(p.items, it_begin + 1);
-    if (it_begin < it_end) M_nx = load_meta_of(I_nx);
     for (int it = it_begin; it < it_end && ok; ++it) {
-      const Item I = I_nx;
-      M_cur = M_nx;
-      I_nx = I_af;
-      const int qb0 = M_cur.qb0;
-      const int q_len = M_cur.qe - qb0;
-      const int seq_len = M_cur.seq_len;
+      const Item I = p.items[it];
+      const int qb0 = __ldg(p.qsl + I.r);
+      const int q_len = __ldg(p.qsl + I.r + 1) - qb0;
+      const int seq_len = __ldg(p.seq_lens + I.r);
       const int nsplit = I.split >> 16;
       const int split = I.split & 0xFFFF;
       const bool to_rows = I.sgroup == kSgroupRows;  // keys to the workspace, selected later
@@ -1156,9 +1127,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const int t = I.t0 + g;
         if (sets_up) {
           for (int h = tid; h < H; h += 128)
-            wq_all[g * H + h] = g == g_first && h == tid
-                                    ? M_cur.w * M_cur.qs
-                                    : __ldg(p.w + (int64_t)t * H + h) * __ldg(p.q_scale + (int64_t)t * H + h);
+            wq_all[g * H + h] =
+                __ldg(p.w + (int64_t)t * H + h) * __ldg(p.q_scale + (int64_t)t * H + h);
           if (tid == 0) {
             tok[g].count = 0;
             tok[g].thr = 0u;
@@ -1169,10 +1139,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
       for (int g = g_first; g < I.gcount; g += 2) clear_bins(S, hist_of(g), kBins);
       named_bar_sync(3, 256);
-      // read ahead: the next item's metadata (its Item arrived one item ago),
-      // the Item after it
-      if (it + 1 < it_end) M_nx = load_meta_of(I_nx);
-      if (it + 2 < it_end) I_af = load_item(p.items, it + 2);
       const int ntiles = (I.k1 - I.k0 + KS - 1) / KS;
       const int units = ntiles * p.BPS;  // 128-key blocks of the item
       const bool may_fill = (I.k1 - I.k0) > p.C;
