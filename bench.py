@@ -103,10 +103,20 @@ def read_peaks() -> dict:
             "source": "fallback"}
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and with whitespace collapsed, so that an
+    edit to comments or layout leaves the hash (and the counters taken on the
+    same code) valid."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        h.update((ROOT / "dsa_sparse_attention_fp8_gb300" / "csrc" / name).read_bytes())
+        text = (ROOT / "dsa_sparse_attention_fp8_gb300" / "csrc" / name).read_text()
+        h.update(_code_only(text).encode())
     return h.hexdigest()[:16]
 
 

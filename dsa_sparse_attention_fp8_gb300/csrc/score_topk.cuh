@@ -883,13 +883,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // The whole warp walks the tiles.  Per tile, lane 0 waits for the stage and
-    // issues the two key-page copies (each bulk-copy issue costs the thread
-    // ~100 cycles, so it issues nothing else); every lane copies 16 bytes of
-    // the two pages' scales (lanes 0-15 the first page, 16-31 the second) into
-    // the tile's slot of the scale ring with cp.async, zero-filled for a page
-    // outside the pool or the key range, and arrives on the stage's full
-    // barrier when its copy lands.  Tile s uses scale slot s % NR with
+    // The whole warp walks the tiles.  Per tile, lane 0 waits for the stage
+    // (from the NS-th tile on; the first NS stages start free); every lane
+    // copies 16 bytes of the tile's pages' scales (lanes 0-15 one page, 16-31
+    // the next) into the tile's slot of the scale ring with cp.async,
+    // zero-filled for a page outside the pool or the key range, and arrives on
+    // the stage's full barrier when its copy lands; then the lanes that hold
+    // the tile's page ids issue one key-page copy each.  Issuing a tile costs
+    // the warp about 1,000-1,400 cycles, most of it in the barrier and
+    // cp.async instructions, so the warp does nothing else.  Tile s uses scale slot s % NR with
     // NR >= NS + NB: the producer reaches tile s only after the epilogue has
     // released tile s - NS - NB, so a slot is never overwritten while read.
     // The page ids of 16 tiles (32 pages) come from one coalesced load,
