@@ -66,3 +66,25 @@ def test_non_zero_ranks_print_nothing_and_exit_0(extra):
                          env=env, capture_output=True, text=True, timeout=300)
     assert res.returncode == 0, res.stderr[-2000:]
     assert res.stdout.strip() == ""
+
+
+def test_committed_counters_follow_the_kernel_code():
+    """The ncu traffic figure in profiles/ is used only while the kernel
+    sources hash to the value recorded beside it; comments and layout do not
+    count, code does."""
+    sys.path.insert(0, str(ROOT))
+    import bench
+    a = "int f(int x) {  // a comment\n  return x + 1; /* another */\n}\n"
+    b = "int f(int x) {\n    return x + 1;\n}  // reworded comment\n"
+    c = "int f(int x) {\n  return x + 2;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    h = bench.kernel_source_hash()
+    assert len(h) == 16 and h == bench.kernel_source_hash()
+    text = (ROOT / "profiles" / "score_topk_batched_decode.md").read_text()
+    import re
+    m = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    assert m is not None
+    # valid summary -> its figure; stale summary -> no figure (never a wrong one)
+    got = bench.profiled_traffic("batched_decode")
+    assert (got is not None) == (m.group(1) == h)
