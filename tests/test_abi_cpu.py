@@ -121,3 +121,20 @@ def test_stack_rejects_bad_schedules(lib):
     assert lib.dsa_layer_stack_run(3, b"FSS", 1, 2, empty, 0, 64, fake, fake, 1, fake, 4, 16,
                                    2048, fake, 4, None, None, fake, 1 << 30, None, None) == 0
     assert lib.dsa_last_launch_count() == 0
+
+
+def test_workspace_rows_sizing(lib):
+    """max_ctx in (0, 8192] adds T rows of max_ctx rounded up to 128 keys (4 B
+    each) plus T key counts (rounded to 256 B); beyond 8192, or rows over
+    256 MB in all, adds nothing (the batch keeps the in-kernel selection)."""
+    from dsa_sparse_attention_fp8_gb300 import binding
+    base = binding.workspace_bytes(64, 64, 64, 2048)
+    extra = lambda mc, T=64: binding.workspace_bytes(T, 64, T, 2048, max_ctx=mc) - \
+        binding.workspace_bytes(T, 64, T, 2048)
+    assert extra(0) == 0 and extra(-5) == 0
+    for mc, stride in ((1, 128), (128, 128), (129, 256), (1000, 1024), (8192, 8192)):
+        assert extra(mc) == 64 * stride * 4 + 256, mc
+    assert extra(8193) == 0 and extra(1 << 20) == 0
+    assert extra(8192, T=8192) == 8192 * 8192 * 4 + 8192 * 4          # exactly 256 MB of rows
+    assert extra(8192, T=8193) == 0                                    # above 256 MB: none
+    assert base == binding.workspace_bytes(64, 64, 64, 2048, max_ctx=0)
