@@ -1,19 +1,24 @@
 """Benchmark of the DSA lightning-indexer step on GB300.
 
-Default workload: batched decode -- 64 requests with one new token each,
-contexts uniform in [1024, 8192], H = 64 indexer heads, index_topk = 2048,
-4-layer stack (all F).  One step = one pass of the whole path over the batch:
-for every F layer, write the new keys into the paged FP8 cache, score every
-query row against its request's cached keys, select the top-k into the shared
-buffer (S layers launch nothing).  Metric: query-key pairs per second
-(sum over F layers of the keys each query row sees, divided by step time).
+Headline workload: long-context decode -- 4 requests with 1,048,576 cached
+tokens and one new token each, H = 64 indexer heads, index_topk = 2048, a
+78-layer stack with 21 F layers (explicit seeded pattern).  One step = one
+pass of the whole path over the batch: for every F layer, write the new keys
+into the paged FP8 cache, score every query row against its request's cached
+keys, select the top-k into the shared buffer (S layers launch nothing).
+Metric: query-key pairs per second (sum over F layers of the keys each query
+row sees, divided by step time).  `per_config` repeats the measurement on
+every workload of the suite (tiny prefill, batched decode, prefix-hit
+chunked prefill, mixed batch, long-context decode), each at full size.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload ID] [--configs 0,1,2,3,4|none]
 
 `--impl reference` times the FP64 CPU oracle (the correctness reference) on a
 bounded sample of the same workload, on this machine's host cores.
-Under torchrun each rank runs its own batch (weak scaling, no data-path
-collective); rank 0 prints one JSON line.
+`--gpus N` (N > 1) starts N ranks itself unless it already runs under a
+launcher; each rank runs its own batch (weak scaling, no data-path
+collective) and rank 0 prints one JSON line.
 """
 
 from __future__ import annotations
@@ -52,13 +57,17 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=1, help="workload id (1 = batched decode)")
+    ap.add_argument("--workload", type=int, default=None,
+                    help="headline workload id (default 4 = long-context decode)")
+    ap.add_argument("--configs", default="0,1,2,3,4",
+                    help="workloads measured for per_config (comma list, or 'none')")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--scale", type=float, default=1.0,
                     help="context/row scale of the workload (1 = its stated size; smaller for "
                          "profiling captures)")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--cpu-budget-per-config-s", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bf16", action="store_true",
                     help="BF16 keys and queries, quantised by the cache-write launch")
@@ -191,11 +200,13 @@ class ClockSampler:
 # CPU oracle legs
 # ----------------------------------------------------------------------------
 
-def oracle_sample_setup(wl, layer=0):
-    """Oracle state for timing: the page pool holding every cached prefix (not timed)."""
+def oracle_sample_setup(wl, layer=0, requests=None):
+    """Oracle state for timing (not timed): the page pool holding the cached
+    prefix of the given requests (all by default), the step's keys and
+    quantised queries."""
     import oracle as O
     cache = np.zeros((wl.num_pages, O.PAGE_BYTES), np.uint8)
-    for r in range(wl.R):
+    for r in (range(wl.R) if requests is None else sorted(set(requests))):
         E = int(wl.prefix_entries[r])
         if E:
             O.write_k_cache(cache, wl.k_prefix(layer, r),
@@ -219,34 +230,53 @@ def oracle_time_rows(wl, state, rows):
     return pairs, dt
 
 
+def sample_rows(wl, max_pairs: int = 4_000_000):
+    """Query rows in order from row 0, as many as keep the sample's pairs (and
+    so its oracle time) bounded, at least one; and their requests."""
+    import oracle as O
+    req, pos = O.token_positions(wl.query_start_loc, wl.seq_lens)
+    rows, pairs = [], 0
+    for t in range(wl.T):
+        n = int(O.visible_entries(pos[t], wl.compress_ratio))
+        if rows and pairs + n > max_pairs:
+            break
+        rows.append(t)
+        pairs += n
+    return rows, sorted({int(req[t]) for t in rows})
+
+
 def cpu_cores() -> int:
     return len(os.sched_getaffinity(0))
 
 
 def cpu_baseline(wl, budget_s: float) -> dict:
-    """The oracle on layer 0 of the same workload, rows in order (wrapping to
-    row 0 again) until about `budget_s` seconds of CPU work are done."""
-    state = oracle_sample_setup(wl)
+    """The oracle on layer 0 of the same workload, on a bounded prefix of its
+    query rows (see sample_rows), repeated in chunks until about `budget_s`
+    seconds of CPU work are done."""
+    rows, reqs = sample_rows(wl)
+    state = oracle_sample_setup(wl, requests=reqs)
     done_pairs, done_s, n = 0, 0.0, 0
-    chunk = max(1, wl.T // 16)
+    chunk = max(1, len(rows) // 16)
     while done_s < budget_s:
-        a = n % wl.T
-        rows = list(range(a, min(wl.T, a + chunk)))
-        p, dt = oracle_time_rows(wl, state, rows)
+        a = n % len(rows)
+        sel = rows[a:a + chunk]
+        p, dt = oracle_time_rows(wl, state, sel)
         done_pairs += p
         done_s += dt
-        n += len(rows)
+        n += len(sel)
     return {"value": done_pairs / done_s, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"layer 0, {n} query rows in order ({n / wl.T:.2f} x the {wl.T}-row batch; "
-                      f"{done_pairs} pairs, {done_s:.1f} s; numpy FP64, BLAS threads per the host default)"}
+            "sample": f"layer 0, {n} query rows cycling over rows 0..{len(rows) - 1} of the "
+                      f"{wl.T}-row batch ({done_pairs} pairs, {done_s:.1f} s; numpy FP64, BLAS "
+                      f"threads per the host default)"}
 
 
 def run_reference(args, wl):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    state = oracle_sample_setup(wl)
-    rows = list(range(min(wl.T, 8)))
+    rows, reqs = sample_rows(wl, max_pairs=1_200_000)
+    state = oracle_sample_setup(wl, requests=reqs)
+    rows = rows[:8]
     for _ in range(args.warmup):
         oracle_time_rows(wl, state, rows)
     pairs = secs = 0.0
@@ -256,10 +286,11 @@ def run_reference(args, wl):
         secs += dt
     value = pairs / secs
     sample = (f"layer 0, query rows 0..{len(rows) - 1} of {wl.T} per step "
-              f"({int(pairs / args.steps)} pairs per step)")
+              f"({int(pairs / max(1, args.steps))} pairs per step)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": wl.name, **{k: v for k, v in wl.describe().items()
                                                                 if k != "workload"}},
@@ -441,7 +472,8 @@ def run_sparse_mla(args, wl):
             "kernel": "sparse_mla_kernel", "kernel_ms": kms, "algorithmic_flops": flops,
             "algorithmic_bytes": bytes_, "peak_source": peaks["source"] + " bf16",
             "executed_flops_note": "each of the 4 CTAs of a row recomputes QK^T: executed tensor "
-                                   "work is (4*576 + 512) / (576 + 512) = 2.59x the algorithmic",
+                                   "work is (4*576 + 512) / (576 + 512) = 2.59x the algorithmic; "
+                                   "each CTA gathers every selected record itself",
             "other_bound": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
                             "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}}
     line = {
@@ -472,34 +504,78 @@ def run_sparse_mla(args, wl):
 
 
 # ----------------------------------------------------------------------------
+# FP8 dense tensor peak (measured here, next to the driver's BF16 and HBM peaks)
+# ----------------------------------------------------------------------------
+
+def fp8_peak_probe(dev, sustain_s: float = 2.0) -> dict:
+    """Dense E4M3 GEMM rate of this GPU through cuBLASLt (torch._scaled_mm,
+    8192^3, FP32 accumulate, BF16 out): best of 10 back-to-back launches
+    (burst) and the mean over a loop of about `sustain_s` seconds (sustained).
+    Falls back to the measured BF16 rate x 2 (the nominal FP8:BF16 dense
+    ratio) when the probe cannot run."""
+    import torch
+    peaks = read_peaks()
+    fallback = {"fp8_tflops": 2.0 * peaks["bf16_tflops"], "fp8_tflops_sustained": None,
+                "source": f"{peaks['source']} bf16 x 2 (nominal fp8:bf16 dense ratio)"}
+    try:
+        n = 8192
+        g = torch.Generator(device=dev).manual_seed(0)
+        a = torch.randn((n, n), device=dev, generator=g).to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), device=dev, generator=g).to(torch.float8_e4m3fn)
+        one = torch.ones((), device=dev, dtype=torch.float32)
+
+        def mm():
+            return torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+        for _ in range(3):
+            mm()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            mm()
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        flops = 2.0 * n ** 3
+        reps = max(10, int(sustain_s * 1e3 / best))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            mm()
+        e1.record()
+        e1.synchronize()
+        sus = e0.elapsed_time(e1) / reps
+        del a, b
+        return {"fp8_tflops": flops / (best * 1e-3) / 1e12,
+                "fp8_tflops_sustained": flops / (sus * 1e-3) / 1e12,
+                "source": "measured here: torch._scaled_mm e4m3 8192^3 (cuBLASLt), burst best of 10, "
+                          f"sustained mean of {reps}"}
+    except Exception as e:  # noqa: BLE001 -- any failure falls back to the nominal ratio
+        fallback["probe_error"] = f"{type(e).__name__}: {e}"[:200]
+        return fallback
+
+
+# ----------------------------------------------------------------------------
 # GPU leg
 # ----------------------------------------------------------------------------
 
-def main():
-    args = parse()
-    rank, world, local = dist_env()
-    wl = synth.make_workload(args.workload, seed=args.seed + rank, scale=args.scale)
-    if args.sparse_mla:
-        run_sparse_mla(args, wl)
-        return
-    if args.impl == "reference":
-        run_reference(args, wl)
-        return
+HEADLINE_WORKLOAD = 4           # long-context decode: the largest single-GPU workload
+PER_CONFIG_WORKLOADS = (0, 1, 2, 3, 4)
 
+
+def measure_workload(args, wid: int, dev, peaks: dict, fp8: dict, world: int, rank: int,
+                     cpu_budget_s: float) -> dict:
+    """Stage workload `wid`, time `args.steps` graph-replayed steps (L2 flushed
+    between them), time every scoring + selection launch, the end-to-end path
+    from pinned host buffers, and (rank 0, one rank) the oracle on a bounded
+    sample.  Returns the workload's JSON fields."""
     import torch
-    from dsa_sparse_attention_fp8_gb300 import _build, binding, staging
+    from dsa_sparse_attention_fp8_gb300 import binding, staging
     from dsa_sparse_attention_fp8_gb300.step import IndexerStep
 
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
-    _build.build_library(quiet=True)
-    dev = torch.device("cuda", torch.cuda.current_device())
-
-    # ---- stage: caches with every cached prefix, this step's inputs
+    wl = synth.make_workload(wid, seed=args.seed + rank, scale=args.scale)
     meta = staging.stage_metadata(wl, dev)
     full = [binding.layer_is_full(l, wl.pattern, wl.freq, wl.offset) for l in range(wl.num_layers)]
     caches, host_layers = [], {}
@@ -515,6 +591,7 @@ def main():
         else:
             ins = (io["k"], io["q_fp8"], io["q_scale"], io["w"])
         host_layers[l] = tuple(t.cpu().pin_memory() for t in ins)
+        del io
     step = IndexerStep(num_layers=wl.num_layers, pattern=wl.pattern, freq=wl.freq,
                        offset=wl.offset, H=wl.H, index_topk=wl.index_topk, T=wl.T, R=wl.R,
                        max_blocks=wl.max_blocks, num_pages=wl.num_pages,
@@ -564,8 +641,8 @@ def main():
             ev1[i].record(stream)
             ev1[i].synchronize()
         torch.cuda.synchronize()
-        # the same steps again with events around every scoring kernel (the
-        # roofline's per-launch durations)
+        # the same steps again with events around every layer's scoring +
+        # selection launches (the roofline's per-launch durations)
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
             step.run(timed=True)
@@ -580,8 +657,6 @@ def main():
         torch.distributed.barrier()
     step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     if timing_failed:
-        # the graph did not record the per-kernel events: time the same kernels
-        # in eager steps right after the timed region
         score_ms, kernel_timing = [], "events around each launch, eager steps after the timed region"
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
@@ -609,9 +684,11 @@ def main():
 
     (ms, e2e_ms), total_pairs = reduce_over_ranks([ms, e2e_ms], pairs_per_step, world, dev)
     clk = clocks.summary()
+    uses_rows = step.uses_row_selection()
+    del step, caches, flush
+    torch.cuda.empty_cache()
 
-    # ---- roofline of the dominant kernel (scoring + top-k), per launch
-    peaks = read_peaks()
+    # ---- roofline of the dominant kernel pair (scoring + top-k selection), per layer
     k_ms = sum(score_ms) / len(score_ms)
     rows_bytes = wl.T * (wl.H * (128 + 4 + 4) + wl.index_topk * 4)   # q, q_scale, w in; top-k out
     # every key (cache entry) of a request is read once, whatever the number of
@@ -619,48 +696,126 @@ def main():
     key_bytes = float(wl.entries[wl.q_lens > 0].astype(np.int64).sum()) * BYTES_PER_PAIR
     alg_bytes = key_bytes + rows_bytes
     achieved = alg_bytes / (k_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(wl.name)
-    # FP8 tensor peak: the measured BF16 GEMM rate times the nominal FP8:BF16
-    # dense ratio (4.5 : 2.25 PFLOP/s)
-    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    kernel = "score_topk_kernel + rows_topk_kernel" if uses_rows else "score_topk_kernel"
+    traffic = profiled_traffic(wl.name) if not uses_rows else None
+    fp8_peak = fp8["fp8_tflops"]
     alg_flops = wl.pairs_per_full_layer * 2.0 * wl.H * 128
     tflops = alg_flops / (k_ms * 1e-3) / 1e12
     hbm = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-           "frac": achieved / peaks["hbm_gbs"], "traffic": traffic}
+           "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+           "peak_source": f"{peaks['source']} copy (MEASURED_PEAKS.json hbm_gbs)"}
     tensor = {"bound": "tensor", "achieved": tflops, "peak": fp8_peak, "unit": "TFLOP/s",
               "frac": tflops / fp8_peak, "traffic": traffic,
-              "peak_note": f"{peaks['source']} bf16 x 2 (nominal fp8:bf16 dense ratio)"}
+              "peak_source": f"fp8 e4m3 dense, burst: {fp8['source']}"}
     # HBM-bound unless the work's FP8 FLOP per algorithmic byte exceed the
     # machine balance (peak FLOP/s over peak bytes/s): prefill chunks reuse each
     # key across many rows, decode batches (also with a few MTP rows) do not
     prefill = alg_flops / alg_bytes > fp8_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     roof = dict(tensor if prefill else hbm)
-    roof.update({"kernel": "score_topk_kernel", "kernel_ms": k_ms, "algorithmic_bytes": alg_bytes,
+    roof.update({"kernel": kernel, "kernel_ms": k_ms, "algorithmic_bytes": alg_bytes,
                  "algorithmic_flops": alg_flops, "kernel_timing": kernel_timing,
-                 "peak_source": peaks["source"],
                  "other_bound": {k: v for k, v in (hbm if prefill else tensor).items()
                                  if k != "traffic"}})
-
-    line = {
-        "metric": METRIC, "value": total_pairs / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8_e4m3 (fp32 accumulate)", "data": "synthetic",
+    res = {
+        "workload": wl.name, "value": total_pairs / (ms * 1e-3), "ms_per_step": ms,
+        "tokens_per_s": wl.T * n_full * world / (ms * 1e-3),
         "config": {"workload": wl.name, **{k: v for k, v in wl.describe().items() if k != "workload"},
                    "pairs_per_step": pairs_per_step, "full_layers": n_full,
                    "cuda_graph": not args.no_graph, "l2": "flushed between timed steps",
                    "inputs": ("bf16 keys and queries, quantised in the cache-write launch"
                               if args.bf16 else "fp32 keys, e4m3 queries + fp32 scales"),
                    "parallelism": f"replicas x{world}"},
-        "tokens_per_s": wl.T * n_full * world / (ms * 1e-3),
         "roofline": roof,
         "e2e": {"value": total_pairs / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "clocks": clk,
         "gpu_launches": launches * args.steps,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget_s)
+    if rank == 0 and world == 1 and cpu_budget_s > 0:
+        res["cpu_baseline"] = cpu_baseline(wl, cpu_budget_s)
+    return res
+
+
+def spawn_replicas(args):
+    """`--gpus N` with N > 1 outside a launcher: run this command as N local
+    ranks under torch.distributed.run (one replica per GPU) and return its exit
+    code; None when this process is already a rank or N == 1."""
+    if args.gpus <= 1 or "WORLD_SIZE" in os.environ:
+        return None
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+           f"--master-port={port}", str(Path(__file__).resolve()), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
+def main():
+    args = parse()
+    rc = spawn_replicas(args)
+    if rc is not None:
+        sys.exit(rc)
+    rank, world, local = dist_env()
+    if world != args.gpus:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; run with matching "
+                 "values (or without a launcher: --gpus N starts N ranks itself)")
+    wid = HEADLINE_WORKLOAD if args.workload is None else args.workload
+    if args.sparse_mla:
+        run_sparse_mla(args, synth.make_workload(1 if args.workload is None else args.workload,
+                                                 seed=args.seed + rank, scale=args.scale))
+        return
+    if args.impl == "reference":
+        run_reference(args, synth.make_workload(wid, seed=args.seed + rank, scale=args.scale))
+        return
+
+    import torch
+    from dsa_sparse_attention_fp8_gb300 import _build
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    _build.build_library(quiet=True)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks = read_peaks()
+    fp8 = fp8_peak_probe(dev)
+    budget = 0.0 if args.no_cpu_baseline else args.cpu_budget_s
+
+    head = measure_workload(args, wid, dev, peaks, fp8, world, rank, budget)
+    per_config = {}
+    configs = [] if args.configs.strip() in ("", "none") else [int(c) for c in args.configs.split(",")]
+    for c in configs:
+        if c == wid:
+            r = head
+        else:
+            r = measure_workload(args, c, dev, peaks, fp8, world, rank,
+                                 min(budget, args.cpu_budget_per_config_s))
+        per_config[r["workload"]] = {k: r[k] for k in ("value", "tokens_per_s", "ms_per_step",
+                                                       "roofline", "e2e", "cpu_baseline", "config")
+                                     if k in r}
+
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3 (fp32 accumulate)", "data": "synthetic",
+        "config": head["config"],
+        "tokens_per_s": head["tokens_per_s"],
+        "roofline": head["roofline"],
+        "e2e": head["e2e"],
+        "clocks": head["clocks"],
+        "gpu_launches": head["gpu_launches"],
+        "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
+                  "source": peaks["source"], **fp8},
+    }
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    if per_config:
+        line["per_config"] = per_config
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -106,6 +106,7 @@ int env_int(const char* name, int dflt, int lo, int hi) {
 // ---------------------------------------------------------------- launch shape
 struct ScoreShape {
   int G, C, NS, NB, NQ, NR, BPS, n_max, q_box_per_token;
+  int lg_nb, lg_nr, lg_bps;
   uint32_t q_bytes;
   size_t smem_bytes;
   dsa::ScoreParams offs;  // only the off_* fields are filled
@@ -146,6 +147,12 @@ int choose_group(int T, int R, int H, int k) {
 
 size_t up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+int floor_log2(int x) {
+  int l = 0;
+  while ((2 << l) <= x) ++l;
+  return l;
+}
+
 bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   s->G = choose_group(T, R, H, k);
   s->C = candidate_capacity(k, s->G, s->G == 1);
@@ -155,9 +162,12 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   // still holds 4 stage accumulators; halves the per-key barrier and issue work
   s->BPS = (s->G == 1 && dsa::kTmemCols / (2 * s->n_max) >= 4) ? 2 : 1;
   if (env_int("DSA_STAGE_KEYS", 256, 128, 256) < 256) s->BPS = 1;
-  s->NB = dsa::kTmemCols / (s->BPS * s->n_max);
-  if (s->NB > dsa::kMaxAccBufs) s->NB = dsa::kMaxAccBufs;
+  s->lg_bps = s->BPS == 2 ? 1 : 0;
+  // accumulator buffers: a power of two, so the kernel's ring positions are masks
+  s->NB = std::min(dsa::kTmemCols / (s->BPS * s->n_max), dsa::kMaxAccBufs);
   if (s->NB < 2) return false;
+  s->lg_nb = floor_log2(s->NB);
+  s->NB = 1 << s->lg_nb;
   s->q_bytes = (uint32_t)up((size_t)s->G * H * 128, 1024);
   s->NQ = s->q_bytes <= 16384 ? 2 : 1;
   size_t fixed = 0;
@@ -168,16 +178,20 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
   fixed += (size_t)s->G * dsa::kBins * 4;
   fixed += up(sizeof(dsa::Misc), 16);
   fixed += (2 * dsa::kMaxStages + 2 * dsa::kMaxAccBufs + 2 * dsa::kMaxQBufs + 1) * 8;
-  fixed += (size_t)s->NB * s->BPS * dsa::kScaleSlotBytes;  // scale ring: NS + NB slots
-  const size_t per_stage = (size_t)s->BPS * (dsa::kStageBytes + dsa::kScaleSlotBytes);
+  const size_t stage_bytes = (size_t)s->BPS * dsa::kStageBytes;
+  const size_t slot_bytes = (size_t)s->BPS * dsa::kScaleSlotBytes;
   const size_t budget = kSmemLimit - 1024 - 64;
-  if (fixed + 2 * per_stage > budget) return false;
-  s->NS = (int)((budget - fixed) / per_stage);
-  if (s->NS > dsa::kMaxStages) s->NS = dsa::kMaxStages;
-  s->NR = s->NS + s->NB;
+  // stages, and a scale ring of NR >= NS + NB slots, NR a power of two
+  auto ring = [&](int ns) { return 1 << floor_log2(2 * (ns + s->NB) - 1); };
+  int ns = dsa::kMaxStages;
+  while (ns >= 2 && fixed + ns * stage_bytes + ring(ns) * slot_bytes > budget) --ns;
+  if (ns < 2) return false;
+  s->NS = ns;
+  s->NR = ring(ns);
+  s->lg_nr = floor_log2(s->NR);
   size_t o = 0;  // stages first: every key stage starts on a 1024-byte boundary
-  s->offs.off_stage = (uint32_t)o; o += (size_t)s->NS * s->BPS * dsa::kStageBytes;
-  s->offs.off_scale = (uint32_t)o; o += (size_t)s->NR * s->BPS * dsa::kScaleSlotBytes;
+  s->offs.off_stage = (uint32_t)o; o += (size_t)s->NS * stage_bytes;
+  s->offs.off_scale = (uint32_t)o; o += (size_t)s->NR * slot_bytes;
   s->offs.off_q = (uint32_t)o;     o += (size_t)s->NQ * s->q_bytes;
   s->offs.off_ckeys = (uint32_t)o; o += up((size_t)s->G * s->C * 4, 16);
   s->offs.off_cidx = (uint32_t)o;  o += up((size_t)s->G * s->C * 4, 16);
@@ -362,6 +376,9 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   p.NQ = s.NQ;
   p.NR = s.NR;
   p.BPS = s.BPS;
+  p.lg_bps = s.lg_bps;
+  p.lg_nb = s.lg_nb;
+  p.lg_nr = s.lg_nr;
   p.ratio = b.ratio;
   p.q_bytes = s.q_bytes;
   p.n_max = s.n_max;
@@ -475,14 +492,42 @@ __global__ void copy_rows_kernel(const int4* __restrict__ src, int4* __restrict_
 // file-scope device array, so every GPU that loads this library holds it
 // until the process exits.  Host code must not use the symbol itself as a
 // device address (on the host it is only a stand-in): the real address is
-// looked up once per device with cudaGetSymbolAddress while that device is
-// current, and cached.
+// looked up with cudaGetSymbolAddress while the device is current, on the
+// first call on that device, and cached together with the identity of the
+// device's current context, so that a call after a device reset (a new
+// context, in which the array may sit elsewhere) looks it up again.
 constexpr size_t kStaticWorkspaceBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_static_ws_mutex;
 void* g_static_ws_ptr[kMaxDevices] = {};
+unsigned long long g_static_ws_ctx[kMaxDevices] = {};
+
+// Unique id of the calling thread's current context (0 if unavailable).
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 int static_workspace(void** out) {
   int dev = 0;
@@ -490,13 +535,20 @@ int static_workspace(void** out) {
   if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(DSA_ERR_UNSUPPORTED, "device %d >= %d", dev, kMaxDevices);
   std::lock_guard<std::mutex> lock(g_static_ws_mutex);
+  // the runtime makes the device's primary context current on first use
   if (!g_static_ws_ptr[dev]) {
+    e = cudaFree(nullptr);
+    if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "device %d: %s", dev, cudaGetErrorString(e));
+  }
+  const unsigned long long ctx = current_context_id();
+  if (!g_static_ws_ptr[dev] || g_static_ws_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_static_workspace);
     if (e != cudaSuccess || !p)
       return fail(DSA_ERR_CUDA, "cudaGetSymbolAddress of the built-in workspace: %s",
                   cudaGetErrorString(e));
     g_static_ws_ptr[dev] = p;
+    g_static_ws_ctx[dev] = ctx;
   }
   *out = g_static_ws_ptr[dev];
   return DSA_OK;
@@ -574,12 +626,12 @@ int stack_run(int num_layers, const char* pattern, int freq, int offset, const I
       // the cache write, a plain launch, lies between the plan and this launch
       rc = launch_score_layer(b, s, lq, &launches, true, QueriesAreInputs<IO>::value);
       if (rc) break;
+      rc = launch_rows_topk(b, s, &launches);
+      if (rc) break;
       if (io.score_end && record_event(io.score_end, b.st) != cudaSuccess) {
         rc = fail(DSA_ERR_CUDA, "recording score_end of layer %d failed", l);
         break;
       }
-      rc = launch_rows_topk(b, s, &launches);
-      if (rc) break;
     }
     if (per_layer_topk_out && per_layer_topk_out[l]) {
       const int64_t bytes = (int64_t)b.T * b.k * 4;
@@ -751,17 +803,21 @@ int dsa_indexer_score_topk_no_alloc(const uint8_t* q_fp8, const float* q_scale, 
                                     int32_t* topk_buffer, int max_num_batched_tokens,
                                     int32_t* dev_status, dsa_stream_t stream) {
   g_last_launches = 0;
+  // the same argument checks, in the same order, as dsa_indexer_score_topk
+  // (a stand-in workspace of the built-in size: its address is not used)
+  Batch b{T, H, R, max_blocks, index_topk, max_num_batched_tokens, num_pages, query_start_loc,
+          seq_lens, block_table, topk_buffer, reinterpret_cast<void*>(uintptr_t(256)),
+          ~size_t(0), dev_status, (cudaStream_t)stream, 1};
+  int rc = check_batch(b);
+  if (rc) return rc;
   const size_t need = dsa_indexer_workspace_bytes(T, H, R, 0, index_topk);
-  if (need == 0)
-    return fail(DSA_ERR_UNSUPPORTED, "no workspace size for T=%d, H=%d, R=%d, index_topk=%d", T,
-                H, R, index_topk);
   if (need > kStaticWorkspaceBytes)
     return fail(DSA_ERR_WORKSPACE_TOO_SMALL,
                 "this batch needs %zu bytes of workspace; the built-in workspace holds %zu "
                 "(use dsa_indexer_score_topk with a caller-provided workspace)",
                 need, kStaticWorkspaceBytes);
   void* ws = nullptr;
-  const int rc = static_workspace(&ws);
+  rc = static_workspace(&ws);
   if (rc) return rc;
   return dsa_indexer_score_topk(q_fp8, q_scale, w, T, H, k_cache, num_pages, query_start_loc,
                                 seq_lens, R, block_table, max_blocks, index_topk, topk_buffer,
@@ -924,19 +980,12 @@ int dsa_sparse_mla_attention(const void* q, int T, int Hq, const uint8_t* kv_cac
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   p.status = dev_status;
-  // the four quarter CTAs of a row form one cluster
+  // four CTAs per row, one per 128-wide quarter of the output
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(T * dsa::kMlaCluster));
+  cfg.gridDim = dim3((unsigned)(T * dsa::kMlaQuarters));
   cfg.blockDim = dim3(dsa::kMlaThreads);
   cfg.dynamicSmemBytes = dsa::kMlaSmemBytes;
   cfg.stream = (cudaStream_t)stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = dsa::kMlaCluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, dsa::sparse_mla_kernel, p);
   if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "sparse_mla_kernel launch: %s", cudaGetErrorString(e));
   g_last_launches = 1;

@@ -39,12 +39,10 @@
 //               and O += P V (N = 128 dimensions, K = 64 tokens);
 //   warp 11     loader: the selected records into a ring of raw half tiles.
 //
-// Gathering 656-byte records from random pages runs at ~8 bytes per cycle
-// per SM however the copies are issued, so the four CTAs of a row form a
-// thread-block cluster and gather each record once: CTA c copies the records
-// n = c (mod 4) of every half tile with a bulk copy multicast to all four,
-// and a raw slot is refilled only after every CTA of the cluster has
-// converted it (each one arrives on the slot's empty barrier in every CTA).
+// Each CTA gathers the records of its row's half tiles into its own shared
+// memory with one bulk copy per record (the four CTAs of a row read the same
+// records; three of the four reads hit L2), and a raw slot is refilled once
+// its own converters have dequantised it.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -129,7 +127,7 @@ constexpr int kMlaThreads = (kMlaSoftmaxWarps + kMlaProducerWarps + 2) * 32;
 constexpr int kMlaProducers = kMlaProducerWarps * 32;
 constexpr int kMlaMmaWarp = kMlaSoftmaxWarps + kMlaProducerWarps;
 constexpr int kMlaLoaderWarp = kMlaMmaWarp + 1;
-constexpr int kMlaCluster = 4;                       // the four quarter CTAs of a query row
+constexpr int kMlaQuarters = 4;                      // CTAs per query row (128 output dimensions each)
 // tensor-memory columns
 constexpr uint32_t kMlaColO = 0;       // 128 FP32: this CTA's quarter of the output
 constexpr uint32_t kMlaColS = 128;     // 64 FP32: the score tile
@@ -199,7 +197,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
   const uint32_t raw_s = smem_u32(raw);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x >> 2, qd = blockIdx.x & 3;
+  const int t = blockIdx.x / kMlaQuarters, qd = blockIdx.x % kMlaQuarters;
   const int r = find_request(p.qsl, p.R, t);
   const int seq_len = __ldg(p.seq_lens + r);
 
@@ -211,7 +209,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
     }
     for (int i = 0; i < kMlaRawStages; ++i) {
       mbar_init(smem_u32(&sm->rfull[i]), 1);
-      mbar_init(smem_u32(&sm->rempty[i]), kMlaCluster);
+      mbar_init(smem_u32(&sm->rempty[i]), 1);
     }
     mbar_init(smem_u32(&sm->sfull), 1);
     mbar_init(smem_u32(&sm->sfree), 128);
@@ -274,8 +272,6 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // every CTA's barriers exist before any multicast copy targets them
-  const uint32_t crank = cluster_ctarank();
   const uint32_t tmem = sm->tmem_base;
   const int n_valid = sm->n_valid;
   const int n_tiles = (n_valid + kMlaTile - 1) / kMlaTile;
@@ -453,12 +449,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
         }
         named_bar_sync(2, kMlaProducers);  // every converter is done with raw slot rb
         good = sm->conv_fail == 0;
-        if (pt < kMlaCluster && g < n_halves && good) {
-          // the slot may be refilled: tell the loader of every CTA of the
-          // cluster (one thread each; the slot's reads are complete, nothing
-          // to publish)
-          mbar_arrive_cluster_relaxed(cluster_map(smem_u32(&sm->rempty[rb]), (uint32_t)pt));
-        }
+        // the slot may be refilled (its reads are complete)
+        if (pt == 0 && g < n_halves && good) mbar_arrive(smem_u32(&sm->rempty[rb]));
       }
       if (!good) { ok = false; break; }
       fence_proxy_async_smem();
@@ -467,8 +459,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
     if (!ok) sm->abort = 1;
   } else if (warp == kMlaLoaderWarp) {
     // ================================================================ loader
-    // Each CTA expects every record of a half tile (all four copy into it)
-    // and copies its own share, records n = rank (mod 4), to all four.
+    // One bulk copy per selected record of the half tile, by the lane that
+    // holds its slot.
     bool ok = true;
     int issued = 0;
     for (int g = 0; g < n_halves && ok; ++g) {
@@ -487,11 +479,11 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
         mbar_arrive_expect_tx(bar, (uint32_t)__popc(live) * (uint32_t)kMlaRecBytes);
       }
       __syncwarp();
-      if (sl >= 0 && (uint32_t)(lane % kMlaCluster) == crank)
-        bulk_load_multicast(raw_s + (uint32_t)(rb * kMlaRawBytes + lane * kMlaRecBytes),
-                            p.cache + (int64_t)(sl / kPageTokens) * kMlaPageBytes +
-                                (int64_t)(sl % kPageTokens) * kMlaRecBytes,
-                            (uint32_t)kMlaRecBytes, bar, (uint16_t)((1u << kMlaCluster) - 1u));
+      if (sl >= 0)
+        bulk_load(raw_s + (uint32_t)(rb * kMlaRawBytes + lane * kMlaRecBytes),
+                  p.cache + (int64_t)(sl / kPageTokens) * kMlaPageBytes +
+                      (int64_t)(sl % kPageTokens) * kMlaRecBytes,
+                  (uint32_t)kMlaRecBytes, bar);
       issued = g + 1;
     }
     if (!ok) sm->abort = 1;
@@ -551,18 +543,11 @@ __global__ void __launch_bounds__(kMlaThreads, 1) sparse_mla_kernel(const __grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // No CTA leaves while a peer may still copy into it or arrive on its
-  // barriers.  After a wait gave up anywhere in the cluster, copies a peer
-  // issued before giving up may still be landing: wait ~100 us for them.
-  cluster_sync();
-  {
-    bool any_abort = false;
-    for (uint32_t c = 0; c < kMlaCluster; ++c)
-      any_abort |= ld_cluster_u32(cluster_map(smem_u32(&sm->abort), c)) != 0;
-    if (any_abort)
-      for (int k = 0; k < 100; ++k) __nanosleep(1000);
-  }
-  cluster_sync();
+  // After a wait gave up, copies issued before it may still be landing in
+  // this CTA's shared memory (the loader's own drain waits are bounded too):
+  // wait ~100 us for them before the CTA leaves.
+  if (sm->abort)
+    for (int k = 0; k < 100; ++k) __nanosleep(1000);
   if (warp == kMlaMmaWarp) tmem_dealloc(tmem, 512);
 }
 

@@ -62,7 +62,9 @@ struct ScoreParams {
   const float* q_scale;
   const float* w;
   int T, H, G, k, C, NS, NB, NQ, NR, n_max;
+  int lg_nb, lg_nr;  // NB = 1 << lg_nb accumulator buffers, NR = 1 << lg_nr scale slots
   int BPS;           // 128-key MMA blocks per pipeline stage (1 or 2); a tile = one stage
+  int lg_bps;        // BPS = 1 << lg_bps
   int ratio;         // tokens per cache entry: a row at pos sees entries < (pos + 1) / ratio
   int q_box_per_token;
   // 1 when the kernel that precedes this one in the stream is this layer's
@@ -713,15 +715,34 @@ __device__ __forceinline__ Item load_item(const Item* items, int i) {
 // sum_h wq[h] * ReLU(acc[h]) over the H accumulator columns at taddr (this
 // thread's TMEM lane); wq_s is the shared-memory address of the H weights.
 // The weights are read (explicit shared loads) before the tensor-memory
-// wait, and four partial sums keep the FMA chains short.
+// wait; the products are accumulated pairwise with the packed two-lane FMA
+// (fma.rn.f32x2: two FP32 FMAs per instruction, each rounded as fmaf), in
+// four pair accumulators so that the FMA chains stay short.
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack_f32x2(unsigned long long v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ unsigned long long fma_f32x2(unsigned long long a, unsigned long long b,
+                                                        unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 template <int H>
 __device__ __forceinline__ float relu_weighted_sum(uint32_t taddr, uint32_t wq_s) {
   constexpr int CH = H >= 32 ? 32 : H;              // columns per tcgen05.ld
   constexpr int BATCH = H >= 64 ? 64 : H;           // columns loaded before one wait
-  constexpr int NA = BATCH >= 16 ? 4 : BATCH / 4;   // partial sums
-  float acc[NA];
+  constexpr int NA = BATCH >= 16 ? 4 : BATCH / 4;   // pair accumulators
+  unsigned long long acc[NA];
 #pragma unroll
-  for (int i = 0; i < NA; ++i) acc[i] = 0.f;
+  for (int i = 0; i < NA; ++i) acc[i] = 0ull;
 #pragma unroll
   for (int c0 = 0; c0 < H; c0 += BATCH) {
     uint4 ww[BATCH / 4];
@@ -733,18 +754,25 @@ __device__ __forceinline__ float relu_weighted_sum(uint32_t taddr, uint32_t wq_s
     tmem_ld_wait();
 #pragma unroll
     for (int h = 0; h < BATCH; h += 4) {
-      float& a = acc[(h / 4) % NA];
-      a = fmaf(__uint_as_float(ww[h / 4].x), fmaxf(__uint_as_float(v[h + 0]), 0.f), a);
-      a = fmaf(__uint_as_float(ww[h / 4].y), fmaxf(__uint_as_float(v[h + 1]), 0.f), a);
-      a = fmaf(__uint_as_float(ww[h / 4].z), fmaxf(__uint_as_float(v[h + 2]), 0.f), a);
-      a = fmaf(__uint_as_float(ww[h / 4].w), fmaxf(__uint_as_float(v[h + 3]), 0.f), a);
+      unsigned long long& a = acc[(h / 4) % NA];
+      a = fma_f32x2(pack_f32x2(__uint_as_float(ww[h / 4].x), __uint_as_float(ww[h / 4].y)),
+                    pack_f32x2(fmaxf(__uint_as_float(v[h + 0]), 0.f),
+                               fmaxf(__uint_as_float(v[h + 1]), 0.f)),
+                    a);
+      a = fma_f32x2(pack_f32x2(__uint_as_float(ww[h / 4].z), __uint_as_float(ww[h / 4].w)),
+                    pack_f32x2(fmaxf(__uint_as_float(v[h + 2]), 0.f),
+                               fmaxf(__uint_as_float(v[h + 3]), 0.f)),
+                    a);
     }
   }
+  float2 t = unpack_f32x2(acc[0]);
+  float sum = t.x + t.y;
 #pragma unroll
-  for (int s2 = NA / 2; s2 >= 1; s2 /= 2)
-#pragma unroll
-    for (int i = 0; i < s2; ++i) acc[i] += acc[i + s2];
-  return acc[0];
+  for (int i = 1; i < NA; ++i) {
+    t = unpack_f32x2(acc[i]);
+    sum += t.x + t.y;
+  }
+  return sum;
 }
 
 template <int H>
@@ -894,6 +922,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     // cp.async instructions, so the warp does nothing else.  Tile s uses scale slot s % NR with
     // NR >= NS + NB: the producer reaches tile s only after the epilogue has
     // released tile s - NS - NB, so a slot is never overwritten while read.
+    // NB and NR are powers of two, so the per-tile ring positions are masks
+    // and shifts (a 64-bit division by a runtime value costs hundreds of
+    // cycles of dependent instructions on the per-tile path).
     // The page ids of 16 tiles (32 pages) come from one coalesced load,
     // fetched one chunk ahead.
     // Items are pipelined three deep: the current item and the next two are
@@ -980,7 +1011,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           // the first NS stages are free from the start
           if (lane == 0 && seq >= p.NS) okv = mbar_wait(bar_empty + 8 * stage, sphase ^ 1, abort_flag);
           if (!__shfl_sync(0xffffffffu, okv, 0)) { ok = false; break; }
-          const uint32_t slot = scale_ring_s + (uint32_t)(seq % p.NR) * slot_bytes;
+          const uint32_t slot = scale_ring_s + ((uint32_t)seq & (uint32_t)(p.NR - 1)) * slot_bytes;
           const uint8_t* scales = p.k_cache + kPageScaleOffset + (lane & 15) * 16;
           cp_async16(slot + (uint32_t)lane * 16u, sp0 >= 0 ? scales + (int64_t)sp0 * kPageBytes : p.k_cache,
                      sp0 >= 0 ? 16u : 0u);
@@ -1148,11 +1179,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const int iters = alt ? (units + 1) / 2 : units;
       for (int m = 0; m < iters; ++m) {
         const int u = u0 + m * step;  // block u = (tile j, block b of the tile)
-        const int j = u / p.BPS, b = u - j * p.BPS;
+        const int j = u >> p.lg_bps, b = u & (p.BPS - 1);
         if (u < units && ok) {
           const long long seq = tile_base + j;
-          const int acc = (int)(seq % p.NB);
-          const uint32_t aphase = (uint32_t)((seq / p.NB) & 1);
+          const int acc = (int)((uint32_t)seq & (uint32_t)(p.NB - 1));
+          const uint32_t aphase = (uint32_t)(seq >> p.lg_nb) & 1u;
           const int key = I.k0 + j * KS + b * kTileKeys + row;
           // no early exit on the abort flag here: the warps of a warpgroup must take
           // the same branch, so they all wait on the same phase with the same limit
@@ -1161,7 +1192,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             tc_fence_after();
             // the key's scale; zero (never a written scale) for a page outside the pool
             const float sc = __uint_as_float(
-                lds_u32(scale_ring_s + (uint32_t)(seq % p.NR) * (uint32_t)(p.BPS * kScaleSlotBytes) +
+                lds_u32(scale_ring_s + ((uint32_t)seq & (uint32_t)(p.NR - 1)) * (uint32_t)(p.BPS * kScaleSlotBytes) +
                         (uint32_t)(b * kTileKeys + row) * 4u));
             const bool kvalid = sc > 0.f && key < I.k1;
             const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) +

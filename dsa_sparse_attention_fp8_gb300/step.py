@@ -128,8 +128,16 @@ class IndexerStep:
         else:
             self.launch(timed)
 
+    def uses_row_selection(self) -> bool:
+        """True when this batch's rows are scored into workspace rows and
+        selected by the row kernel (the workspace was sized with room for
+        them), False when the scoring kernel selects in place."""
+        base = binding.workspace_bytes(self.T, self.H, self.R, self.k)
+        return self.workspace.numel() > base
+
     def score_kernel_ms(self) -> list[float]:
-        """Durations of the last step's scoring kernels (needs time_score_kernels)."""
+        """Durations of the last step's scoring + selection launches, per F layer
+        (needs time_score_kernels)."""
         return [io["score_begin"].elapsed_time(io["score_end"])
                 for io in self.layers if io is not None and "score_begin" in io]
 

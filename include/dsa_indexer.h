@@ -231,8 +231,13 @@ int dsa_indexer_score_topk_compressed(const uint8_t* q_fp8, const float* q_scale
  *   - Memory: every GPU that loads this library holds the array until the
  *     process exits.
  *   - Set-up: the first call on each device looks the array's device address
- *     up (cudaGetSymbolAddress) with that device current and caches it; make
- *     that first call before any stream capture.
+ *     up (cudaGetSymbolAddress) with that device current and caches it with
+ *     the identity of the device's current context; make that first call
+ *     before any stream capture.  After a device reset (cudaDeviceReset) the
+ *     next call sees a new context and looks the address up again, so make
+ *     that call, too, before any capture.
+ *   - Errors: the argument checks of dsa_indexer_score_topk, with the same
+ *     codes, come first.
  *   - Sharing: all calls share the one array and it keeps the previous call's
  *     contents (each call re-initialises what it needs).  Calls whose kernels
  *     overlap on the GPU (other streams, other threads) race on it: serialise
@@ -262,8 +267,10 @@ int dsa_layer_is_full(int layer_id, const char* pattern, int freq, int offset);
 
 /* Per-layer inputs of dsa_layer_stack_run; S layers may leave every field NULL.
  * score_begin / score_end: optional cudaEvent_t handles (NULL = none) that are
- * recorded on the stream immediately before and after this layer's scoring
- * kernel, so a caller can time that kernel inside a larger (or captured) step. */
+ * recorded on the stream immediately before this layer's scoring kernel and
+ * after its top-k selection (the scoring kernel, and the row-selection kernel
+ * when the batch takes that path), so a caller can time scoring + selection
+ * inside a larger (or captured) step. */
 typedef struct dsa_layer_io {
   const float* k;         /* [T, 128] FP32 new-token keys of this layer */
   const uint8_t* q_fp8;   /* [T, H, 128] E4M3 queries */

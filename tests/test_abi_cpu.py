@@ -138,3 +138,29 @@ def test_workspace_rows_sizing(lib):
     assert extra(8192, T=8192) == 8192 * 8192 * 4 + 8192 * 4          # exactly 256 MB of rows
     assert extra(8192, T=8193) == 0                                    # above 256 MB: none
     assert base == binding.workspace_bytes(64, 64, 64, 2048, max_ctx=0)
+
+
+def test_no_alloc_entry_point_checks_arguments_like_the_workspace_one(lib):
+    """The allocation-free scoring call reports a bad argument with the same
+    code as dsa_indexer_score_topk (its checks run before its workspace-size
+    check), and an oversized batch as WORKSPACE_TOO_SMALL; all before any
+    CUDA call."""
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+
+    def both(T, H, R, k, mnbt=8, meta=fake):
+        a = lib.dsa_indexer_score_topk(fake, fake, fake, T, H, fake, 16, meta, meta, R, meta, 4,
+                                       k, fake, mnbt, None, 0, fake, 1 << 40, None, None)
+        b = lib.dsa_indexer_score_topk_no_alloc(fake, fake, fake, T, H, fake, 16, meta, meta, R,
+                                                meta, 4, k, fake, mnbt, None, None)
+        return a, b
+
+    assert both(-1, 64, 1, 2048) == (-1, -1)      # T < 0
+    assert both(4, 64, 0, 2048) == (-1, -1)       # R < 1
+    assert both(4, 12, 1, 2048) == (-2, -2)       # unsupported H
+    assert both(4, 64, 1, 4096) == (-2, -2)       # index_topk too large
+    assert both(9, 64, 1, 2048) == (-1, -1)       # T > max_num_batched_tokens
+    assert both(4, 64, 1, 2048, meta=None) == (-1, -1)   # null metadata
+    rc = lib.dsa_indexer_score_topk_no_alloc(fake, fake, fake, 8192, 64, fake, 16, fake, fake, 1,
+                                             fake, 4, 2048, fake, 8192, None, None)
+    assert rc == -3 and b"built-in workspace" in lib.dsa_last_error()

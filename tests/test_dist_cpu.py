@@ -62,9 +62,38 @@ def test_non_zero_ranks_print_nothing_and_exit_0(extra):
     without work and without output."""
     env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1", MASTER_ADDR="127.0.0.1")
     res = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--impl", "reference",
-                          "--steps", "1", "--warmup", "0", "--scale", "0.05", *extra],
+                          "--gpus", "2", "--steps", "1", "--warmup", "0", "--scale", "0.05",
+                          *extra],
                          env=env, capture_output=True, text=True, timeout=300)
     assert res.returncode == 0, res.stderr[-2000:]
+    assert res.stdout.strip() == ""
+
+
+def test_gpus_n_starts_n_ranks_and_rank_0_alone_prints():
+    """`bench.py --gpus 2` without a launcher starts two ranks itself (one
+    replica per GPU); rank 0 alone prints its line, with n_gpus = 2.  The
+    reference arm runs on the CPU, so this needs no GPU."""
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    res = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--impl", "reference",
+                          "--gpus", "2", "--workload", "0", "--steps", "1", "--warmup", "0"],
+                         env=env, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+
+
+def test_gpus_must_match_the_launchers_world_size():
+    """Under a launcher, --gpus must equal WORLD_SIZE (a mismatch would report
+    the wrong number of GPUs)."""
+    env = dict(os.environ, RANK="0", WORLD_SIZE="2", LOCAL_RANK="0", MASTER_ADDR="127.0.0.1")
+    res = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--impl", "reference",
+                          "--workload", "0", "--steps", "1", "--warmup", "0"],
+                         env=env, capture_output=True, text=True, timeout=300)
+    assert res.returncode != 0
+    assert "WORLD_SIZE=2" in res.stderr
     assert res.stdout.strip() == ""
 
 
