@@ -76,8 +76,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D uint8 view [rows, 128] with a box of `box_rows` x 128 bytes, 128-byte swizzle.
-int make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+// 2-D uint8 view [rows, 128] with a box of `box_rows` x 128 bytes, 128-byte
+// swizzle (or none).
+int make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows,
+                     bool swizzle = true) {
   auto fn = encode_fn();
   if (!fn) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[2] = {128, rows};
@@ -85,7 +87,8 @@ int make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t b
   cuuint32_t box[2] = {128, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return DSA_OK;
@@ -206,8 +209,8 @@ bool score_shape(int T, int R, int H, int k, ScoreShape* s) {
 }
 
 template <int H>
-int launch_score_h(const CUtensorMap& tk, const CUtensorMap& tq, const dsa::ScoreParams& p,
-                   size_t smem, int grid, cudaStream_t st) {
+int launch_score_h(const CUtensorMap& tk, const CUtensorMap& ts, const CUtensorMap& tq,
+                   const dsa::ScoreParams& p, size_t smem, int grid, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -229,20 +232,20 @@ int launch_score_h(const CUtensorMap& tk, const CUtensorMap& tq, const dsa::Scor
   attr[0].val.programmaticStreamSerializationAllowed = env_int("DSA_PDL", 1, 0, 1);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, dsa::score_topk_kernel<H>, tk, tq, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, dsa::score_topk_kernel<H>, tk, ts, tq, p);
   if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "score_topk_kernel launch: %s", cudaGetErrorString(e));
   return check_launch("score_topk_kernel");
 }
 
-int launch_score(int H, const CUtensorMap& tk, const CUtensorMap& tq, const dsa::ScoreParams& p,
-                 size_t smem, int grid, cudaStream_t st) {
+int launch_score(int H, const CUtensorMap& tk, const CUtensorMap& ts, const CUtensorMap& tq,
+                 const dsa::ScoreParams& p, size_t smem, int grid, cudaStream_t st) {
   switch (H) {
-    case 4: return launch_score_h<4>(tk, tq, p, smem, grid, st);
-    case 8: return launch_score_h<8>(tk, tq, p, smem, grid, st);
-    case 16: return launch_score_h<16>(tk, tq, p, smem, grid, st);
-    case 32: return launch_score_h<32>(tk, tq, p, smem, grid, st);
-    case 64: return launch_score_h<64>(tk, tq, p, smem, grid, st);
-    case 128: return launch_score_h<128>(tk, tq, p, smem, grid, st);
+    case 4: return launch_score_h<4>(tk, ts, tq, p, smem, grid, st);
+    case 8: return launch_score_h<8>(tk, ts, tq, p, smem, grid, st);
+    case 16: return launch_score_h<16>(tk, ts, tq, p, smem, grid, st);
+    case 32: return launch_score_h<32>(tk, ts, tq, p, smem, grid, st);
+    case 64: return launch_score_h<64>(tk, ts, tq, p, smem, grid, st);
+    case 128: return launch_score_h<128>(tk, ts, tq, p, smem, grid, st);
     default: return fail(DSA_ERR_UNSUPPORTED, "H=%d is not supported", H);
   }
 }
@@ -348,8 +351,13 @@ struct LayerQ {
 // q_ready: that cache write does not produce q_fp8 (FP32-input layers).
 int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, int* launches,
                        bool meta_ready, bool q_ready) {
-  CUtensorMap tk, tq;
+  // the pool as 128-byte rows: a page is rows [66 p, 66 p + 66), its 64 key
+  // rows then 2 rows of scales; key boxes of 64 rows (swizzled into the MMA
+  // operand layout), scale boxes of 2 rows (plain)
+  CUtensorMap tk, ts, tq;
   int rc = make_rows128_map(&tk, lq.k_cache, (uint64_t)b.num_pages * (DSA_PAGE_BYTES / 128), 64);
+  if (rc) return rc;
+  rc = make_rows128_map(&ts, lq.k_cache, (uint64_t)b.num_pages * (DSA_PAGE_BYTES / 128), 2, false);
   if (rc) return rc;
   rc = make_rows128_map(&tq, lq.q_fp8, (uint64_t)b.T * b.H,
                         s.q_box_per_token ? (uint32_t)b.H : (uint32_t)(s.G * b.H));
@@ -393,6 +401,7 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   p.cand_idx = reinterpret_cast<int32_t*>(ws + L.cand_idx);
   p.cand_hist = reinterpret_cast<uint16_t*>(ws + L.cand_hist);
   p.cand_start = reinterpret_cast<uint16_t*>(ws + L.cand_start);
+  p.ghist = reinterpret_cast<uint32_t*>(ws + L.ghist);
   p.cand_count = reinterpret_cast<int32_t*>(ws + L.cand_count);
   p.done = reinterpret_cast<int32_t*>(ws + L.done);
   p.topk = b.topk;
@@ -401,7 +410,7 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   p.score_rows = reinterpret_cast<uint32_t*>(ws + L.score_rows);
   p.score_stride = L.score_stride;
   p.status = b.status;
-  rc = launch_score(b.H, tk, tq, p, s.smem_bytes, grid, b.st);
+  rc = launch_score(b.H, tk, ts, tq, p, s.smem_bytes, grid, b.st);
   if (rc == DSA_OK) ++*launches;
   return rc;
 }

@@ -75,9 +75,13 @@ constexpr int kBlockBins = 2048;  // level-1 bins published with every candidate
 // 128, at most kScoreRowMax; 0 = never).
 constexpr int kScoreRowMax = 8192;   // longer rows merge faster across SMs (measured)
 
+// A row cut into at least this many pieces shares a histogram of its keys'
+// level-1 bins across the pieces (see the scoring kernel's epilogue).
+constexpr int kWideSplit = 4;
+
 struct WsLayout {
   size_t header, group_prefix, cta_start, heads, items, done, cand_count, cand_keys, cand_idx,
-      cand_hist, cand_start, row_keys, score_rows, total;
+      cand_hist, cand_start, ghist, row_keys, score_rows, total;
   int max_items, max_split_groups, max_cand_blocks, cb, score_stride;
 };
 
@@ -108,6 +112,7 @@ __host__ __device__ inline WsLayout ws_layout(int T, int R, int G, int k, int n_
   L.cand_idx = o;     o = align256(o + sizeof(int32_t) * (size_t)L.max_cand_blocks * L.cb);
   L.cand_hist = o;    o = align256(o + sizeof(uint16_t) * (size_t)L.max_cand_blocks * kBlockBins);
   L.cand_start = o;   o = align256(o + sizeof(uint16_t) * (size_t)L.max_cand_blocks * kBlockBins);
+  L.ghist = o;        o = align256(o + sizeof(uint32_t) * (size_t)L.max_split_groups * G * kBlockBins);
   L.row_keys = o;     o = align256(o + (score_stride > 0 ? sizeof(int32_t) * (size_t)T : 0));
   L.score_rows = o;   o = align256(o + sizeof(uint32_t) * (size_t)T * (size_t)score_stride);
   L.total = o;
@@ -175,6 +180,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   __shared__ long long s_Q;
   __shared__ unsigned long long s_max_keys;
   __shared__ int2 s_empty[kPlanThreads];  // (first row, rows) of groups that see no entry
+  __shared__ unsigned char s_wide[kMaxCtas];  // split group cut into >= kWideSplit pieces
   __shared__ int s_n_empty;
   // the group prefix of a batch of at most kPlanSmemRequests requests, for the
   // per-group binary search (a search over global memory is a chain of
@@ -272,6 +278,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   const bool rows_ok = G == 1 && p.L.score_stride > 0 && s_max_keys <= (unsigned long long)p.L.score_stride;
   const int n_used = (int)((W + Q - 1) / Q);
 
+  for (int i = threadIdx.x; i < kMaxCtas; i += kPlanThreads) s_wide[i] = 0;
+  __syncthreads();
   // Phase C: emit the pieces in tile order; CTA c's items are contiguous.
   // Group g takes stream positions [P, P + item_cost + tiles): the charged
   // tiles first, then its own from V = P + item_cost on.
@@ -303,6 +311,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
                       (!is_split || (my_sg < p.L.max_split_groups &&
                                      my_cb + (long long)gc * pieces <= p.L.max_cand_blocks));
     if (!fits) overflow = true;
+    if (fits && is_split) s_wide[my_sg] = pieces >= kWideSplit ? 1 : 0;
     for (long long j = 0; j < pieces && fits; ++j) {
       const long long c = V / Q + j;  // CTA of this piece
       const long long s0 = max(V, c * Q), s1 = min(V + tiles, (c + 1) * Q);
@@ -344,6 +353,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     }
   }
   const int any_overflow = __syncthreads_or(overflow ? 1 : 0);
+  // the shared histograms of wide split groups start empty (a merge empties
+  // its group's again, for the next layer of a stack)
+  {
+    uint4* gh = reinterpret_cast<uint4*>(p.ws + p.L.ghist);
+    const int per_sg = G * kBlockBins / 4;
+    const int nsg = (int)min(sg_carry, (long long)p.L.max_split_groups);
+    for (int sg = 0; sg < nsg && !any_overflow; ++sg)
+      if (s_wide[sg])
+        for (int i = threadIdx.x; i < per_sg; i += kPlanThreads)
+          gh[(size_t)sg * per_sg + i] = make_uint4(0u, 0u, 0u, 0u);
+  }
   if (any_overflow) raise_status(p.status, kStatusBadMetadata);
   if (any_overflow && p.L.score_stride > 0)
     for (int t = threadIdx.x; t < p.T; t += kPlanThreads) row_keys[t] = 0;

@@ -159,21 +159,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 // ---------------------------------------------------------------------------
-// 16-byte asynchronous copy global -> shared (both 16-byte aligned), L2 only.
-// The first `src_bytes` (0 or 16) bytes come from `src`, the rest are zero;
-// with src_bytes = 0 nothing is read.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
-               : "memory");
-}
-
-// Arrive on `bar` once every cp.async this thread issued so far has landed.
-// The arrival is not pre-counted: the barrier's expected count includes it.
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory and the 5th-generation tensor-core MMA
 // ---------------------------------------------------------------------------

@@ -84,6 +84,7 @@ struct ScoreParams {
   uint16_t* cand_hist;   // per candidate block: level-1 histogram (kBlockBins; counts <= CB)
   uint16_t* cand_start;  // per candidate block: start offset of every bin
   int32_t* cand_count;
+  uint32_t* ghist;       // per row of a wide split group: the pieces' shared level-1 histogram
   int32_t* done;
   int32_t* topk;
   float* scores_out;
@@ -227,6 +228,47 @@ __device__ __noinline__ BinCut find_bin(const Selector S, uint32_t hist_s, int n
   named_bar_sync(S.bar, S.nt);
   const BinCut r{S.s->res[0], S.s->res[1], S.s->res[2]};
   named_bar_sync(S.bar, S.nt);  // result read before the scratch is reused
+  return r;
+}
+
+// find_bin over a histogram in global memory (read from L2: other SMs add to
+// it); the bin is -1 when the histogram holds fewer than `need` keys.
+__device__ __noinline__ BinCut find_bin_global(const Selector S, const uint32_t* hist, int need) {
+  const int per = kBins / S.nt;
+  const uint32_t lo = (uint32_t)(kBins - (S.tid + 1) * per);
+  uint4 q[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    q[i] = 4 * i < per ? __ldcg(reinterpret_cast<const uint4*>(hist + lo + 4u * i)) : make_uint4(0, 0, 0, 0);
+  uint32_t local = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) local += q[i].x + q[i].y + q[i].z + q[i].w;
+  uint32_t tot;
+  uint32_t above = sel_scan(S, local, &tot);
+  const uint32_t un = (uint32_t)need;
+  if (S.tid == 0 && tot < un) S.s->res[0] = -1;
+  if (tot >= un && above < un && un <= above + local) {
+    int bin = (int)lo + per - 1;
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int i = 15; i >= 0; --i) {
+      if (i < per) {
+        const uint32_t c = u4_at(q[i >> 2], i & 3);
+        if (cnt == 0 && un <= above + c) {
+          bin = (int)lo + i;
+          cnt = c;
+        } else if (cnt == 0) {
+          above += c;
+        }
+      }
+    }
+    S.s->res[0] = bin;
+    S.s->res[1] = (int)above;
+    S.s->res[2] = (int)cnt;
+  }
+  named_bar_sync(S.bar, S.nt);
+  const BinCut r{S.s->res[0], S.s->res[1], S.s->res[2]};
+  named_bar_sync(S.bar, S.nt);
   return r;
 }
 
@@ -778,6 +820,7 @@ __device__ __forceinline__ float relu_weighted_sum(uint32_t taddr, uint32_t wq_s
 template <int H>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_topk_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_s,
                       const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ ScoreParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -808,8 +851,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
-      // the producer's expect-tx arrival plus one cp.async arrival per producer lane
-      mbar_init(bar_full + 8 * s, 1 + 32);
+      // one arrival (with its expected bytes) per page of the tile
+      mbar_init(bar_full + 8 * s, 2 * p.BPS);
       mbar_init(bar_empty + 8 * s, 1);  // freed by the MMA commit
     }
     for (int b = 0; b < p.NB; ++b) {
@@ -836,6 +879,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_s);
     tma_prefetch_desc(&tm_q);
   }
   // Keys per tile and the producer's view of a chunk of an item's page ids:
@@ -912,21 +956,21 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // The whole warp walks the tiles.  Per tile, lane 0 waits for the stage
-    // (from the NS-th tile on; the first NS stages start free); every lane
-    // copies 16 bytes of the tile's pages' scales (lanes 0-15 one page, 16-31
-    // the next) into the tile's slot of the scale ring with cp.async,
-    // zero-filled for a page outside the pool or the key range, and arrives on
-    // the stage's full barrier when its copy lands; then the lanes that hold
-    // the tile's page ids issue one key-page copy each.  Issuing a tile costs
-    // the warp about 1,000-1,400 cycles, most of it in the barrier and
-    // cp.async instructions, so the warp does nothing else.  Tile s uses scale slot s % NR with
-    // NR >= NS + NB: the producer reaches tile s only after the epilogue has
-    // released tile s - NS - NB, so a slot is never overwritten while read.
-    // NB and NR are powers of two, so the per-tile ring positions are masks
-    // and shifts (a 64-bit division by a runtime value costs hundreds of
-    // cycles of dependent instructions on the per-tile path).
-    // The page ids of 16 tiles (32 pages) come from one coalesced load,
-    // fetched one chunk ahead.
+    // (from the NS-th tile on; the first NS stages start free); then each lane
+    // that holds one of the tile's page ids arrives on the stage's full
+    // barrier with that page's bytes and issues two copies: the page's 64 key
+    // rows (8 KB, 128-byte swizzle, into the stage) and its 256 bytes of
+    // scales (into the tile's slot of the scale ring).  A lane whose page is
+    // missing (beyond the item, or outside the pool) writes zero scales (a
+    // zero scale marks its keys invalid) and arrives without bytes.  Tile s
+    // uses scale slot s % NR with NR >= NS + NB: the producer reaches tile s
+    // only after the epilogue has released tile s - NS - NB, so a slot is
+    // never overwritten while read.  NB and NR are powers of two, so the
+    // per-tile ring positions are masks and shifts (a 64-bit division by a
+    // runtime value costs hundreds of cycles of dependent instructions on the
+    // per-tile path).
+    // The page ids of the next 32 pages come from one coalesced load (lane l
+    // holds page 32 * chunk + l of the item), fetched one chunk ahead.
     // Items are pipelined three deep: the current item and the next two are
     // held with their first chunk's page ids; the item three ahead is loaded
     // once the current item's first tile is issued, and its page ids when the
@@ -950,6 +994,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     };
     const uint32_t stage_bytes = (uint32_t)(p.BPS * kStageBytes);
     const uint32_t slot_bytes = (uint32_t)(p.BPS * kScaleSlotBytes);
+    constexpr int kPageScaleBytes = kPageTokens * 4;  // 256: rows 64 and 65 of the page
     Item I_far{};
     for (int it = it_begin; it < it_end && ok; ++it, ++item_i) {
       const Item I = I_cur;
@@ -995,11 +1040,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           // the tile's pages are held by chunk lanes first .. first + ppt - 1,
           // and those lanes issue their own page copies
           const int first = ppt * jj;
-          const bool my_page = lane >= first && lane < first + ppt && cur >= 0;
-          const uint32_t pages = __ballot_sync(0xffffffffu, my_page);
-          // scale chunk h*32 + lane (16 bytes) belongs to the tile's page 2h + lane/16
-          const int32_t sp0 = __shfl_sync(0xffffffffu, cur, first + (lane >> 4));
-          const int32_t sp1 = __shfl_sync(0xffffffffu, cur, (first + 2 + (lane >> 4)) & 31);
+          const bool mine = lane >= first && lane < first + ppt;
           if (!waited) {
             // the tile's pages end at a page boundary: all of them below stable_end?
             const int tile_end = min(I.k0 + (c * tpc + jj + 1) * KS, I.k1);
@@ -1011,22 +1052,24 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           // the first NS stages are free from the start
           if (lane == 0 && seq >= p.NS) okv = mbar_wait(bar_empty + 8 * stage, sphase ^ 1, abort_flag);
           if (!__shfl_sync(0xffffffffu, okv, 0)) { ok = false; break; }
-          const uint32_t slot = scale_ring_s + ((uint32_t)seq & (uint32_t)(p.NR - 1)) * slot_bytes;
-          const uint8_t* scales = p.k_cache + kPageScaleOffset + (lane & 15) * 16;
-          cp_async16(slot + (uint32_t)lane * 16u, sp0 >= 0 ? scales + (int64_t)sp0 * kPageBytes : p.k_cache,
-                     sp0 >= 0 ? 16u : 0u);
-          if (p.BPS == 2)
-            cp_async16(slot + (uint32_t)(32 + lane) * 16u,
-                       sp1 >= 0 ? scales + (int64_t)sp1 * kPageBytes : p.k_cache, sp1 >= 0 ? 16u : 0u);
-          cp_async_arrive_noinc(bar_full + 8 * stage);
-          if (lane == 0)
-            mbar_arrive_expect_tx(bar_full + 8 * stage,
-                                  (uint32_t)__popc(pages) * (uint32_t)(kPageTokens * kHeadDim));
+          if (mine) {
+            const uint32_t pi = (uint32_t)(lane - first);  // page of the tile
+            const uint32_t sdst = scale_ring_s + ((uint32_t)seq & (uint32_t)(p.NR - 1)) * slot_bytes +
+                                  pi * (uint32_t)kPageScaleBytes;
+            const uint32_t full = bar_full + 8 * stage;
+            if (cur >= 0) {
+              mbar_arrive_expect_tx(full, (uint32_t)(kPageTokens * kHeadDim + kPageScaleBytes));
+              const int32_t row = cur * (kPageBytes / kHeadDim);  // the page's first 128-byte row
+              tma_load_2d(smem_u32(stage_base) + (uint32_t)stage * stage_bytes +
+                              pi * (uint32_t)(kPageTokens * kHeadDim),
+                          &tm_k, 0, row, full);
+              tma_load_2d(sdst, &tm_s, 0, row + kPageTokens, full);
+            } else {
+              for (uint32_t i = 0; i < (uint32_t)kPageScaleBytes; i += 16u) sts_v4(sdst + i, make_uint4(0u, 0u, 0u, 0u));
+              mbar_arrive(full);
+            }
+          }
           __syncwarp();
-          if (my_page)
-            tma_load_2d(smem_u32(stage_base) + (uint32_t)stage * stage_bytes +
-                            (uint32_t)((lane - first) * kPageTokens * kHeadDim),
-                        &tm_k, 0, cur * (kPageBytes / kHeadDim), bar_full + 8 * stage);
           if (++stage == p.NS) { stage = 0; sphase ^= 1; }
           if (!ahead) {
             ahead = true;
@@ -1141,9 +1184,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     auto ck_of = [&](int g) -> uint32_t* { return ckeys_all + (size_t)g * p.C; };
     auto ci_of = [&](int g) -> int32_t* { return cidx_all + (size_t)g * p.C; };
     auto out_row = [&](int g) -> int32_t* { return p.topk + (int64_t)tok[g].t * p.k; };
-    // buffer-fill checks every `chk` iterations, leaving room for what they append
-    const int chk = alt ? 8 : 4;
-    const int headroom = chk * kTileKeys * (alt ? 2 : 1);
+    // buffer-fill checks every `chk` iterations (a power of two), leaving room
+    // for what the row's warps append in between (kpi keys per iteration):
+    // every 8 iterations while the buffer keeps room for 2k candidates next to
+    // that headroom (a shrink keeps at most C - headroom), else every 4
+    const int kpi = kTileKeys * (alt ? 2 : 1);
+    const int chk = p.C - 8 * kpi >= 2 * p.k ? 8 : 4;
+    const int headroom = chk * kpi;
     long long tile_base = 0;  // tiles of earlier items of this CTA (all roles count alike)
     bool ok = true;
     const int g_first = alt ? 0 : wg;  // this thread's rows: g_first, g_first + 2, ...
@@ -1156,6 +1203,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const int nsplit = I.split >> 16;
       const int split = I.split & 0xFFFF;
       const bool to_rows = I.sgroup == kSgroupRows;  // keys to the workspace, selected later
+      // A row cut into many pieces shares a histogram of its candidates' level-1
+      // bins: each piece adds its own once, early in its range, and somewhat later
+      // raises its admission threshold to the bin where that histogram's count
+      // from the top reaches k.  The histogram counts distinct keys of the row
+      // (each piece publishes once, pieces are disjoint), so at least k keys of
+      // the row lie in or above that bin: no key below it is among the row's
+      // top k, in any piece.  Pieces that publish late only make the bound weaker.
+      const bool wide = !to_rows && nsplit >= kWideSplit;
+      int gstate = 0;  // 0: nothing yet, 1: published, 2: threshold adopted
       for (int g = g_first; g < I.gcount; g += 2) {
         const int t = I.t0 + g;
         if (sets_up) {
@@ -1217,9 +1273,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
           }
         }
-        if (may_fill && (m % chk) == chk - 1 && m + 1 < iters) {
+        if (may_fill && (m & (chk - 1)) == chk - 1 && m + 1 < iters) {
+          // the row's appending warps only (its warpgroup, or both for a decode row)
           if (!ok) misc->epi_abort = 1;
-          named_bar_sync(3, 256);  // every append so far is visible
+          named_bar_sync(S.bar, S.nt);  // every append so far is visible
           if (misc->epi_abort) {
             ok = false;
           } else {
@@ -1236,8 +1293,38 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 }
               }
             }
+            if (wide && gstate == 0) {
+              named_bar_sync(S.bar, S.nt);  // the histograms are current
+              for (int g = g_first; g < I.gcount; g += 2) {
+                uint32_t* gh = p.ghist + ((int64_t)I.sgroup * p.G + g) * kBins;
+                for (int b = S.tid; b < kBins; b += S.nt) {
+                  const uint32_t c = lds_u32(hist_of(g) + 4u * (uint32_t)b);
+                  if (c) atomicAdd(gh + b, c);
+                }
+              }
+              gstate = 1;
+            } else if (wide && gstate == 1) {
+              for (int g = g_first; g < I.gcount; g += 2) {
+                const BinCut c = find_bin_global(S, p.ghist + ((int64_t)I.sgroup * p.G + g) * kBins, p.k);
+                const uint32_t gthr = c.bin > 0 ? ((uint32_t)c.bin << kHistShift) - 1u : 0u;
+                if (gthr > tok[g].thr) {
+                  // keep only the candidates at or above that bin
+                  const int n = tok[g].count;
+                  uint32_t thr = 0;
+                  const BinCut cut{c.bin, 0, 0};
+                  const int kept = slot_select(S, kSelInPlace, n, smem_u32(ck_of(g)),
+                                               smem_u32(ci_of(g)), hist_of(g), p.k, 0, nullptr,
+                                               nullptr, &thr, &cut);
+                  if (S.tid == 0) {
+                    tok[g].count = kept;
+                    tok[g].thr = gthr;
+                  }
+                }
+              }
+              gstate = 2;
+            }
           }
-          named_bar_sync(3, 256);
+          named_bar_sync(S.bar, S.nt);
         }
       }
       tile_base += ntiles;
@@ -1284,6 +1371,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                          &tok[g], pre, out_row(g));
             named_bar_sync(S.bar, S.nt);  // the slot is free for the next row
           }
+          if (wide)  // the shared histograms are empty again for the next layer
+            for (int g = g_first; g < I.gcount; g += 2)
+              for (int b = S.tid; b < kBins; b += S.nt)
+                __stcg(p.ghist + ((int64_t)I.sgroup * p.G + g) * kBins + b, 0u);
           if (epi == 0 && lane == 0) p.done[I.sgroup] = 0;  // ready for the next layer
         }
       }

@@ -13,7 +13,7 @@ import torch
 import oracle as O
 import synth
 from conftest import gpu_available
-from oracle_side import check_topk_row, oracle_rows
+from oracle_side import check_scores, check_topk_row, oracle_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -139,9 +139,17 @@ def test_full_prefix_hit_chunked_prefill(B):
 
 
 def test_full_mixed_batch(B):
-    wl = synth.make_workload(3)                       # 256 decode + 4 x 1024 prefill rows
-    full, layers, outs, _ = _run_stack(B, wl, "FSS", 1, 2, 3)
-    _check_rows(wl, 0, layers[0], outs[0], _sample_rows(wl, 12))
+    """The mixed batch at full size (256 decode rows with contexts up to 65,536
+    + 4 prefill chunks of 1024) through its real 61-layer stack, freq 4 and
+    offset 2 (16 F layers): sampled rows of the first, a middle and the last F
+    layer against the oracle; every S layer equals the F layer before it."""
+    wl = synth.make_workload(3)
+    full, layers, outs, _ = _run_stack(B, wl, None, wl.freq, wl.offset, wl.num_layers)
+    f_layers = [l for l, f in enumerate(full) if f]
+    assert len(f_layers) == 16 and f_layers[:3] == [0, 1, 5] and f_layers[-1] == 57
+    _check_rows(wl, f_layers[0], layers[f_layers[0]], outs[f_layers[0]], _sample_rows(wl, 8))
+    for l in (f_layers[len(f_layers) // 2], f_layers[-1]):
+        _check_rows(wl, l, layers[l], outs[l], _sample_rows(wl, 3, seed=l))
     _check_shared(full, outs)
 
 
@@ -153,7 +161,48 @@ def test_full_mtp_decode_stack(B):
 
 
 def test_full_long_context_decode(B):
-    wl = synth.make_workload(4)                       # 4 x (1,048,576 cached + 1) tokens
-    full, layers, outs, _ = _run_stack(B, wl, "FS", 1, 2, 2)
-    _check_rows(wl, 0, layers[0], outs[0], range(wl.T))
+    """The 1M-context decode batch at full size (4 x (1,048,576 + 1) tokens)
+    through its real 78-layer stack with the seeded 21-F pattern: every row of
+    the first F layer, one row each of a middle and the last F layer against
+    the oracle; every S layer equals the F layer before it."""
+    wl = synth.make_workload(4)
+    full, layers, outs, _ = _run_stack(B, wl, wl.pattern, wl.freq, wl.offset, wl.num_layers)
+    f_layers = [l for l, f in enumerate(full) if f]
+    assert len(f_layers) == 21 and f_layers[:2] == [0, 1]
+    _check_rows(wl, f_layers[0], layers[f_layers[0]], outs[f_layers[0]], range(wl.T))
+    _check_rows(wl, f_layers[10], layers[f_layers[10]], outs[f_layers[10]], [1])
+    _check_rows(wl, f_layers[-1], layers[f_layers[-1]], outs[f_layers[-1]], [3])
     _check_shared(full, outs)
+
+
+def test_full_prefix_hit_scores_on_sampled_rows(B):
+    """The prefix-hit chunked prefill at full size (8192 rows x up to 24,576
+    keys) through dsa_indexer_score_topk with the debug score dump: every
+    visible score of sampled rows within 2e-3 x the row's max |score| of the
+    oracle, and the rows' index sets."""
+    binding, staging = B
+    wl = synth.make_workload(2)
+    meta = staging.stage_metadata(wl)
+    io = staging.stage_layer(wl, 0, meta)
+    binding.write_k(io["k"], meta.query_start_loc, meta.seq_lens, meta.block_table, io["k_cache"])
+    topk = torch.full((wl.max_num_batched_tokens, wl.index_topk), -7, dtype=torch.int32,
+                      device="cuda")
+    ld = int(wl.seq_lens.max())
+    sc = torch.full((wl.T, ld), float("nan"), dtype=torch.float32, device="cuda")
+    ws = binding.alloc_workspace(wl.T, wl.H, wl.R, wl.index_topk)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.score_topk(io["q_fp8"], io["q_scale"], io["w"], io["k_cache"], meta.query_start_loc,
+                       meta.seq_lens, meta.block_table, wl.index_topk, topk, ws, scores_out=sc,
+                       status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    rows = sorted({0, 1, 127, 128, 2047, 4096, 6001, 8190, 8191}
+                  | set(np.random.default_rng(11).integers(0, wl.T, 7).tolist()))
+    got = topk.cpu().numpy()
+    assert np.all(got[wl.T:] == -7)
+    oc, os_ = O.quantize_blocks(wl.q(0))
+    ref = oracle_rows(wl, 0, rows, oc, os_, wl.w(0))
+    for t, s in ref.items():
+        row = sc[t, :s.shape[0]].cpu().numpy()
+        check_scores(row, s, f"row {t}")
+        check_topk_row(got[t], s, wl.index_topk, f"row {t}")
