@@ -97,8 +97,11 @@ int make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t b
 // Tuning overrides read from the environment: DSA_MIN_SPLIT (keys, the
 // smallest per-CTA share of key tiles worth a piece of its own, default 1024),
 // DSA_STAGE_KEYS (128 or 256, the decode layout's keys per pipeline stage,
-// default 256), DSA_GROUP_ROWS (cap on query rows per group) and DSA_PDL (0
-// turns off programmatic dependent launch of the scoring kernel).
+// default 256), DSA_GROUP_ROWS (cap on query rows per group), DSA_PDL (0
+// turns off programmatic dependent launch of the scoring kernel) and
+// DSA_WAIT_LIMIT (iterations a scoring-kernel wait on another role may take,
+// default and maximum kWaitLimit; 0 makes every such wait give up at once, to
+// exercise the timeout path: the call then reports DSA_STATUS_TIMEOUT).
 int env_int(const char* name, int dflt, int lo, int hi) {
   const char* v = getenv(name);
   if (!v || !*v) return dflt;
@@ -402,6 +405,7 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   p.cand_hist = reinterpret_cast<uint16_t*>(ws + L.cand_hist);
   p.cand_start = reinterpret_cast<uint16_t*>(ws + L.cand_start);
   p.ghist = reinterpret_cast<uint32_t*>(ws + L.ghist);
+  p.wide_of = reinterpret_cast<const int32_t*>(ws + L.wide_of);
   p.cand_count = reinterpret_cast<int32_t*>(ws + L.cand_count);
   p.done = reinterpret_cast<int32_t*>(ws + L.done);
   p.topk = b.topk;
@@ -410,6 +414,7 @@ int launch_score_layer(const Batch& b, const ScoreShape& s, const LayerQ& lq, in
   p.score_rows = reinterpret_cast<uint32_t*>(ws + L.score_rows);
   p.score_stride = L.score_stride;
   p.status = b.status;
+  p.wait_limit = (uint32_t)env_int("DSA_WAIT_LIMIT", (int)dsa::kWaitLimit, 0, (int)dsa::kWaitLimit);
   rc = launch_score(b.H, tk, ts, tq, p, s.smem_bytes, grid, b.st);
   if (rc == DSA_OK) ++*launches;
   return rc;

@@ -75,14 +75,22 @@ constexpr int kBlockBins = 2048;  // level-1 bins published with every candidate
 // 128, at most kScoreRowMax; 0 = never).
 constexpr int kScoreRowMax = 8192;   // longer rows merge faster across SMs (measured)
 
-// A row cut into at least this many pieces shares a histogram of its keys'
-// level-1 bins across the pieces (see the scoring kernel's epilogue).
+// A decode row (one row per group) cut into at least this many pieces is
+// "wide": its pieces share two level-1 histograms of its keys (see the
+// scoring kernel's epilogue): one they publish early to bound the row's k-th
+// score, and one of their final candidates for the merge.  A wide group spends
+// kWideSplit - 1 of the n_cta - 1 CTA boundaries, which bounds their number.
+// (A finer early histogram -- 8192 bins of the key's top 13 bits, published
+// per candidate -- measured slower: the bound it gives after the first few
+// thousand keys of each piece is weaker than the level-1 bound a piece gives
+// from a fuller buffer.)
 constexpr int kWideSplit = 4;
+constexpr int kSharedHistWords = 2 * kBlockBins;  // per wide split group
 
 struct WsLayout {
-  size_t header, group_prefix, cta_start, heads, items, done, cand_count, cand_keys, cand_idx,
-      cand_hist, cand_start, ghist, row_keys, score_rows, total;
-  int max_items, max_split_groups, max_cand_blocks, cb, score_stride;
+  size_t header, group_prefix, cta_start, heads, items, done, wide_of, cand_count, cand_keys,
+      cand_idx, cand_hist, cand_start, ghist, row_keys, score_rows, total;
+  int max_items, max_split_groups, max_cand_blocks, cb, score_stride, max_wide;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -100,6 +108,10 @@ __host__ __device__ inline WsLayout ws_layout(int T, int R, int G, int k, int n_
   L.max_split_groups = (int)(groups < n_cta ? groups : n_cta);
   L.max_cand_blocks = G * (L.max_split_groups + n_cta);
   L.cb = cand_block_capacity(k);
+  L.max_wide = G == 1 ? (L.max_split_groups < (n_cta - 1) / (kWideSplit - 1)
+                             ? L.max_split_groups
+                             : (n_cta - 1) / (kWideSplit - 1))
+                      : 0;
   size_t o = 0;
   L.header = o;       o = align256(o + sizeof(PlanHeader));
   L.group_prefix = o; o = align256(o + sizeof(int32_t) * (size_t)(R + 1));
@@ -107,12 +119,13 @@ __host__ __device__ inline WsLayout ws_layout(int T, int R, int G, int k, int n_
   L.heads = o;        o = align256(o + sizeof(CtaHead) * (size_t)n_cta);
   L.items = o;        o = align256(o + sizeof(Item) * (size_t)L.max_items);
   L.done = o;         o = align256(o + sizeof(int32_t) * (size_t)L.max_split_groups);
+  L.wide_of = o;      o = align256(o + sizeof(int32_t) * (size_t)L.max_split_groups);
   L.cand_count = o;   o = align256(o + sizeof(int32_t) * (size_t)L.max_cand_blocks);
   L.cand_keys = o;    o = align256(o + sizeof(uint32_t) * (size_t)L.max_cand_blocks * L.cb);
   L.cand_idx = o;     o = align256(o + sizeof(int32_t) * (size_t)L.max_cand_blocks * L.cb);
   L.cand_hist = o;    o = align256(o + sizeof(uint16_t) * (size_t)L.max_cand_blocks * kBlockBins);
   L.cand_start = o;   o = align256(o + sizeof(uint16_t) * (size_t)L.max_cand_blocks * kBlockBins);
-  L.ghist = o;        o = align256(o + sizeof(uint32_t) * (size_t)L.max_split_groups * G * kBlockBins);
+  L.ghist = o;        o = align256(o + sizeof(uint32_t) * (size_t)L.max_wide * kSharedHistWords);
   L.row_keys = o;     o = align256(o + (score_stride > 0 ? sizeof(int32_t) * (size_t)T : 0));
   L.score_rows = o;   o = align256(o + sizeof(uint32_t) * (size_t)T * (size_t)score_stride);
   L.total = o;
@@ -180,7 +193,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   __shared__ long long s_Q;
   __shared__ unsigned long long s_max_keys;
   __shared__ int2 s_empty[kPlanThreads];  // (first row, rows) of groups that see no entry
-  __shared__ unsigned char s_wide[kMaxCtas];  // split group cut into >= kWideSplit pieces
+  __shared__ int32_t s_wide[kMaxCtas];  // per split group: its wide index, or -1
   __shared__ int s_n_empty;
   // the group prefix of a batch of at most kPlanSmemRequests requests, for the
   // per-group binary search (a search over global memory is a chain of
@@ -278,12 +291,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   const bool rows_ok = G == 1 && p.L.score_stride > 0 && s_max_keys <= (unsigned long long)p.L.score_stride;
   const int n_used = (int)((W + Q - 1) / Q);
 
-  for (int i = threadIdx.x; i < kMaxCtas; i += kPlanThreads) s_wide[i] = 0;
+  for (int i = threadIdx.x; i < kMaxCtas; i += kPlanThreads) s_wide[i] = -1;
   __syncthreads();
   // Phase C: emit the pieces in tile order; CTA c's items are contiguous.
   // Group g takes stream positions [P, P + item_cost + tiles): the charged
   // tiles first, then its own from V = P + item_cost on.
-  long long tile_carry = 0, item_carry = 0, sg_carry = 0, cb_carry = 0;
+  long long tile_carry = 0, item_carry = 0, sg_carry = 0, cb_carry = 0, wide_carry = 0;
   bool overflow = false;
   for (int base = 0; base < total_groups; base += kPlanThreads) {
     const int gi = base + threadIdx.x;
@@ -311,7 +324,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
                       (!is_split || (my_sg < p.L.max_split_groups &&
                                      my_cb + (long long)gc * pieces <= p.L.max_cand_blocks));
     if (!fits) overflow = true;
-    if (fits && is_split) s_wide[my_sg] = pieces >= kWideSplit ? 1 : 0;
+    const bool is_wide = fits && is_split && G == 1 && pieces >= kWideSplit;
+    long long t_wide;
+    const long long my_wide = wide_carry + block_exclusive_scan(is_wide ? 1 : 0, &t_wide, warp_sums);
+    if (is_wide && my_wide < p.L.max_wide) s_wide[my_sg] = (int32_t)my_wide;
+    wide_carry += t_wide;
     for (long long j = 0; j < pieces && fits; ++j) {
       const long long c = V / Q + j;  // CTA of this piece
       const long long s0 = max(V, c * Q), s1 = min(V + tiles, (c + 1) * Q);
@@ -353,16 +370,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     }
   }
   const int any_overflow = __syncthreads_or(overflow ? 1 : 0);
-  // the shared histograms of wide split groups start empty (a merge empties
-  // its group's again, for the next layer of a stack)
+  // each split group's wide index; the shared histograms of wide groups start
+  // empty (a merge empties its group's again, for the next layer of a stack)
   {
-    uint4* gh = reinterpret_cast<uint4*>(p.ws + p.L.ghist);
-    const int per_sg = G * kBlockBins / 4;
+    int32_t* wide_of = reinterpret_cast<int32_t*>(p.ws + p.L.wide_of);
     const int nsg = (int)min(sg_carry, (long long)p.L.max_split_groups);
-    for (int sg = 0; sg < nsg && !any_overflow; ++sg)
-      if (s_wide[sg])
-        for (int i = threadIdx.x; i < per_sg; i += kPlanThreads)
-          gh[(size_t)sg * per_sg + i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int sg = threadIdx.x; sg < nsg; sg += kPlanThreads) wide_of[sg] = s_wide[sg];
+    uint4* gh = reinterpret_cast<uint4*>(p.ws + p.L.ghist);
+    const int n_wide = any_overflow ? 0 : (int)min(wide_carry, (long long)p.L.max_wide);
+    for (int i = threadIdx.x; i < n_wide * (kSharedHistWords / 4); i += kPlanThreads)
+      gh[i] = make_uint4(0u, 0u, 0u, 0u);
   }
   if (any_overflow) raise_status(p.status, kStatusBadMetadata);
   if (any_overflow && p.L.score_stride > 0)

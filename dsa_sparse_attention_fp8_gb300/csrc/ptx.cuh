@@ -120,9 +120,13 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 
 // Bounded wait; returns false on timeout.  `abort_flag` (shared memory)
 // lets a role stop early when another role of the CTA has already given up.
+// `limit` (iterations) is kWaitLimit except where a caller lowers it to test
+// the timeout path; waits that drain a CTA's own copies and MMAs before it
+// exits always take the full limit.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                         const volatile int* abort_flag) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+                                         const volatile int* abort_flag,
+                                         uint32_t limit = kWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 1023u) == 1023u) {
       if (abort_flag && *abort_flag) return false;

@@ -84,7 +84,9 @@ struct ScoreParams {
   uint16_t* cand_hist;   // per candidate block: level-1 histogram (kBlockBins; counts <= CB)
   uint16_t* cand_start;  // per candidate block: start offset of every bin
   int32_t* cand_count;
-  uint32_t* ghist;       // per row of a wide split group: the pieces' shared level-1 histogram
+  uint32_t* ghist;       // per wide split group: the pieces' shared histograms
+                         // (early-bound level-1 bins, then final-candidate level-1 bins)
+  const int32_t* wide_of;  // per split group: its wide index, or -1
   int32_t* done;
   int32_t* topk;
   float* scores_out;
@@ -92,6 +94,9 @@ struct ScoreParams {
   uint32_t* score_rows;      // [T, score_stride] keys of rows scored into the workspace
   int score_stride;
   int32_t* status;
+  // iterations a wait on another role may take before it gives up (kWaitLimit
+  // unless lowered to test the timeout path)
+  uint32_t wait_limit;
   // dynamic shared memory offsets (from a 1024-aligned base)
   uint32_t off_stage, off_scale, off_q, off_ckeys, off_cidx, off_wq, off_tok, off_hist, off_misc,
       off_bar;
@@ -231,40 +236,49 @@ __device__ __noinline__ BinCut find_bin(const Selector S, uint32_t hist_s, int n
   return r;
 }
 
-// find_bin over a histogram in global memory (read from L2: other SMs add to
-// it); the bin is -1 when the histogram holds fewer than `need` keys.
-__device__ __noinline__ BinCut find_bin_global(const Selector S, const uint32_t* hist, int need) {
-  const int per = kBins / S.nt;
-  const uint32_t lo = (uint32_t)(kBins - (S.tid + 1) * per);
-  uint4 q[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    q[i] = 4 * i < per ? __ldcg(reinterpret_cast<const uint4*>(hist + lo + 4u * i)) : make_uint4(0, 0, 0, 0);
+// find_bin over a histogram of nbins bins in global memory (read from L2:
+// other SMs add to it; nbins / S.nt a multiple of 4); the bin is -1 when the
+// histogram holds fewer than `need` keys.
+__device__ __noinline__ BinCut find_bin_global(const Selector S, const uint32_t* hist, int nbins,
+                                               int need) {
+  const int per = nbins / S.nt;
+  const int nq = per / 4;  // this thread's bins as uint4 words
+  const uint32_t lo = (uint32_t)(nbins - (S.tid + 1) * per);
+  const uint4* h4 = reinterpret_cast<const uint4*>(hist + lo);
   uint32_t local = 0;
+  for (int i = 0; i < nq; i += 4) {
+    uint4 q[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) local += q[i].x + q[i].y + q[i].z + q[i].w;
+    for (int u = 0; u < 4; ++u) q[u] = i + u < nq ? __ldcg(h4 + i + u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) local += q[u].x + q[u].y + q[u].z + q[u].w;
+  }
   uint32_t tot;
   uint32_t above = sel_scan(S, local, &tot);
   const uint32_t un = (uint32_t)need;
   if (S.tid == 0 && tot < un) S.s->res[0] = -1;
   if (tot >= un && above < un && un <= above + local) {
-    int bin = (int)lo + per - 1;
-    uint32_t cnt = 0;
+    // walk this thread's bins from the top, 16 at a time
+    for (int c = (nq + 3) / 4 - 1; c >= 0; --c) {
+      uint4 q[4];
 #pragma unroll
-    for (int i = 15; i >= 0; --i) {
-      if (i < per) {
-        const uint32_t c = u4_at(q[i >> 2], i & 3);
-        if (cnt == 0 && un <= above + c) {
-          bin = (int)lo + i;
-          cnt = c;
-        } else if (cnt == 0) {
-          above += c;
+      for (int u = 0; u < 4; ++u)
+        q[u] = 4 * c + u < nq ? __ldcg(h4 + 4 * c + u) : make_uint4(0, 0, 0, 0);
+      bool found = false;
+#pragma unroll
+      for (int i = 15; i >= 0; --i) {
+        const uint32_t cnt = u4_at(q[i >> 2], i & 3);
+        if (16 * c + i < per && !found && un <= above + cnt) {
+          S.s->res[0] = (int)lo + 16 * c + i;
+          S.s->res[1] = (int)above;
+          S.s->res[2] = (int)cnt;
+          found = true;
+        } else if (!found) {
+          above += cnt;
         }
       }
+      if (found) break;
     }
-    S.s->res[0] = bin;
-    S.s->res[1] = (int)above;
-    S.s->res[2] = (int)cnt;
   }
   named_bar_sync(S.bar, S.nt);
   const BinCut r{S.s->res[0], S.s->res[1], S.s->res[2]};
@@ -394,7 +408,8 @@ enum SelMode {
 __device__ __noinline__ int slot_select(const Selector S, int mode, int n, uint32_t ck_s,
                                         uint32_t ci_s, uint32_t hist_s, int k, int limit,
                                         uint32_t* gk, int32_t* gi, uint32_t* thr,
-                                        const BinCut* known = nullptr) {
+                                        const BinCut* known = nullptr,
+                                        const Thresh* given = nullptr) {
   if (mode == kSelRow && n <= k) {
     for (int i = S.tid; i < k; i += S.nt)
       __stcg(gi + i, i < n ? (int32_t)lds_u32(ci_s + 4u * (uint32_t)i) : -1);
@@ -408,13 +423,17 @@ __device__ __noinline__ int slot_select(const Selector S, int mode, int n, uint3
       }
     return n;
   }
-  // the level-1 cut, found in the histogram unless the caller knows it
-  const BinCut c = known ? *known : find_bin(S, hist_s, kBins, k);
   Thresh th;
-  if (mode != kSelRow && c.above + c.cnt <= limit)
-    th = Thresh{(uint32_t)c.bin << kHistShift, 0, 1};
-  else
-    th = refine_in_bin(S, ck_s, n, c, k, hist_s);
+  if (given) {
+    th = *given;  // the caller's threshold (in place: keep the keys it takes)
+  } else {
+    // the level-1 cut, found in the histogram unless the caller knows it
+    const BinCut c = known ? *known : find_bin(S, hist_s, kBins, k);
+    if (mode != kSelRow && c.above + c.cnt <= limit)
+      th = Thresh{(uint32_t)c.bin << kHistShift, 0, 1};
+    else
+      th = refine_in_bin(S, ck_s, n, c, k, hist_s);
+  }
   const uint32_t quota = th.early ? 0u : (uint32_t)th.need;
   const bool in_place = mode == kSelInPlace;
   if (in_place) {
@@ -520,7 +539,8 @@ __device__ __forceinline__ uint2 pack16(uint4 v) {
 
 __device__ __noinline__ void slot_emit_sorted(const Selector S, int n, uint32_t ck_s, uint32_t ci_s,
                                               uint32_t hist_s, uint32_t* gk, int32_t* gi,
-                                              uint16_t* ghist, uint16_t* gstart) {
+                                              uint16_t* ghist, uint16_t* gstart,
+                                              uint32_t* shared_hist = nullptr) {
   const int per = kBins / S.nt;  // 8 or 16 consecutive bins per thread, the top first
   const uint32_t lo = (uint32_t)(kBins - (S.tid + 1) * per);
   uint4 q[4];
@@ -532,6 +552,13 @@ __device__ __noinline__ void slot_emit_sorted(const Selector S, int n, uint32_t 
   for (int i = 0; i < 4; ++i) {
     if (4 * i < per) __stcg(reinterpret_cast<uint2*>(ghist + lo + 4 * i), pack16(q[i]));
     local += q[i].x + q[i].y + q[i].z + q[i].w;
+  }
+  if (shared_hist) {  // the group's summed histogram, for its merge
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t c = i < per ? u4_at(q[i >> 2], i & 3) : 0u;
+      if (c) atomicAdd(shared_hist + lo + i, c);
+    }
   }
   uint32_t tot;
   uint32_t run = sel_scan(S, local, &tot);  // candidates in higher bins; every bin is read
@@ -589,13 +616,15 @@ __device__ __forceinline__ int piece_of(const PieceCut* pre, int nsplit, int f, 
 __device__ __noinline__ void merge_pieces(const Selector S, const ScoreParams& p, int64_t blk0,
                                           int nsplit, uint32_t ck_s, uint32_t ci_s,
                                           uint32_t hist_s, TokSlot* ts, PieceCut* pre,
-                                          int32_t* out_row) {
+                                          int32_t* out_row, const uint32_t* summed = nullptr) {
   const int k = p.k;
-  // summed histogram of all pieces (thread: 4-bin words tid, tid + nt, ...)
+  // summed histogram of all pieces (thread: 4-bin words tid, tid + nt, ...),
+  // read from the group's shared one when the pieces kept it
   uint32_t local = 0;
   for (int w = S.tid; w < kBins / 4; w += S.nt) {
     uint4 acc = make_uint4(0, 0, 0, 0);
-    for (int sj0 = 0; sj0 < nsplit; sj0 += 8) {
+    if (summed) acc = __ldcg(reinterpret_cast<const uint4*>(summed) + w);
+    for (int sj0 = 0; sj0 < nsplit && !summed; sj0 += 8) {
       uint2 v[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u)
@@ -1003,7 +1032,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const uint32_t qpar = (uint32_t)((item_i / p.NQ) & 1);
       int okv = 1;
       // the first NQ query buffers are free from the start
-      if (lane == 0 && item_i >= p.NQ) okv = mbar_wait(bar_qempty + 8 * qb, qpar ^ 1, abort_flag);
+      if (lane == 0 && item_i >= p.NQ) okv = mbar_wait(bar_qempty + 8 * qb, qpar ^ 1, abort_flag, p.wait_limit);
       if (!__shfl_sync(0xffffffffu, okv, 0)) { ok = false; break; }
       bool q_pending = true;
       auto issue_q = [&] {
@@ -1050,7 +1079,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           if (q_pending && (p.q_ready || waited) && (item_i > 0 || seq > 0)) issue_q();
           okv = 1;
           // the first NS stages are free from the start
-          if (lane == 0 && seq >= p.NS) okv = mbar_wait(bar_empty + 8 * stage, sphase ^ 1, abort_flag);
+          if (lane == 0 && seq >= p.NS) okv = mbar_wait(bar_empty + 8 * stage, sphase ^ 1, abort_flag, p.wait_limit);
           if (!__shfl_sync(0xffffffffu, okv, 0)) { ok = false; break; }
           if (mine) {
             const uint32_t pi = (uint32_t)(lane - first);  // page of the tile
@@ -1124,7 +1153,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const uint32_t N = (uint32_t)((I.gcount * H + 15) & ~15);
         const uint32_t idesc = idesc_e4m3_f32(128, N);
         const int qb = item_i % p.NQ;
-        if (!mbar_wait(bar_qfull + 8 * qb, (uint32_t)((item_i / p.NQ) & 1), abort_flag)) {
+        if (!mbar_wait(bar_qfull + 8 * qb, (uint32_t)((item_i / p.NQ) & 1), abort_flag,
+                       p.wait_limit)) {
           ok = false;
           break;
         }
@@ -1132,8 +1162,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         const uint32_t qaddr = smem_u32(q_base + qb * p.q_bytes);
         const int ntiles = (I.k1 - I.k0 + kTileKeys * p.BPS - 1) / (kTileKeys * p.BPS);
         for (int j = 0; j < ntiles; ++j) {
-          if (!mbar_wait(bar_full + 8 * stage, sphase, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(bar_tempty + 8 * acc, aphase ^ 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar_full + 8 * stage, sphase, abort_flag, p.wait_limit)) { ok = false; break; }
+          if (!mbar_wait(bar_tempty + 8 * acc, aphase ^ 1, abort_flag, p.wait_limit)) { ok = false; break; }
           tc_fence_after();
           mbar_arrive(bar_tfull + 8 * acc);  // the tile's scales (seen via full) are ready
           const uint32_t aaddr = smem_u32(stage_base) + (uint32_t)(stage * p.BPS * kStageBytes);
@@ -1184,13 +1214,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     auto ck_of = [&](int g) -> uint32_t* { return ckeys_all + (size_t)g * p.C; };
     auto ci_of = [&](int g) -> int32_t* { return cidx_all + (size_t)g * p.C; };
     auto out_row = [&](int g) -> int32_t* { return p.topk + (int64_t)tok[g].t * p.k; };
-    // buffer-fill checks every `chk` iterations (a power of two), leaving room
-    // for what the row's warps append in between (kpi keys per iteration):
-    // every 8 iterations while the buffer keeps room for 2k candidates next to
-    // that headroom (a shrink keeps at most C - headroom), else every 4
+    // Buffer-fill checks: the rows' warps append at most kpi keys per
+    // iteration, so the next check comes after as many iterations as the
+    // fullest row's free room holds (at most 32); a row with less free room
+    // than `headroom` shrinks to a superset of its top-k first (keeping at
+    // most C - headroom), so checks stay at least headroom / kpi apart.
     const int kpi = kTileKeys * (alt ? 2 : 1);
-    const int chk = p.C - 8 * kpi >= 2 * p.k ? 8 : 4;
-    const int headroom = chk * kpi;
+    const int headroom = (p.C - 8 * kpi >= 2 * p.k ? 8 : 4) * kpi;
     long long tile_base = 0;  // tiles of earlier items of this CTA (all roles count alike)
     bool ok = true;
     const int g_first = alt ? 0 : wg;  // this thread's rows: g_first, g_first + 2, ...
@@ -1204,14 +1234,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const int split = I.split & 0xFFFF;
       const bool to_rows = I.sgroup == kSgroupRows;  // keys to the workspace, selected later
       // A row cut into many pieces shares a histogram of its candidates' level-1
-      // bins: each piece adds its own once, early in its range, and somewhat later
-      // raises its admission threshold to the bin where that histogram's count
-      // from the top reaches k.  The histogram counts distinct keys of the row
-      // (each piece publishes once, pieces are disjoint), so at least k keys of
-      // the row lie in or above that bin: no key below it is among the row's
-      // top k, in any piece.  Pieces that publish late only make the bound weaker.
-      const bool wide = !to_rows && nsplit >= kWideSplit;
-      int gstate = 0;  // 0: nothing yet, 1: published, 2: threshold adopted
+      // bins: each piece adds its own once, at its first fill check, and at its
+      // first three checks raises its admission threshold to the bin where that
+      // histogram's count from the top reaches k.  The histogram counts distinct
+      // keys of the row (each piece publishes once, pieces are disjoint), so at
+      // least k keys of the row lie in or above that bin: no key below it is
+      // among the row's top k, in any piece.  Pieces that publish late only make
+      // the bound weaker.  The pieces also sum their final candidates' bins
+      // into a second shared histogram, which the merge reads instead of
+      // adding up every piece's.
+      const int wid = (!to_rows && nsplit >= kWideSplit && p.G == 1) ? __ldg(p.wide_of + I.sgroup) : -1;
+      const bool wide = wid >= 0;
+      int gstate = 0;  // checks done since the item began (wide items publish at the first)
+      auto early_hist = [&](int) { return p.ghist + (int64_t)wid * kSharedHistWords; };
+      auto final_hist = [&](int g) { return early_hist(g) + kBins; };
       for (int g = g_first; g < I.gcount; g += 2) {
         const int t = I.t0 + g;
         if (sets_up) {
@@ -1230,9 +1266,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       named_bar_sync(3, 256);
       const int ntiles = (I.k1 - I.k0 + KS - 1) / KS;
       const int units = ntiles * p.BPS;  // 128-key blocks of the item
-      const bool may_fill = (I.k1 - I.k0) > p.C;
+      const bool may_fill = !to_rows && (I.k1 - I.k0) > p.C;
       const int u0 = alt ? wg : 0;
       const int iters = alt ? (units + 1) / 2 : units;
+      // iteration of the next fill check; a wide item checks after 4 and 8
+      // iterations, so that its pieces share their bound early
+      int next_chk = wide ? 3 : min(32, p.C / kpi) - 1;
+
       for (int m = 0; m < iters; ++m) {
         const int u = u0 + m * step;  // block u = (tile j, block b of the tile)
         const int j = u >> p.lg_bps, b = u & (p.BPS - 1);
@@ -1243,7 +1283,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           const int key = I.k0 + j * KS + b * kTileKeys + row;
           // no early exit on the abort flag here: the warps of a warpgroup must take
           // the same branch, so they all wait on the same phase with the same limit
-          if (!mbar_wait(bar_tfull + 8 * acc, aphase, nullptr)) ok = false;
+          if (!mbar_wait(bar_tfull + 8 * acc, aphase, nullptr, p.wait_limit)) ok = false;
           if (ok) {
             tc_fence_after();
             // the key's scale; zero (never a written scale) for a page outside the pool
@@ -1273,7 +1313,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
           }
         }
-        if (may_fill && (m & (chk - 1)) == chk - 1 && m + 1 < iters) {
+        const bool check = may_fill && m == next_chk && m + 1 < iters;
+        if (check) {
           // the row's appending warps only (its warpgroup, or both for a decode row)
           if (!ok) misc->epi_abort = 1;
           named_bar_sync(S.bar, S.nt);  // every append so far is visible
@@ -1296,35 +1337,40 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             if (wide && gstate == 0) {
               named_bar_sync(S.bar, S.nt);  // the histograms are current
               for (int g = g_first; g < I.gcount; g += 2) {
-                uint32_t* gh = p.ghist + ((int64_t)I.sgroup * p.G + g) * kBins;
+                uint32_t* gh = early_hist(g);
                 for (int b = S.tid; b < kBins; b += S.nt) {
                   const uint32_t c = lds_u32(hist_of(g) + 4u * (uint32_t)b);
                   if (c) atomicAdd(gh + b, c);
                 }
               }
-              gstate = 1;
-            } else if (wide && gstate == 1) {
+            }
+            if (wide && gstate < 3) {
+              // adopt the shared bound (at the first three checks: it only rises
+              // as the other pieces publish)
               for (int g = g_first; g < I.gcount; g += 2) {
-                const BinCut c = find_bin_global(S, p.ghist + ((int64_t)I.sgroup * p.G + g) * kBins, p.k);
+                const BinCut c = find_bin_global(S, early_hist(g), kBins, p.k);
                 const uint32_t gthr = c.bin > 0 ? ((uint32_t)c.bin << kHistShift) - 1u : 0u;
                 if (gthr > tok[g].thr) {
                   // keep only the candidates at or above that bin
                   const int n = tok[g].count;
                   uint32_t thr = 0;
-                  const BinCut cut{c.bin, 0, 0};
+                  const Thresh keep{gthr + 1u, 0, 1};
                   const int kept = slot_select(S, kSelInPlace, n, smem_u32(ck_of(g)),
                                                smem_u32(ci_of(g)), hist_of(g), p.k, 0, nullptr,
-                                               nullptr, &thr, &cut);
+                                               nullptr, &thr, nullptr, &keep);
                   if (S.tid == 0) {
                     tok[g].count = kept;
                     tok[g].thr = gthr;
                   }
                 }
               }
-              gstate = 2;
             }
+            ++gstate;
           }
           named_bar_sync(S.bar, S.nt);
+          int room = p.C;
+          for (int g = g_first; g < I.gcount; g += 2) room = min(room, p.C - tok[g].count);
+          next_chk = m + max(1, min(wide && gstate < 2 ? 4 : 32, room / kpi));
         }
       }
       tile_base += ntiles;
@@ -1349,7 +1395,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           }
           slot_emit_sorted(S, n, smem_u32(ck_of(g)), smem_u32(ci_of(g)), hist_of(g),
                            p.cand_keys + blk * p.CB, p.cand_idx + blk * p.CB,
-                           p.cand_hist + blk * kBlockBins, p.cand_start + blk * kBlockBins);
+                           p.cand_hist + blk * kBlockBins, p.cand_start + blk * kBlockBins,
+                           wide ? final_hist(g) : nullptr);
           if (S.tid == 0) __stcg(p.cand_count + blk, n);
         }
       }
@@ -1368,13 +1415,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             const int64_t blk0 = (int64_t)I.cand_block + (int64_t)g * nsplit;
             PieceCut* pre = reinterpret_cast<PieceCut*>(misc->piece_pre) + (alt ? 0 : wg * (kMaxCtas + 1));
             merge_pieces(S, p, blk0, nsplit, smem_u32(ck_of(g)), smem_u32(ci_of(g)), hist_of(g),
-                         &tok[g], pre, out_row(g));
+                         &tok[g], pre, out_row(g), wide ? final_hist(g) : nullptr);
             named_bar_sync(S.bar, S.nt);  // the slot is free for the next row
           }
           if (wide)  // the shared histograms are empty again for the next layer
             for (int g = g_first; g < I.gcount; g += 2)
-              for (int b = S.tid; b < kBins; b += S.nt)
-                __stcg(p.ghist + ((int64_t)I.sgroup * p.G + g) * kBins + b, 0u);
+              for (int b = S.tid; b < kSharedHistWords; b += S.nt) __stcg(early_hist(g) + b, 0u);
           if (epi == 0 && lane == 0) p.done[I.sgroup] = 0;  // ready for the next layer
         }
       }
