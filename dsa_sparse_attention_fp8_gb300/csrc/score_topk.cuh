@@ -846,6 +846,54 @@ __device__ __forceinline__ float relu_weighted_sum(uint32_t taddr, uint32_t wq_s
   return sum;
 }
 
+// The same sums for two blocks at once (TMEM column bases ta and tb, same
+// weights): the two FMA chains are independent, so each hides the other's
+// latency, and the weights are read once for both.  Columns go in chunks of
+// 32 per block so that both chunks and their weights stay in registers.
+template <int H>
+__device__ __forceinline__ float2 relu_weighted_sum2(uint32_t ta, uint32_t tb, uint32_t wq_s) {
+  constexpr int CH = H >= 32 ? 32 : H;             // columns per chunk and block
+  constexpr int NA = CH >= 16 ? 4 : CH / 4;        // pair accumulators per block
+  unsigned long long aa[NA], ab[NA];
+#pragma unroll
+  for (int i = 0; i < NA; ++i) aa[i] = ab[i] = 0ull;
+#pragma unroll
+  for (int c0 = 0; c0 < H; c0 += CH) {
+    uint4 ww[CH / 4];
+#pragma unroll
+    for (int i = 0; i < CH / 4; ++i) ww[i] = lds_v4(wq_s + 4u * (uint32_t)(c0 + 4 * i));
+    uint32_t va[CH], vb[CH];
+    tmem_ld<CH>(ta + c0, va);
+    tmem_ld<CH>(tb + c0, vb);
+    tmem_ld_wait();
+#pragma unroll
+    for (int h = 0; h < CH; h += 4) {
+      const unsigned long long w01 =
+          pack_f32x2(__uint_as_float(ww[h / 4].x), __uint_as_float(ww[h / 4].y));
+      const unsigned long long w23 =
+          pack_f32x2(__uint_as_float(ww[h / 4].z), __uint_as_float(ww[h / 4].w));
+      unsigned long long& a = aa[(h / 4) % NA];
+      unsigned long long& b = ab[(h / 4) % NA];
+      a = fma_f32x2(w01, pack_f32x2(fmaxf(__uint_as_float(va[h]), 0.f),
+                                    fmaxf(__uint_as_float(va[h + 1]), 0.f)), a);
+      b = fma_f32x2(w01, pack_f32x2(fmaxf(__uint_as_float(vb[h]), 0.f),
+                                    fmaxf(__uint_as_float(vb[h + 1]), 0.f)), b);
+      a = fma_f32x2(w23, pack_f32x2(fmaxf(__uint_as_float(va[h + 2]), 0.f),
+                                    fmaxf(__uint_as_float(va[h + 3]), 0.f)), a);
+      b = fma_f32x2(w23, pack_f32x2(fmaxf(__uint_as_float(vb[h + 2]), 0.f),
+                                    fmaxf(__uint_as_float(vb[h + 3]), 0.f)), b);
+    }
+  }
+  float2 r = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < NA; ++i) {
+    const float2 ta2 = unpack_f32x2(aa[i]), tb2 = unpack_f32x2(ab[i]);
+    r.x += ta2.x + ta2.y;
+    r.y += tb2.x + tb2.y;
+  }
+  return r;
+}
+
 template <int H>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     score_topk_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -1269,51 +1317,83 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const bool may_fill = !to_rows && (I.k1 - I.k0) > p.C;
       const int u0 = alt ? wg : 0;
       const int iters = alt ? (units + 1) / 2 : units;
-      // iteration of the next fill check; a wide item checks after 4 and 8
-      // iterations, so that its pieces share their bound early
-      int next_chk = wide ? 3 : min(32, p.C / kpi) - 1;
-
-      for (int m = 0; m < iters; ++m) {
-        const int u = u0 + m * step;  // block u = (tile j, block b of the tile)
-        const int j = u >> p.lg_bps, b = u & (p.BPS - 1);
-        if (u < units && ok) {
-          const long long seq = tile_base + j;
-          const int acc = (int)((uint32_t)seq & (uint32_t)(p.NB - 1));
-          const uint32_t aphase = (uint32_t)(seq >> p.lg_nb) & 1u;
-          const int key = I.k0 + j * KS + b * kTileKeys + row;
+      // This warpgroup's blocks go two at a time (iterations m and m + 1):
+      // their head sums interleave (two independent FMA chains per thread)
+      // and share the weight loads, and each pair pays the loop's waits and
+      // fences once.  Fill checks come after pairs: `next_chk` is the pair
+      // after which the next one runs; a wide item checks after its 2nd and
+      // 4th pair, so that its pieces share their bound early.
+      int next_chk = wide ? 1 : max(0, min(16, p.C / (2 * kpi)) - 1);
+      for (int m = 0; m < iters; m += 2) {
+        const int uA = u0 + m * step, uB = uA + step;  // block u = (tile j, block b of the tile)
+        const bool hasA = uA < units;
+        const bool hasB = hasA && m + 1 < iters && uB < units;
+        const int jA = uA >> p.lg_bps, bA = uA & (p.BPS - 1);
+        const int jB = uB >> p.lg_bps, bB = uB & (p.BPS - 1);
+        const long long seqA = tile_base + jA, seqB = tile_base + jB;
+        const int accA = (int)((uint32_t)seqA & (uint32_t)(p.NB - 1));
+        const int accB = (int)((uint32_t)seqB & (uint32_t)(p.NB - 1));
+        if (hasA && ok) {
+          const int keyA = I.k0 + jA * KS + bA * kTileKeys + row;
+          const int keyB = I.k0 + jB * KS + bB * kTileKeys + row;
           // no early exit on the abort flag here: the warps of a warpgroup must take
           // the same branch, so they all wait on the same phase with the same limit
-          if (!mbar_wait(bar_tfull + 8 * acc, aphase, nullptr, p.wait_limit)) ok = false;
+          if (!mbar_wait(bar_tfull + 8 * accA, (uint32_t)(seqA >> p.lg_nb) & 1u, nullptr,
+                         p.wait_limit))
+            ok = false;
+          if (ok && hasB &&
+              !mbar_wait(bar_tfull + 8 * accB, (uint32_t)(seqB >> p.lg_nb) & 1u, nullptr,
+                         p.wait_limit))
+            ok = false;
           if (ok) {
             tc_fence_after();
-            // the key's scale; zero (never a written scale) for a page outside the pool
-            const float sc = __uint_as_float(
-                lds_u32(scale_ring_s + ((uint32_t)seq & (uint32_t)(p.NR - 1)) * (uint32_t)(p.BPS * kScaleSlotBytes) +
-                        (uint32_t)(b * kTileKeys + row) * 4u));
-            const bool kvalid = sc > 0.f && key < I.k1;
-            const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) +
-                                   (uint32_t)((acc * p.BPS + b) * p.n_max);
+            // the keys' scales; zero (never a written scale) for a page outside the pool
+            const uint32_t slot_b = (uint32_t)(p.BPS * kScaleSlotBytes);
+            const float scA = __uint_as_float(
+                lds_u32(scale_ring_s + ((uint32_t)seqA & (uint32_t)(p.NR - 1)) * slot_b +
+                        (uint32_t)(bA * kTileKeys + row) * 4u));
+            const float scB = hasB ? __uint_as_float(lds_u32(
+                                         scale_ring_s + ((uint32_t)seqB & (uint32_t)(p.NR - 1)) * slot_b +
+                                         (uint32_t)(bB * kTileKeys + row) * 4u))
+                                   : 0.f;
+            const bool kvalidA = scA > 0.f && keyA < I.k1;
+            const bool kvalidB = hasB && scB > 0.f && keyB < I.k1;
+            const uint32_t lanes = tmem_base + ((uint32_t)(quad * 32) << 16);
+            const uint32_t tA = lanes + (uint32_t)((accA * p.BPS + bA) * p.n_max);
+            // without a second block the pair's second sum repeats the first (unused)
+            const uint32_t tB = hasB ? lanes + (uint32_t)((accB * p.BPS + bB) * p.n_max) : tA;
             for (int g = g_first; g < I.gcount; g += 2) {
-              const float sum =
-                  relu_weighted_sum<H>(tbase + (uint32_t)(g * H), smem_u32(wq_all + g * H));
-              const float score = sum * sc;
-              const bool valid = kvalid && key <= tok[g].pos;
-              if (p.scores_out && valid && key < p.scores_ld)
-                p.scores_out[(int64_t)tok[g].t * p.scores_ld + key] = score;
-              const uint32_t kk = valid ? score_key(score) : 0u;
+              const float2 sum = relu_weighted_sum2<H>(tA + (uint32_t)(g * H), tB + (uint32_t)(g * H),
+                                                       smem_u32(wq_all + g * H));
+              const float scoreA = sum.x * scA, scoreB = sum.y * scB;
+              const int pos = tok[g].pos;
+              const bool validA = kvalidA && keyA <= pos, validB = kvalidB && keyB <= pos;
+              if (p.scores_out) {
+                if (validA && keyA < p.scores_ld) p.scores_out[(int64_t)tok[g].t * p.scores_ld + keyA] = scoreA;
+                if (validB && keyB < p.scores_ld) p.scores_out[(int64_t)tok[g].t * p.scores_ld + keyB] = scoreB;
+              }
+              const uint32_t kkA = validA ? score_key(scoreA) : 0u;
+              const uint32_t kkB = validB ? score_key(scoreB) : 0u;
               if (to_rows) {
-                if (key < I.k1) p.score_rows[(int64_t)tok[g].t * p.score_stride + key] = kk;
+                uint32_t* srow = p.score_rows + (int64_t)tok[g].t * p.score_stride;
+                if (keyA < I.k1) srow[keyA] = kkA;
+                if (hasB && keyB < I.k1) srow[keyB] = kkB;
               } else {
-                slot_append(kk, key, tok[g].thr, &tok[g], ckeys_all + (size_t)g * p.C,
+                slot_append(kkA, keyA, tok[g].thr, &tok[g], ckeys_all + (size_t)g * p.C,
+                            cidx_all + (size_t)g * p.C, hist_of(g));
+                slot_append(kkB, keyB, tok[g].thr, &tok[g], ckeys_all + (size_t)g * p.C,
                             cidx_all + (size_t)g * p.C, hist_of(g));
               }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+            if (lane == 0) {
+              mbar_arrive(bar_tempty + 8 * accA);
+              if (hasB) mbar_arrive(bar_tempty + 8 * accB);
+            }
           }
         }
-        const bool check = may_fill && m == next_chk && m + 1 < iters;
+        const bool check = may_fill && m / 2 == next_chk && m + 2 < iters;
         if (check) {
           // the row's appending warps only (its warpgroup, or both for a decode row)
           if (!ok) misc->epi_abort = 1;
@@ -1370,7 +1450,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           named_bar_sync(S.bar, S.nt);
           int room = p.C;
           for (int g = g_first; g < I.gcount; g += 2) room = min(room, p.C - tok[g].count);
-          next_chk = m + max(1, min(wide && gstate < 2 ? 4 : 32, room / kpi));
+          // the pairs until the next check: as many as the free room holds
+          next_chk = m / 2 + max(1, min(wide && gstate < 2 ? 2 : 16, room / (2 * kpi)));
         }
       }
       tile_base += ntiles;
