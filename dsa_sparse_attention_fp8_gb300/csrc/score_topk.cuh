@@ -12,19 +12,24 @@
 // the shared [max_num_batched_tokens, index_topk] buffer).
 //
 // Structure (one CTA per SM, 10 warps):
-//   warp 0      producer: per key tile (128 keys = 2 pages) two TMA loads of
-//               64 x 128 B key rows into a 128B-swizzled stage, and 16-byte
-//               cp.async copies of the pages' 2 x 256 B of scales into a ring
-//               of scale slots; the query tile of each item (double-buffered
-//               when it is small).
+//   warp 0      producer: per page of a key tile (128 keys = 2 pages, or 4
+//               pages for the 256-key decode stages) one TMA load of its
+//               64 x 128 B key rows into a 128B-swizzled stage and one of its
+//               256 B of scales into a ring of scale slots, both counted by
+//               one expect-tx arrival; the query tile of each item
+//               (double-buffered when it is small).
 //   warp 1      owns tensor memory; one lane issues 4 tcgen05.mma (K = 32
-//               each) per tile: D[key, row*H + head] += k . q, FP32 in TMEM.
+//               each) per 128-key block: D[key, row*H + head] += k . q, FP32
+//               in TMEM.
 //   warps 2-9   epilogue, two warpgroups; thread = one key row of the tile
-//               (its TMEM lane).  For each query row of the group: read the
-//               H accumulators, ReLU, weight, sum, times the key's scale,
-//               then stream the score into an exact top-k buffer in shared
-//               memory (append above the running threshold; when the buffer
-//               fills, radix-select the k largest and raise the threshold).
+//               (its TMEM lane).  Each warpgroup takes two of its blocks per
+//               iteration: for each query row of the group it reads the H
+//               accumulators of both, ReLU, weight and sum them in two
+//               interleaved chains, times the keys' scales, then streams the
+//               scores into an exact top-k buffer in shared memory (append
+//               above the running threshold; when the buffer nears full,
+//               select in place the candidates at or above the k-th largest's
+//               bin and raise the threshold).
 // No score row goes to global memory (except the optional debug dump).
 #pragma once
 
@@ -348,7 +353,7 @@ __device__ __forceinline__ BinCut find_bin_warp(uint32_t hist_s, int nbins, int 
 // every warp on its own).  Stops as soon as a whole sub-bin is taken.  The
 // caller's reads of scratch_s are complete.
 __device__ __noinline__ Thresh refine_in_bin(const Selector S, uint32_t ck_s, int n, BinCut c,
-                                             int k, uint32_t scratch_s) {
+                                             int k, uint32_t scratch_s, int coarse_limit = 0) {
   Thresh th{(uint32_t)c.bin << kHistShift, k - c.above, 0};
   uint32_t mask = 0xFFFFFFFFu << kHistShift;
   if (c.cnt == th.need) {
@@ -375,6 +380,12 @@ __device__ __noinline__ Thresh refine_in_bin(const Selector S, uint32_t ck_s, in
     }
     named_bar_sync(S.bar, S.nt);
     const BinCut c2 = find_bin_warp(scratch_s, nb, th.need);
+    if (level == 0 && c.above + c2.above + c2.cnt <= coarse_limit) {
+      // keep the whole sub-bin of the k-th largest: a superset within the limit
+      th.prefix |= (uint32_t)c2.bin << shift;
+      th.early = 1;
+      break;
+    }
     th.need -= c2.above;
     th.prefix |= (uint32_t)c2.bin << shift;
     mask |= dm << shift;
@@ -429,10 +440,15 @@ __device__ __noinline__ int slot_select(const Selector S, int mode, int n, uint3
   } else {
     // the level-1 cut, found in the histogram unless the caller knows it
     const BinCut c = known ? *known : find_bin(S, hist_s, kBins, k);
-    if (mode != kSelRow && c.above + c.cnt <= limit)
+    // in place, a kept set near the limit would leave little room and bring
+    // the next shrink soon: keep the whole cut bin only while it frees at
+    // least half the room above k, else cut at the k-th's sub-bin (one more
+    // pass), else exactly
+    const int keep = mode == kSelInPlace ? k + (limit - k) / 2 : limit;
+    if (mode != kSelRow && c.above + c.cnt <= keep)
       th = Thresh{(uint32_t)c.bin << kHistShift, 0, 1};
     else
-      th = refine_in_bin(S, ck_s, n, c, k, hist_s);
+      th = refine_in_bin(S, ck_s, n, c, k, hist_s, mode == kSelInPlace ? keep : 0);
   }
   const uint32_t quota = th.early ? 0u : (uint32_t)th.need;
   const bool in_place = mode == kSelInPlace;
@@ -515,6 +531,33 @@ __device__ __forceinline__ void slot_append(uint32_t key, int32_t idx, uint32_t 
     const int p = base + __popc(m & lanemask_lt());
     ckeys[p] = key;
     cidx[p] = idx;
+  }
+}
+
+// The same for two candidates per thread (two blocks of keys): one shared
+// atomic reserves the warp's slots for both.
+__device__ __forceinline__ void slot_append2(uint32_t ka, int32_t ia, uint32_t kb, int32_t ib,
+                                             uint32_t thr, TokSlot* ts, uint32_t* ckeys,
+                                             int32_t* cidx, uint32_t hist_s) {
+  const bool pa = ka > thr, pb = kb > thr;
+  const uint32_t ma = __ballot_sync(0xffffffffu, pa), mb = __ballot_sync(0xffffffffu, pb);
+  if ((ma | mb) == 0) return;
+  const uint32_t na = (uint32_t)__popc(ma);
+  int base = 0;
+  if (lane_id() == 0) base = (int)atom_add_shared(smem_u32(&ts->count), na + (uint32_t)__popc(mb));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  red_add_shared_if(pa, hist_s + 4 * (ka >> kHistShift), 1u);
+  red_add_shared_if(pb, hist_s + 4 * (kb >> kHistShift), 1u);
+  const uint32_t lt = lanemask_lt();
+  if (pa) {
+    const int q = base + __popc(ma & lt);
+    ckeys[q] = ka;
+    cidx[q] = ia;
+  }
+  if (pb) {
+    const int q = base + (int)na + __popc(mb & lt);
+    ckeys[q] = kb;
+    cidx[q] = ib;
   }
 }
 
@@ -1379,10 +1422,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 if (keyA < I.k1) srow[keyA] = kkA;
                 if (hasB && keyB < I.k1) srow[keyB] = kkB;
               } else {
-                slot_append(kkA, keyA, tok[g].thr, &tok[g], ckeys_all + (size_t)g * p.C,
-                            cidx_all + (size_t)g * p.C, hist_of(g));
-                slot_append(kkB, keyB, tok[g].thr, &tok[g], ckeys_all + (size_t)g * p.C,
-                            cidx_all + (size_t)g * p.C, hist_of(g));
+                slot_append2(kkA, keyA, kkB, keyB, tok[g].thr, &tok[g],
+                             ckeys_all + (size_t)g * p.C, cidx_all + (size_t)g * p.C, hist_of(g));
               }
             }
             tc_fence_before();
