@@ -110,7 +110,7 @@ struct ScoreParams {
 struct SelScratch {
   int scan[16];                // per-warp partials of a scan (up to 256 threads), 2 buffers
   int res[4];                  // a bin search's result (bin, above, count)
-  uint32_t table[256];         // per-(chunk, warp) counts of a compaction, then their offsets
+  uint32_t table[256];         // sub-bin counts while a cut bin is refined
 };
 
 struct Misc {
@@ -398,6 +398,58 @@ __device__ __noinline__ Thresh refine_in_bin(const Selector S, uint32_t ck_s, in
   return th;
 }
 
+constexpr int kCompactGroups = 8;  // 32-candidate groups per warp and batch
+
+// In-place compaction of a slot's n candidates to those with key >= lo
+// (an early threshold: no ties to ration); returns how many are kept.
+// Batches of kCompactGroups groups of 32 consecutive candidates per warp: a
+// group's kept ones go out in lane order after those of the warp's earlier
+// groups, of the lower warps and of earlier batches, so every write lands at
+// or below the candidates still to be read; one barrier per batch exchanges
+// the warps' counts once every thread holds its batch.
+__device__ __noinline__ int compact_early(const Selector S, int n, uint32_t ck_s, uint32_t ci_s,
+                                          uint32_t lo) {
+  const int lane = S.tid & 31, w = S.tid >> 5, nw = S.nt >> 5;
+  const uint32_t lt = lanemask_lt();
+  if (lo == 0u) lo = 1u;  // key 0 never enters a slot
+  const int per_batch = kCompactGroups * S.nt;
+  int carry = 0;
+  for (int b0 = 0, it = 0; b0 < n; b0 += per_batch, ++it) {
+    const int i0 = b0 + w * (kCompactGroups * 32) + lane;
+    uint32_t kk[kCompactGroups], ix[kCompactGroups], m[kCompactGroups];
+#pragma unroll
+    for (int u = 0; u < kCompactGroups; ++u) kk[u] = lds_u32_if(i0 + 32 * u < n, ck_s + 4u * (uint32_t)(i0 + 32 * u));
+    int cnt = 0;
+#pragma unroll
+    for (int u = 0; u < kCompactGroups; ++u) {
+      m[u] = __ballot_sync(0xffffffffu, kk[u] >= lo);
+      cnt += __popc(m[u]);
+    }
+    int* buf = S.s->scan + 8 * (it & 1);
+    if (lane == 0) buf[w] = cnt;
+#pragma unroll
+    for (int u = 0; u < kCompactGroups; ++u)
+      ix[u] = lds_u32_if((m[u] >> lane) & 1u, ci_s + 4u * (uint32_t)(i0 + 32 * u));
+    named_bar_sync(S.bar, S.nt);
+    int a = carry, tot = 0;
+    for (int v = 0; v < nw; ++v) {
+      const int c = buf[v];
+      a += v < w ? c : 0;
+      tot += c;
+    }
+#pragma unroll
+    for (int u = 0; u < kCompactGroups; ++u) {
+      const uint32_t pos = (uint32_t)(a + __popc(m[u] & lt));
+      const bool wr = (m[u] >> lane) & 1u;
+      sts_u32_if(wr, ck_s + 4u * pos, kk[u]);
+      sts_u32_if(wr, ci_s + 4u * pos, ix[u]);
+      a += __popc(m[u]);
+    }
+    carry += tot;
+  }
+  return carry;
+}
+
 enum SelMode {
   kSelRow = 0,     // exact top-min(n, k) indices to a row of the top-k buffer, -1 after
   kSelBlock = 1,   // a superset of the top-k of at most `limit` to a candidate block
@@ -407,10 +459,9 @@ enum SelMode {
 // One selection over a slot's n candidates (key buffer ck_s, index buffer
 // ci_s, level-1 histogram hist_s).  kSelBlock / kSelInPlace keep every
 // candidate if n <= limit, else every one in or above the level-1 bin of the
-// k-th largest if that fits, else exactly k.  Output order is thread-major
-// (thread t's candidates in visiting order after those of threads before
-// it): deterministic, ties at an exact threshold taken in that order up to
-// the quota.  `known`, if given, is the level-1 cut of the k-th largest
+// k-th largest if that fits, else exactly k.  Output order is the buffer's
+// order (deterministic); ties at an exact threshold are taken in that order
+// up to the quota.  `known`, if given, is the level-1 cut of the k-th largest
 // (hist_s is then only scratch).  Row output is staged in shared memory
 // (hist_s, after its last use) and copied out coalesced; in place, the kept candidates are staged in
 // registers one batch at a time behind a barrier per batch.  Returns the
@@ -435,6 +486,7 @@ __device__ __noinline__ int slot_select(const Selector S, int mode, int n, uint3
     return n;
   }
   Thresh th;
+  int above_cut = 0;  // candidates in the bins above the cut bin
   if (given) {
     th = *given;  // the caller's threshold (in place: keep the keys it takes)
   } else {
@@ -445,65 +497,82 @@ __device__ __noinline__ int slot_select(const Selector S, int mode, int n, uint3
     // least half the room above k, else cut at the k-th's sub-bin (one more
     // pass), else exactly
     const int keep = mode == kSelInPlace ? k + (limit - k) / 2 : limit;
+    above_cut = c.above;
     if (mode != kSelRow && c.above + c.cnt <= keep)
       th = Thresh{(uint32_t)c.bin << kHistShift, 0, 1};
     else
-      th = refine_in_bin(S, ck_s, n, c, k, hist_s, mode == kSelInPlace ? keep : 0);
+      th = refine_in_bin(S, ck_s, n, c, k, smem_u32(S.s->table), mode == kSelInPlace ? keep : 0);
   }
   const uint32_t quota = th.early ? 0u : (uint32_t)th.need;
   const bool in_place = mode == kSelInPlace;
-  if (in_place) {
-    clear_bins(S, hist_s, kBins);
-    named_bar_sync(S.bar, S.nt);
-  }
   // Batch-major output order: batch b's candidates follow every kept one of
   // earlier batches, so in place a batch's writes land at or below its own
   // candidates; once every thread holds the batch it may be overwritten.
+  // Inside a batch, warp w holds kSelBatch groups of 32 consecutive
+  // candidates; a group's kept ones go out in lane order after those of the
+  // warp's earlier groups and of the lower warps (counts from ballots, one
+  // barrier to exchange the warps' totals).  An early threshold has no ties.
   uint32_t carry_a = 0, carry_t = 0;  // kept-above / tie counts of earlier batches
-  const int batches = (n + kSelBatch * S.nt - 1) / (kSelBatch * S.nt);
-  for (int b = 0; b < batches; ++b) {
-    const int i0 = b * kSelBatch * S.nt + S.tid;
-    uint32_t kk[kSelBatch], ix[kSelBatch];
+  if (in_place && th.early) {
+    carry_a = (uint32_t)compact_early(S, n, ck_s, ci_s, th.prefix);
+  } else {
+    const int lane = S.tid & 31, w = S.tid >> 5, nw = S.nt >> 5;
+    const uint32_t lt = lanemask_lt();
+    const int per_batch = kSelBatch * S.nt;
+    const bool ties = !th.early;
+    for (int b0 = 0, it = 0; b0 < n; b0 += per_batch, ++it) {
+      const int i0 = b0 + w * (kSelBatch * 32) + lane;
+      uint32_t kk[kSelBatch], ix[kSelBatch], am[kSelBatch], tm[kSelBatch];
 #pragma unroll
-    for (int u = 0; u < kSelBatch; ++u) {
-      const int i = i0 + u * S.nt;
-      kk[u] = lds_u32_if(i < n, ck_s + 4u * (uint32_t)i);
-    }
-    uint32_t cnt = 0;  // above | ties << 16
-#pragma unroll
-    for (int u = 0; u < kSelBatch; ++u)
-      cnt += (sel_above(kk[u], th) ? 1u : 0u) + (sel_tie(kk[u], th) ? 0x10000u : 0u);
-    uint32_t tot;
-    const uint32_t off = sel_scan(S, cnt, &tot, b & 1);
-    uint32_t a = carry_a + (off & 0xFFFFu), t = carry_t + (off >> 16);
-#pragma unroll
-    for (int u = 0; u < kSelBatch; ++u) {
-      const int i = i0 + u * S.nt;
-      ix[u] = lds_u32_if(sel_above(kk[u], th) || sel_tie(kk[u], th), ci_s + 4u * (uint32_t)i);
-    }
-    if (in_place) named_bar_sync(S.bar, S.nt);
-#pragma unroll
-    for (int u = 0; u < kSelBatch; ++u) {
-      const bool above = sel_above(kk[u], th), tie = sel_tie(kk[u], th);
-      const bool wr = above || (tie && t < quota);
-      const uint32_t pos = a + min(quota, t);
-      if (mode == kSelRow) {
-        sts_u32_if(wr, hist_s + 4u * pos, ix[u]);
-      } else if (mode == kSelBlock) {
-        if (wr) {
-          __stcg(gk + pos, kk[u]);
-          __stcg(gi + pos, (int32_t)ix[u]);
-        }
-      } else {
-        sts_u32_if(wr, ck_s + 4u * pos, kk[u]);
-        sts_u32_if(wr, ci_s + 4u * pos, ix[u]);
-        red_add_shared_if(wr, hist_s + 4u * (kk[u] >> kHistShift), 1u);
+      for (int u = 0; u < kSelBatch; ++u) {
+        const int i = i0 + 32 * u;
+        kk[u] = lds_u32_if(i < n, ck_s + 4u * (uint32_t)i);
       }
-      a += above ? 1u : 0u;
-      t += tie ? 1u : 0u;
+      uint32_t cnt = 0;  // this warp's above | ties << 16
+#pragma unroll
+      for (int u = 0; u < kSelBatch; ++u) {
+        am[u] = __ballot_sync(0xffffffffu, sel_above(kk[u], th));
+        tm[u] = ties ? __ballot_sync(0xffffffffu, sel_tie(kk[u], th)) : 0u;
+        cnt += (uint32_t)__popc(am[u]) + ((uint32_t)__popc(tm[u]) << 16);
+      }
+      int* buf = S.s->scan + 8 * (it & 1);
+      if (lane == 0) buf[w] = (int)cnt;
+#pragma unroll
+      for (int u = 0; u < kSelBatch; ++u)
+        ix[u] = lds_u32_if(((am[u] | tm[u]) >> lane) & 1u, ci_s + 4u * (uint32_t)(i0 + 32 * u));
+      named_bar_sync(S.bar, S.nt);  // the warps' totals; every thread holds its batch
+      uint32_t a = carry_a, t = carry_t, tot = 0;
+      for (int v = 0; v < nw; ++v) {
+        const uint32_t c = (uint32_t)buf[v];
+        if (v < w) {
+          a += c & 0xFFFFu;
+          t += c >> 16;
+        }
+        tot += c;
+      }
+#pragma unroll
+      for (int u = 0; u < kSelBatch; ++u) {
+        const bool above = (am[u] >> lane) & 1u, tie = (tm[u] >> lane) & 1u;
+        const uint32_t ta = t + (uint32_t)__popc(tm[u] & lt);
+        const bool wr = above || (tie && ta < quota);
+        const uint32_t pos = a + (uint32_t)__popc(am[u] & lt) + min(quota, ta);
+        if (mode == kSelRow) {
+          sts_u32_if(wr, hist_s + 4u * pos, ix[u]);
+        } else if (mode == kSelBlock) {
+          if (wr) {
+            __stcg(gk + pos, kk[u]);
+            __stcg(gi + pos, (int32_t)ix[u]);
+          }
+        } else {
+          sts_u32_if(wr, ck_s + 4u * pos, kk[u]);
+          sts_u32_if(wr, ci_s + 4u * pos, ix[u]);
+        }
+        a += (uint32_t)__popc(am[u]);
+        t += (uint32_t)__popc(tm[u]);
+      }
+      carry_a += tot & 0xFFFFu;
+      carry_t += tot >> 16;
     }
-    carry_a += tot & 0xFFFFu;
-    carry_t += tot >> 16;
   }
   const int total = (int)(carry_a + min(quota, carry_t));
   named_bar_sync(S.bar, S.nt);
@@ -512,8 +581,85 @@ __device__ __noinline__ int slot_select(const Selector S, int mode, int n, uint3
       __stcg(gi + i, i < total ? (int32_t)lds_u32(hist_s + 4u * (uint32_t)i) : -1);
   } else if (in_place) {
     *thr = th.early ? (th.prefix > 0u ? th.prefix - 1u : 0u) : th.prefix;
+    // The kept set's histogram without recounting: every candidate of the
+    // bins above the cut bin is kept, none below it; the cut bin keeps its
+    // count when the threshold is its lower edge, else the rest of `total`.
+    const uint32_t cb = th.prefix >> kHistShift;
+    const bool whole = th.early && (th.prefix & ((1u << kHistShift) - 1u)) == 0u;
+    for (uint32_t b = (uint32_t)S.tid; b <= cb; b += (uint32_t)S.nt)
+      if (b < cb || !whole) sts_u32(hist_s + 4u * b, b < cb ? 0u : (uint32_t)(total - above_cut));
+    named_bar_sync(S.bar, S.nt);
   }
   return total;
+}
+
+// Exact top-k of a slot's n candidates to the row gi (-1 after the last):
+// one pass sends every candidate of the bins above the k-th largest's
+// level-1 bin straight to the row (in the slot's order) and moves that bin's
+// candidates to the front of the slot; the exact selection then runs over
+// those alone.
+__device__ __noinline__ void select_row(const Selector S, int n, uint32_t ck_s, uint32_t ci_s,
+                                        uint32_t hist_s, int k, int32_t* gi) {
+  if (n <= k) {
+    slot_select(S, kSelRow, n, ck_s, ci_s, hist_s, k, 0, nullptr, gi, nullptr);
+    return;
+  }
+  const BinCut c = find_bin(S, hist_s, kBins, k);
+  const uint32_t lo = (uint32_t)c.bin << kHistShift;
+  const bool top = c.bin == kBins - 1;  // no bin above
+  const uint32_t hi = top ? 0xFFFFFFFFu : ((uint32_t)(c.bin + 1) << kHistShift);
+  const int lane = S.tid & 31, w = S.tid >> 5, nw = S.nt >> 5;
+  const uint32_t lt = lanemask_lt();
+  const int per_batch = kCompactGroups * S.nt;
+  int carry_a = 0, carry_c = 0;
+  for (int b0 = 0, it = 0; b0 < n; b0 += per_batch, ++it) {
+    const int i0 = b0 + w * (kCompactGroups * 32) + lane;
+    uint32_t kk[kCompactGroups], ix[kCompactGroups], ma[kCompactGroups], mc[kCompactGroups];
+#pragma unroll
+    for (int u = 0; u < kCompactGroups; ++u)
+      kk[u] = lds_u32_if(i0 + 32 * u < n, ck_s + 4u * (uint32_t)(i0 + 32 * u));
+    uint32_t cnt = 0;  // this warp's above | cut << 16
+#pragma unroll
+    for (int u = 0; u < kCompactGroups; ++u) {
+      const bool above = !top && kk[u] >= hi;
+      ma[u] = __ballot_sync(0xffffffffu, above);
+      mc[u] = __ballot_sync(0xffffffffu, !above && kk[u] != 0u && kk[u] >= lo);
+      cnt += (uint32_t)__popc(ma[u]) + ((uint32_t)__popc(mc[u]) << 16);
+    }
+    int* buf = S.s->scan + 8 * (it & 1);
+    if (lane == 0) buf[w] = (int)cnt;
+#pragma unroll
+    for (int u = 0; u < kCompactGroups; ++u)
+      ix[u] = lds_u32_if(((ma[u] | mc[u]) >> lane) & 1u, ci_s + 4u * (uint32_t)(i0 + 32 * u));
+    named_bar_sync(S.bar, S.nt);  // the warps' counts; every thread holds its batch
+    int a = carry_a, cc = carry_c;
+    uint32_t tot = 0;
+    for (int v = 0; v < nw; ++v) {
+      const uint32_t x = (uint32_t)buf[v];
+      if (v < w) {
+        a += (int)(x & 0xFFFFu);
+        cc += (int)(x >> 16);
+      }
+      tot += x;
+    }
+#pragma unroll
+    for (int u = 0; u < kCompactGroups; ++u) {
+      if ((ma[u] >> lane) & 1u) __stcg(gi + a + __popc(ma[u] & lt), (int32_t)ix[u]);
+      const uint32_t pos = (uint32_t)(cc + __popc(mc[u] & lt));
+      const bool wc = (mc[u] >> lane) & 1u;
+      sts_u32_if(wc, ck_s + 4u * pos, kk[u]);
+      sts_u32_if(wc, ci_s + 4u * pos, ix[u]);
+      a += __popc(ma[u]);
+      cc += __popc(mc[u]);
+    }
+    carry_a += (int)(tot & 0xFFFFu);
+    carry_c += (int)(tot >> 16);
+  }
+  named_bar_sync(S.bar, S.nt);  // the cut bin's candidates are at the front of the slot
+  // carry_a == c.above and carry_c == c.cnt (the histogram counts the slot)
+  const BinCut cut{c.bin, 0, carry_c};
+  slot_select(S, kSelRow, carry_c, ck_s, ci_s, hist_s, k - carry_a, 0, nullptr, gi + carry_a,
+              nullptr, &cut);
 }
 
 // Append one candidate per thread of a warp if its key beats the threshold,
@@ -1504,8 +1650,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       for (int g = g_first; g < I.gcount && !to_rows; g += 2) {
         const int n0 = tok[g].count;
         if (nsplit == 1) {
-          slot_select(S, kSelRow, n0, smem_u32(ck_of(g)), smem_u32(ci_of(g)), hist_of(g), p.k, 0,
-                      nullptr, out_row(g), nullptr);
+          select_row(S, n0, smem_u32(ck_of(g)), smem_u32(ci_of(g)), hist_of(g), p.k, out_row(g));
         } else {
           // a superset of the piece's top-k, at most one block
           const int64_t blk = (int64_t)I.cand_block + (int64_t)g * nsplit + split;
