@@ -399,6 +399,7 @@ __device__ __noinline__ Thresh refine_in_bin(const Selector S, uint32_t ck_s, in
 }
 
 constexpr int kCompactGroups = 8;  // 32-candidate groups per warp and batch
+constexpr int kMergeBatch = 16;    // candidates per thread and batch of a merge's gather
 
 // In-place compaction of a slot's n candidates to those with key >= lo
 // (an early threshold: no ties to ration); returns how many are kept.
@@ -593,21 +594,14 @@ __device__ __noinline__ int slot_select(const Selector S, int mode, int n, uint3
   return total;
 }
 
-// Exact top-k of a slot's n candidates to the row gi (-1 after the last):
-// one pass sends every candidate of the bins above the k-th largest's
-// level-1 bin straight to the row (in the slot's order) and moves that bin's
-// candidates to the front of the slot; the exact selection then runs over
-// those alone.
-__device__ __noinline__ void select_row(const Selector S, int n, uint32_t ck_s, uint32_t ci_s,
-                                        uint32_t hist_s, int k, int32_t* gi) {
-  if (n <= k) {
-    slot_select(S, kSelRow, n, ck_s, ci_s, hist_s, k, 0, nullptr, gi, nullptr);
-    return;
-  }
-  const BinCut c = find_bin(S, hist_s, kBins, k);
-  const uint32_t lo = (uint32_t)c.bin << kHistShift;
-  const bool top = c.bin == kBins - 1;  // no bin above
-  const uint32_t hi = top ? 0xFFFFFFFFu : ((uint32_t)(c.bin + 1) << kHistShift);
+// One pass over a slot's n candidates: every one with key >= hi goes to the
+// row gi (in the slot's order), every one in [lo, hi) to the front of the
+// slot (in place), the rest are dropped.  Returns the two counts (x: sent to
+// the row, y: kept in the slot); the slot is consistent after the call.
+// Batches of kCompactGroups groups of 32 consecutive candidates per warp,
+// counts by ballots, one barrier per batch as in compact_early.
+__device__ __noinline__ int2 split_pass(const Selector S, int n, uint32_t ck_s, uint32_t ci_s,
+                                        uint32_t lo, uint64_t hi, int32_t* gi) {
   const int lane = S.tid & 31, w = S.tid >> 5, nw = S.nt >> 5;
   const uint32_t lt = lanemask_lt();
   const int per_batch = kCompactGroups * S.nt;
@@ -621,7 +615,7 @@ __device__ __noinline__ void select_row(const Selector S, int n, uint32_t ck_s, 
     uint32_t cnt = 0;  // this warp's above | cut << 16
 #pragma unroll
     for (int u = 0; u < kCompactGroups; ++u) {
-      const bool above = !top && kk[u] >= hi;
+      const bool above = (uint64_t)kk[u] >= hi;
       ma[u] = __ballot_sync(0xffffffffu, above);
       mc[u] = __ballot_sync(0xffffffffu, !above && kk[u] != 0u && kk[u] >= lo);
       cnt += (uint32_t)__popc(ma[u]) + ((uint32_t)__popc(mc[u]) << 16);
@@ -655,11 +649,47 @@ __device__ __noinline__ void select_row(const Selector S, int n, uint32_t ck_s, 
     carry_a += (int)(tot & 0xFFFFu);
     carry_c += (int)(tot >> 16);
   }
-  named_bar_sync(S.bar, S.nt);  // the cut bin's candidates are at the front of the slot
-  // carry_a == c.above and carry_c == c.cnt (the histogram counts the slot)
-  const BinCut cut{c.bin, 0, carry_c};
-  slot_select(S, kSelRow, carry_c, ck_s, ci_s, hist_s, k - carry_a, 0, nullptr, gi + carry_a,
-              nullptr, &cut);
+  named_bar_sync(S.bar, S.nt);  // the kept candidates are in place
+  return make_int2(carry_a, carry_c);
+}
+
+// Exact top-`need` of m <= S.nt candidates at the front of a slot to
+// gi[0, need) (need <= m): thread t ranks candidate t against all m (ties by
+// slot position); the ranks are distinct, so each selected candidate goes to
+// its rank's position.
+__device__ __forceinline__ void rank_small(const Selector S, int m, uint32_t ck_s, uint32_t ci_s,
+                                           int need, int32_t* gi) {
+  if (S.tid < m) {
+    const uint32_t key = lds_u32(ck_s + 4u * (uint32_t)S.tid);
+    int rank = 0;
+    for (int j = 0; j < m; ++j) {
+      const uint32_t kj = lds_u32(ck_s + 4u * (uint32_t)j);
+      rank += (kj > key || (kj == key && j < S.tid)) ? 1 : 0;
+    }
+    if (rank < need) __stcg(gi + rank, (int32_t)lds_u32(ci_s + 4u * (uint32_t)S.tid));
+  }
+}
+
+// Exact top-k of a slot's n candidates to the row gi (-1 after the last):
+// one pass sends every candidate of the bins above the k-th largest's
+// level-1 bin straight to the row and moves that bin's candidates to the
+// front of the slot; the exact selection then runs over those alone.
+__device__ __noinline__ void select_row(const Selector S, int n, uint32_t ck_s, uint32_t ci_s,
+                                        uint32_t hist_s, int k, int32_t* gi) {
+  if (n <= k) {
+    slot_select(S, kSelRow, n, ck_s, ci_s, hist_s, k, 0, nullptr, gi, nullptr);
+    return;
+  }
+  const BinCut c = find_bin(S, hist_s, kBins, k);
+  const uint32_t lo = (uint32_t)c.bin << kHistShift;
+  const int2 r = split_pass(S, n, ck_s, ci_s, lo, (uint64_t)lo + (1ull << kHistShift), gi);
+  // r.x == c.above and r.y == c.cnt (the histogram counts the slot)
+  if (r.y <= S.nt) {
+    rank_small(S, r.y, ck_s, ci_s, k - r.x, gi + r.x);
+  } else {
+    const BinCut cut{c.bin, 0, r.y};
+    slot_select(S, kSelRow, r.y, ck_s, ci_s, hist_s, k - r.x, 0, nullptr, gi + r.x, nullptr, &cut);
+  }
 }
 
 // Append one candidate per thread of a warp if its key beats the threshold,
@@ -807,113 +837,148 @@ __device__ __noinline__ void merge_pieces(const Selector S, const ScoreParams& p
                                           uint32_t hist_s, TokSlot* ts, PieceCut* pre,
                                           int32_t* out_row, const uint32_t* summed = nullptr) {
   const int k = p.k;
-  // summed histogram of all pieces (thread: 4-bin words tid, tid + nt, ...),
-  // read from the group's shared one when the pieces kept it
-  uint32_t local = 0;
-  for (int w = S.tid; w < kBins / 4; w += S.nt) {
-    uint4 acc = make_uint4(0, 0, 0, 0);
-    if (summed) acc = __ldcg(reinterpret_cast<const uint4*>(summed) + w);
-    for (int sj0 = 0; sj0 < nsplit && !summed; sj0 += 8) {
-      uint2 v[8];
+  BinCut c{-1, 0, 0};  // bin -1: at most k candidates in all, every one definite
+  if (summed) {
+    // the pieces' shared histogram, searched where it lies (one pass from L2)
+    c = find_bin_global(S, summed, kBins, k);
+  } else {
+    // summed histogram of all pieces (thread: 4-bin words tid, tid + nt, ...)
+    uint32_t local = 0;
+    for (int w = S.tid; w < kBins / 4; w += S.nt) {
+      uint4 acc = make_uint4(0, 0, 0, 0);
+      for (int sj0 = 0; sj0 < nsplit; sj0 += 8) {
+        uint2 v[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        v[u] = sj0 + u < nsplit ? __ldcg(reinterpret_cast<const uint2*>(
-                                      p.cand_hist + (blk0 + sj0 + u) * kBlockBins + 4 * w))
-                                : make_uint2(0, 0);
+        for (int u = 0; u < 8; ++u)
+          v[u] = sj0 + u < nsplit ? __ldcg(reinterpret_cast<const uint2*>(
+                                        p.cand_hist + (blk0 + sj0 + u) * kBlockBins + 4 * w))
+                                  : make_uint2(0, 0);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        acc.x += v[u].x & 0xFFFFu; acc.y += v[u].x >> 16;
-        acc.z += v[u].y & 0xFFFFu; acc.w += v[u].y >> 16;
-      }
-    }
-    sts_v4(hist_s + 16u * (uint32_t)w, acc);
-    local += acc.x + acc.y + acc.z + acc.w;
-  }
-  uint32_t total;
-  sel_scan(S, local, &total, 1);  // also: the summed histogram is complete
-  BinCut c{-1, 0, 0};
-  if ((int)total > k) c = find_bin(S, hist_s, kBins, k);
-  // per piece: definite = bins above the cut (a prefix of its block), then the cut bin
-  if (S.tid < 32) {
-    uint32_t ca = 0, cc = 0;
-    for (int b = 0; b < nsplit; b += 32) {
-      const int sj = b + S.tid;
-      uint32_t a = 0, cnt = 0;
-      if (sj < nsplit) {
-        const int64_t blk = blk0 + sj;
-        if (c.bin < 0) {
-          a = (uint32_t)__ldcg(p.cand_count + blk);
-        } else {
-          a = __ldcg(p.cand_start + blk * kBlockBins + c.bin);
-          cnt = __ldcg(p.cand_hist + blk * kBlockBins + c.bin);  // 16-bit counts
+        for (int u = 0; u < 8; ++u) {
+          acc.x += v[u].x & 0xFFFFu; acc.y += v[u].x >> 16;
+          acc.z += v[u].y & 0xFFFFu; acc.w += v[u].y >> 16;
         }
       }
-      const uint32_t ia = warp_inclusive_sum(a), ic = warp_inclusive_sum(cnt);
-      if (sj < nsplit) pre[sj] = PieceCut{(int)(ca + ia - a), (int)(cc + ic - cnt)};
-      ca += __shfl_sync(0xffffffffu, ia, 31);
-      cc += __shfl_sync(0xffffffffu, ic, 31);
+      sts_v4(hist_s + 16u * (uint32_t)w, acc);
+      local += acc.x + acc.y + acc.z + acc.w;
+    }
+    uint32_t total;
+    sel_scan(S, local, &total, 1);  // also: the summed histogram is complete
+    if ((int)total > k) c = find_bin(S, hist_s, kBins, k);
+  }
+  // per piece: definite = bins above the cut (a prefix of its block), then
+  // the cut bin; every piece's two counts are loaded before they are summed
+  if (S.tid < 32) {
+    uint32_t ca = 0, cc = 0;
+    for (int b = 0; b < nsplit; b += 128) {
+      uint32_t a[4], cnt[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int sj = b + 32 * u + S.tid;
+        a[u] = 0;
+        cnt[u] = 0;
+        if (sj < nsplit) {
+          const int64_t blk = blk0 + sj;
+          if (c.bin < 0) {
+            a[u] = (uint32_t)__ldcg(p.cand_count + blk);
+          } else {
+            a[u] = __ldcg(p.cand_start + blk * kBlockBins + c.bin);
+            cnt[u] = __ldcg(p.cand_hist + blk * kBlockBins + c.bin);  // 16-bit counts
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int sj = b + 32 * u + S.tid;
+        const uint32_t ia = warp_inclusive_sum(a[u]), ic = warp_inclusive_sum(cnt[u]);
+        if (sj < nsplit) pre[sj] = PieceCut{(int)(ca + ia - a[u]), (int)(cc + ic - cnt[u])};
+        ca += __shfl_sync(0xffffffffu, ia, 31);
+        cc += __shfl_sync(0xffffffffu, ic, 31);
+      }
     }
     if (S.tid == 0) pre[nsplit] = PieceCut{(int)ca, (int)cc};
   }
   named_bar_sync(S.bar, S.nt);
   const int n_def = pre[nsplit].a_pre, n_cut = pre[nsplit].c_pre;
-  // definite candidates straight to the row
-  {
-    int sj = 0;
-    for (int f0 = S.tid; f0 < n_def; f0 += kSelBatch * S.nt) {
-      int32_t v[kSelBatch];
-#pragma unroll
-      for (int u = 0; u < kSelBatch; ++u) {
-        const int f = f0 + u * S.nt;
-        v[u] = 0;
-        if (f < n_def) {
-          const int q = piece_of<false>(pre, nsplit, f, &sj);
-          v[u] = __ldcg(p.cand_idx + (blk0 + q) * p.CB + (f - pre[q].a_pre));
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kSelBatch; ++u)
-        if (f0 + u * S.nt < n_def) __stcg(out_row + f0 + u * S.nt, v[u]);
-    }
-  }
-  if (c.bin < 0) {
-    for (int i = n_def + S.tid; i < k; i += S.nt) __stcg(out_row + i, -1);
-    return;
-  }
   const int need = k - n_def;
   // the cut bin's candidates: block q holds them at [definite_q, definite_q + cut_q)
   auto cut_pos = [&](int q, int f) -> int64_t {
     const int a_q = pre[q + 1].a_pre - pre[q].a_pre;
     return (blk0 + q) * p.CB + a_q + (f - pre[q].c_pre);
   };
-  if (n_cut <= p.C) {
-    int sj = 0;
-    for (int f0 = S.tid; f0 < n_cut; f0 += kSelBatch * S.nt) {
-      uint32_t kk[kSelBatch];
-      int32_t ix[kSelBatch];
+  // One pass: the definite candidates straight to the row; the cut bin's
+  // candidates, when the slot holds them, into the slot, with counts of
+  // their sub-bins (key bits 20..13) in the selector's scratch.
+  const bool gather = c.bin >= 0 && n_cut <= p.C;
+  const uint32_t table_s = smem_u32(S.s->table);
+  if (gather) {
+    for (int b = S.tid; b < 256; b += S.nt) sts_u32(table_s + 4u * (uint32_t)b, 0u);
+    named_bar_sync(S.bar, S.nt);
+  }
+  {
+    const int n_all = n_def + (gather ? n_cut : 0);
+    int top = 1;  // the highest power of two <= nsplit
+    while (2 * top <= nsplit) top *= 2;
+    for (int f0 = S.tid; f0 < n_all; f0 += kMergeBatch * S.nt) {
+      uint32_t kk[kMergeBatch];
+      int32_t ix[kMergeBatch];
+      int64_t src[kMergeBatch];
+      // each candidate's piece by binary search over the prefix sums (the
+      // searches of a batch are independent, so their loads overlap)
 #pragma unroll
-      for (int u = 0; u < kSelBatch; ++u) {
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const int f = f0 + u * S.nt;
+        const bool def = f < n_def;
+        const int g = def ? f : f - n_def;
+        int q = 0;
+        for (int step = top; step > 0; step >>= 1) {
+          const int t = q + step;
+          if (t < nsplit && (def ? pre[t].a_pre : pre[t].c_pre) <= g) q = t;
+        }
+        src[u] = def ? (blk0 + q) * p.CB + (g - pre[q].a_pre) : cut_pos(q, g);
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
         const int f = f0 + u * S.nt;
         kk[u] = 0u;
         ix[u] = 0;
-        if (f < n_cut) {
-          const int64_t o = cut_pos(piece_of<true>(pre, nsplit, f, &sj), f);
-          kk[u] = __ldcg(p.cand_keys + o);
-          ix[u] = __ldcg(p.cand_idx + o);
+        if (f < n_all) {
+          ix[u] = __ldcg(p.cand_idx + src[u]);
+          if (f >= n_def) kk[u] = __ldcg(p.cand_keys + src[u]);
         }
       }
 #pragma unroll
-      for (int u = 0; u < kSelBatch; ++u) {
+      for (int u = 0; u < kMergeBatch; ++u) {
         const int f = f0 + u * S.nt;
-        sts_u32_if(f < n_cut, ck_s + 4u * (uint32_t)f, kk[u]);
-        sts_u32_if(f < n_cut, ci_s + 4u * (uint32_t)f, (uint32_t)ix[u]);
+        if (f < n_def) {
+          __stcg(out_row + f, ix[u]);
+        } else if (f < n_all) {
+          const uint32_t g = (uint32_t)(f - n_def);
+          sts_u32(ck_s + 4u * g, kk[u]);
+          sts_u32(ci_s + 4u * g, (uint32_t)ix[u]);
+          red_add_shared_if(true, table_s + 4u * ((kk[u] >> 13) & 255u), 1u);
+        }
       }
     }
-    named_bar_sync(S.bar, S.nt);  // the gathered candidates are visible
-    // all of them lie in the cut bin: start the selection from that cut
-    const BinCut cut{c.bin, 0, n_cut};
-    slot_select(S, kSelRow, n_cut, ck_s, ci_s, hist_s, need, 0, nullptr, out_row + n_def, nullptr,
-                &cut);
+  }
+  if (c.bin < 0) {
+    for (int i = n_def + S.tid; i < k; i += S.nt) __stcg(out_row + i, -1);
+    return;
+  }
+  if (gather) {
+    named_bar_sync(S.bar, S.nt);  // the gathered candidates and their sub-bin counts
+    // the sub-bin of the need-th largest: the higher sub-bins go to the row,
+    // that sub-bin is selected exactly
+    const BinCut c2 = find_bin_warp(table_s, 256, need);
+    const uint32_t lo = ((uint32_t)c.bin << kHistShift) | ((uint32_t)c2.bin << 13);
+    const int2 r = split_pass(S, n_cut, ck_s, ci_s, lo, (uint64_t)lo + (1ull << 13), out_row + n_def);
+    if (r.y <= S.nt) {
+      rank_small(S, r.y, ck_s, ci_s, need - r.x, out_row + n_def + r.x);
+    } else {
+      const BinCut cut{c.bin, 0, r.y};
+      slot_select(S, kSelRow, r.y, ck_s, ci_s, hist_s, need - r.x, 0, nullptr,
+                  out_row + n_def + r.x, nullptr, &cut);
+    }
     return;
   }
   // Rare: more cut-bin candidates than the slot holds (heavily tied scores).
@@ -1262,6 +1327,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const uint32_t slot_bytes = (uint32_t)(p.BPS * kScaleSlotBytes);
     constexpr int kPageScaleBytes = kPageTokens * 4;  // 256: rows 64 and 65 of the page
     Item I_far{};
+    // a decode batch (one query row per group) reads every page once per
+    // launch: its lines go first from L2, so that the launch's metadata,
+    // candidate blocks and code stay
+    const bool read_once = p.G == 1;
+    const uint64_t l2_once = l2_policy_evict_first();
     for (int it = it_begin; it < it_end && ok; ++it, ++item_i) {
       const Item I = I_cur;
       const int stable_end = se_cur;
@@ -1326,10 +1396,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             if (cur >= 0) {
               mbar_arrive_expect_tx(full, (uint32_t)(kPageTokens * kHeadDim + kPageScaleBytes));
               const int32_t row = cur * (kPageBytes / kHeadDim);  // the page's first 128-byte row
-              tma_load_2d(smem_u32(stage_base) + (uint32_t)stage * stage_bytes +
-                              pi * (uint32_t)(kPageTokens * kHeadDim),
-                          &tm_k, 0, row, full);
-              tma_load_2d(sdst, &tm_s, 0, row + kPageTokens, full);
+              const uint32_t kdst = smem_u32(stage_base) + (uint32_t)stage * stage_bytes +
+                                    pi * (uint32_t)(kPageTokens * kHeadDim);
+              if (read_once) {
+                tma_load_2d_hint(kdst, &tm_k, 0, row, full, l2_once);
+                tma_load_2d_hint(sdst, &tm_s, 0, row + kPageTokens, full, l2_once);
+              } else {
+                tma_load_2d(kdst, &tm_k, 0, row, full);
+                tma_load_2d(sdst, &tm_s, 0, row + kPageTokens, full);
+              }
             } else {
               for (uint32_t i = 0; i < (uint32_t)kPageScaleBytes; i += 16u) sts_v4(sdst + i, make_uint4(0u, 0u, 0u, 0u));
               mbar_arrive(full);
