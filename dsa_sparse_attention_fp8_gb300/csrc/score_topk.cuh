@@ -399,7 +399,7 @@ __device__ __noinline__ Thresh refine_in_bin(const Selector S, uint32_t ck_s, in
 }
 
 constexpr int kCompactGroups = 8;  // 32-candidate groups per warp and batch
-constexpr int kMergeBatch = 16;    // candidates per thread and batch of a merge's gather
+constexpr int kMergeUnits = 8;     // 32-candidate units per warp and batch of a merge's gather
 
 // In-place compaction of a slot's n candidates to those with key >= lo
 // (an early threshold: no ties to ration); returns how many are kept.
@@ -916,47 +916,68 @@ __device__ __noinline__ void merge_pieces(const Selector S, const ScoreParams& p
     named_bar_sync(S.bar, S.nt);
   }
   {
+    // The candidates needed from piece q are a prefix of its block: its
+    // a_q definite ones, then (when gathered) its c_q of the cut bin.  In
+    // piece-major order piece q's run starts at e_pre(q); each lane finds the
+    // piece of its element by a binary search, the searches of a batch
+    // advancing together (branch-free, so their loads overlap).
     const int n_all = n_def + (gather ? n_cut : 0);
+    const int lane = S.tid & 31, w = S.tid >> 5, nw = S.nt >> 5;
     int top = 1;  // the highest power of two <= nsplit
     while (2 * top <= nsplit) top *= 2;
-    for (int f0 = S.tid; f0 < n_all; f0 += kMergeBatch * S.nt) {
-      uint32_t kk[kMergeBatch];
-      int32_t ix[kMergeBatch];
-      int64_t src[kMergeBatch];
-      // each candidate's piece by binary search over the prefix sums (the
-      // searches of a batch are independent, so their loads overlap)
+    const uint32_t pre_s = smem_u32(pre);
+    auto e_pre = [&](int q) {
+      const uint2 v = lds_v2(pre_s + 8u * (uint32_t)q);
+      return (int)v.x + (gather ? (int)v.y : 0);
+    };
+    const int units = (n_all + 31) >> 5;
+    for (int j0 = w; j0 < units; j0 += nw * kMergeUnits) {
+      int q[kMergeUnits], o[kMergeUnits];
+      uint32_t kk[kMergeUnits];
+      int32_t ix[kMergeUnits];
 #pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) {
-        const int f = f0 + u * S.nt;
-        const bool def = f < n_def;
-        const int g = def ? f : f - n_def;
-        int q = 0;
-        for (int step = top; step > 0; step >>= 1) {
-          const int t = q + step;
-          if (t < nsplit && (def ? pre[t].a_pre : pre[t].c_pre) <= g) q = t;
+      for (int u = 0; u < kMergeUnits; ++u) q[u] = 0;
+      for (int step = top; step > 0; step >>= 1) {
+#pragma unroll
+        for (int u = 0; u < kMergeUnits; ++u) {
+          const int t = q[u] + step;
+          const bool le = e_pre(min(t, nsplit)) <= (j0 + nw * u) * 32 + lane;  // pre[nsplit] exists
+          q[u] = (le & (t < nsplit)) ? t : q[u];
         }
-        src[u] = def ? (blk0 + q) * p.CB + (g - pre[q].a_pre) : cut_pos(q, g);
+      }
+      int a_q[kMergeUnits], d_q[kMergeUnits], c_q[kMergeUnits];  // piece's a_q, a_pre, c_pre
+#pragma unroll
+      for (int u = 0; u < kMergeUnits; ++u) {
+        const uint2 v0 = lds_v2(pre_s + 8u * (uint32_t)q[u]);
+        const uint2 v1 = lds_v2(pre_s + 8u * (uint32_t)(q[u] + 1));
+        d_q[u] = (int)v0.x;
+        c_q[u] = (int)v0.y;
+        a_q[u] = (int)v1.x - (int)v0.x;
+        o[u] = (j0 + nw * u) * 32 + lane - (d_q[u] + (gather ? c_q[u] : 0));
       }
 #pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) {
-        const int f = f0 + u * S.nt;
+      for (int u = 0; u < kMergeUnits; ++u) {
+        const int e = (j0 + nw * u) * 32 + lane;
         kk[u] = 0u;
         ix[u] = 0;
-        if (f < n_all) {
-          ix[u] = __ldcg(p.cand_idx + src[u]);
-          if (f >= n_def) kk[u] = __ldcg(p.cand_keys + src[u]);
+        if (e < n_all) {
+          const int64_t at = (blk0 + q[u]) * p.CB + o[u];
+          ix[u] = __ldcg(p.cand_idx + at);
+          if (o[u] >= a_q[u]) kk[u] = __ldcg(p.cand_keys + at);
         }
       }
 #pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) {
-        const int f = f0 + u * S.nt;
-        if (f < n_def) {
-          __stcg(out_row + f, ix[u]);
-        } else if (f < n_all) {
-          const uint32_t g = (uint32_t)(f - n_def);
-          sts_u32(ck_s + 4u * g, kk[u]);
-          sts_u32(ci_s + 4u * g, (uint32_t)ix[u]);
-          red_add_shared_if(true, table_s + 4u * ((kk[u] >> 13) & 255u), 1u);
+      for (int u = 0; u < kMergeUnits; ++u) {
+        const int e = (j0 + nw * u) * 32 + lane;
+        if (e < n_all) {
+          if (o[u] < a_q[u]) {
+            __stcg(out_row + d_q[u] + o[u], ix[u]);
+          } else {
+            const uint32_t g = (uint32_t)(c_q[u] + o[u] - a_q[u]);
+            sts_u32(ck_s + 4u * g, kk[u]);
+            sts_u32(ci_s + 4u * g, (uint32_t)ix[u]);
+            red_add_shared_if(true, table_s + 4u * ((kk[u] >> 13) & 255u), 1u);
+          }
         }
       }
     }
