@@ -1709,23 +1709,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             }
             if (wide && gstate < 3) {
               // adopt the shared bound (at the first three checks: it only rises
-              // as the other pieces publish)
+              // as the other pieces publish) as the admission threshold; the
+              // candidates already held below it stay until the next shrink
+              // (they are keys of the row, so any superset kept stays valid)
               for (int g = g_first; g < I.gcount; g += 2) {
                 const BinCut c = find_bin_global(S, early_hist(g), kBins, p.k);
                 const uint32_t gthr = c.bin > 0 ? ((uint32_t)c.bin << kHistShift) - 1u : 0u;
-                if (gthr > tok[g].thr) {
-                  // keep only the candidates at or above that bin
-                  const int n = tok[g].count;
-                  uint32_t thr = 0;
-                  const Thresh keep{gthr + 1u, 0, 1};
-                  const int kept = slot_select(S, kSelInPlace, n, smem_u32(ck_of(g)),
-                                               smem_u32(ci_of(g)), hist_of(g), p.k, 0, nullptr,
-                                               nullptr, &thr, nullptr, &keep);
-                  if (S.tid == 0) {
-                    tok[g].count = kept;
-                    tok[g].thr = gthr;
-                  }
-                }
+                if (S.tid == 0 && gthr > tok[g].thr) tok[g].thr = gthr;
               }
             }
             ++gstate;
