@@ -1647,9 +1647,22 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             const uint32_t tA = lanes + (uint32_t)((accA * p.BPS + bA) * p.n_max);
             // without a second block the pair's second sum repeats the first (unused)
             const uint32_t tB = hasB ? lanes + (uint32_t)((accB * p.BPS + bB) * p.n_max) : tA;
+            // the pair's accumulators go back to the MMA as soon as this warp's
+            // last tensor-memory read of them is done (before its appends)
+            bool released = false;
+            auto release = [&] {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) {
+                mbar_arrive(bar_tempty + 8 * accA);
+                if (hasB) mbar_arrive(bar_tempty + 8 * accB);
+              }
+              released = true;
+            };
             for (int g = g_first; g < I.gcount; g += 2) {
               const float2 sum = relu_weighted_sum2<H>(tA + (uint32_t)(g * H), tB + (uint32_t)(g * H),
                                                        smem_u32(wq_all + g * H));
+              if (g + 2 >= I.gcount) release();
               const float scoreA = sum.x * scA, scoreB = sum.y * scB;
               const int pos = tok[g].pos;
               const bool validA = kvalidA && keyA <= pos, validB = kvalidB && keyB <= pos;
@@ -1668,12 +1681,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                              ckeys_all + (size_t)g * p.C, cidx_all + (size_t)g * p.C, hist_of(g));
               }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              mbar_arrive(bar_tempty + 8 * accA);
-              if (hasB) mbar_arrive(bar_tempty + 8 * accB);
-            }
+            if (!released) release();  // a warpgroup without a row in this item
           }
         }
         const bool check = may_fill && m / 2 == next_chk && m + 2 < iters;
