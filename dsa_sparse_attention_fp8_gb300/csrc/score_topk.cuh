@@ -464,10 +464,11 @@ enum SelMode {
 // order (deterministic); ties at an exact threshold are taken in that order
 // up to the quota.  `known`, if given, is the level-1 cut of the k-th largest
 // (hist_s is then only scratch).  Row output is staged in shared memory
-// (hist_s, after its last use) and copied out coalesced; in place, the kept candidates are staged in
-// registers one batch at a time behind a barrier per batch.  Returns the
-// number written; for kSelInPlace *thr gets the admission threshold of the
-// kept set.
+// (hist_s, after its last use) and copied out coalesced; in place, the kept
+// candidates are held in registers one batch at a time behind a barrier per
+// batch (an early threshold goes to compact_early), and the histogram is
+// updated without recounting.  Returns the number written; for kSelInPlace
+// *thr gets the admission threshold of the kept set.
 __device__ __noinline__ int slot_select(const Selector S, int mode, int n, uint32_t ck_s,
                                         uint32_t ci_s, uint32_t hist_s, int k, int limit,
                                         uint32_t* gk, int32_t* gi, uint32_t* thr,
@@ -741,10 +742,10 @@ __device__ __forceinline__ void slot_append2(uint32_t ka, int32_t ia, uint32_t k
 // Pieces and their merge.  A piece of a split group writes, per row, a
 // candidate block: its candidates (keys, indices) sorted by level-1 bin from
 // the top, the block's level-1 histogram and each bin's start offset.  The
-// merger sums the pieces' histograms, finds the bin of the row's k-th largest
-// key, copies every candidate of the higher bins straight to the output row
-// (they are a prefix of every block), and selects exactly among the
-// candidates of that one bin.
+// merger finds the bin of the row's k-th largest key from the pieces'
+// histograms, copies every candidate of the higher bins straight to the
+// output row (they are a prefix of every block), and selects exactly among
+// the candidates of that one bin.
 // ---------------------------------------------------------------------------
 
 // Publish a slot's n candidates as a bin-sorted block: histogram to ghist,
@@ -831,7 +832,13 @@ __device__ __forceinline__ int piece_of(const PieceCut* pre, int nsplit, int f, 
 // blk0 + nsplit - 1) into its output row: the exact top-min(total, k).
 // Shared memory: the row slot's buffers (ck_s, ci_s, capacity C, with the
 // slot's TokSlot for the rare streaming fallback), its histogram hist_s, and
-// pre (nsplit + 1 entries).
+// pre (nsplit + 1 entries).  The level-1 cut comes from the pieces' summed
+// histogram (`summed`, kept in L2 by a wide group's pieces) or from adding up
+// the blocks' histograms.  One pass then reads every piece's prefix down to
+// the cut bin: the definite candidates go to the row, the cut bin's into the
+// slot with counts of their sub-bins (key bits 20..13); a split at the
+// sub-bin of the row's k-th key leaves the exact selection a few candidates.
+// A cut bin larger than the slot (heavy ties) is streamed through the slot.
 __device__ __noinline__ void merge_pieces(const Selector S, const ScoreParams& p, int64_t blk0,
                                           int nsplit, uint32_t ck_s, uint32_t ci_s,
                                           uint32_t hist_s, TokSlot* ts, PieceCut* pre,
