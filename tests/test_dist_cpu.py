@@ -110,10 +110,18 @@ def test_committed_counters_follow_the_kernel_code():
     assert bench._code_only(a) != bench._code_only(c)
     h = bench.kernel_source_hash()
     assert len(h) == 16 and h == bench.kernel_source_hash()
-    text = (ROOT / "profiles" / "score_topk_batched_decode.md").read_text()
     import re
-    m = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    assert m is not None
-    # valid summary -> its figure; stale summary -> no figure (never a wrong one)
-    got = bench.profiled_traffic("batched_decode")
-    assert (got is not None) == (m.group(1) == h)
+    for name in ("batched_decode", "long_context_decode"):
+        text = (ROOT / "profiles" / f"score_topk_{name}.md").read_text()
+        m = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+        assert m is not None, name
+        # valid summary -> its figure; stale summary -> no figure (never a wrong one)
+        got = bench.profiled_traffic(name)
+        assert (got is not None) == (m.group(1) == h), name
+        if got is not None:
+            # the counters cover at least the algorithmic bytes of a launch and not
+            # much more (no wasted re-reads), per the summary's own figures
+            alg = (re.search(r"Algorithmic bytes of a full launch: ([0-9.]+) MB", text)
+                   or re.search(r"algorithmic ([0-9.]+) MB", text))
+            assert alg is not None, name
+            assert 0.95 <= got / (float(alg.group(1)) * 1e6) <= 1.1, name
