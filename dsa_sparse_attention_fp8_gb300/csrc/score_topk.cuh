@@ -596,13 +596,15 @@ __device__ __noinline__ int slot_select(const Selector S, int mode, int n, uint3
 }
 
 // One pass over a slot's n candidates: every one with key >= hi goes to the
-// row gi (in the slot's order), every one in [lo, hi) to the front of the
-// slot (in place), the rest are dropped.  Returns the two counts (x: sent to
-// the row, y: kept in the slot); the slot is consistent after the call.
+// row gi (in the slot's order; places at or beyond gi_cap, which a consistent
+// histogram never yields, are not written), every one in [lo, hi) to the
+// front of the slot (in place), the rest are dropped.  Returns the two counts
+// (x: sent to the row, y: kept in the slot); the slot is consistent after the
+// call.
 // Batches of kCompactGroups groups of 32 consecutive candidates per warp,
 // counts by ballots, one barrier per batch as in compact_early.
 __device__ __noinline__ int2 split_pass(const Selector S, int n, uint32_t ck_s, uint32_t ci_s,
-                                        uint32_t lo, uint64_t hi, int32_t* gi) {
+                                        uint32_t lo, uint64_t hi, int32_t* gi, int gi_cap) {
   const int lane = S.tid & 31, w = S.tid >> 5, nw = S.nt >> 5;
   const uint32_t lt = lanemask_lt();
   const int per_batch = kCompactGroups * S.nt;
@@ -639,7 +641,8 @@ __device__ __noinline__ int2 split_pass(const Selector S, int n, uint32_t ck_s, 
     }
 #pragma unroll
     for (int u = 0; u < kCompactGroups; ++u) {
-      if ((ma[u] >> lane) & 1u) __stcg(gi + a + __popc(ma[u] & lt), (int32_t)ix[u]);
+      const int pa = a + __popc(ma[u] & lt);
+      if (((ma[u] >> lane) & 1u) && pa < gi_cap) __stcg(gi + pa, (int32_t)ix[u]);
       const uint32_t pos = (uint32_t)(cc + __popc(mc[u] & lt));
       const bool wc = (mc[u] >> lane) & 1u;
       sts_u32_if(wc, ck_s + 4u * pos, kk[u]);
@@ -683,13 +686,15 @@ __device__ __noinline__ void select_row(const Selector S, int n, uint32_t ck_s, 
   }
   const BinCut c = find_bin(S, hist_s, kBins, k);
   const uint32_t lo = (uint32_t)c.bin << kHistShift;
-  const int2 r = split_pass(S, n, ck_s, ci_s, lo, (uint64_t)lo + (1ull << kHistShift), gi);
+  const int2 r = split_pass(S, n, ck_s, ci_s, lo, (uint64_t)lo + (1ull << kHistShift), gi, k);
   // r.x == c.above and r.y == c.cnt (the histogram counts the slot)
+  const int above = min(r.x, k), rest = k - above;
+  if (rest <= 0) return;
   if (r.y <= S.nt) {
-    rank_small(S, r.y, ck_s, ci_s, k - r.x, gi + r.x);
+    rank_small(S, r.y, ck_s, ci_s, rest, gi + above);
   } else {
     const BinCut cut{c.bin, 0, r.y};
-    slot_select(S, kSelRow, r.y, ck_s, ci_s, hist_s, k - r.x, 0, nullptr, gi + r.x, nullptr, &cut);
+    slot_select(S, kSelRow, r.y, ck_s, ci_s, hist_s, rest, 0, nullptr, gi + above, nullptr, &cut);
   }
 }
 
@@ -999,13 +1004,16 @@ __device__ __noinline__ void merge_pieces(const Selector S, const ScoreParams& p
     // that sub-bin is selected exactly
     const BinCut c2 = find_bin_warp(table_s, 256, need);
     const uint32_t lo = ((uint32_t)c.bin << kHistShift) | ((uint32_t)c2.bin << 13);
-    const int2 r = split_pass(S, n_cut, ck_s, ci_s, lo, (uint64_t)lo + (1ull << 13), out_row + n_def);
+    const int2 r = split_pass(S, n_cut, ck_s, ci_s, lo, (uint64_t)lo + (1ull << 13), out_row + n_def,
+                              need);
+    const int above = min(r.x, need), rest = need - above;
+    if (rest <= 0) return;
     if (r.y <= S.nt) {
-      rank_small(S, r.y, ck_s, ci_s, need - r.x, out_row + n_def + r.x);
+      rank_small(S, r.y, ck_s, ci_s, rest, out_row + n_def + above);
     } else {
       const BinCut cut{c.bin, 0, r.y};
-      slot_select(S, kSelRow, r.y, ck_s, ci_s, hist_s, need - r.x, 0, nullptr,
-                  out_row + n_def + r.x, nullptr, &cut);
+      slot_select(S, kSelRow, r.y, ck_s, ci_s, hist_s, rest, 0, nullptr, out_row + n_def + above,
+                  nullptr, &cut);
     }
     return;
   }
